@@ -1,0 +1,441 @@
+"""Plain CPU oracle of the canvas-denoising core of a block-diffusion text model.
+
+TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this module.  The CUDA library and its Python
+binding never import it, and it imports nothing from them: the two sides share no code,
+headers, tables or constants.  The only thing they share is the seeded input generator
+module (``discrete_diffusion_text_gb300.synth``), which holds none of the method's arithmetic.
+
+Everything here is numpy in float64 (integer work in uint64/int64), written so that each
+function can be checked against the passage it follows by eye.  A library matmul, a
+logsumexp or an argmax serves as a step where the definition is that operation; there is no
+blocking, fusion or reordering beyond what the definitions state.  Long rows are processed
+in row chunks purely to bound memory; each row's arithmetic is unchanged by that.
+
+Sources (web pages on DiffusionGemma; cited by title and section):
+  [TR]  "DiffusionGemma Technical Report 정리" (juhoplayground), sections
+        "이산 디퓨전 정식화", "Forward Process", "Backward Denoising Process",
+        "블록 자기회귀(Block-AR) 생성", "디노이징 반복과 self-conditioning",
+        "DiffusionGemma 샘플러", "추론 효율 지표", "1단계: Supervised Finetuning".
+  [BLOG] "DiffusionGemma 완전분석" (cell-devlog), section "스펙 정리".
+  [PBD] "Google DiffusionGemma 출시: 병렬 블록 디코딩" (molayo), glossary entry
+        "Iterative denoising" and the FAQ.
+  [P11] Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3", SC'11
+        (the Philox4x32-10 counter-based generator).
+
+Readings taken where the pages are silent (each listed in the design notes):
+  * time runs from t=1 (noise) to t=0 (clean); step n of T maps t_n=(T-n)/T to t_n-h, h=1/T;
+  * the Euler step of the factorised uniform-source mixture path jumps to a fresh sample
+    of the posterior with probability lambda_n = min(1, h * (-kappa'(t_n)) / (1 - kappa(t_n)));
+  * schedules: linear kappa(t)=1-t and cosine kappa(t)=cos^2(pi t / 2);
+  * confidence locking (optional): a position whose top-1 posterior log-probability is at
+    least log(theta) is locked to its top-1 token and frozen; the lock test precedes the jump;
+  * the decoder is a one-layer stand-in: embedding, one bidirectional attention layer over
+    [prefix KV ; canvas] with GQA and an optional sliding window, output projection with a
+    residual, and an LM head tied to the embedding; no norm, no RoPE, no time input;
+  * intermediate activations (q, k, v, attention output, y) are rounded to bfloat16.
+
+Counter-based random numbers (Philox4x32-10 keyed by the 64-bit seed) replace every random
+draw the method makes, so that both implementations see identical random bits:
+  noising / canvas init : counter (pos, canvas, 0, 1<<24); word 0 = keep draw, word 1 = token
+  Gumbel noise          : counter (v>>2, pos, canvas, (2<<24)|step); vocab v uses word v&3
+  Euler jump            : counter (0, pos, canvas, (3<<24)|step); word 0
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+MASK32 = np.uint64(0xFFFFFFFF)
+TWO32 = 1 << 32
+
+# [P11] Philox4x32 round multipliers and Weyl key increments.
+_PHILOX_M0 = np.uint64(0xD2511F53)
+_PHILOX_M1 = np.uint64(0xCD9E8D57)
+_PHILOX_W0 = np.uint64(0x9E3779B9)
+_PHILOX_W1 = np.uint64(0xBB67AE85)
+
+STREAM_NOISE = 1
+STREAM_GUMBEL = 2
+STREAM_JUMP = 3
+
+SCHED_LINEAR = 0
+SCHED_COSINE = 1
+
+
+# ----------------------------------------------------------------------------------------
+# Counter-based generator [P11]
+# ----------------------------------------------------------------------------------------
+
+def seed_key(seed: int) -> tuple[np.uint64, np.uint64]:
+    """Split a 64-bit seed into the two 32-bit Philox key words (low word first)."""
+    seed = int(seed) & 0xFFFFFFFFFFFFFFFF
+    return np.uint64(seed & 0xFFFFFFFF), np.uint64(seed >> 32)
+
+
+def philox4x32_10(c0, c1, c2, c3, k0, k1):
+    """Philox4x32 with 10 rounds [P11].
+
+    One round: (hi0, lo0) = M0*c0, (hi1, lo1) = M1*c2 as 64-bit products;
+    the new counter is (hi1 ^ c1 ^ k0, lo1, hi0 ^ c3 ^ k1, lo0); then the key is bumped by
+    the Weyl constants.  Inputs broadcast; every word is a 32-bit value held in uint64.
+    """
+    c0, c1, c2, c3 = (np.asarray(c, dtype=np.uint64) & MASK32 for c in (c0, c1, c2, c3))
+    k0 = np.asarray(k0, dtype=np.uint64) & MASK32
+    k1 = np.asarray(k1, dtype=np.uint64) & MASK32
+    for _ in range(10):
+        p0 = _PHILOX_M0 * c0
+        p1 = _PHILOX_M1 * c2
+        hi0, lo0 = p0 >> np.uint64(32), p0 & MASK32
+        hi1, lo1 = p1 >> np.uint64(32), p1 & MASK32
+        c0, c1, c2, c3 = hi1 ^ c1 ^ k0, lo1, hi0 ^ c3 ^ k1, lo0
+        k0 = (k0 + _PHILOX_W0) & MASK32
+        k1 = (k1 + _PHILOX_W1) & MASK32
+    return c0, c1, c2, c3
+
+
+def u32_to_token(u, V: int):
+    """Map a 32-bit draw to a token uniform over [0, V): floor(u * V / 2^32)."""
+    return ((np.asarray(u, dtype=np.uint64) * np.uint64(V)) >> np.uint64(32)).astype(np.int64)
+
+
+def u32_to_open_unit(u):
+    """Map a 32-bit draw to W = (u + 1/2) / 2^32, uniform on the open interval (0, 1)."""
+    return (np.asarray(u, dtype=np.uint64).astype(np.float64) + 0.5) / float(TWO32)
+
+
+def gumbel_from_u32(u):
+    """Standard Gumbel variate from a draw: g = -log(E), E = -log(1 - W) ~ Exp(1).
+
+    1 - W is itself uniform on (0, 1), so this is the textbook g = -log(-log U).  Writing
+    E through log1p keeps full relative precision for the large-g tail (W near 0).
+    """
+    W = u32_to_open_unit(u)
+    E = -np.log1p(-W)
+    return -np.log(E)
+
+
+# ----------------------------------------------------------------------------------------
+# Schedules [TR "Forward Process"; reading: linear and cosine families]
+# ----------------------------------------------------------------------------------------
+
+def kappa(schedule: int, t):
+    """kappa_t, monotone from kappa_0 = 1 to kappa_1 = 0 [TR "Forward Process"]."""
+    t = np.asarray(t, dtype=np.float64)
+    if schedule == SCHED_LINEAR:
+        return 1.0 - t
+    if schedule == SCHED_COSINE:
+        return np.cos(0.5 * math.pi * t) ** 2
+    raise ValueError("unknown schedule")
+
+
+def neg_dkappa(schedule: int, t):
+    """-d kappa / dt for the two schedule families."""
+    t = np.asarray(t, dtype=np.float64)
+    if schedule == SCHED_LINEAR:
+        return np.ones_like(t)
+    if schedule == SCHED_COSINE:
+        return math.pi * np.cos(0.5 * math.pi * t) * np.sin(0.5 * math.pi * t)
+    raise ValueError("unknown schedule")
+
+
+def one_minus_kappa(schedule: int, t):
+    """1 - kappa_t written in closed form (t for linear, sin^2(pi t / 2) for cosine), so
+    that no cancellation enters the Euler rate near t = 0."""
+    t = np.asarray(t, dtype=np.float64)
+    if schedule == SCHED_LINEAR:
+        return t.copy()
+    if schedule == SCHED_COSINE:
+        return np.sin(0.5 * math.pi * t) ** 2
+    raise ValueError("unknown schedule")
+
+
+def step_times(T: int):
+    """t_n = (T - n) / T for n = 0..T-1, step size h = 1/T [TR "디노이징 반복과 self-conditioning"]."""
+    n = np.arange(T, dtype=np.float64)
+    return (T - n) / T, 1.0 / T
+
+
+def jump_rate(schedule: int, T: int):
+    """lambda_n = min(1, h * (-kappa'(t_n)) / (1 - kappa(t_n))): the probability that the
+    discrete Euler step at t_n replaces a token by a fresh posterior sample.
+
+    Reading of [TR "Backward Denoising Process"] (the Euler update of the mixture path): the
+    factorised velocity is u_t = (-kappa'/(1-kappa)) * (p_hat - delta_{x_t}); one Euler step
+    of size h moves a token to a posterior sample with probability h times that rate.
+    """
+    t, h = step_times(T)
+    lam = h * neg_dkappa(schedule, t) / one_minus_kappa(schedule, t)
+    return np.minimum(1.0, lam)
+
+
+def probability_threshold(p):
+    """A probability p in [0, 1] as the integer threshold floor(p * 2^32); a 32-bit draw u
+    passes iff u < threshold, so p = 1 gives 2^32 (always) and p = 0 gives 0 (never)."""
+    p = np.clip(np.asarray(p, dtype=np.float64), 0.0, 1.0)
+    return np.floor(p * float(TWO32)).astype(np.uint64)
+
+
+def schedule_thresholds(schedule: int, T: int):
+    """keep_thr[n] = floor(kappa(t_n) * 2^32) for n = 0..T (t_T = 0) and
+    jump_thr[n] = floor(lambda_n * 2^32) for n = 0..T-1."""
+    t_all = (T - np.arange(T + 1, dtype=np.float64)) / T
+    keep = probability_threshold(kappa(schedule, t_all))
+    jump = probability_threshold(jump_rate(schedule, T))
+    return keep, jump
+
+
+def keep_threshold_from_t(schedule: int, t):
+    """Per-canvas keep threshold for noising a clean canvas to level t."""
+    return probability_threshold(kappa(schedule, t))
+
+
+# ----------------------------------------------------------------------------------------
+# Forward noising [TR "Forward Process", eq. p_t(x_t|x_0); "1단계: Supervised Finetuning"]
+# ----------------------------------------------------------------------------------------
+
+def forward_noise(x0, keep_thr, V: int, seed: int):
+    """x_t^i = x_0^i with probability kappa_t, else a token uniform over V (positions
+    independent).  Because the uniform replacement may hit x_0^i itself, the marginal is
+    P(x_t^i = x_0^i) = kappa_t + (1 - kappa_t)/|V|, as in the closed form.
+
+    x0: int [B, L]; keep_thr: uint64 [B] (floor(kappa_t * 2^32) per canvas).
+    """
+    x0 = np.asarray(x0, dtype=np.int64)
+    B, L = x0.shape
+    k0, k1 = seed_key(seed)
+    pos = np.arange(L, dtype=np.uint64)[None, :]
+    canvas = np.arange(B, dtype=np.uint64)[:, None]
+    u_keep, u_tok, _, _ = philox4x32_10(pos, canvas, 0, STREAM_NOISE << 24, k0, k1)
+    keep = u_keep < np.asarray(keep_thr, dtype=np.uint64)[:, None]
+    return np.where(keep, x0, u32_to_token(u_tok, V))
+
+
+def initial_canvas(B: int, L: int, V: int, seed: int):
+    """x_1: every position uniform over the vocabulary [TR "블록 자기회귀(Block-AR) 생성"]
+    (the noising stream with kappa = 0)."""
+    return forward_noise(np.zeros((B, L), np.int64), np.zeros(B, np.uint64), V, seed)
+
+
+# ----------------------------------------------------------------------------------------
+# Stand-in decoder [TR "디노이징 반복과 self-conditioning"; "블록 자기회귀(Block-AR) 생성"]
+# ----------------------------------------------------------------------------------------
+
+def round_bf16(x):
+    """Round to the nearest bfloat16 (ties to even) and return float64."""
+    import torch  # library conversion routine only
+
+    t = torch.from_numpy(np.ascontiguousarray(np.asarray(x, dtype=np.float64)))
+    return t.to(torch.bfloat16).to(torch.float64).numpy()
+
+
+def attention_mask(L: int, P: int, window: int):
+    """Boolean [L, P + L]: query i (absolute position P + i) sees every canvas key
+    (bidirectional inside the canvas) and prefix key k iff window == 0 or P + i - k < window
+    [TR "블록 자기회귀(Block-AR) 생성": bidirectional canvas, cross-attention to the cache;
+    BLOG "스펙 정리": sliding window of 1,024]."""
+    i = np.arange(L)[:, None]
+    k = np.arange(P)[None, :]
+    pre = np.ones((L, P), dtype=bool) if window == 0 else ((P + i - k) < window)
+    return np.concatenate([pre, np.ones((L, L), dtype=bool)], axis=1)
+
+
+def canvas_attention(q, k_pre, v_pre, k_can, v_can, window: int, scale: float):
+    """O = softmax(q K^T * scale + mask) V over keys = [prefix ; canvas], per canvas and head.
+
+    q [B, L, H, hd]; k_pre/v_pre [B, P, Hkv, hd]; k_can/v_can [B, L, Hkv, hd].
+    Query head hq reads KV head floor(hq * Hkv / H) (grouped-query attention).
+    Returns O [B, L, H, hd] and the natural-log log-sum-exp of the scaled scores [B, H, L].
+    """
+    q = np.asarray(q, np.float64)
+    B, L, H, hd = q.shape
+    P, Hkv = k_pre.shape[1], k_pre.shape[2]
+    mask = attention_mask(L, P, window)
+    O = np.zeros((B, L, H, hd))
+    lse = np.zeros((B, H, L))
+    for b in range(B):
+        for hq in range(H):
+            g = (hq * Hkv) // H
+            K = np.concatenate([k_pre[b, :, g, :], k_can[b, :, g, :]], axis=0).astype(np.float64)
+            Vv = np.concatenate([v_pre[b, :, g, :], v_can[b, :, g, :]], axis=0).astype(np.float64)
+            s = (q[b, :, hq, :] @ K.T) * scale
+            s = np.where(mask, s, -np.inf)
+            m = s.max(axis=1, keepdims=True)
+            e = np.exp(s - m)
+            den = e.sum(axis=1, keepdims=True)
+            O[b, :, hq, :] = (e / den) @ Vv
+            lse[b, hq, :] = (m + np.log(den))[:, 0]
+    return O, lse
+
+
+def decoder_front(x, E, Wqkv, H: int, Hkv: int, hd: int):
+    """h = E[x_t]; [q | k_c | v_c] = h Wqkv^T, each rounded to bfloat16.
+
+    x [B, L] int; E [V, d]; Wqkv [(H + 2 Hkv) hd, d] (rows: q heads, then k heads, then v).
+    """
+    x = np.asarray(x, np.int64)
+    B, L = x.shape
+    h = np.asarray(E, np.float64)[x]                       # [B, L, d]
+    qkv = round_bf16(h.reshape(B * L, -1) @ np.asarray(Wqkv, np.float64).T)
+    q = qkv[:, : H * hd].reshape(B, L, H, hd)
+    k = qkv[:, H * hd:(H + Hkv) * hd].reshape(B, L, Hkv, hd)
+    v = qkv[:, (H + Hkv) * hd:].reshape(B, L, Hkv, hd)
+    return h, q, k, v
+
+
+def decoder_back(h, O, Wo):
+    """y = h + O Wo^T, rounded to bfloat16.  h [B, L, d]; O [B, L, H, hd]; Wo [d, H hd]."""
+    B, L, d = h.shape
+    O = round_bf16(O).reshape(B * L, -1)
+    y = h.reshape(B * L, d) + O @ np.asarray(Wo, np.float64).T
+    return round_bf16(y).reshape(B, L, d)
+
+
+# ----------------------------------------------------------------------------------------
+# Posterior, Gumbel-max sample, top-1 [TR "디노이징 반복과 self-conditioning":
+# p_hat_0 = Softmax(logits / tau)]
+# ----------------------------------------------------------------------------------------
+
+def posterior(y, E, inv_tau: float, seed: int, step: int, L: int, rows=None, chunk=None):
+    """Per row r (canvas r // L, position r % L) of y [R, d], with logits z = y E^T
+    (LM head tied to the embedding) and z~ = z * inv_tau:
+
+      lse        = log sum_v exp(z~_v)
+      top1       = argmax_v z~_v                     (lowest index on ties)
+      logp_top1  = z~_top1 - lse
+      x0hat      = argmax_v (z~_v + g_v)              (Gumbel-max sample of Softmax(z~))
+      logp_x0hat = z~_x0hat - lse
+
+    g_v comes from the Gumbel stream of (step, canvas, position, v).  Also returned, for the
+    parity bars: the gap between the two largest perturbed scores and between the two
+    largest logits.  ``rows`` selects a subset of rows (default: all).
+    """
+    y = np.asarray(y, np.float64)
+    E64 = np.asarray(E, np.float64)
+    R = y.shape[0]
+    V = E64.shape[0]
+    rows = np.arange(R) if rows is None else np.asarray(rows, np.int64)
+    if chunk is None:  # rows per batch, so that one [rows, V] float64 block stays ~128 MiB
+        chunk = max(1, (1 << 24) // V)
+    k0, k1 = seed_key(seed)
+    v = np.arange(V, dtype=np.uint64)
+    out = {k: np.zeros(len(rows), np.float64) for k in
+           ("lse", "logp_top1", "logp_x0hat", "gap_perturbed", "gap_logit")}
+    out["top1"] = np.zeros(len(rows), np.int64)
+    out["x0hat"] = np.zeros(len(rows), np.int64)
+    for s in range(0, len(rows), chunk):
+        rr = rows[s:s + chunk]
+        z = (y[rr] @ E64.T) * inv_tau                      # [c, V]
+        m = z.max(axis=1, keepdims=True)
+        lse = (m + np.log(np.exp(z - m).sum(axis=1, keepdims=True)))[:, 0]
+        canvas = (rr // L).astype(np.uint64)[:, None]
+        pos = (rr % L).astype(np.uint64)[:, None]
+        words = philox4x32_10(v[None, :] >> np.uint64(2), pos, canvas,
+                              (STREAM_GUMBEL << 24) | int(step), k0, k1)
+        sel = (v & np.uint64(3)).astype(np.int64)[None, :]
+        u = np.choose(np.broadcast_to(sel, (len(rr), V)), words)
+        score = z + gumbel_from_u32(u)
+        top1 = np.argmax(z, axis=1)
+        x0hat = np.argmax(score, axis=1)
+        idx = np.arange(len(rr))
+        sl = slice(s, s + len(rr))
+        out["lse"][sl] = lse
+        out["top1"][sl] = top1
+        out["x0hat"][sl] = x0hat
+        out["logp_top1"][sl] = z[idx, top1] - lse
+        out["logp_x0hat"][sl] = z[idx, x0hat] - lse
+        two = -np.partition(-score, 1, axis=1)[:, :2]
+        out["gap_perturbed"][sl] = two[:, 0] - two[:, 1]
+        twz = -np.partition(-z, 1, axis=1)[:, :2]
+        out["gap_logit"][sl] = twz[:, 0] - twz[:, 1]
+    return out
+
+
+# ----------------------------------------------------------------------------------------
+# Discrete Euler step with optional confidence locking
+# [TR "Backward Denoising Process": x_(t-h) ~ Step(x_t, p_theta(.|x_t)), factorised per
+# position; PBD glossary "Iterative denoising": confident tokens are locked in]
+# ----------------------------------------------------------------------------------------
+
+def euler_update(x_in, x0hat, top1, logp_top1, lock, seed: int, step: int, jump_thr: int,
+                 lock_logthr: float):
+    """One reverse step at every position of every canvas (arrays [B, L]):
+
+      locked already                      -> unchanged
+      lock on and logp_top1 >= log theta  -> lock, x <- top1
+      jump draw u < jump_thr              -> x <- x0hat (jump = 1)
+      otherwise                           -> unchanged
+
+    lock_logthr = +inf switches locking off; the comparison is made in float32 on float32
+    inputs.  Returns x_out, lock_out (uint8), jump (uint8), done (uint8 [B], all locked).
+    """
+    x_in = np.asarray(x_in, np.int64)
+    B, L = x_in.shape
+    lock = np.asarray(lock, np.uint8).astype(bool)
+    k0, k1 = seed_key(seed)
+    pos = np.arange(L, dtype=np.uint64)[None, :]
+    canvas = np.arange(B, dtype=np.uint64)[:, None]
+    u, _, _, _ = philox4x32_10(0, pos, canvas, (STREAM_JUMP << 24) | int(step), k0, k1)
+    lp = np.asarray(logp_top1, np.float32)
+    new_lock = (~lock) & (lp >= np.float32(lock_logthr))
+    jump = (~lock) & (~new_lock) & (u < np.uint64(jump_thr))
+    x_out = np.where(new_lock, np.asarray(top1, np.int64),
+                     np.where(jump, np.asarray(x0hat, np.int64), x_in))
+    lock_out = lock | new_lock
+    done = lock_out.all(axis=1)
+    return x_out, lock_out.astype(np.uint8), jump.astype(np.uint8), done.astype(np.uint8)
+
+
+# ----------------------------------------------------------------------------------------
+# One denoising step and the loop [TR "디노이징 반복과 self-conditioning", without s_t]
+# ----------------------------------------------------------------------------------------
+
+def denoise_step(model, k_pre, v_pre, window: int, x, lock, n: int, jump_thr: int,
+                 inv_tau: float, lock_logthr: float, seed: int):
+    """logits = Decoder(x_t, KV); p_hat_0 = Softmax(logits / tau); x_(t-h) ~ Step(x_t, p_hat_0).
+
+    model: dict with E [V, d], Wqkv, Wo, H, Hkv, hd.  Returns (x_out, lock_out, jump, done,
+    diagnostics) where diagnostics holds the posterior tuple per row.
+    """
+    E, H, Hkv, hd = model["E"], model["H"], model["Hkv"], model["hd"]
+    B, L = np.asarray(x).shape
+    h, q, kc, vc = decoder_front(x, E, model["Wqkv"], H, Hkv, hd)
+    O, _ = canvas_attention(q, k_pre, v_pre, kc, vc, window, hd ** -0.5)
+    y = decoder_back(h, O, model["Wo"])
+    post = posterior(y.reshape(B * L, -1), E, inv_tau, seed, n, L)
+    shape = (B, L)
+    x_out, lock_out, jump, done = euler_update(
+        x, post["x0hat"].reshape(shape), post["top1"].reshape(shape),
+        post["logp_top1"].reshape(shape).astype(np.float32), lock, seed, n, jump_thr,
+        lock_logthr)
+    return x_out, lock_out, jump, done, post
+
+
+def denoise_loop(model, k_pre, v_pre, window: int, x, lock, T: int, schedule: int,
+                 inv_tau: float, lock_logthr: float, seed: int, start_step: int = 0,
+                 stop_when_all_locked: bool = False, end_step: int | None = None):
+    """Steps n = start_step .. end_step-1 (default T-1) of at most T [TR "DiffusionGemma 샘플러":
+    cap T].  A canvas whose positions are all locked stops when ``stop_when_all_locked``.
+    Returns the final canvas, the lock mask and the number of steps applied per canvas."""
+    x = np.asarray(x, np.int64).copy()
+    lock = np.asarray(lock, np.uint8).copy()
+    B = x.shape[0]
+    _, jump_thr = schedule_thresholds(schedule, T)
+    steps = np.zeros(B, np.int64)
+    active = np.ones(B, bool)
+    if stop_when_all_locked:
+        active &= ~lock.astype(bool).all(axis=1)
+    end = T if end_step is None else end_step
+    for n in range(start_step, end):
+        if not active.any():
+            break
+        x_new, lock_new, _, done, _ = denoise_step(model, k_pre, v_pre, window, x, lock, n,
+                                                   int(jump_thr[n]), inv_tau, lock_logthr, seed)
+        x[active] = x_new[active]
+        lock[active] = lock_new[active]
+        steps[active] += 1
+        if stop_when_all_locked:
+            active &= ~done.astype(bool)
+    return x, lock, steps

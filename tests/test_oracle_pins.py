@@ -1,0 +1,444 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Every test here runs on the CPU.  Each one checks the oracle against something other than
+itself: an independent library routine, a closed form, an invariant of the definition, or a
+brute-force / statistical consequence, chosen so that a plausible slip (a dropped term, a
+wrong sign or index, a swapped word) fails at least one of them.
+"""
+
+import json
+import math
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+import torch
+from scipy import stats
+from scipy.special import logsumexp
+
+from oracle import dgoracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+# ------------------------------------------------------------------ Philox4x32-10 -----
+
+_TRITON_SCRIPT = r"""
+import json, os, sys
+os.environ["TRITON_INTERPRET"] = "1"
+import torch, triton, triton.language as tl
+
+@triton.jit
+def kern(out_ptr, c_ptr, seed, N: tl.constexpr):
+    i = tl.arange(0, N)
+    c0 = tl.load(c_ptr + 4 * i)
+    c1 = tl.load(c_ptr + 4 * i + 1)
+    c2 = tl.load(c_ptr + 4 * i + 2)
+    c3 = tl.load(c_ptr + 4 * i + 3)
+    a, b, c, d = tl.philox(seed, c0, c1, c2, c3)
+    tl.store(out_ptr + 4 * i, a)
+    tl.store(out_ptr + 4 * i + 1, b)
+    tl.store(out_ptr + 4 * i + 2, c)
+    tl.store(out_ptr + 4 * i + 3, d)
+
+req = json.loads(sys.stdin.read())
+res = []
+for seed, ctr in zip(req["seeds"], req["counters"]):
+    c = torch.tensor(ctr, dtype=torch.int64).to(torch.int32)
+    out = torch.zeros_like(c)
+    kern[(1,)](out, c, seed, N=len(ctr) // 4)
+    res.append([v & 0xFFFFFFFF for v in out.tolist()])
+print(json.dumps(res))
+"""
+
+
+def test_philox_matches_triton_reference_implementation():
+    """Bit-identical to Triton's Philox4x32-10 (run by its CPU interpreter), an implementation
+    independent of the oracle, over random counters and 64-bit seeds."""
+    pytest.importorskip("triton")
+    rng = np.random.default_rng(123)
+    seeds = [0, 1, 0xDEADBEEF, int(rng.integers(0, 2**63 - 1)), 2**63 - 1]
+    counters = []
+    for _ in seeds:
+        c = rng.integers(0, 2**32, size=(64, 4), dtype=np.uint64)
+        c[0] = 0
+        c[1] = 0xFFFFFFFF
+        counters.append(c)
+    req = {"seeds": seeds,
+           "counters": [[int(v) - (1 << 32) if v >= (1 << 31) else int(v) for v in c.reshape(-1)]
+                        for c in counters]}
+    env = dict(os.environ, TRITON_INTERPRET="1")
+    p = subprocess.run([sys.executable, "-c", _TRITON_SCRIPT], input=json.dumps(req),
+                       capture_output=True, text=True, env=env, timeout=600)
+    assert p.returncode == 0, p.stderr[-2000:]
+    got = json.loads(p.stdout.strip().splitlines()[-1])
+    for seed, c, ref in zip(seeds, counters, got):
+        k0, k1 = O.seed_key(seed)
+        w = O.philox4x32_10(c[:, 0], c[:, 1], c[:, 2], c[:, 3], k0, k1)
+        mine = np.stack(w, axis=1).reshape(-1)
+        assert np.array_equal(mine, np.asarray(ref, dtype=np.uint64)), seed
+
+
+def test_philox_words_are_uniform_and_decorrelated():
+    k0, k1 = O.seed_key(7)
+    n = np.arange(200000, dtype=np.uint64)
+    w = O.philox4x32_10(n, 0, 0, 0, k0, k1)
+    for word in w:
+        bins = np.bincount((word >> np.uint64(24)).astype(np.int64), minlength=256)
+        assert stats.chisquare(bins).pvalue > 1e-4
+    r = np.corrcoef(w[0].astype(np.float64), w[1].astype(np.float64))[0, 1]
+    assert abs(r) < 0.02
+
+
+# ---------------------------------------------------------------- draw conversions -----
+
+@pytest.mark.parametrize("V", [16, 4096, 262144, 1000])
+def test_u32_to_token_edges(V):
+    u = np.array([0, 1, 2**31, 2**32 - 1], dtype=np.uint64)
+    t = O.u32_to_token(u, V)
+    assert t[0] == 0 and t[1] == 0
+    assert t[2] == V // 2 if V % 2 == 0 else True
+    assert t[3] == V - 1
+    if V & (V - 1) == 0:  # power of two: the top log2(V) bits
+        uu = np.random.default_rng(0).integers(0, 2**32, 10000, dtype=np.uint64)
+        shift = 32 - int(math.log2(V))
+        assert np.array_equal(O.u32_to_token(uu, V), (uu >> np.uint64(shift)).astype(np.int64))
+
+
+def test_open_unit_interval_and_gumbel_distribution():
+    u = np.array([0, 2**32 - 1], dtype=np.uint64)
+    W = O.u32_to_open_unit(u)
+    assert 0.0 < W[0] < 1e-9 and 1.0 - 1e-9 < W[1] < 1.0
+    k0, k1 = O.seed_key(11)
+    draws = O.philox4x32_10(np.arange(250000, dtype=np.uint64), 5, 6, 7, k0, k1)
+    g = O.gumbel_from_u32(np.concatenate(draws))
+    # standard Gumbel: mean = Euler-Mascheroni constant, variance = pi^2 / 6
+    assert abs(g.mean() - np.euler_gamma) < 5 * math.sqrt(math.pi**2 / 6 / g.size)
+    assert abs(g.var() - math.pi**2 / 6) < 0.02
+    assert stats.kstest(g, stats.gumbel_r.cdf).pvalue > 1e-3
+
+
+# --------------------------------------------------------------------- schedules -----
+
+@pytest.mark.parametrize("T", [1, 2, 12, 48, 192])
+def test_linear_jump_rate_is_one_over_remaining_steps(T):
+    _, jump = O.schedule_thresholds(O.SCHED_LINEAR, T)
+    for n in range(T):
+        assert int(jump[n]) == (1 << 32) // (T - n)   # floor(2^32 / (T - n)), exact integers
+    keep, _ = O.schedule_thresholds(O.SCHED_LINEAR, T)
+    assert int(keep[0]) == 0 and int(keep[T]) == 1 << 32
+
+
+@pytest.mark.parametrize("T", [2, 12, 48])
+def test_cosine_rate_endpoints_and_derivative(T):
+    lam = O.jump_rate(O.SCHED_COSINE, T)
+    assert lam[0] == pytest.approx(0.0, abs=1e-15)      # kappa'(1) = 0: first step never jumps
+    assert lam[-1] == 1.0                                # last step is clamped to 1
+    _, thr = O.schedule_thresholds(O.SCHED_COSINE, T)
+    assert int(thr[0]) == 0 and int(thr[-1]) == 1 << 32
+    # -kappa' against a central finite difference of kappa itself
+    t, h = O.step_times(T)
+    eps = 1e-6
+    fd = -(O.kappa(O.SCHED_COSINE, t + eps) - O.kappa(O.SCHED_COSINE, t - eps)) / (2 * eps)
+    lam_fd = np.minimum(1.0, h * fd / (1.0 - O.kappa(O.SCHED_COSINE, t)))
+    assert np.allclose(lam_fd, lam, atol=1e-6)
+    k = O.kappa(O.SCHED_COSINE, np.array([0.0, 1.0]))
+    assert k[0] == 1.0 and k[1] == pytest.approx(0.0, abs=1e-15)
+
+
+@pytest.mark.parametrize("T", [4, 12, 48])
+def test_linear_euler_matches_exact_bridge_and_forward_marginal(T):
+    """For linear kappa the Euler jump probability equals the exact mixture-path bridge
+    (kappa_{t-h} - kappa_t) / (1 - kappa_t), so the reverse chain driven by the true one-hot
+    posterior reproduces the forward marginal: P(not yet jumped after n steps) = 1 - kappa(t_n)."""
+    lam = O.jump_rate(O.SCHED_LINEAR, T)
+    t, h = O.step_times(T)
+    bridge = (O.kappa(O.SCHED_LINEAR, t - h) - O.kappa(O.SCHED_LINEAR, t)) / (1 - O.kappa(O.SCHED_LINEAR, t))
+    assert np.allclose(lam, bridge, rtol=1e-12)
+    stay = np.cumprod(1.0 - lam)
+    assert np.allclose(stay, 1.0 - O.kappa(O.SCHED_LINEAR, t - h), atol=1e-12)
+
+
+# ------------------------------------------------------------------ forward noise -----
+
+@pytest.mark.parametrize("V", [4096, 262144])
+@pytest.mark.parametrize("t", [0.1, 0.5, 0.9])
+def test_noising_marginal_matches_closed_form(V, t):
+    """P(x_t = x_0) = kappa_t + (1 - kappa_t)/|V| per position (Forward Process closed form);
+    with linear kappa, each token is replaced by a uniform draw with probability t."""
+    B, L = 256, 256
+    x0 = np.random.default_rng(1).integers(0, V, (B, L))
+    thr = O.keep_threshold_from_t(O.SCHED_LINEAR, np.full(B, t))
+    xt = O.forward_noise(x0, thr, V, seed=99)
+    k = 1.0 - t
+    p = k + (1.0 - k) / V
+    n = B * L
+    assert abs((xt == x0).mean() - p) < 5 * math.sqrt(p * (1 - p) / n)
+    # replaced tokens are uniform over the vocabulary
+    rep = xt[xt != x0]
+    bins = np.bincount(rep * 64 // V, minlength=64)
+    assert stats.chisquare(bins).pvalue > 1e-4
+
+
+def test_noising_extremes_and_independence():
+    V, B, L = 4096, 4, 256
+    x0 = np.random.default_rng(2).integers(0, V, (B, L))
+    assert np.array_equal(O.forward_noise(x0, np.full(B, 1 << 32, np.uint64), V, 5), x0)
+    a = O.forward_noise(x0, np.zeros(B, np.uint64), V, 5)
+    b = O.forward_noise(np.zeros_like(x0), np.zeros(B, np.uint64), V, 5)
+    assert np.array_equal(a, b)                                # independent of x_0 at kappa = 0
+    assert np.array_equal(a, O.initial_canvas(B, L, V, 5))
+    assert (a == x0).mean() < 0.01
+    c = O.forward_noise(x0, np.zeros(B, np.uint64), V, 6)
+    assert (a != c).mean() > 0.99                              # the seed changes the draws
+
+
+# ---------------------------------------------------------------------- attention -----
+
+def _sdpa(q, K, V, scale):
+    return torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q)[None], torch.from_numpy(K)[None], torch.from_numpy(V)[None],
+        scale=scale)[0].numpy()
+
+
+@pytest.mark.parametrize("P", [0, 1, 37, 256])
+@pytest.mark.parametrize("window", [0, 16, 100])
+@pytest.mark.parametrize("H,Hkv", [(4, 2), (2, 2)])
+def test_attention_equals_sdpa_on_visible_keys(P, window, H, Hkv):
+    """Per query, the oracle equals torch's float64 scaled-dot-product attention over exactly
+    the visible keys: the prefix keys k >= P + i - window + 1 (all of them when window = 0)
+    followed by every canvas key, with KV head floor(h * Hkv / H)."""
+    B, L, hd = 2, 64, 16
+    rng = np.random.default_rng(P * 100 + window + H)
+    q = rng.standard_normal((B, L, H, hd))
+    kp, vp = rng.standard_normal((2, B, P, Hkv, hd))
+    kc, vc = rng.standard_normal((2, B, L, Hkv, hd))
+    scale = hd ** -0.5
+    out, lse = O.canvas_attention(q, kp, vp, kc, vc, window, scale)
+    for b in range(B):
+        for h in range(H):
+            g = h // (H // Hkv)
+            for i in range(L):
+                lo = 0 if window == 0 else max(0, P + i - window + 1)
+                K = np.concatenate([kp[b, lo:, g], kc[b, :, g]])
+                Vv = np.concatenate([vp[b, lo:, g], vc[b, :, g]])
+                ref = _sdpa(q[b, i:i + 1, h], K, Vv, scale)
+                assert np.allclose(out[b, i, h], ref[0], atol=1e-10)
+                s = (K @ q[b, i, h]) * scale
+                assert lse[b, h, i] == pytest.approx(logsumexp(s), abs=1e-10)
+
+
+def test_attention_is_bidirectional_in_the_canvas():
+    """Changing a later canvas value changes earlier canvas outputs (no causal mask)."""
+    B, L, H, hd, P = 1, 64, 2, 16, 8
+    rng = np.random.default_rng(5)
+    q = rng.standard_normal((B, L, H, hd))
+    kp, vp = rng.standard_normal((2, B, P, H, hd))
+    kc, vc = rng.standard_normal((2, B, L, H, hd))
+    o1, _ = O.canvas_attention(q, kp, vp, kc, vc, 0, 0.25)
+    vc2 = vc.copy()
+    vc2[0, L - 1] += 1.0
+    o2, _ = O.canvas_attention(q, kp, vp, kc, vc2, 0, 0.25)
+    assert np.abs(o1[0, 0] - o2[0, 0]).max() > 1e-4
+
+
+# ---------------------------------------------------------------------- posterior -----
+
+def test_posterior_uniform_logits():
+    """All logits equal: lse = log V, top-1 is the lowest index, log p = -log V, and the
+    Gumbel-max sample is uniform over the vocabulary."""
+    V, d, R, L = 64, 8, 4096, 256
+    E = np.random.default_rng(0).standard_normal((V, d))
+    y = np.zeros((R, d))
+    post = O.posterior(y, E, 1.0, seed=3, step=0, L=L)
+    assert np.allclose(post["lse"], math.log(V), atol=1e-12)
+    assert np.all(post["top1"] == 0)
+    assert np.allclose(post["logp_top1"], -math.log(V), atol=1e-12)
+    bins = np.bincount(post["x0hat"], minlength=V)
+    assert stats.chisquare(bins).pvalue > 1e-4
+
+
+def test_posterior_normalisation_and_temperature():
+    V, d, R, L = 512, 32, 64, 16
+    rng = np.random.default_rng(1)
+    E = rng.standard_normal((V, d)) * 0.5
+    y = rng.standard_normal((R, d))
+    p1 = O.posterior(y, E, 2.0, seed=4, step=3, L=L)
+    p2 = O.posterior(2.0 * y, E, 1.0, seed=4, step=3, L=L)
+    for k in ("lse", "logp_top1", "logp_x0hat"):
+        assert np.allclose(p1[k], p2[k], atol=1e-9)
+    for k in ("top1", "x0hat"):
+        assert np.array_equal(p1[k], p2[k])
+    z = (y @ E.T) * 2.0
+    # sum_v exp(logp_v) = 1, with logp_v = z_v - lse
+    assert np.allclose(np.exp(z - p1["lse"][:, None]).sum(axis=1), 1.0, atol=1e-12)
+    assert np.allclose(p1["lse"], logsumexp(z, axis=1), atol=1e-10)
+    assert np.array_equal(p1["top1"], np.argmax(z, axis=1))
+    assert np.all(p1["logp_x0hat"] <= p1["logp_top1"] + 1e-12)
+
+
+def test_gumbel_max_samples_the_softmax():
+    """Gumbel-max over 10^6 rows with distinct counters is a categorical draw from
+    Softmax(z / tau): chi-square against the exact probabilities."""
+    V, d = 16, 16
+    z_target = np.linspace(-1.5, 1.0, V)
+    E = np.eye(V, d)
+    tau = 0.7
+    R, L = 1_000_000, 1000
+    y = np.broadcast_to(z_target, (R, d))
+    post = O.posterior(y, E, 1.0 / tau, seed=2024, step=5, L=L, chunk=250000)
+    counts = np.bincount(post["x0hat"], minlength=V)
+    p = np.exp(z_target / tau - logsumexp(z_target / tau))
+    assert stats.chisquare(counts, p * R).pvalue > 1e-3
+
+
+def test_posterior_rows_subset_equals_full():
+    V, d, R, L = 256, 16, 48, 16
+    rng = np.random.default_rng(9)
+    E, y = rng.standard_normal((V, d)), rng.standard_normal((R, d))
+    full = O.posterior(y, E, 1.0, 1, 2, L)
+    rows = np.array([0, 5, 17, 47])
+    sub = O.posterior(y, E, 1.0, 1, 2, L, rows=rows)
+    for k in full:
+        assert np.allclose(full[k][rows], sub[k])
+
+
+# -------------------------------------------------------------------- Euler step -----
+
+def test_euler_one_hot_posterior_at_last_step_returns_x0():
+    """With the posterior one-hot at x_0 and h = t (the last step, lambda = 1) every position
+    lands on x_0."""
+    V, B, L, T = 4096, 3, 256, 12
+    rng = np.random.default_rng(3)
+    x0 = rng.integers(0, V, (B, L))
+    xt = rng.integers(0, V, (B, L))
+    _, jump = O.schedule_thresholds(O.SCHED_COSINE, T)
+    lock = np.zeros((B, L), np.uint8)
+    x, lk, jmp, done = O.euler_update(xt, x0, x0, np.zeros((B, L), np.float32), lock, 1, T - 1,
+                                      int(jump[T - 1]), float("inf"))
+    assert np.array_equal(x, x0) and jmp.all() and not lk.any() and not done.any()
+
+
+def test_euler_delta_posterior_is_a_fixed_point_and_rate_matches():
+    V, B, L, T, n = 4096, 64, 256, 12, 4
+    rng = np.random.default_rng(4)
+    xt = rng.integers(0, V, (B, L))
+    x0hat = rng.integers(0, V, (B, L))
+    lock = np.zeros((B, L), np.uint8)
+    _, jump = O.schedule_thresholds(O.SCHED_LINEAR, T)
+    x, _, jmp, _ = O.euler_update(xt, xt, xt, np.full((B, L), -9.0, np.float32), lock, 3, n,
+                                  int(jump[n]), float("inf"))
+    assert np.array_equal(x, xt)                               # posterior delta_{x_t}: no move
+    x, _, jmp, _ = O.euler_update(xt, x0hat, x0hat, np.full((B, L), -9.0, np.float32), lock, 3,
+                                  n, int(jump[n]), float("inf"))
+    lam = 1.0 / (T - n)
+    N = B * L
+    assert abs(jmp.mean() - lam) < 5 * math.sqrt(lam * (1 - lam) / N)
+    assert np.array_equal(x, np.where(jmp.astype(bool), x0hat, xt))
+
+
+def test_euler_lock_precedes_jump_and_locked_positions_freeze():
+    V, B, L = 100, 2, 64
+    rng = np.random.default_rng(5)
+    xt = rng.integers(0, V, (B, L))
+    x0hat = (xt + 1) % V
+    top1 = (xt + 2) % V
+    lp = np.full((B, L), -5.0, np.float32)
+    lp[:, ::3] = -0.01                                          # confident positions
+    lock = np.zeros((B, L), np.uint8)
+    lock[:, 1] = 1                                              # already locked
+    thr = np.float32(math.log(0.9))
+    x, lk, jmp, done = O.euler_update(xt, x0hat, top1, lp, lock, 8, 0, 1 << 32, float(thr))
+    conf = np.zeros((B, L), bool)
+    conf[:, ::3] = True
+    assert np.array_equal(x[:, 1], xt[:, 1]) and lk[:, 1].all()
+    assert np.array_equal(x[conf], top1[conf]) and lk[conf].all() and not jmp[conf].any()
+    rest = ~conf
+    rest[:, 1] = False
+    assert np.array_equal(x[rest], x0hat[rest]) and jmp[rest].all() and not lk[rest].any()
+    assert not done.any()
+    lock_all = np.ones((B, L), np.uint8)
+    _, _, _, done = O.euler_update(xt, x0hat, top1, lp, lock_all, 8, 0, 1 << 32, float(thr))
+    assert done.all()
+
+
+# ------------------------------------------------------------------------- loop -----
+
+def _planted_model(V, d, H, Hkv, hd, scale=8.0):
+    """A decoder whose posterior is (numerically) delta at the input token: orthogonal
+    embeddings of norm `scale` and a zero output projection, so y = E[x_t] and the logits
+    are scale^2 at x_t and 0 elsewhere."""
+    rng = np.random.default_rng(0)
+    E = np.zeros((V, d))
+    E[np.arange(V), np.arange(V)] = scale
+    return {"E": E, "Wqkv": rng.standard_normal(((H + 2 * Hkv) * hd, d)) * 0.02,
+            "Wo": np.zeros((d, H * hd)), "H": H, "Hkv": Hkv, "hd": hd}
+
+
+def test_loop_with_delta_posterior_keeps_canvas_and_locks_at_once():
+    V, d, H, Hkv, hd, B, L, P, T = 64, 64, 2, 1, 16, 2, 64, 16, 6
+    m = _planted_model(V, d, H, Hkv, hd)
+    rng = np.random.default_rng(1)
+    kp, vp = rng.standard_normal((2, B, P, Hkv, hd))
+    x1 = O.initial_canvas(B, L, V, 42)
+    lock = np.zeros((B, L), np.uint8)
+    x, lk, steps = O.denoise_loop(m, kp, vp, 0, x1, lock, T, O.SCHED_LINEAR, 1.0,
+                                  float("inf"), 42)
+    assert np.array_equal(x, x1) and not lk.any() and np.all(steps == T)
+    x, lk, steps = O.denoise_loop(m, kp, vp, 0, x1, lock, T, O.SCHED_LINEAR, 1.0,
+                                  float(np.float32(math.log(0.9))), 42, stop_when_all_locked=True)
+    assert np.array_equal(x, x1) and lk.all() and np.all(steps == 1)
+
+
+def test_loop_resume_is_deterministic():
+    """Running steps 0..5 and then 6..11 equals running 0..11 (counters depend only on
+    seed, step, canvas and position)."""
+    V, d, H, Hkv, hd, B, L, P, T = 512, 64, 4, 2, 16, 2, 64, 32, 12
+    rng = np.random.default_rng(2)
+    m = {"E": O.round_bf16(rng.standard_normal((V, d)) * 0.3),
+         "Wqkv": O.round_bf16(rng.standard_normal(((H + 2 * Hkv) * hd, d)) * 0.2),
+         "Wo": O.round_bf16(rng.standard_normal((d, H * hd)) * 0.2), "H": H, "Hkv": Hkv, "hd": hd}
+    kp, vp = O.round_bf16(rng.standard_normal((2, B, P, Hkv, hd)))
+    x1 = O.initial_canvas(B, L, V, 7)
+    lock = np.zeros((B, L), np.uint8)
+    thr = float(np.float32(math.log(0.3)))
+    xa, la, sa = O.denoise_loop(m, kp, vp, 24, x1, lock, T, O.SCHED_COSINE, 1.0, thr, 7)
+    xh, lh, sh = O.denoise_loop(m, kp, vp, 24, x1, lock, T, O.SCHED_COSINE, 1.0, thr, 7,
+                                end_step=6)
+    xb, lb, sb = O.denoise_loop(m, kp, vp, 24, xh, lh, T, O.SCHED_COSINE, 1.0, thr, 7,
+                                start_step=6)
+    assert np.array_equal(xa, xb) and np.array_equal(la, lb)
+    assert np.array_equal(sa, sh + sb)
+    assert (xa != x1).mean() > 0.2                              # the canvas did move
+    assert 0 < la.mean() < 1                                    # and some positions locked
+
+
+# ---------------------------------------------------------------------- metrics -----
+
+def _golden(name):
+    vals = {}
+    for line in open(os.path.join(ROOT, "tests", "golden", name), encoding="utf-8"):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            k, *v = line.split()
+            vals[k] = [float(x) for x in v]
+    return vals
+
+
+def test_metrics_match_the_pages():
+    from discrete_diffusion_text_gb300 import metrics as M
+
+    g = _golden("tps_batch1.txt")
+    tps = M.tokens_per_second(g["tpf"][0], g["t_fwd_ms"][0] / 1000.0)
+    assert round(tps) == g["tps"][0]
+    for k in ("aime2026", "gpqa_diamond", "gsm8k"):
+        tpf, tps_k = g[k]
+        assert 0.010 < tpf / tps_k < 0.020
+    # hand-made two-canvas example: n = (256, 100), s = (12, 6)
+    n, s = [256, 100], [12, 6]
+    assert M.total_tokens(n) == 356 and M.total_denoising_steps(s) == 18
+    assert M.effective_denoising_steps(n, s) == pytest.approx((256 * 12 + 100 * 6) / 356)
+    assert M.tokens_per_forward(n, s) == pytest.approx(356 / 19)
+    assert M.valid_tokens([5, 7, 1, 9]) == 2 and M.valid_tokens([5, 7]) == 2
