@@ -1,0 +1,358 @@
+"""Benchmark of the canvas-denoising core on GB300.
+
+One benchmark step = one pass of the whole hot path over one batch of synthetic canvases:
+the canvas is initialised from the uniform prior with the forward-noising kernel, then
+dg_denoise_loop runs all T Euler steps (embedding + QKV, canvas attention, output projection,
+fused LM head / posterior / Gumbel-max / Euler update).  Metric: canvas tokens/s.step =
+L x B x T / (seconds per benchmark step).
+
+  python bench.py [--gpus N --steps K --warmup W --workload window1k --impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica on its own canvases (no data
+exchange), the timed region is bracketed by barriers, and the slowest rank's time is used.
+--impl reference times the CPU oracle (on this machine's cores) on a bounded sample of the
+same workload instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "canvas tokens/sec·step (256×batch×steps/s) at 1 GB300; % of tensor/HBM roofline"
+UNIT = "canvas_token_steps/s"
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="window1k")
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["hbm_gbs"], d["bf16_tflops"], d["bf16_tflops_sustained"], "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        self.proc.terminate()
+        self.proc.wait(timeout=10)
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def traffic_from_profile(kernel_file: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current
+    source of the kernel (the summary records the kernel source's sha256); else None."""
+    p = os.path.join(PROFILE_DIR, "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    src = os.path.join(ROOT, "discrete_diffusion_text_gb300", "csrc", kernel_file)
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    e = d.get(kernel_file)
+    if not e or e.get("source_sha256") != h:
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------------ oracle arm -----
+
+def oracle_step_sample(w, rows: int, seed_shift: int = 0):
+    """One denoising step of the workload by the CPU oracle: the decoder over the whole canvas
+    of one batch element, the posterior and Euler step for `rows` positions.  Returns seconds."""
+    import numpy as np
+
+    from discrete_diffusion_text_gb300 import synth
+    from oracle import dgoracle as O
+
+    m = synth.make_model(w)
+    kp, vp = synth.make_prefix_kv(w, B=1)
+    om = {k: (v.double().numpy() if hasattr(v, "double") else v) for k, v in m.items()}
+    kp, vp = kp.double().numpy(), vp.double().numpy()
+    x = O.initial_canvas(1, w.L, w.V, w.seed + seed_shift)
+    _, jump = O.schedule_thresholds(w.schedule, w.T)
+    n = w.T - 1
+    t0 = time.perf_counter()
+    h, q, k, v = O.decoder_front(x, om["E"], om["Wqkv"], w.H, w.Hkv, w.hd)
+    Oa, _ = O.canvas_attention(q, kp, vp, k, v, w.window, w.hd ** -0.5)
+    y = O.decoder_back(h, Oa, om["Wo"]).reshape(w.L, w.d)
+    sel = np.arange(rows)
+    post = O.posterior(y, om["E"], w.inv_tau, w.seed, n, w.L, rows=sel)
+    O.euler_update(x[:, :rows], post["x0hat"][None], post["top1"][None],
+                   post["logp_top1"][None].astype(np.float32), np.zeros((1, rows), np.uint8),
+                   w.seed, n, int(jump[n]), math.inf)
+    return time.perf_counter() - t0
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    rows = 32
+    for i in range(args.warmup):
+        oracle_step_sample(w, rows, i)
+    ts = [oracle_step_sample(w, rows, 100 + i) for i in range(args.steps)]
+    sec = sum(ts) / len(ts)
+    value = rows / sec
+    sample = (f"one denoising step of the {w.name} workload per benchmark step: decoder over the "
+              f"256-token canvas, posterior + Euler step for {rows} of the 256 positions "
+              f"(numpy float64; BLAS threaded, elementwise work on one thread)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": sec * 1000, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.describe(), "global_batch": w.B, "seq_len": w.L,
+                       "prefix": w.P, "parallelism": "cpu"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# -------------------------------------------------------------------------- GPU arm -----
+
+def run_ours(args, w):
+    import numpy as np
+    import torch
+
+    from discrete_diffusion_text_gb300 import dgcanvas as dgc
+    from discrete_diffusion_text_gb300 import synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dgc.load()
+
+    B = w.B
+    m = synth.make_model(w, dev)
+    kp, vp = synth.make_prefix_kv(w, dev)
+    model = dgc.make_model(m["E"], m["Wqkv"], m["Wo"], w.H, w.Hkv, w.hd)
+    lock_thr = math.log(w.lock_theta) if w.lock_theta else math.inf
+    lock_thr = float(np.float32(lock_thr))
+    ws = dgc.workspace(dgc.dg_denoise_loop_workspace(model, B, w.L, w.P, w.window), dev)
+    canvas = torch.zeros((B, w.L), dtype=torch.int32, device=dev)
+    lock = torch.zeros((B, w.L), dtype=torch.uint8, device=dev)
+    steps_taken = torch.zeros(B, dtype=torch.int32, device=dev)
+    keep0 = torch.zeros(B, dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        seed = (w.seed << 32) + 1000003 * rank + i
+        dgc.dg_forward_noise(canvas, canvas, keep0, w.V, seed)        # x_1: uniform prior
+        lock.zero_()
+        cfg = dgc.make_cfg(w.T, w.schedule, w.inv_tau, lock_thr, seed,
+                           stop_when_all_locked=w.stop_when_all_locked)
+        dgc.dg_denoise_loop(model, kp, vp, w.window, canvas, lock, steps_taken, cfg, ws)
+
+    for i in range(args.warmup):
+        step(i)
+    dgc.dg_workspace_status(ws)
+    torch.cuda.synchronize()
+
+    # ---- device-timed region
+    clocks = ClockSampler(local)
+    clocks.start()
+    dgc.dg_kernel_timer_enable(True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    steps_done = 0
+    for i in range(args.steps):
+        step(args.warmup + i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    steps_done = int(steps_taken.sum().item())  # last step's canvases (all run T steps here)
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    vocab_ms, vocab_n = dgc.dg_kernel_timer_read(0)
+    attn_ms, attn_n = dgc.dg_kernel_timer_read(1)
+    dgc.dg_kernel_timer_enable(False)
+    dgc.dg_workspace_status(ws)
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    denoise_steps = steps_done / B if steps_done else w.T
+    value = world * w.L * B * denoise_steps / (ms_per_step / 1000.0)
+
+    # ---- end to end through the public API with host buffers: the prefix KV of the step's
+    # requests goes host -> device, the final canvas and step counts come back.
+    kp_h = kp.cpu().pin_memory()
+    vp_h = vp.cpu().pin_memory()
+    out_h = torch.empty((B, w.L), dtype=torch.int32).pin_memory()
+    st_h = torch.empty(B, dtype=torch.int32).pin_memory()
+    kp_d, vp_d = torch.empty_like(kp), torch.empty_like(vp)
+
+    def e2e_step(i):
+        kp_d.copy_(kp_h, non_blocking=True)
+        vp_d.copy_(vp_h, non_blocking=True)
+        seed = (w.seed << 32) + 7777 + i
+        dgc.dg_forward_noise(canvas, canvas, keep0, w.V, seed)
+        lock.zero_()
+        cfg = dgc.make_cfg(w.T, w.schedule, w.inv_tau, lock_thr, seed,
+                           stop_when_all_locked=w.stop_when_all_locked)
+        dgc.dg_denoise_loop(model, kp_d, vp_d, w.window, canvas, lock, steps_taken, cfg, ws)
+        out_h.copy_(canvas, non_blocking=True)
+        st_h.copy_(steps_taken, non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * w.L * B * w.T / (e2e_ms / args.steps / 1000.0)
+    h2d = kp.numel() * 2 * 2
+    d2h = out_h.numel() * 4 + st_h.numel() * 4
+
+    hbm, tf_burst, tf_sust, peak_kind = peaks()
+    flops_per_launch = 2.0 * B * w.L * w.d * w.V
+    vocab_avg_s = vocab_ms / max(vocab_n, 1) / 1000.0
+    achieved = flops_per_launch / vocab_avg_s / 1e12
+    roofline = {"kernel": "vocab_posterior_kernel (fused LM head + posterior + Gumbel-max)",
+                "bound": "tensor", "achieved": achieved, "peak": tf_sust, "unit": "TFLOP/s",
+                "frac": achieved / tf_sust, "traffic": traffic_from_profile("vocab.cu"),
+                "peak_kind": f"{peak_kind} sustained bf16",
+                "launches": vocab_n, "avg_ms": vocab_avg_s * 1000.0,
+                "hbm_frac": (2.0 * w.V * w.d + 2.0 * B * w.L * w.d) / vocab_avg_s / 1e9 / hbm,
+                "attention_avg_ms": attn_ms / max(attn_n, 1)}
+    launches = args.steps * (1 + dgc.dg_denoise_loop_kernel_count(model, B, w.L, w.P, w.window,
+                                                                  w.T))
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rows = 256
+        sec = oracle_step_sample(w, rows)
+        cpu = {"value": rows / sec, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"one denoising step of the {w.name} workload (decoder over the canvas, "
+                         f"posterior over all 262,144 tokens and Euler step for all {rows} "
+                         f"positions), numpy float64; BLAS threaded, elementwise on one thread"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic (seeded N(0,0.02) weights, N(0,1) prefix KV, "
+                                         "uniform-prior canvases)",
+                "config": {"workload": w.describe(), "global_batch": B * world, "seq_len": w.L,
+                           "prefix": w.P, "denoise_steps": w.T,
+                           "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                           "l2": "inputs larger than L2: the 1 GiB LM-head weight and the prefix "
+                                 "KV are streamed every denoising step; no flush"},
+                "clocks": clk, "e2e": {"value": e2e_value, "unit": UNIT,
+                                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "gpu_launches": launches, "roofline": roofline, "cpu_baseline": cpu}
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    from discrete_diffusion_text_gb300 import synth
+
+    w = synth.WORKLOADS[args.workload]
+    if args.batch:
+        w = w.with_batch(args.batch)
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

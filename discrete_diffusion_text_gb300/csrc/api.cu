@@ -1,0 +1,627 @@
+// C ABI of libdgcanvas: argument validation, workspace layout, schedules and the denoising
+// loop.  Every step of the path runs in the library's own kernels.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "dg_common.cuh"
+#include "kernels.cuh"
+
+namespace dg {
+
+// --------------------------------------------------------------------- errors -----
+
+static thread_local std::string g_last_error = "ok";
+
+void set_error(const std::string& msg) { g_last_error = msg; }
+
+dg_status fail(dg_status code, const std::string& msg) {
+  set_error(msg);
+  return code;
+}
+
+dg_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(DG_ECUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+// ------------------------------------------------------------- device properties -----
+
+int device_id() {
+  int d = 0;
+  cudaGetDevice(&d);
+  return d;
+}
+
+int num_sms() {
+  static std::mutex mu;
+  static std::vector<int> cache;
+  const int d = device_id();
+  std::lock_guard<std::mutex> lk(mu);
+  if (static_cast<int>(cache.size()) <= d) cache.resize(d + 1, 0);
+  if (cache[d] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d) != cudaSuccess || n <= 0)
+      n = 1;
+    cache[d] = n;
+  }
+  return cache[d];
+}
+
+// Library-owned status word for calls that take no workspace.
+__device__ uint32_t g_fallback_status_word;
+
+uint32_t* status_or_fallback(uint32_t* status) {
+  if (status) return status;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_fallback_status_word) != cudaSuccess) return nullptr;
+  return static_cast<uint32_t*>(p);
+}
+
+// -------------------------------------------------------------------- tensor maps -----
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                    const uint64_t* strides_bytes, const uint32_t* box) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t gd[5];
+  cuuint64_t gs[4];
+  cuuint32_t bx[5];
+  cuuint32_t es[5];
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+    if (i + 1 < rank) gs[i] = strides_bytes[i];
+  }
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
+                        const_cast<void*>(base), gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------- kernel timer -----
+
+namespace {
+struct TimerRec {
+  int kind;
+  cudaEvent_t start, stop;
+};
+std::mutex g_timer_mu;
+bool g_timer_on = false;
+std::vector<cudaEvent_t> g_timer_pool;
+std::vector<TimerRec> g_timer_recs;
+cudaEvent_t g_timer_open[2] = {nullptr, nullptr};
+
+cudaEvent_t timer_event() {
+  if (!g_timer_pool.empty()) {
+    cudaEvent_t e = g_timer_pool.back();
+    g_timer_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+void timer_reset_locked() {
+  for (auto& r : g_timer_recs) {
+    g_timer_pool.push_back(r.start);
+    g_timer_pool.push_back(r.stop);
+  }
+  g_timer_recs.clear();
+  for (auto& e : g_timer_open)
+    if (e) {
+      g_timer_pool.push_back(e);
+      e = nullptr;
+    }
+}
+}  // namespace
+
+void timer_begin(int kind, cudaStream_t st) {
+  std::lock_guard<std::mutex> lk(g_timer_mu);
+  if (!g_timer_on) return;
+  cudaEvent_t e = timer_event();
+  cudaEventRecord(e, st);
+  g_timer_open[kind] = e;
+}
+
+void timer_end(int kind, cudaStream_t st) {
+  std::lock_guard<std::mutex> lk(g_timer_mu);
+  if (!g_timer_on || !g_timer_open[kind]) return;
+  cudaEvent_t e = timer_event();
+  cudaEventRecord(e, st);
+  g_timer_recs.push_back({kind, g_timer_open[kind], e});
+  g_timer_open[kind] = nullptr;
+}
+
+// ------------------------------------------------------------------ schedules -----
+
+static bool schedule_rate(int schedule, int T, int n, double* lam) {
+  const double t = static_cast<double>(T - n) / T;
+  const double h = 1.0 / T;
+  double v;
+  if (schedule == DG_SCHED_LINEAR) {
+    v = h / t;  // -kappa' = 1, 1 - kappa = t
+  } else if (schedule == DG_SCHED_COSINE) {
+    const double x = 0.5 * M_PI * t;
+    v = h * (M_PI * std::cos(x) * std::sin(x)) / (std::sin(x) * std::sin(x));
+  } else {
+    return false;
+  }
+  *lam = v < 1.0 ? (v > 0.0 ? v : 0.0) : 1.0;
+  return true;
+}
+
+static bool schedule_kappa(int schedule, double t, double* k) {
+  if (schedule == DG_SCHED_LINEAR) {
+    *k = 1.0 - t;
+  } else if (schedule == DG_SCHED_COSINE) {
+    const double c = std::cos(0.5 * M_PI * t);
+    *k = c * c;
+  } else {
+    return false;
+  }
+  return true;
+}
+
+static uint64_t prob_threshold(double p) {
+  if (!(p > 0.0)) return 0;
+  if (p >= 1.0) return 1ull << 32;
+  return static_cast<uint64_t>(std::floor(p * 4294967296.0));
+}
+
+}  // namespace dg
+
+using namespace dg;
+
+namespace {
+
+constexpr size_t kStatusBytes = 256;
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+bool bad_ptr(const void* p) { return p == nullptr || !aligned16(p); }
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+dg_status check_launch(const char* what) {
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  return DG_OK;
+}
+
+// Loop workspace regions (all 256-byte aligned).
+struct LoopWs {
+  uint32_t* status;
+  uint8_t* active;
+  int* n_active;
+  uint16_t *h, *q, *k, *v, *o, *y;
+  void* attn;
+  VocabPart* parts;
+  size_t total;
+};
+
+LoopWs loop_layout(const dg_model* m, int B, int L, int P, int window, uint8_t* base) {
+  LoopWs w{};
+  const size_t BL = static_cast<size_t>(B) * L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    uint8_t* p = base ? base + off : nullptr;
+    off += align256(bytes);
+    return p;
+  };
+  w.status = reinterpret_cast<uint32_t*>(take(kStatusBytes));
+  w.active = take(B);
+  w.n_active = reinterpret_cast<int*>(take(sizeof(int)));
+  w.h = reinterpret_cast<uint16_t*>(take(BL * m->d * 2));
+  w.q = reinterpret_cast<uint16_t*>(take(BL * m->H * m->hd * 2));
+  w.k = reinterpret_cast<uint16_t*>(take(BL * m->Hkv * m->hd * 2));
+  w.v = reinterpret_cast<uint16_t*>(take(BL * m->Hkv * m->hd * 2));
+  w.o = reinterpret_cast<uint16_t*>(take(BL * m->H * m->hd * 2));
+  w.y = reinterpret_cast<uint16_t*>(take(BL * m->d * 2));
+  const AttnPlan ap = plan_attention(B, L, P, m->H, m->hd, window);
+  w.attn = take(ap.part_bytes > 0 ? ap.part_bytes : 16);
+  const VocabPlan vp = plan_vocab(static_cast<int>(BL), m->V);
+  w.parts = reinterpret_cast<VocabPart*>(take(vp.part_bytes));
+  w.total = off;
+  return w;
+}
+
+dg_status check_attn_dims(int B, int L, int P, int H, int Hkv, int hd, int window) {
+  if (B < 0 || L <= 0 || P < 0 || H <= 0 || Hkv <= 0 || window < 0)
+    return fail(DG_EINVAL, "attention: negative or zero size");
+  if (L > 256 || L % 64 != 0) return fail(DG_ENOTSUP, "attention: L must be 64, 128, 192 or 256");
+  if (hd != 64 && hd != 128) return fail(DG_ENOTSUP, "attention: hd must be 64 or 128");
+  if (H % Hkv != 0) return fail(DG_EINVAL, "attention: H must be a multiple of Hkv");
+  if (static_cast<int64_t>(B) * H * ((L + 127) / 128) > 0x7FFFFFFF)
+    return fail(DG_ENOTSUP, "attention: too many query tiles");
+  return DG_OK;
+}
+
+dg_status check_model(const dg_model* m) {
+  if (!m) return fail(DG_EINVAL, "model: NULL");
+  if (bad_ptr(m->E) || bad_ptr(m->Wqkv) || bad_ptr(m->Wo))
+    return fail(DG_EINVAL, "model: NULL or misaligned weight pointer");
+  if (m->V <= 0 || m->d <= 0 || m->H <= 0 || m->Hkv <= 0)
+    return fail(DG_EINVAL, "model: non-positive size");
+  if (m->d % 64 != 0) return fail(DG_ENOTSUP, "model: d must be a multiple of 64");
+  if (m->V % 256 != 0) return fail(DG_ENOTSUP, "model: V must be a multiple of 256");
+  if (m->hd != 64 && m->hd != 128) return fail(DG_ENOTSUP, "model: hd must be 64 or 128");
+  if (m->H % m->Hkv != 0) return fail(DG_EINVAL, "model: H must be a multiple of Hkv");
+  return DG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dg_last_error(void) { return g_last_error.c_str(); }
+
+int dg_abi_version(void) { return 1; }
+
+dg_status dg_schedule_thresholds(int schedule, int T, uint64_t* keep_thr, uint64_t* jump_thr) {
+  if (T < 1) return fail(DG_EINVAL, "schedule: T must be >= 1");
+  if (schedule != DG_SCHED_LINEAR && schedule != DG_SCHED_COSINE)
+    return fail(DG_EINVAL, "schedule: unknown schedule");
+  for (int n = 0; n <= T; ++n) {
+    double k;
+    schedule_kappa(schedule, static_cast<double>(T - n) / T, &k);
+    if (keep_thr) keep_thr[n] = prob_threshold(k);
+    if (jump_thr && n < T) {
+      double lam;
+      schedule_rate(schedule, T, n, &lam);
+      jump_thr[n] = prob_threshold(lam);
+    }
+  }
+  return DG_OK;
+}
+
+dg_status dg_keep_thresholds(int schedule, const double* t, int B, uint64_t* keep_thr) {
+  if (B < 0 || (B > 0 && (!t || !keep_thr))) return fail(DG_EINVAL, "keep thresholds: bad arrays");
+  if (schedule != DG_SCHED_LINEAR && schedule != DG_SCHED_COSINE)
+    return fail(DG_EINVAL, "keep thresholds: unknown schedule");
+  for (int b = 0; b < B; ++b) {
+    if (!(t[b] >= 0.0 && t[b] <= 1.0)) return fail(DG_EINVAL, "keep thresholds: t outside [0, 1]");
+    double k;
+    schedule_kappa(schedule, t[b], &k);
+    keep_thr[b] = prob_threshold(k);
+  }
+  return DG_OK;
+}
+
+dg_status dg_forward_noise(const int32_t* x0, int32_t* xt, const uint64_t* keep_thr, int B, int L,
+                           int V, uint64_t seed, void* stream) {
+  if (B < 0 || L < 0 || V < 1) return fail(DG_EINVAL, "forward_noise: bad sizes");
+  if (static_cast<int64_t>(B) * L >= (1ll << 31)) return fail(DG_ENOTSUP, "forward_noise: too large");
+  if (static_cast<int64_t>(B) * L == 0) return DG_OK;
+  if (bad_ptr(x0) || bad_ptr(xt) || keep_thr == nullptr || (reinterpret_cast<uintptr_t>(keep_thr) & 7))
+    return fail(DG_EINVAL, "forward_noise: NULL or misaligned pointer");
+  launch_forward_noise(x0, xt, keep_thr, B, L, V, seed, as_stream(stream));
+  return check_launch("forward_noise launch");
+}
+
+dg_status dg_embed_qkv(const int32_t* x, const uint16_t* E, const uint16_t* Wqkv, uint16_t* h,
+                       uint16_t* q, uint16_t* k, uint16_t* v, int BL, int V, int d, int H,
+                       int Hkv, int hd, void* stream) {
+  if (BL < 0 || V <= 0 || d <= 0 || H <= 0 || Hkv <= 0) return fail(DG_EINVAL, "embed_qkv: bad sizes");
+  if (d % 64 != 0) return fail(DG_ENOTSUP, "embed_qkv: d must be a multiple of 64");
+  if (hd != 64 && hd != 128) return fail(DG_ENOTSUP, "embed_qkv: hd must be 64 or 128");
+  if (H % Hkv != 0) return fail(DG_EINVAL, "embed_qkv: H must be a multiple of Hkv");
+  if (BL == 0) return DG_OK;
+  if (bad_ptr(x) || bad_ptr(E) || bad_ptr(Wqkv) || bad_ptr(h) || bad_ptr(q) || bad_ptr(k) || bad_ptr(v))
+    return fail(DG_EINVAL, "embed_qkv: NULL or misaligned pointer");
+  cudaStream_t st = as_stream(stream);
+  launch_embed_gather(x, E, h, BL, V, d, nullptr, st);
+  dg_status s = check_launch("embed gather launch");
+  if (s != DG_OK) return s;
+  GemmOut out{};
+  out.nseg = 3;
+  out.seg_begin[0] = 0;
+  out.seg_begin[1] = H * hd;
+  out.seg_begin[2] = (H + Hkv) * hd;
+  out.seg_begin[3] = (H + 2 * Hkv) * hd;
+  out.ptr[0] = q;
+  out.ptr[1] = k;
+  out.ptr[2] = v;
+  out.ld[0] = H * hd;
+  out.ld[1] = Hkv * hd;
+  out.ld[2] = Hkv * hd;
+  const cudaError_t e = launch_gemm(h, Wqkv, BL, (H + 2 * Hkv) * hd, d, out, nullptr, 0,
+                                    status_or_fallback(nullptr), nullptr, st);
+  if (e != cudaSuccess) return cuda_fail(e, "qkv gemm launch");
+  return DG_OK;
+}
+
+size_t dg_canvas_attn_workspace(int B, int L, int P, int H, int Hkv, int hd, int window) {
+  (void)Hkv;
+  if (B < 0 || L <= 0 || H <= 0 || (hd != 64 && hd != 128)) return kStatusBytes;
+  return kStatusBytes + align256(plan_attention(B, L, P, H, hd, window).part_bytes);
+}
+
+dg_status dg_canvas_attn(const uint16_t* q, const uint16_t* k_pre, const uint16_t* v_pre,
+                         const uint16_t* k_can, const uint16_t* v_can, uint16_t* out, float* lse,
+                         int B, int L, int P, int H, int Hkv, int hd, int window, float scale,
+                         void* ws, size_t ws_bytes, void* stream) {
+  dg_status s = check_attn_dims(B, L, P, H, Hkv, hd, window);
+  if (s != DG_OK) return s;
+  if (B == 0) return DG_OK;
+  if (bad_ptr(q) || bad_ptr(k_can) || bad_ptr(v_can) || bad_ptr(out) || bad_ptr(ws))
+    return fail(DG_EINVAL, "attention: NULL or misaligned pointer");
+  if (P > 0 && (bad_ptr(k_pre) || bad_ptr(v_pre)))
+    return fail(DG_EINVAL, "attention: NULL or misaligned prefix pointer");
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3)) return fail(DG_EINVAL, "attention: misaligned lse");
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(DG_EINVAL, "attention: bad scale");
+  if (ws_bytes < dg_canvas_attn_workspace(B, L, P, H, Hkv, hd, window))
+    return fail(DG_EINVAL, "attention: workspace too small");
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  const cudaError_t e = launch_attention(q, k_pre, v_pre, k_can, v_can, out, lse, B, L, P, H, Hkv,
+                                         hd, window, scale, w + kStatusBytes,
+                                         reinterpret_cast<uint32_t*>(w), nullptr, as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+  return DG_OK;
+}
+
+dg_status dg_out_proj(const uint16_t* h, const uint16_t* O, const uint16_t* Wo, uint16_t* y, int BL,
+                      int d, int Hhd, void* stream) {
+  if (BL < 0 || d <= 0 || Hhd <= 0) return fail(DG_EINVAL, "out_proj: bad sizes");
+  if (d % 64 != 0 || Hhd % 64 != 0) return fail(DG_ENOTSUP, "out_proj: sizes must be multiples of 64");
+  if (BL == 0) return DG_OK;
+  if (bad_ptr(h) || bad_ptr(O) || bad_ptr(Wo) || bad_ptr(y)) return fail(DG_EINVAL, "out_proj: bad pointer");
+  if (y == h) return fail(DG_EINVAL, "out_proj: y must not alias h");
+  GemmOut out{};
+  out.nseg = 1;
+  out.seg_begin[0] = 0;
+  out.seg_begin[1] = d;
+  out.ptr[0] = y;
+  out.ld[0] = d;
+  const cudaError_t e = launch_gemm(O, Wo, BL, d, Hhd, out, h, d, status_or_fallback(nullptr),
+                                    nullptr, as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "out_proj gemm launch");
+  return DG_OK;
+}
+
+size_t dg_vocab_posterior_workspace(int B, int L, int V) {
+  if (B <= 0 || L <= 0 || V < 256) return kStatusBytes;
+  return kStatusBytes + align256(plan_vocab(B * L, V).part_bytes);
+}
+
+dg_status dg_vocab_posterior_step(const uint16_t* y, const uint16_t* W, int B, int L, int d, int V,
+                                  float inv_tau, uint64_t seed, int step, const int32_t* x_in,
+                                  int32_t* x_out, uint8_t* lock, uint8_t* jump, uint8_t* done,
+                                  uint64_t jump_thr, float lock_logthr,
+                                  const dg_posterior_out* out, void* ws, size_t ws_bytes,
+                                  void* stream) {
+  if (B < 0 || L <= 0 || d <= 0 || V <= 0) return fail(DG_EINVAL, "vocab_posterior: bad sizes");
+  if (d % 64 != 0) return fail(DG_ENOTSUP, "vocab_posterior: d must be a multiple of 64");
+  if (V % 256 != 0) return fail(DG_ENOTSUP, "vocab_posterior: V must be a multiple of 256");
+  if (L > 256 || L % 64 != 0) return fail(DG_ENOTSUP, "vocab_posterior: L must be 64..256, multiple of 64");
+  if (step < 0 || step >= (1 << 24)) return fail(DG_EINVAL, "vocab_posterior: step out of range");
+  if (!(inv_tau > 0.f) || !std::isfinite(inv_tau)) return fail(DG_EINVAL, "vocab_posterior: bad inv_tau");
+  if (jump_thr > (1ull << 32)) return fail(DG_EINVAL, "vocab_posterior: jump_thr above 2^32");
+  if (static_cast<int64_t>(B) * L >= (1ll << 31)) return fail(DG_ENOTSUP, "vocab_posterior: too many rows");
+  if (B == 0) return DG_OK;
+  if (bad_ptr(y) || bad_ptr(W) || bad_ptr(ws)) return fail(DG_EINVAL, "vocab_posterior: bad pointer");
+  if (x_in && !x_out) return fail(DG_EINVAL, "vocab_posterior: x_out required with x_in");
+  if (ws_bytes < dg_vocab_posterior_workspace(B, L, V))
+    return fail(DG_EINVAL, "vocab_posterior: workspace too small");
+  cudaStream_t st = as_stream(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  uint32_t* status = reinterpret_cast<uint32_t*>(w);
+  VocabPart* parts = reinterpret_cast<VocabPart*>(w + kStatusBytes);
+  const VocabPlan vp = plan_vocab(B * L, V);
+  cudaError_t e = launch_vocab_pass(y, W, B * L, L, d, V, inv_tau, seed, step, parts, status,
+                                    nullptr, st);
+  if (e != cudaSuccess) return cuda_fail(e, "vocab pass launch");
+  FinalizeParams fp{};
+  fp.parts = parts;
+  fp.num_mt = vp.num_mt;
+  fp.S = vp.S;
+  fp.L = L;
+  if (out) {
+    fp.out_x0hat = out->x0hat;
+    fp.out_top1 = out->top1;
+    fp.out_logp_top1 = out->logp_top1;
+    fp.out_lse = out->lse;
+    fp.out_logp_x0hat = out->logp_x0hat;
+  }
+  fp.x_in = x_in;
+  fp.x_out = x_out;
+  fp.lock = lock;
+  fp.jump = jump;
+  fp.done = done;
+  fp.jump_thr = jump_thr;
+  fp.lock_logthr = lock_logthr;
+  fp.k0 = static_cast<uint32_t>(seed);
+  fp.k1 = static_cast<uint32_t>(seed >> 32);
+  fp.step = static_cast<uint32_t>(step);
+  launch_vocab_finalize(fp, B, st);
+  return check_launch("vocab finalize launch");
+}
+
+dg_status dg_euler_update(const int32_t* x_in, const int32_t* x0hat, const int32_t* top1,
+                          const float* logp_top1, int32_t* x_out, uint8_t* lock, uint8_t* jump,
+                          uint8_t* done, int B, int L, uint64_t seed, int step, uint64_t jump_thr,
+                          float lock_logthr, void* stream) {
+  if (B < 0 || L <= 0 || L > 1024) return fail(DG_EINVAL, "euler_update: bad sizes (1 <= L <= 1024)");
+  if (step < 0 || step >= (1 << 24)) return fail(DG_EINVAL, "euler_update: step out of range");
+  if (jump_thr > (1ull << 32)) return fail(DG_EINVAL, "euler_update: jump_thr above 2^32");
+  if (B == 0) return DG_OK;
+  if (!x_in || !x0hat || !top1 || !logp_top1 || !x_out || !lock)
+    return fail(DG_EINVAL, "euler_update: NULL pointer");
+  launch_euler_update(x_in, x0hat, top1, logp_top1, x_out, lock, jump, done, B, L, seed, step,
+                      jump_thr, lock_logthr, as_stream(stream));
+  return check_launch("euler_update launch");
+}
+
+size_t dg_denoise_loop_workspace(const dg_model* m, int B, int L, int P, int window) {
+  if (!m || B <= 0 || L <= 0 || m->d <= 0 || m->H <= 0 || m->Hkv <= 0 ||
+      (m->hd != 64 && m->hd != 128) || m->V < 256)
+    return kStatusBytes;
+  return loop_layout(m, B, L, P, window, nullptr).total;
+}
+
+int dg_denoise_loop_kernel_count(const dg_model* m, int B, int L, int P, int window, int steps) {
+  if (!m || B <= 0 || L <= 0 || steps < 0 || m->H <= 0 || (m->hd != 64 && m->hd != 128))
+    return -1;
+  const AttnPlan ap = plan_attention(B, L, P, m->H, m->hd, window);
+  // loop init, then per step: embedding gather, QKV GEMM, attention (+ split merge),
+  // output projection, vocabulary pass, finalisation
+  return 1 + steps * (6 + (ap.splits > 1 ? 1 : 0));
+}
+
+dg_status dg_denoise_loop(const dg_model* m, const uint16_t* k_pre, const uint16_t* v_pre, int B,
+                          int L, int P, int window, int32_t* canvas, uint8_t* lock,
+                          int32_t* steps_taken, const dg_sampler_cfg* cfg, void* ws,
+                          size_t ws_bytes, void* stream) {
+  dg_status s = check_model(m);
+  if (s != DG_OK) return s;
+  s = check_attn_dims(B, L, P, m->H, m->Hkv, m->hd, window);
+  if (s != DG_OK) return s;
+  if (!cfg) return fail(DG_EINVAL, "loop: NULL cfg");
+  if (cfg->T < 1 || cfg->T >= (1 << 24)) return fail(DG_EINVAL, "loop: T out of range");
+  if (cfg->schedule != DG_SCHED_LINEAR && cfg->schedule != DG_SCHED_COSINE)
+    return fail(DG_EINVAL, "loop: unknown schedule");
+  if (!(cfg->inv_tau > 0.f) || !std::isfinite(cfg->inv_tau)) return fail(DG_EINVAL, "loop: bad inv_tau");
+  const int end = cfg->end_step > 0 ? cfg->end_step : cfg->T;
+  if (cfg->start_step < 0 || end > cfg->T || cfg->start_step > end)
+    return fail(DG_EINVAL, "loop: bad start/end step");
+  if (static_cast<int64_t>(B) * L >= (1ll << 31)) return fail(DG_ENOTSUP, "loop: too many rows");
+  if (B == 0) return DG_OK;
+  if (bad_ptr(canvas) || bad_ptr(lock) || bad_ptr(steps_taken) || bad_ptr(ws))
+    return fail(DG_EINVAL, "loop: NULL or misaligned canvas/lock/steps/workspace");
+  if (P > 0 && (bad_ptr(k_pre) || bad_ptr(v_pre))) return fail(DG_EINVAL, "loop: bad prefix pointer");
+  if (ws_bytes < dg_denoise_loop_workspace(m, B, L, P, window))
+    return fail(DG_EINVAL, "loop: workspace too small");
+
+  std::vector<uint64_t> jump(cfg->T);
+  dg_schedule_thresholds(cfg->schedule, cfg->T, nullptr, jump.data());
+  cudaStream_t st = as_stream(stream);
+  const LoopWs w = loop_layout(m, B, L, P, window, static_cast<uint8_t*>(ws));
+  const int BL = B * L;
+  const int Hhd = m->H * m->hd;
+  const int KVhd = m->Hkv * m->hd;
+  const VocabPlan vp = plan_vocab(BL, m->V);
+
+  cudaError_t e = cudaMemsetAsync(w.n_active, 0, sizeof(int), st);
+  if (e != cudaSuccess) return cuda_fail(e, "loop: memset");
+  launch_loop_init(lock, w.active, w.n_active, steps_taken, B, L, cfg->stop_when_all_locked, st);
+  if ((s = check_launch("loop init launch")) != DG_OK) return s;
+
+  GemmOut qkv{};
+  qkv.nseg = 3;
+  qkv.seg_begin[0] = 0;
+  qkv.seg_begin[1] = Hhd;
+  qkv.seg_begin[2] = Hhd + KVhd;
+  qkv.seg_begin[3] = Hhd + 2 * KVhd;
+  qkv.ptr[0] = w.q;
+  qkv.ptr[1] = w.k;
+  qkv.ptr[2] = w.v;
+  qkv.ld[0] = Hhd;
+  qkv.ld[1] = KVhd;
+  qkv.ld[2] = KVhd;
+  GemmOut yo{};
+  yo.nseg = 1;
+  yo.seg_begin[0] = 0;
+  yo.seg_begin[1] = m->d;
+  yo.ptr[0] = w.y;
+  yo.ld[0] = m->d;
+  const float scale = 1.0f / std::sqrt(static_cast<float>(m->hd));
+
+  for (int n = cfg->start_step; n < end; ++n) {
+    launch_embed_gather(canvas, m->E, w.h, BL, m->V, m->d, w.n_active, st);
+    if ((s = check_launch("loop: embed launch")) != DG_OK) return s;
+    e = launch_gemm(w.h, m->Wqkv, BL, Hhd + 2 * KVhd, m->d, qkv, nullptr, 0, w.status, w.n_active,
+                    st);
+    if (e != cudaSuccess) return cuda_fail(e, "loop: qkv gemm launch");
+    e = launch_attention(w.q, k_pre, v_pre, w.k, w.v, w.o, nullptr, B, L, P, m->H, m->Hkv, m->hd,
+                         window, scale, w.attn, w.status, w.n_active, st);
+    if (e != cudaSuccess) return cuda_fail(e, "loop: attention launch");
+    e = launch_gemm(w.o, m->Wo, BL, m->d, Hhd, yo, w.h, m->d, w.status, w.n_active, st);
+    if (e != cudaSuccess) return cuda_fail(e, "loop: out_proj gemm launch");
+    e = launch_vocab_pass(w.y, m->E, BL, L, m->d, m->V, cfg->inv_tau, cfg->seed, n, w.parts,
+                          w.status, w.n_active, st);
+    if (e != cudaSuccess) return cuda_fail(e, "loop: vocab pass launch");
+    FinalizeParams fp{};
+    fp.parts = w.parts;
+    fp.num_mt = vp.num_mt;
+    fp.S = vp.S;
+    fp.L = L;
+    fp.x_in = canvas;
+    fp.x_out = canvas;
+    fp.lock = lock;
+    fp.jump_thr = jump[n];
+    fp.lock_logthr = cfg->lock_logthr;
+    fp.k0 = static_cast<uint32_t>(cfg->seed);
+    fp.k1 = static_cast<uint32_t>(cfg->seed >> 32);
+    fp.step = static_cast<uint32_t>(n);
+    fp.active = w.active;
+    fp.steps_taken = steps_taken;
+    fp.n_active = w.n_active;
+    fp.stop_when_all_locked = cfg->stop_when_all_locked;
+    launch_vocab_finalize(fp, B, st);
+    if ((s = check_launch("loop: finalize launch")) != DG_OK) return s;
+  }
+  return DG_OK;
+}
+
+dg_status dg_workspace_status(const void* ws, void* stream) {
+  cudaStream_t st = as_stream(stream);
+  uint32_t* word = ws ? static_cast<uint32_t*>(const_cast<void*>(ws)) : status_or_fallback(nullptr);
+  if (!word) return fail(DG_ECUDA, "status: no status word");
+  uint32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, word, sizeof(v), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(word, 0, sizeof(v), st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "status: read");
+  if (v & kStatusTimeout) return fail(DG_ETIMEOUT, "a kernel gave up waiting on an on-chip barrier");
+  if (v & kStatusBadIndex) return fail(DG_EKERNEL, "a kernel skipped an out-of-range index");
+  return DG_OK;
+}
+
+dg_status dg_kernel_timer_enable(int enable) {
+  std::lock_guard<std::mutex> lk(g_timer_mu);
+  timer_reset_locked();
+  g_timer_on = enable != 0;
+  return DG_OK;
+}
+
+dg_status dg_kernel_timer_read(int kind, double* total_ms, int* launches) {
+  if (!total_ms || !launches || kind < 0 || kind > 1) return fail(DG_EINVAL, "timer: bad arguments");
+  std::lock_guard<std::mutex> lk(g_timer_mu);
+  double tot = 0.0;
+  int n = 0;
+  for (auto& r : g_timer_recs) {
+    if (r.kind != kind) continue;
+    cudaError_t e = cudaEventSynchronize(r.stop);
+    if (e != cudaSuccess) return cuda_fail(e, "timer: event sync");
+    float ms = 0.f;
+    e = cudaEventElapsedTime(&ms, r.start, r.stop);
+    if (e != cudaSuccess) return cuda_fail(e, "timer: elapsed");
+    tot += ms;
+    ++n;
+  }
+  *total_ms = tot;
+  *launches = n;
+  return DG_OK;
+}
+
+}  // extern "C"

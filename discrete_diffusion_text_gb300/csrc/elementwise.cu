@@ -1,0 +1,206 @@
+// Integer-decision kernels: forward noising, the Euler jump/lock/commit step, and the
+// finalisation of the fused vocabulary pass (split merge + posterior outputs + Euler step).
+#include "dg_common.cuh"
+#include "kernels.cuh"
+
+namespace dg {
+
+// ------------------------------------------------------------------ forward noising ----
+// [TR "Forward Process"]: x_t = x_0 when the keep draw passes kappa's threshold, else a
+// uniform token.  One Philox call per position; four positions per thread with 16-byte
+// loads and stores when the four lie in the array.
+__global__ void forward_noise_kernel(const int32_t* __restrict__ x0, int32_t* __restrict__ xt,
+                                     const uint64_t* __restrict__ keep_thr, int B, int L,
+                                     uint32_t V, uint32_t k0, uint32_t k1) {
+  const int64_t n = static_cast<int64_t>(B) * L;
+  const int64_t n4 = (n + 3) / 4;
+  for (int64_t i4 = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i4 < n4;
+       i4 += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t p0 = i4 * 4;
+    int32_t in[4] = {0, 0, 0, 0}, out[4];
+    const bool full = p0 + 3 < n;
+    if (full) {
+      const int4 v = *reinterpret_cast<const int4*>(x0 + p0);
+      in[0] = v.x;
+      in[1] = v.y;
+      in[2] = v.z;
+      in[3] = v.w;
+    } else {
+      for (int e = 0; e < 4; ++e)
+        if (p0 + e < n) in[e] = x0[p0 + e];
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int64_t p = p0 + e;
+      const uint32_t canvas = static_cast<uint32_t>(p / L);
+      const uint32_t pos = static_cast<uint32_t>(p % L);
+      const Words4 w = philox4x32_10(pos, canvas, 0u, kStreamNoise, k0, k1);
+      const bool keep = p < n && static_cast<uint64_t>(w.x) < keep_thr[p < n ? canvas : 0];
+      out[e] = keep ? in[e] : draw_token(w.y, V);
+    }
+    if (full) {
+      *reinterpret_cast<int4*>(xt + p0) = make_int4(out[0], out[1], out[2], out[3]);
+    } else {
+      for (int e = 0; e < 4; ++e)
+        if (p0 + e < n) xt[p0 + e] = out[e];
+    }
+  }
+}
+
+void launch_forward_noise(const int32_t* x0, int32_t* xt, const uint64_t* keep_thr, int B, int L,
+                          int V, uint64_t seed, cudaStream_t st) {
+  const int64_t n4 = (static_cast<int64_t>(B) * L + 3) / 4;
+  const int threads = 256;
+  int64_t blocks = (n4 + threads - 1) / threads;
+  const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  forward_noise_kernel<<<static_cast<int>(blocks), threads, 0, st>>>(
+      x0, xt, keep_thr, B, L, static_cast<uint32_t>(V), static_cast<uint32_t>(seed),
+      static_cast<uint32_t>(seed >> 32));
+}
+
+// --------------------------------------------------------------- Euler update ----------
+// One CTA per canvas, one thread per position; `done` is a block-wide AND of the locks.
+__global__ void euler_update_kernel(const int32_t* __restrict__ x_in,
+                                    const int32_t* __restrict__ x0hat,
+                                    const int32_t* __restrict__ top1,
+                                    const float* __restrict__ logp_top1, int32_t* x_out,
+                                    uint8_t* lock, uint8_t* jump, uint8_t* done, int L,
+                                    uint32_t k0, uint32_t k1, uint32_t step, uint64_t jump_thr,
+                                    float lock_logthr) {
+  const int b = blockIdx.x;
+  const int i = threadIdx.x;
+  bool locked_after = true;
+  if (i < L) {
+    const int64_t r = static_cast<int64_t>(b) * L + i;
+    const uint32_t u = jump_draw(static_cast<uint32_t>(i), static_cast<uint32_t>(b), step, k0, k1);
+    const EulerOut o = euler_decide(x_in[r], x0hat[r], top1[r], logp_top1[r], lock[r] != 0, u,
+                                    jump_thr, lock_logthr);
+    x_out[r] = o.x;
+    lock[r] = o.lock ? 1 : 0;
+    if (jump) jump[r] = o.jump ? 1 : 0;
+    locked_after = o.lock;
+  }
+  const int all = __syncthreads_and(locked_after ? 1 : 0);
+  if (done && i == 0) done[b] = all ? 1 : 0;
+}
+
+void launch_euler_update(const int32_t* x_in, const int32_t* x0hat, const int32_t* top1,
+                         const float* logp_top1, int32_t* x_out, uint8_t* lock, uint8_t* jump,
+                         uint8_t* done, int B, int L, uint64_t seed, int step, uint64_t jump_thr,
+                         float lock_logthr, cudaStream_t st) {
+  const int threads = ((L + 31) / 32) * 32;
+  euler_update_kernel<<<B, threads, 0, st>>>(x_in, x0hat, top1, logp_top1, x_out, lock, jump,
+                                             done, L, static_cast<uint32_t>(seed),
+                                             static_cast<uint32_t>(seed >> 32),
+                                             static_cast<uint32_t>(step), jump_thr, lock_logthr);
+}
+
+// ------------------------------------------------- vocabulary-pass finalisation -------
+// One CTA per canvas, one thread per position.  Merges the position's partial tuples from
+// every vocabulary chunk in a fixed order (deterministic), writes the posterior outputs and
+// applies the Euler step.  In the loop, `active` freezes finished canvases, `steps_taken`
+// counts applied steps and `n_active` counts canvases that have not stopped.
+__global__ void vocab_finalize_kernel(FinalizeParams p) {
+  if (p.n_active && *p.n_active == 0) return;
+  const int b = blockIdx.x;
+  const int i = threadIdx.x;
+  const bool is_active = p.active == nullptr || p.active[b] != 0;
+  bool locked_after = true;
+  if (i < p.L) {
+    const int row = b * p.L + i;
+    const int mt = row >> 7;
+    const int row_in = row & 127;
+    VocabPart acc = p.parts[static_cast<int64_t>(mt) * 128 + row_in];
+    for (int c = 1; c < p.S; ++c) {
+      const VocabPart q = p.parts[(static_cast<int64_t>(c) * p.num_mt + mt) * 128 + row_in];
+      merge_part(acc, q);
+    }
+    const float lse = acc.m + logf(acc.s);
+    const float lp_top1 = acc.top_z - lse;
+    if (p.out_x0hat) p.out_x0hat[row] = acc.best_idx;
+    if (p.out_top1) p.out_top1[row] = acc.top_idx;
+    if (p.out_logp_top1) p.out_logp_top1[row] = lp_top1;
+    if (p.out_lse) p.out_lse[row] = lse;
+    if (p.out_logp_x0hat) p.out_logp_x0hat[row] = acc.best_z - lse;
+    if (p.x_in != nullptr && is_active) {
+      const bool was_locked = p.lock != nullptr && p.lock[row] != 0;
+      const uint32_t u = jump_draw(static_cast<uint32_t>(i), static_cast<uint32_t>(b), p.step,
+                                   p.k0, p.k1);
+      const EulerOut o = euler_decide(p.x_in[row], acc.best_idx, acc.top_idx, lp_top1,
+                                      was_locked, u, p.jump_thr, p.lock_logthr);
+      p.x_out[row] = o.x;
+      if (p.lock) p.lock[row] = o.lock ? 1 : 0;
+      if (p.jump) p.jump[row] = o.jump ? 1 : 0;
+      locked_after = o.lock && p.lock != nullptr;
+    } else if (p.x_in != nullptr) {
+      if (p.x_out != p.x_in) p.x_out[row] = p.x_in[row];
+      if (p.jump) p.jump[row] = 0;
+      locked_after = p.lock != nullptr && p.lock[row] != 0;
+    } else {
+      locked_after = false;
+    }
+  }
+  const int all = __syncthreads_and(locked_after ? 1 : 0);
+  if (i == 0) {
+    if (p.done) p.done[b] = all ? 1 : 0;
+    if (is_active && p.x_in != nullptr) {
+      if (p.steps_taken) p.steps_taken[b] += 1;
+      if (p.active && p.stop_when_all_locked && all) {
+        p.active[b] = 0;
+        if (p.n_active) atomicSub(p.n_active, 1);
+      }
+    }
+  }
+}
+
+void launch_vocab_finalize(const FinalizeParams& p, int B, cudaStream_t st) {
+  const int threads = ((p.L + 31) / 32) * 32;
+  vocab_finalize_kernel<<<B, threads, 0, st>>>(p);
+}
+
+// Loop bookkeeping: active[b] = 1 unless the canvas is already fully locked and stopping is
+// on; n_active = number of active canvases; steps_taken = 0.
+__global__ void loop_init_kernel(const uint8_t* lock, uint8_t* active, int* n_active,
+                                 int32_t* steps_taken, int L, int stop_when_all_locked) {
+  const int b = blockIdx.x;
+  bool locked = true;
+  for (int i = threadIdx.x; i < L; i += blockDim.x)
+    locked = locked && lock[static_cast<int64_t>(b) * L + i] != 0;
+  const int all = __syncthreads_and(locked ? 1 : 0);
+  if (threadIdx.x == 0) {
+    const bool act = !(stop_when_all_locked && all);
+    active[b] = act ? 1 : 0;
+    steps_taken[b] = 0;
+    if (act) atomicAdd(n_active, 1);
+  }
+}
+
+void launch_loop_init(const uint8_t* lock, uint8_t* active, int* n_active, int32_t* steps_taken,
+                      int B, int L, int stop_when_all_locked, cudaStream_t st) {
+  loop_init_kernel<<<B, 256, 0, st>>>(lock, active, n_active, steps_taken, L,
+                                      stop_when_all_locked);
+}
+
+// h[r, :] = E[x[r], :]; ids outside [0, V) give a zero row.  16 bytes per thread.
+__global__ void embed_gather_kernel(const int32_t* __restrict__ x, const uint4* __restrict__ E,
+                                    uint4* __restrict__ h, int V, int d16, const int* n_active) {
+  if (n_active && *n_active == 0) return;
+  const int r = blockIdx.x;
+  const int id = x[r];
+  const bool ok = id >= 0 && id < V;
+  for (int c = threadIdx.x; c < d16; c += blockDim.x)
+    h[static_cast<int64_t>(r) * d16 + c] =
+        ok ? E[static_cast<int64_t>(id) * d16 + c] : make_uint4(0, 0, 0, 0);
+}
+
+void launch_embed_gather(const int32_t* x, const uint16_t* E, uint16_t* h, int BL, int V, int d,
+                         const int* n_active, cudaStream_t st) {
+  const int d16 = d / 8;
+  const int threads = d16 < 256 ? ((d16 + 31) / 32) * 32 : 256;
+  embed_gather_kernel<<<BL, threads, 0, st>>>(x, reinterpret_cast<const uint4*>(E),
+                                              reinterpret_cast<uint4*>(h), V, d16, n_active);
+}
+
+}  // namespace dg

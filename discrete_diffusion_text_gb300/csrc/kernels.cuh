@@ -1,0 +1,83 @@
+// Launch interfaces of the library's kernels (host side of each translation unit).
+#pragma once
+
+#include "dg_common.cuh"
+
+namespace dg {
+
+struct FinalizeParams {
+  const VocabPart* parts;  // [S * num_mt * 128]
+  int num_mt, S, L;
+  int32_t* out_x0hat;
+  int32_t* out_top1;
+  float* out_logp_top1;
+  float* out_lse;
+  float* out_logp_x0hat;
+  const int32_t* x_in;  // NULL: posterior only
+  int32_t* x_out;
+  uint8_t* lock;
+  uint8_t* jump;
+  uint8_t* done;
+  uint64_t jump_thr;
+  float lock_logthr;
+  uint32_t k0, k1, step;
+  uint8_t* active;       // loop only
+  int32_t* steps_taken;  // loop only
+  int* n_active;         // loop only
+  int stop_when_all_locked;
+};
+
+void launch_forward_noise(const int32_t* x0, int32_t* xt, const uint64_t* keep_thr, int B, int L,
+                          int V, uint64_t seed, cudaStream_t st);
+void launch_euler_update(const int32_t* x_in, const int32_t* x0hat, const int32_t* top1,
+                         const float* logp_top1, int32_t* x_out, uint8_t* lock, uint8_t* jump,
+                         uint8_t* done, int B, int L, uint64_t seed, int step, uint64_t jump_thr,
+                         float lock_logthr, cudaStream_t st);
+void launch_vocab_finalize(const FinalizeParams& p, int B, cudaStream_t st);
+void launch_loop_init(const uint8_t* lock, uint8_t* active, int* n_active, int32_t* steps_taken,
+                      int B, int L, int stop_when_all_locked, cudaStream_t st);
+void launch_embed_gather(const int32_t* x, const uint16_t* E, uint16_t* h, int BL, int V, int d,
+                         const int* n_active, cudaStream_t st);
+
+// ---------------------------------------------------------------- projection GEMM -----
+// C[M, N] = A[M, K] W[N, K]^T (+ R[M, N]) in bf16 with fp32 accumulation; the N columns are
+// routed to up to three output tensors (column ranges [seg_begin[i], seg_begin[i+1])).
+struct GemmOut {
+  int nseg;
+  int seg_begin[4];
+  uint16_t* ptr[3];
+  int ld[3];
+};
+
+cudaError_t launch_gemm(const uint16_t* A, const uint16_t* W, int M, int N, int K,
+                        const GemmOut& out, const uint16_t* residual, int ld_res,
+                        uint32_t* status, const int* n_active, cudaStream_t st);
+
+// ------------------------------------------------------------------- attention -----
+struct AttnPlan {
+  int splits;
+  size_t part_bytes;  // fp32 partials for split > 1
+};
+AttnPlan plan_attention(int B, int L, int P, int H, int hd, int window);
+cudaError_t launch_attention(const uint16_t* q, const uint16_t* k_pre, const uint16_t* v_pre,
+                             const uint16_t* k_can, const uint16_t* v_can, uint16_t* out,
+                             float* lse, int B, int L, int P, int H, int Hkv, int hd, int window,
+                             float scale, void* part_ws, uint32_t* status, const int* n_active,
+                             cudaStream_t st);
+
+// -------------------------------------------------------------- vocabulary pass -----
+struct VocabPlan {
+  int num_mt, nvt, per, S, units, grid;
+  size_t part_bytes;
+};
+VocabPlan plan_vocab(int R, int V);
+cudaError_t launch_vocab_pass(const uint16_t* y, const uint16_t* W, int R, int L, int d, int V,
+                              float inv_tau, uint64_t seed, int step, VocabPart* parts,
+                              uint32_t* status, const int* n_active, cudaStream_t st);
+
+// Optional CUDA-event timing around the heavy kernels (kind 0: vocabulary pass,
+// kind 1: attention).
+void timer_begin(int kind, cudaStream_t st);
+void timer_end(int kind, cudaStream_t st);
+
+}  // namespace dg

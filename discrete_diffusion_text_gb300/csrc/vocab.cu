@@ -1,0 +1,382 @@
+// Fused LM head + posterior statistics + Gumbel-max sampling over the vocabulary.
+//
+// z = y W^T (rows = canvas positions, columns = vocabulary) is computed on the 5th-generation
+// tensor cores tile by tile; no logit ever leaves the SM.  Each CTA is persistent over "units"
+// = (128-row tile, contiguous vocabulary chunk):
+//   warp 0      TMA: k-blocks of y (128 x 64) and W (256 x 64) into a 4-stage ring;
+//   warp 1      one thread issues tcgen05.mma M=128, N=256, K=16 into one of two TMEM
+//               accumulators (2 x 256 columns), so the next tile's MMA overlaps this epilogue;
+//   warps 2..9  epilogue, one thread per (row, half of the 256 columns): tempered logits
+//               z~ = z / tau, online (max, sum exp) for the log-sum-exp, the top-1 (lowest index on
+//               ties), and the Gumbel-max sample argmax(z~ + g) with g from Philox.
+// Only rows' partial tuples are written; a per-canvas finalisation kernel merges them in a
+// fixed order and applies the Euler step.
+//
+// Gumbel candidates: g_v = -log(E_v) with E_v = -log(1 - W_v) >= W_v (W_v the open-unit draw),
+// so entry v can only beat the current best score b if W_v < exp(z~_v - b).  exp(z~_v - m) is
+// already computed for the sum, so the test costs one multiply; the two logarithms are taken
+// only for the rare entries that pass (with a safety margin for rounding).
+#include "kernels.cuh"
+#include "sm103.cuh"
+
+namespace dg {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr int kThreads = 320;     // 10 warps
+constexpr int kEpiThreads = 256;  // warps 2..9
+
+struct VocabParams {
+  int R, L, d, V;
+  int num_mt, nvt, per, S, units;
+  float inv_tau;
+  uint32_t k0, k1, c3;  // Philox key and counter word 3 (stream tag | step)
+  VocabPart* parts;
+  uint32_t* status;
+  const int* n_active;
+};
+
+struct VocabLayout {
+  static constexpr int kABytes = kBM * kBK * 2;   // 16 KiB
+  static constexpr int kBBytes = kBN * kBK * 2;   // 32 KiB
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kScratchOff = kStages * kStageBytes;
+  static constexpr int kScratchBytes = kBM * sizeof(VocabPart);
+  static constexpr int kBarOff = kScratchOff + kScratchBytes;
+  static constexpr int kSmemBytes = kBarOff + 256 + 1024;
+};
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Running per-row state of one epilogue thread.
+struct RowState {
+  float m;       // running max of z~ (natural units)
+  float s;       // sum of exp(z~ - m)
+  float top_z;
+  int top_idx;
+  float best;    // best perturbed score z~ + g
+  int best_idx;
+  float best_z;
+  float cthr;    // exp(m - best) * (1 + margin): candidate test is W < exp(z~ - m) * cthr
+};
+
+__device__ __forceinline__ void refresh_cthr(RowState& st) {
+  // best == -inf: everything is a candidate.
+  st.cthr = st.best == -INFINITY ? INFINITY : __expf(st.m - st.best) * 1.001f;
+}
+
+__device__ __forceinline__ void process_chunk(RowState& st, const float (&z)[32], int vbase,
+                                              float inv_tau, uint32_t pos, uint32_t canvas,
+                                              uint32_t k0, uint32_t k1, uint32_t c3) {
+  float zt[32];
+  float cm = -INFINITY;
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    zt[e] = z[e] * inv_tau;
+    cm = fmaxf(cm, zt[e]);
+  }
+  // top-1: strictly greater keeps the lowest index within this thread's increasing order
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    if (zt[e] > st.top_z) {
+      st.top_z = zt[e];
+      st.top_idx = vbase + e;
+    }
+  }
+  if (cm > st.m) {
+    st.s *= ex2_approx((st.m - cm) * kLog2e);
+    st.m = cm;
+    refresh_cthr(st);
+  }
+  const float mlog2 = st.m * kLog2e;
+  float ssum = 0.f;
+  float pe[32];
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    pe[e] = ex2_approx(fmaf(zt[e], kLog2e, -mlog2));
+    ssum += pe[e];
+  }
+  st.s += ssum;
+  // Gumbel perturbation, 4 vocabulary entries per Philox call.
+#pragma unroll
+  for (int g4 = 0; g4 < 8; ++g4) {
+    const Words4 w = philox4x32_10(static_cast<uint32_t>(vbase >> 2) + g4, pos, canvas, c3, k0,
+                                   k1);
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int e = g4 * 4 + q;
+      // W = (u + 1/2) / 2^32, rounded to fp32 (full relative precision near 0)
+      const float W = fmaf(__uint2float_rn(u[q]), 2.3283064365386963e-10f, 1.1641532182693481e-10f);
+      if (W < pe[e] * st.cthr) {
+        const float E = -log1pf(-W);
+        const float sc = zt[e] - logf(E);
+        if (sc > st.best) {
+          st.best = sc;
+          st.best_idx = vbase + e;
+          st.best_z = zt[e];
+          refresh_cthr(st);
+        }
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    vocab_posterior_kernel(const __grid_constant__ CUtensorMap tmA,
+                           const __grid_constant__ CUtensorMap tmB, VocabParams p) {
+  using Lay = VocabLayout;
+  if (p.n_active && *p.n_active == 0) return;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  VocabPart* scratch = reinterpret_cast<VocabPart*>(smem + Lay::kScratchOff);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lay::kBarOff);
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;  // [2]
+  uint64_t* tempty = tfull + 2;       // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int nkb = p.d / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], kEpiThreads);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_map(&tmA);
+      tma_prefetch_map(&tmB);
+      uint32_t g = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+        const int mt = u % p.num_mt;
+        const int chunk = u / p.num_mt;
+        const int vt0 = chunk * p.per;
+        const int vt1 = min(vt0 + p.per, p.nvt);
+        for (int vt = vt0; ok && vt < vt1; ++vt) {
+          for (int kb = 0; kb < nkb; ++kb, ++g) {
+            const int s = g % kStages;
+            if (!mbar_wait(&empty[s], ((g / kStages) & 1) ^ 1, abort_flag)) { ok = false; break; }
+            uint8_t* sa = smem + s * Lay::kStageBytes;
+            mbar_arrive_expect_tx(&full[s], Lay::kStageBytes);
+            tma_load_2d(sa, &tmA, &full[s], kb * kBK, mt * kBM);
+            tma_load_2d(sa + Lay::kABytes, &tmB, &full[s], kb * kBK, vt * kBN);
+          }
+        }
+      }
+      if (!ok) {
+        for (uint32_t q = (g > kStages ? g - kStages : 0); q < g; ++q)
+          mbar_wait_drain(&full[q % kStages], (q / kStages) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(kBM, kBN, false);
+      uint32_t g = 0, j = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+        const int chunk = u / p.num_mt;
+        const int vt0 = chunk * p.per;
+        const int vt1 = min(vt0 + p.per, p.nvt);
+        for (int vt = vt0; ok && vt < vt1; ++vt, ++j) {
+          const int buf = j & 1;
+          if (!mbar_wait(&tempty[buf], ((j >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem + buf * kBN;
+          for (int kb = 0; kb < nkb; ++kb, ++g) {
+            const int s = g % kStages;
+            if (!mbar_wait(&full[s], (g / kStages) & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t sa = smem_u32(smem + s * Lay::kStageBytes);
+            const uint32_t sb = sa + Lay::kABytes;
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k)
+              mma_bf16_ss(d_tmem, sdesc_sw128(sa + k * 32, 16, 1024),
+                          sdesc_sw128(sb + k * 32, 16, 1024), idesc, (kb | k) != 0);
+            mma_commit(&empty[s]);
+          }
+          if (ok) mma_commit(&tfull[buf]);
+        }
+      }
+      if (!ok) {
+        mma_commit(&tfull[0]);
+        mbar_wait_drain(&tfull[0], 0);
+        mbar_wait_drain(&tfull[0], 1);
+      }
+    }
+  } else {
+    // --------------------------------------------------------------- epilogue -----
+    const int ew = warp - 2;
+    const int half = ew >> 2;                       // which 128 of the 256 columns
+    const int row_in = (warp & 3) * 32 + lane;      // TMEM lane quarter of this warp
+    const uint32_t lane_base = tmem_lane_base(warp);
+    // After an abort the loop structure is kept (every epilogue warp still reaches each
+    // unit's named barriers); only the waits, loads and stores are skipped.
+    uint32_t j = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+      const int mt = u % p.num_mt;
+      const int chunk = u / p.num_mt;
+      const int vt0 = chunk * p.per;
+      const int vt1 = min(vt0 + p.per, p.nvt);
+      const int row = mt * kBM + row_in;
+      const uint32_t canvas = static_cast<uint32_t>(row / p.L);
+      const uint32_t pos = static_cast<uint32_t>(row % p.L);
+      RowState st;
+      st.m = -INFINITY;
+      st.s = 0.f;
+      st.top_z = -INFINITY;
+      st.top_idx = 0x7FFFFFFF;
+      st.best = -INFINITY;
+      st.best_idx = 0x7FFFFFFF;
+      st.best_z = -INFINITY;
+      st.cthr = INFINITY;
+      for (int vt = vt0; vt < vt1; ++vt, ++j) {
+        const int buf = j & 1;
+        if (ok) ok = warp_wait(&tfull[buf], (j >> 1) & 1, abort_flag);
+        if (!ok) continue;
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float z[32];
+          tmem_ld32(tmem + lane_base + buf * kBN + half * 128 + c * 32, z);
+          process_chunk(st, z, vt * kBN + half * 128 + c * 32, p.inv_tau, pos, canvas, p.k0,
+                        p.k1, p.c3);
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty[buf]);
+      }
+      // Merge the two column halves of each row through shared memory.
+      VocabPart mine;
+      mine.m = st.m;
+      mine.s = st.s;
+      mine.top_z = st.top_z;
+      mine.top_idx = st.top_idx;
+      mine.best_score = st.best;
+      mine.best_idx = st.best_idx;
+      mine.best_z = st.best_z;
+      mine.pad = 0;
+      named_bar_sync(1, kEpiThreads);
+      if (half == 1) scratch[row_in] = mine;
+      named_bar_sync(1, kEpiThreads);
+      if (half == 0) {
+        merge_part(mine, scratch[row_in]);
+        if (ok && row < p.R) p.parts[static_cast<int64_t>(u) * kBM + row_in] = mine;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+  if (threadIdx.x == 0 && *abort_flag) atomicOr(p.status, kStatusTimeout);
+}
+
+}  // namespace
+
+VocabPlan plan_vocab(int R, int V) {
+  VocabPlan pl;
+  pl.num_mt = (R + kBM - 1) / kBM;
+  pl.nvt = V / kBN;
+  const int sms = num_sms();
+  // Choose the number of vocabulary chunks S that minimises (waves x tiles per chunk); ties
+  // go to fewer chunks (less merge work).
+  int bestS = 1, best_per = pl.nvt;
+  int64_t best_cost = -1;
+  for (int S = 1; S <= pl.nvt; ++S) {
+    const int per = (pl.nvt + S - 1) / S;
+    const int S2 = (pl.nvt + per - 1) / per;
+    if (S2 != S) continue;
+    const int64_t units = static_cast<int64_t>(pl.num_mt) * S2;
+    const int64_t waves = (units + sms - 1) / sms;
+    const int64_t cost = waves * per;
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      bestS = S2;
+      best_per = per;
+    }
+  }
+  pl.S = bestS;
+  pl.per = best_per;
+  pl.units = pl.num_mt * pl.S;
+  pl.grid = pl.units < sms ? pl.units : sms;
+  pl.part_bytes = static_cast<size_t>(pl.units) * kBM * sizeof(VocabPart);
+  return pl;
+}
+
+cudaError_t launch_vocab_pass(const uint16_t* y, const uint16_t* W, int R, int L, int d, int V,
+                              float inv_tau, uint64_t seed, int step, VocabPart* parts,
+                              uint32_t* status, const int* n_active, cudaStream_t st) {
+  const VocabPlan pl = plan_vocab(R, V);
+  CUtensorMap ta, tb;
+  const uint64_t dA[2] = {static_cast<uint64_t>(d), static_cast<uint64_t>(R)};
+  const uint64_t sA[1] = {static_cast<uint64_t>(d) * 2};
+  const uint32_t bA[2] = {static_cast<uint32_t>(kBK), static_cast<uint32_t>(kBM)};
+  const uint64_t dB[2] = {static_cast<uint64_t>(d), static_cast<uint64_t>(V)};
+  const uint32_t bB[2] = {static_cast<uint32_t>(kBK), static_cast<uint32_t>(kBN)};
+  if (!make_tmap_bf16(&ta, y, 2, dA, sA, bA)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&tb, W, 2, dB, sA, bB)) return cudaErrorInvalidValue;
+
+  VocabParams p;
+  p.R = R;
+  p.L = L;
+  p.d = d;
+  p.V = V;
+  p.num_mt = pl.num_mt;
+  p.nvt = pl.nvt;
+  p.per = pl.per;
+  p.S = pl.S;
+  p.units = pl.units;
+  p.inv_tau = inv_tau;
+  p.k0 = static_cast<uint32_t>(seed);
+  p.k1 = static_cast<uint32_t>(seed >> 32);
+  p.c3 = kStreamGumbel | (static_cast<uint32_t>(step) & 0xFFFFFFu);
+  p.parts = parts;
+  p.status = status;
+  p.n_active = n_active;
+
+  static int configured_device = -1;
+  const int dev = device_id();
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(vocab_posterior_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         VocabLayout::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  timer_begin(0, st);
+  vocab_posterior_kernel<<<pl.grid, kThreads, VocabLayout::kSmemBytes, st>>>(ta, tb, p);
+  cudaError_t e = cudaGetLastError();
+  timer_end(0, st);
+  return e;
+}
+
+}  // namespace dg

@@ -1,0 +1,259 @@
+/*
+ * libdgcanvas: the per-step canvas-denoising core of a block-diffusion text model
+ * (DiffusionGemma-style uniform-source discrete diffusion), for NVIDIA GB300 (sm_103a).
+ *
+ * Sources, cited by page title and section:
+ *   [TR]   "DiffusionGemma Technical Report 정리": "이산 디퓨전 정식화", "Forward Process",
+ *          "Backward Denoising Process", "블록 자기회귀(Block-AR) 생성",
+ *          "디노이징 반복과 self-conditioning", "DiffusionGemma 샘플러",
+ *          "1단계: Supervised Finetuning", "CPU-GPU 동기화 제거".
+ *   [BLOG] "DiffusionGemma 완전분석": "스펙 정리" (canvas 256, vocabulary 262k, window 1,024).
+ *   [PBD]  "Google DiffusionGemma 출시: 병렬 블록 디코딩": glossary "Iterative denoising",
+ *          FAQ (confident tokens are locked in, the rest re-evaluated).
+ *   [P11]  Salmon et al., "Parallel Random Numbers: As Easy as 1, 2, 3", SC'11 (Philox4x32-10).
+ *
+ * Conventions shared by every call
+ *   - Time runs from t = 1 (uniform noise) to t = 0 (clean) [TR "이산 디퓨전 정식화"]; step n
+ *     of T maps t_n = (T - n)/T to t_n - h with h = 1/T [TR "디노이징 반복과 self-conditioning"].
+ *   - Tokens are int32; activations and weights are bfloat16 passed as uint16_t bit patterns;
+ *     every matrix is row-major; arithmetic accumulates in fp32.
+ *   - Pointers are DEVICE pointers unless marked "host".  The caller owns every buffer; no
+ *     call allocates device memory.  Device pointers must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Device-side calls are
+ *     stream-ordered and asynchronous; they return after enqueueing work.
+ *   - Random draws are Philox4x32-10 [P11] keyed by the 64-bit seed (low word = key 0) with
+ *     counters that depend only on (stream, step, canvas, position, vocab index):
+ *       noising / canvas init: (position, canvas, 0, 1<<24); word 0 = keep draw, word 1 = token
+ *       Gumbel noise:          (v >> 2, position, canvas, (2<<24) | step); vocab v uses word v & 3
+ *       Euler jump:            (0, position, canvas, (3<<24) | step); word 0
+ *     so results do not depend on launch shape, and a run can be resumed at any step.
+ *   - A probability p is passed as the integer threshold floor(p * 2^32) (p = 1 -> 2^32); a
+ *     32-bit draw u "passes" iff u < threshold.  Decisions are therefore exact integer tests.
+ *   - Errors: every call validates its arguments on the host and returns DG_EINVAL /
+ *     DG_ENOTSUP before launching anything; a CUDA launch or API failure returns DG_ECUDA.
+ *     dg_last_error() returns a thread-local message for the last non-OK status.  Kernels
+ *     that wait on on-chip barriers never spin without limit: a wait that exceeds 2 s sets
+ *     a flag in the call's workspace, read by dg_workspace_status().
+ *   - Threading: calls are thread-compatible; the only global state is the thread-local error
+ *     text, a per-device cache of device properties and the optional kernel timer.
+ */
+#ifndef DGCANVAS_H
+#define DGCANVAS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DG_OK = 0,
+  DG_EINVAL = 1,   /* bad argument (null pointer, negative size, misaligned pointer, ...) */
+  DG_ENOTSUP = 2,  /* valid but unsupported shape (see each call's limits) */
+  DG_ECUDA = 3,    /* a CUDA runtime call or kernel launch failed */
+  DG_EKERNEL = 4,  /* a kernel reported an out-of-range index it skipped */
+  DG_ETIMEOUT = 5  /* a kernel gave up waiting on an on-chip barrier */
+} dg_status;
+
+typedef enum { DG_SCHED_LINEAR = 0, DG_SCHED_COSINE = 1 } dg_schedule;
+
+/* Thread-local text of the last non-OK status (never NULL). */
+const char* dg_last_error(void);
+
+/* Version of this ABI (increments on incompatible change). */
+int dg_abi_version(void);
+
+/* ------------------------------------------------------------------ schedules (host) ----
+ * kappa_t falls monotonically from kappa_0 = 1 to kappa_1 = 0 [TR "Forward Process"]; the pages
+ * fix no family, so two are offered: linear kappa = 1 - t and cosine kappa = cos^2(pi t / 2).
+ * The discrete Euler step of the factorised mixture path [TR "Backward Denoising Process"]
+ * replaces a token by a fresh posterior sample with probability
+ *     lambda_n = min(1, h * (-kappa'(t_n)) / (1 - kappa(t_n)))
+ * (linear: 1/(T - n); cosine: h*pi*cot(pi t_n / 2), so lambda_0 = 0 and lambda_{T-1} = 1).
+ *
+ * dg_schedule_thresholds: keep_thr[n] = floor(kappa(t_n) * 2^32) for n = 0..T (host array of
+ * T + 1; t_T = 0) and jump_thr[n] = floor(lambda_n * 2^32) for n = 0..T-1 (host array of T).
+ * Either output may be NULL.  Computed in double precision.  Errors: DG_EINVAL if T < 1 or
+ * the schedule is unknown.
+ */
+dg_status dg_schedule_thresholds(int schedule, int T, uint64_t* keep_thr, uint64_t* jump_thr);
+
+/* keep_thr[b] = floor(kappa(t[b]) * 2^32) for noise levels t[b] in [0, 1] (host arrays of B).
+ * Errors: DG_EINVAL on NULL arrays, B < 0, t outside [0, 1] or an unknown schedule. */
+dg_status dg_keep_thresholds(int schedule, const double* t, int B, uint64_t* keep_thr);
+
+/* ------------------------------------------------------------------- forward noising ----
+ * Closed-form forward process [TR "Forward Process"; "1단계: Supervised Finetuning"]:
+ *     x_t^i = x_0^i if the keep draw of position i passes keep_thr[canvas], else a token uniform
+ *     over [0, V) (word 1 of the same draw), independently per position,
+ * so P(x_t^i = x_0^i) = kappa_t + (1 - kappa_t)/V.  keep_thr = 0 gives the uniform prior x_1
+ * used to initialise a canvas [TR "블록 자기회귀(Block-AR) 생성"].
+ *
+ *   x0 [B, L] int32 (values are copied through, not range-checked); xt [B, L] int32 (may alias
+ *   x0); keep_thr [B] uint64 (device).  Limits: B, L >= 0, B * L < 2^31, 1 <= V < 2^31.
+ *   Errors: DG_EINVAL on NULL or misaligned pointers or bad sizes.
+ */
+dg_status dg_forward_noise(const int32_t* x0, int32_t* xt, const uint64_t* keep_thr, int B, int L,
+                           int V, uint64_t seed, void* stream);
+
+/* ------------------------------------------------- stand-in decoder: embedding + QKV ----
+ * First half of logits = Decoder(x_t, KV) [TR "디노이징 반복과 self-conditioning"] for a
+ * one-layer stand-in decoder: h = E[x_t]; [q | k_c | v_c] = h Wqkv^T (rounded to bf16).
+ *
+ *   x [B*L] int32 token ids in [0, V) (ids outside read as a zero row); E [V, d] bf16;
+ *   Wqkv [(H + 2*Hkv)*hd, d] bf16 (rows: the H query heads, then the Hkv key heads, then the Hkv
+ *   value heads, each hd rows); outputs h [B*L, d], q [B*L, H*hd], k [B*L, Hkv*hd],
+ *   v [B*L, Hkv*hd] bf16 (q, k, v are [B, L, heads, hd] in memory).
+ *   Limits: d % 64 == 0, hd in {64, 128}, H % Hkv == 0.  Errors: DG_EINVAL / DG_ENOTSUP.
+ */
+dg_status dg_embed_qkv(const int32_t* x, const uint16_t* E, const uint16_t* Wqkv, uint16_t* h,
+                       uint16_t* q, uint16_t* k, uint16_t* v, int BL, int V, int d, int H,
+                       int Hkv, int hd, void* stream);
+
+/* ------------------------------------------------------------------- canvas attention ----
+ * The decoder's attention over a cached prefix plus the whole canvas [TR "블록 자기회귀(Block-AR)
+ * 생성": bidirectional inside the canvas, cross-attention to the KV cache; BLOG "스펙 정리":
+ * sliding-window layers of 1,024 tokens]:
+ *     O[b, i, h] = softmax_k( q[b, i, h] . K[b, k, g] * scale ) V[b, k, g],   g = floor(h*Hkv/H)
+ * over keys k = the visible prefix keys followed by all L canvas keys.  Canvas query i sits at
+ * absolute position P + i; prefix key k is visible iff window == 0 or P + i - k < window.
+ *
+ *   q [B, L, H, hd]; k_pre, v_pre [B, P, Hkv, hd] (each canvas has its own prefix);
+ *   k_can, v_can [B, L, Hkv, hd]; out [B, L, H, hd] bf16; lse [B, H, L] fp32 natural-log
+ *   log-sum-exp of the scaled scores, or NULL.  ws: workspace of at least
+ *   dg_canvas_attn_workspace(...) bytes (its first 256 bytes hold the status word).
+ *   Limits: 1 <= L <= 256, L % 64 == 0, P >= 0, hd in {64, 128}, H % Hkv == 0, window >= 0.
+ *   Errors: DG_EINVAL / DG_ENOTSUP; DG_EINVAL if ws_bytes is too small.
+ */
+size_t dg_canvas_attn_workspace(int B, int L, int P, int H, int Hkv, int hd, int window);
+dg_status dg_canvas_attn(const uint16_t* q, const uint16_t* k_pre, const uint16_t* v_pre,
+                         const uint16_t* k_can, const uint16_t* v_can, uint16_t* out, float* lse,
+                         int B, int L, int P, int H, int Hkv, int hd, int window, float scale,
+                         void* ws, size_t ws_bytes, void* stream);
+
+/* --------------------------------------------------- output projection with residual ----
+ * y = h + O Wo^T, rounded to bf16 (the stand-in decoder's attention output projection).
+ *   h [BL, d]; O [BL, H*hd]; Wo [d, H*hd]; y [BL, d] bf16 (y must not alias h).
+ *   Limits: d % 64 == 0, (H*hd) % 64 == 0.
+ */
+dg_status dg_out_proj(const uint16_t* h, const uint16_t* O, const uint16_t* Wo, uint16_t* y, int BL,
+                      int d, int Hhd, void* stream);
+
+/* ---------------------------------------- fused LM head, posterior and Euler update ----
+ * p_hat_0 = Softmax(logits / tau) with logits = y W^T (LM head tied to the embedding), then
+ * x_(t-h) ~ Step(x_t, p_hat_0) [TR "디노이징 반복과 self-conditioning", "Backward Denoising
+ * Process"], with the reverse step factorised per position.  Per row r (canvas r / L,
+ * position r % L), with z~ = z * inv_tau:
+ *     lse        = log sum_v exp(z~_v)
+ *     top1       = argmax_v z~_v (lowest index on ties);   logp_top1 = z~_top1 - lse
+ *     x0hat      = argmax_v (z~_v + g_v)  (Gumbel-max sample; g from the Gumbel stream at `step`;
+ *                  lowest index on ties);                  logp_x0hat = z~_x0hat - lse
+ * and, when x_in != NULL, the Euler step of dg_euler_update at `step`.  No [rows, V] logit
+ * tensor is written to memory.
+ *
+ *   y [B*L, d] bf16; W [V, d] bf16; x_in [B*L] int32 or NULL (posterior only); x_out [B*L] (may
+ *   alias x_in); lock [B*L] uint8 in/out (NULL = nothing locked, no lock state kept);
+ *   jump [B*L] uint8 out or NULL; done [B] uint8 out (1 = every position locked) or NULL;
+ *   out: optional per-row outputs (each field may be NULL).  jump_thr = floor(lambda * 2^32);
+ *   lock_logthr = log(theta) as float, +INFINITY disables locking.  ws: at least
+ *   dg_vocab_posterior_workspace(B, L, V) bytes.
+ *   Limits: d % 64 == 0, V % 256 == 0, L % 64 == 0, 1 <= L <= 256.
+ */
+typedef struct {
+  int32_t* x0hat;
+  int32_t* top1;
+  float* logp_top1;
+  float* lse;
+  float* logp_x0hat;
+} dg_posterior_out;
+
+size_t dg_vocab_posterior_workspace(int B, int L, int V);
+dg_status dg_vocab_posterior_step(const uint16_t* y, const uint16_t* W, int B, int L, int d, int V,
+                                  float inv_tau, uint64_t seed, int step, const int32_t* x_in,
+                                  int32_t* x_out, uint8_t* lock, uint8_t* jump, uint8_t* done,
+                                  uint64_t jump_thr, float lock_logthr,
+                                  const dg_posterior_out* out, void* ws, size_t ws_bytes,
+                                  void* stream);
+
+/* ----------------------------------------------------- Euler jump + lock + commit ----
+ * The reverse Step [TR "Backward Denoising Process"] with optional confidence locking
+ * [PBD glossary "Iterative denoising"]: per position of every canvas,
+ *     already locked                          -> unchanged
+ *     logp_top1 >= lock_logthr (float32)      -> lock; x <- top1
+ *     jump draw < jump_thr                    -> x <- x0hat, jump = 1
+ *     otherwise                               -> unchanged
+ * and done[b] = 1 iff every position of canvas b is locked afterwards.
+ *
+ *   x_in, x0hat, top1 [B, L] int32; logp_top1 [B, L] fp32; x_out [B, L] (may alias x_in);
+ *   lock [B, L] uint8 in/out (0/1); jump [B, L] uint8 out or NULL; done [B] uint8 out or NULL.
+ *   Limits: 1 <= L <= 1024.
+ */
+dg_status dg_euler_update(const int32_t* x_in, const int32_t* x0hat, const int32_t* top1,
+                          const float* logp_top1, int32_t* x_out, uint8_t* lock, uint8_t* jump,
+                          uint8_t* done, int B, int L, uint64_t seed, int step, uint64_t jump_thr,
+                          float lock_logthr, void* stream);
+
+/* -------------------------------------------------------------------- denoising loop ----
+ * Steps n = start_step .. end_step-1 of at most T [TR "디노이징 반복과 self-conditioning";
+ * "DiffusionGemma 샘플러": cap T] of
+ *     h = E[x]; q,k,v = h Wqkv^T; O = attention(q, prefix KV, canvas KV); y = h + O Wo^T;
+ *     posterior + Euler step with jump threshold floor(lambda_n * 2^32),
+ * entirely on the device with no host synchronisation between steps [TR "CPU-GPU 동기화
+ * 제거"].  When stop_when_all_locked is set, a canvas whose positions are all locked stops
+ * (its later steps are skipped), and once every canvas has stopped the remaining kernels
+ * return at once.
+ *
+ *   m: device pointers to the weights (E [V, d] also serves as the LM head) and the sizes;
+ *   k_pre, v_pre [B, P, Hkv, hd]; canvas [B, L] int32 in: x_1 (or the state at start_step),
+ *   out: final state; lock [B, L] uint8 in/out; steps_taken [B] int32 out (steps applied by
+ *   this call).  ws: at least dg_denoise_loop_workspace(m, B, L, P, window) bytes.
+ *   Limits: those of the calls above.  end_step <= 0 means T.
+ */
+typedef struct {
+  const uint16_t* E;
+  const uint16_t* Wqkv;
+  const uint16_t* Wo;
+  int V, d, H, Hkv, hd;
+} dg_model;
+
+typedef struct {
+  int T;                    /* number of steps of the schedule (h = 1/T) */
+  int schedule;             /* dg_schedule */
+  float inv_tau;            /* 1 / temperature */
+  float lock_logthr;        /* log(theta) as float; +INFINITY disables locking */
+  uint64_t seed;
+  int start_step;           /* first step to run (resume) */
+  int end_step;             /* one past the last step to run; <= 0 means T */
+  int stop_when_all_locked; /* nonzero: a fully locked canvas stops */
+} dg_sampler_cfg;
+
+size_t dg_denoise_loop_workspace(const dg_model* m, int B, int L, int P, int window);
+
+/* Number of kernels one dg_denoise_loop call launches for `steps` steps on this device (its
+ * launch plan depends on the SM count); -1 on invalid arguments.  Host only. */
+int dg_denoise_loop_kernel_count(const dg_model* m, int B, int L, int P, int window, int steps);
+dg_status dg_denoise_loop(const dg_model* m, const uint16_t* k_pre, const uint16_t* v_pre, int B,
+                          int L, int P, int window, int32_t* canvas, uint8_t* lock,
+                          int32_t* steps_taken, const dg_sampler_cfg* cfg, void* ws,
+                          size_t ws_bytes, void* stream);
+
+/* ----------------------------------------------------------------- status and timing ----
+ * dg_workspace_status: synchronises `stream`, reads and clears the status word at the start
+ * of a workspace used by dg_canvas_attn, dg_vocab_posterior_step or dg_denoise_loop, and
+ * returns DG_OK, DG_ETIMEOUT or DG_EKERNEL accordingly (DG_ECUDA if the stream failed).
+ *
+ * dg_kernel_timer_enable(1) makes the library record CUDA events on the launching stream
+ * around every launch of its LM-head/posterior kernel (kind 0) and attention kernels (kind 1);
+ * dg_kernel_timer_read synchronises those events and returns the summed milliseconds and the
+ * number of launches since the last reset; dg_kernel_timer_enable(0) stops and resets.
+ */
+dg_status dg_workspace_status(const void* ws, void* stream);
+dg_status dg_kernel_timer_enable(int enable);
+dg_status dg_kernel_timer_read(int kind, double* total_ms, int* launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DGCANVAS_H */

@@ -1,0 +1,409 @@
+"""GPU parity: every call of libdgcanvas, through its C ABI, against the CPU oracle on the same
+seeded inputs.
+
+Bars: integer work (noising, Euler jump/lock/commit) is bit-exact; attention outputs within
+1e-2 max-abs; log-probabilities (lse, logp_top1, logp_x0hat) within 2e-3; sampled tokens may
+differ only where the oracle's two best perturbed scores are within 1e-3 of each other, and
+such differences must stay under 0.1% of positions; top-1 tokens may differ only where the two
+largest logits are within 1e-4; a lock decision may differ only where logp_top1 is within 2e-3
+of log(theta).
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from discrete_diffusion_text_gb300 import synth
+from oracle import dgoracle as O
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+ATTN_TOL = 1e-2
+LOGP_TOL = 2e-3
+GUMBEL_TIE = 1e-3
+LOGIT_TIE = 1e-4
+
+
+@pytest.fixture(scope="module")
+def dgc():
+    from discrete_diffusion_text_gb300 import dgcanvas
+
+    import os
+
+    if not os.path.exists(dgcanvas.LIB_PATH):
+        import __graft_entry__
+
+        __graft_entry__.build()
+    dgcanvas.load()
+    return dgcanvas
+
+
+def bf16(shape, std, seed):
+    return synth.normal_bf16(shape, std, seed)
+
+
+def f64(t):
+    return t.double().cpu().numpy()
+
+
+# ------------------------------------------------------------------- forward noising -----
+
+@pytest.mark.parametrize("B,L,V", [(64, 256, 262144), (3, 100, 1000), (1, 256, 4096), (5, 3, 7),
+                                   (0, 256, 4096)])
+def test_forward_noise_bit_exact(dgc, B, L, V):
+    x0 = synth.zipf_tokens(B, L, V, 1.1, seed=11)
+    t = synth.uniform_times(B, seed=11)
+    thr_lib = dgc.dg_keep_thresholds(dgc.DG_SCHED_LINEAR, t)
+    thr_orc = O.keep_threshold_from_t(O.SCHED_LINEAR, t)
+    assert np.array_equal(thr_lib, thr_orc)
+    seed = 0x1234_5678_9ABC
+    xt = torch.empty((B, L), dtype=torch.int32, device=DEV)
+    dgc.dg_forward_noise(torch.tensor(x0, device=DEV), xt,
+                         torch.tensor(thr_lib.astype(np.int64), device=DEV), V, seed)
+    ref = O.forward_noise(x0, thr_orc, V, seed)
+    assert np.array_equal(xt.cpu().numpy(), ref)
+
+
+def test_forward_noise_extremes_and_in_place(dgc):
+    B, L, V = 4, 256, 4096
+    x0 = synth.random_tokens((B, L), V, 3)
+    x = torch.tensor(x0, device=DEV)
+    full = torch.full((B,), 1 << 32, dtype=torch.int64, device=DEV)
+    dgc.dg_forward_noise(x, x, full, V, 9)             # in place, kappa = 1: identity
+    assert np.array_equal(x.cpu().numpy(), x0)
+    zero = torch.zeros(B, dtype=torch.int64, device=DEV)
+    dgc.dg_forward_noise(x, x, zero, V, 9)             # kappa = 0: the uniform prior x_1
+    assert np.array_equal(x.cpu().numpy(), O.initial_canvas(B, L, V, 9))
+
+
+# ------------------------------------------------------------------------- Euler -----
+
+@pytest.mark.parametrize("B,L", [(16, 256), (3, 100), (1, 1024)])
+@pytest.mark.parametrize("lock_on", [False, True])
+def test_euler_update_bit_exact(dgc, B, L, lock_on):
+    rng = np.random.default_rng(B * 1000 + L)
+    V = 262144
+    x_in = rng.integers(0, V, (B, L)).astype(np.int32)
+    x0hat = rng.integers(0, V, (B, L)).astype(np.int32)
+    top1 = rng.integers(0, V, (B, L)).astype(np.int32)
+    lp = np.where(rng.random((B, L)) < 0.3, -0.01, -3.0).astype(np.float32)
+    lock = (rng.random((B, L)) < 0.2).astype(np.uint8)
+    lock[0, :] = 1  # one canvas fully locked already
+    thr = float(np.float32(math.log(0.9))) if lock_on else math.inf
+    _, jumps = O.schedule_thresholds(O.SCHED_COSINE, 12)
+    for n in (0, 5, 11):
+        T = lambda a: torch.tensor(a, device=DEV)  # noqa: E731
+        xo = torch.empty((B, L), dtype=torch.int32, device=DEV)
+        lk = T(lock.copy())
+        jp = torch.empty((B, L), dtype=torch.uint8, device=DEV)
+        dn = torch.empty(B, dtype=torch.uint8, device=DEV)
+        dgc.dg_euler_update(T(x_in), T(x0hat), T(top1), T(lp), xo, lk, jp, dn, 77, n,
+                            int(jumps[n]), thr)
+        rx, rl, rj, rd = O.euler_update(x_in, x0hat, top1, lp, lock, 77, n, int(jumps[n]), thr)
+        assert np.array_equal(xo.cpu().numpy(), rx)
+        assert np.array_equal(lk.cpu().numpy(), rl)
+        assert np.array_equal(jp.cpu().numpy(), rj)
+        assert np.array_equal(dn.cpu().numpy(), rd)
+
+
+# --------------------------------------------------------- embedding + projections -----
+
+@pytest.mark.parametrize("wname", ["tiny", "window1k"])
+def test_embed_qkv_and_out_proj(dgc, wname):
+    w = synth.WORKLOADS[wname]
+    m = synth.make_model(w)
+    BL = w.B * w.L
+    x = O.initial_canvas(w.B, w.L, w.V, 5).astype(np.int32)
+    E, Wqkv, Wo = (m[k].to(DEV) for k in ("E", "Wqkv", "Wo"))
+    h = torch.empty((BL, w.d), dtype=torch.bfloat16, device=DEV)
+    q = torch.empty((BL, w.H * w.hd), dtype=torch.bfloat16, device=DEV)
+    k = torch.empty((BL, w.Hkv * w.hd), dtype=torch.bfloat16, device=DEV)
+    v = torch.empty_like(k)
+    dgc.dg_embed_qkv(torch.tensor(x.reshape(-1), device=DEV), E, Wqkv, h, q, k, v, w.H, w.Hkv, w.hd)
+    rh, rq, rk, rv = O.decoder_front(x, f64(m["E"]), f64(m["Wqkv"]), w.H, w.Hkv, w.hd)
+    assert np.array_equal(f64(h), rh.reshape(BL, -1))
+    for got, ref in ((q, rq), (k, rk), (v, rv)):
+        assert np.allclose(f64(got), ref.reshape(BL, -1), rtol=2**-7, atol=1e-6)
+    O_in = bf16((BL, w.H * w.hd), 1.0, 99).to(DEV)
+    y = torch.empty((BL, w.d), dtype=torch.bfloat16, device=DEV)
+    dgc.dg_out_proj(h, O_in, Wo, y)
+    ry = O.decoder_back(rh, f64(O_in).reshape(w.B, w.L, w.H, w.hd), f64(m["Wo"]))
+    assert np.allclose(f64(y), ry.reshape(BL, -1), rtol=2**-7, atol=1e-5)
+
+
+# -------------------------------------------------------------------- attention -----
+
+ATTN_CASES = [
+    # B, L, P, H, Hkv, hd, window, q_scale
+    (1, 256, 256, 4, 4, 64, 0, 1.0),        # tiny workload's layer
+    (1, 256, 1024, 16, 8, 128, 1024, 1.0),  # window1k workload's layer
+    (2, 192, 37, 4, 2, 128, 0, 1.0),        # ragged prefix and query tiles
+    (2, 64, 300, 2, 1, 64, 100, 1.0),       # window narrower than the prefix
+    (1, 128, 0, 2, 2, 128, 0, 1.0),         # no prefix
+    (8, 256, 128, 16, 8, 128, 0, 1.0),      # enough CTAs for a single key split
+    (2, 256, 8192, 16, 8, 128, 0, 1.0),     # batch16 workload's prefix length
+    (1, 256, 2048, 4, 2, 128, 0, 4.0),      # sharp scores: exercises the max rescaling
+]
+
+
+def _attn_inputs(B, L, P, H, Hkv, hd, q_scale, seed):
+    q = (bf16((B, L, H, hd), 1.0, seed).float() * q_scale).to(torch.bfloat16)
+    kp, vp = bf16((B, P, Hkv, hd), 1.0, seed + 1), bf16((B, P, Hkv, hd), 1.0, seed + 2)
+    kc, vc = bf16((B, L, Hkv, hd), 1.0, seed + 3), bf16((B, L, Hkv, hd), 1.0, seed + 4)
+    return q, kp, vp, kc, vc
+
+
+def _run_attn(dgc, q, kp, vp, kc, vc, window):
+    B, L, H, hd = q.shape
+    P, Hkv = kp.shape[1], kp.shape[2]
+    out = torch.empty_like(q, device=DEV)
+    lse = torch.empty((B, H, L), dtype=torch.float32, device=DEV)
+    ws = dgc.workspace(dgc.dg_canvas_attn_workspace(B, L, P, H, Hkv, hd, window))
+    dgc.dg_canvas_attn(q.to(DEV), kp.to(DEV), vp.to(DEV), kc.to(DEV), vc.to(DEV), out, lse, window,
+                       None, ws)
+    dgc.dg_workspace_status(ws)
+    return out, lse
+
+
+@pytest.mark.parametrize("case", ATTN_CASES, ids=lambda c: "B{}L{}P{}H{}kv{}hd{}w{}s{}".format(*c))
+def test_attention_matches_oracle(dgc, case):
+    B, L, P, H, Hkv, hd, window, qs = case
+    q, kp, vp, kc, vc = _attn_inputs(B, L, P, H, Hkv, hd, qs, 7)
+    out, lse = _run_attn(dgc, q, kp, vp, kc, vc, window)
+    ro, rl = O.canvas_attention(f64(q), f64(kp), f64(vp), f64(kc), f64(vc), window, hd ** -0.5)
+    err = np.abs(f64(out) - ro).max()
+    assert err <= ATTN_TOL, err
+    assert np.abs(lse.cpu().numpy() - rl).max() <= 1e-3
+
+
+def test_attention_long_prefix_sampled_rows(dgc):
+    """long128k workload (prefix 131,072, global): full GPU run, oracle on sampled rows."""
+    w = synth.LONG128K
+    B, L, P, H, Hkv, hd = 1, w.L, w.P, w.H, w.Hkv, w.hd
+    q = bf16((B, L, H, hd), 1.0, 31)
+    kp, vp = synth.make_prefix_kv(w, DEV)
+    kc, vc = bf16((B, L, Hkv, hd), 1.0, 33), bf16((B, L, Hkv, hd), 1.0, 34)
+    out, lse = _run_attn(dgc, q, kp, vp, kc, vc, 0)
+    rng = np.random.default_rng(0)
+    for _ in range(6):
+        h = int(rng.integers(0, H))
+        i = int(rng.integers(0, L))
+        g = h * Hkv // H
+        K = np.concatenate([f64(kp[0, :, g]), f64(kc[0, :, g])])
+        Vv = np.concatenate([f64(vp[0, :, g]), f64(vc[0, :, g])])
+        s = K @ f64(q[0, i, h]) * hd ** -0.5
+        mx = s.max()
+        p = np.exp(s - mx)
+        ref = (p @ Vv) / p.sum()
+        assert np.abs(f64(out[0, i, h]) - ref).max() <= ATTN_TOL
+        assert abs(float(lse[0, h, i]) - (mx + math.log(p.sum()))) <= 1e-3
+
+
+# ------------------------------------------------------- fused LM head + posterior -----
+
+def _posterior_check(got, ref, rows=None):
+    """Returns the number of near-tie sampled-token differences; asserts every bar."""
+    sel = slice(None) if rows is None else rows
+    for k in ("lse", "logp_top1", "logp_x0hat"):
+        g = got[k][sel]
+        err = np.abs(g - ref[k])
+        if k == "logp_x0hat":  # compare only where both sides sampled the same token
+            err = err[got["x0hat"][sel] == ref["x0hat"]]
+        assert err.max(initial=0.0) <= LOGP_TOL, (k, err.max())
+    d_top = got["top1"][sel] != ref["top1"]
+    assert not np.any(d_top & (ref["gap_logit"] >= LOGIT_TIE))
+    d_x = got["x0hat"][sel] != ref["x0hat"]
+    assert not np.any(d_x & (ref["gap_perturbed"] >= GUMBEL_TIE)), "sampled token off a near-tie"
+    assert d_x.sum() <= max(1, int(0.001 * d_x.size)), d_x.sum()
+    return int(d_x.sum())
+
+
+def _vocab_run(dgc, y, E, B, L, inv_tau, seed, step):
+    R = B * L
+    out = {k: torch.empty(R, dtype=torch.int32 if k in ("x0hat", "top1") else torch.float32,
+                          device=DEV) for k in ("x0hat", "top1", "logp_top1", "lse", "logp_x0hat")}
+    ws = dgc.workspace(dgc.dg_vocab_posterior_workspace(B, L, E.shape[0]))
+    dgc.dg_vocab_posterior_step(y.to(DEV), E, B, L, inv_tau, seed, step, out=out, ws=ws)
+    dgc.dg_workspace_status(ws)
+    return {k: v.cpu().numpy() for k, v in out.items()}
+
+
+@pytest.mark.parametrize("B,L,V,d,ystd,inv_tau", [
+    (1, 256, 4096, 256, 0.05, 1.0),     # tiny workload: near-uniform posterior
+    (16, 256, 4096, 256, 0.05, 1.0),    # many canvases: counters of canvas and position
+    (3, 192, 4096, 256, 1.0, 50.0),     # ragged row tile; sharp, peaked posteriors
+    (1, 64, 8192, 512, 0.5, 5.0),
+])
+def test_vocab_posterior_matches_oracle(dgc, B, L, V, d, ystd, inv_tau):
+    E = bf16((V, d), 0.02 if ystd < 0.5 else 0.1, 41).to(DEV)
+    y = bf16((B * L, d), ystd, 42)
+    got = _vocab_run(dgc, y, E, B, L, inv_tau, 1234, 7)
+    ref = O.posterior(f64(y), f64(E), inv_tau, 1234, 7, L)
+    _posterior_check(got, ref)
+
+
+def test_vocab_posterior_window1k_sampled_rows(dgc):
+    """Full vocabulary (262,144) and d_model 2,048: GPU over every row, oracle on 24 rows."""
+    w = synth.WINDOW1K
+    E = synth.make_model(w, DEV)["E"]
+    y = bf16((w.L, w.d), 0.05, 43)
+    got = _vocab_run(dgc, y, E, 1, w.L, 1.0, w.seed, 3)
+    rows = np.sort(np.random.default_rng(1).choice(w.L, 24, replace=False))
+    ref = O.posterior(f64(y), f64(E), 1.0, w.seed, 3, w.L, rows=rows)
+    _posterior_check(got, ref, rows)
+
+
+@pytest.mark.parametrize("lock_on", [False, True])
+def test_fused_euler_step_matches_oracle(dgc, lock_on):
+    B, L, V, d = 4, 256, 4096, 256
+    E = bf16((V, d), 0.1, 51).to(DEV)
+    y = bf16((B * L, d), 1.0, 52)
+    inv_tau = 20.0
+    rng = np.random.default_rng(3)
+    x_in = rng.integers(0, V, (B, L)).astype(np.int32)
+    lock = (rng.random((B, L)) < 0.1).astype(np.uint8)
+    thr = float(np.float32(math.log(0.9))) if lock_on else math.inf
+    _, jumps = O.schedule_thresholds(O.SCHED_LINEAR, 12)
+    n = 6
+    x = torch.tensor(x_in.reshape(-1), device=DEV)
+    lk = torch.tensor(lock.reshape(-1), device=DEV)
+    jp = torch.empty(B * L, dtype=torch.uint8, device=DEV)
+    dn = torch.empty(B, dtype=torch.uint8, device=DEV)
+    out = {"x0hat": torch.empty(B * L, dtype=torch.int32, device=DEV),
+           "top1": torch.empty(B * L, dtype=torch.int32, device=DEV),
+           "logp_top1": torch.empty(B * L, dtype=torch.float32, device=DEV)}
+    ws = dgc.workspace(dgc.dg_vocab_posterior_workspace(B, L, V))
+    dgc.dg_vocab_posterior_step(y.to(DEV), E, B, L, inv_tau, 99, n, x_in=x, x_out=x, lock=lk,
+                                jump=jp, done=dn, jump_thr=int(jumps[n]), lock_logthr=thr,
+                                out=out, ws=ws)
+    dgc.dg_workspace_status(ws)
+    post = O.posterior(f64(y), f64(E), inv_tau, 99, n, L)
+    rx, rl, rj, _ = O.euler_update(x_in, post["x0hat"].reshape(B, L), post["top1"].reshape(B, L),
+                                   post["logp_top1"].reshape(B, L).astype(np.float32), lock, 99,
+                                   n, int(jumps[n]), thr)
+    gx0 = out["x0hat"].cpu().numpy()
+    gt1 = out["top1"].cpu().numpy()
+    same_inputs = (gx0 == post["x0hat"]) & (gt1 == post["top1"])
+    if lock_on:
+        same_inputs &= np.abs(post["logp_top1"] - thr) >= LOGP_TOL
+    assert same_inputs.mean() > 0.99
+    for g, r in ((x, rx), (lk, rl), (jp, rj)):
+        gg = g.cpu().numpy()
+        assert np.array_equal(gg[same_inputs], r.reshape(-1)[same_inputs])
+    if lock_on:
+        assert rl.mean() > 0.05  # the planted sharp posteriors do lock some positions
+
+
+# ---------------------------------------------------------------- denoising loop -----
+
+def _oracle_model(m):
+    return {"E": f64(m["E"]), "Wqkv": f64(m["Wqkv"]), "Wo": f64(m["Wo"]), "H": m["H"],
+            "Hkv": m["Hkv"], "hd": m["hd"]}
+
+
+def _gpu_loop(dgc, w, m, kp, vp, canvas, lock, cfg):
+    md = dgc.make_model(m["E"].to(DEV), m["Wqkv"].to(DEV), m["Wo"].to(DEV), w.H, w.Hkv, w.hd)
+    c = torch.tensor(canvas, dtype=torch.int32, device=DEV)
+    lk = torch.tensor(lock, dtype=torch.uint8, device=DEV)
+    st = torch.zeros(w.B, dtype=torch.int32, device=DEV)
+    ws = dgc.workspace(dgc.dg_denoise_loop_workspace(md, w.B, w.L, w.P, w.window))
+    dgc.dg_denoise_loop(md, kp.to(DEV), vp.to(DEV), w.window, c, lk, st, cfg, ws)
+    dgc.dg_workspace_status(ws)
+    return c.cpu().numpy(), lk.cpu().numpy(), st.cpu().numpy()
+
+
+def test_loop_tiny_stepwise_and_full(dgc):
+    """tiny workload: each of the 12 steps from the oracle's own state, then the whole loop."""
+    w = synth.TINY
+    m = synth.make_model(w)
+    kp, vp = synth.make_prefix_kv(w)
+    om = _oracle_model(m)
+    okp, ovp = f64(kp), f64(vp)
+    x = O.initial_canvas(w.B, w.L, w.V, w.seed)
+    lock = np.zeros((w.B, w.L), np.uint8)
+    _, jumps = O.schedule_thresholds(w.schedule, w.T)
+    ties = 0
+    for n in range(w.T):
+        cfg = dgc.make_cfg(w.T, w.schedule, 1.0, math.inf, w.seed, start_step=n, end_step=n + 1)
+        gx, _, st = _gpu_loop(dgc, w, m, kp, vp, x, lock, cfg)
+        rx, _, _, _, post = O.denoise_step(om, okp, ovp, w.window, x, lock, n, int(jumps[n]), 1.0,
+                                           math.inf, w.seed)
+        diff = (gx != rx).reshape(-1)
+        near = post["gap_perturbed"] < GUMBEL_TIE
+        assert not np.any(diff & ~near), f"step {n}: {int(diff.sum())} differences off near-ties"
+        ties += int(diff.sum())
+        assert st[0] == 1
+        x = rx
+    assert ties <= max(1, int(0.001 * w.T * w.L))
+    x1 = O.initial_canvas(w.B, w.L, w.V, w.seed)
+    gx, _, st = _gpu_loop(dgc, w, m, kp, vp, x1, lock, dgc.make_cfg(w.T, w.schedule, 1.0,
+                                                                    math.inf, w.seed))
+    assert st[0] == w.T
+    assert (gx == x).mean() >= 0.999
+
+
+def test_loop_resume_is_bit_identical(dgc):
+    w = synth.TINY
+    m = synth.make_model(w)
+    kp, vp = synth.make_prefix_kv(w)
+    x1 = O.initial_canvas(w.B, w.L, w.V, 3)
+    lock = np.zeros((w.B, w.L), np.uint8)
+    a, la, sa = _gpu_loop(dgc, w, m, kp, vp, x1, lock, dgc.make_cfg(w.T, 1, 1.0, math.inf, 3))
+    h, lh, sh = _gpu_loop(dgc, w, m, kp, vp, x1, lock, dgc.make_cfg(w.T, 1, 1.0, math.inf, 3,
+                                                                    end_step=6))
+    b, lb, sb = _gpu_loop(dgc, w, m, kp, vp, h, lh, dgc.make_cfg(w.T, 1, 1.0, math.inf, 3,
+                                                                 start_step=6))
+    assert np.array_equal(a, b) and np.array_equal(la, lb)
+    assert sa[0] == 12 and sh[0] == 6 and sb[0] == 6
+
+
+def test_loop_planted_delta_posterior_and_stop_when_locked(dgc):
+    """A decoder whose posterior is a delta at the input token leaves the canvas unchanged;
+    with locking at 0.9 every position locks at the first step and the canvas stops."""
+    import dataclasses
+
+    w = dataclasses.replace(synth.TINY, B=2, L=64, P=64, d=256, H=2, Hkv=1, hd=64, V=256, T=6)
+    E = (torch.eye(256) * 8.0).to(torch.bfloat16)
+    m = {"E": E, "Wqkv": bf16(((w.H + 2 * w.Hkv) * w.hd, w.d), 0.02, 61),
+         "Wo": torch.zeros((w.d, w.H * w.hd), dtype=torch.bfloat16), "H": w.H, "Hkv": w.Hkv,
+         "hd": w.hd}
+    kp, vp = bf16((w.B, w.P, w.Hkv, w.hd), 1.0, 62), bf16((w.B, w.P, w.Hkv, w.hd), 1.0, 63)
+    x1 = O.initial_canvas(w.B, w.L, w.V, 8)
+    lock = np.zeros((w.B, w.L), np.uint8)
+    gx, gl, st = _gpu_loop(dgc, w, m, kp, vp, x1, lock, dgc.make_cfg(w.T, 0, 1.0, math.inf, 8))
+    assert np.array_equal(gx, x1) and not gl.any() and np.all(st == w.T)
+    thr = float(np.float32(math.log(0.9)))
+    gx, gl, st = _gpu_loop(dgc, w, m, kp, vp, x1, lock,
+                           dgc.make_cfg(w.T, 0, 1.0, thr, 8, stop_when_all_locked=True))
+    assert np.array_equal(gx, x1) and gl.all() and np.all(st == 1)
+
+
+def test_loop_window1k_last_step_sampled_rows(dgc):
+    """window1k workload at full size, in the launch configuration the benchmark times: one
+    loop step (the last, lambda = 1) from the uniform canvas; the oracle recomputes the decoder
+    for the whole canvas and the posterior for 16 sampled positions."""
+    w = synth.WINDOW1K
+    m = synth.make_model(w, DEV)
+    kp, vp = synth.make_prefix_kv(w, DEV)
+    x1 = O.initial_canvas(w.B, w.L, w.V, w.seed)
+    lock = np.zeros((w.B, w.L), np.uint8)
+    n = w.T - 1
+    gx, _, st = _gpu_loop(dgc, w, m, kp, vp, x1, lock,
+                          dgc.make_cfg(w.T, w.schedule, 1.0, math.inf, w.seed, start_step=n,
+                                       end_step=n + 1))
+    assert st[0] == 1
+    om = _oracle_model(m)
+    h, q, k, v = O.decoder_front(x1, om["E"], om["Wqkv"], w.H, w.Hkv, w.hd)
+    Oa, _ = O.canvas_attention(q, f64(kp), f64(vp), k, v, w.window, w.hd ** -0.5)
+    y = O.decoder_back(h, Oa, om["Wo"]).reshape(w.L, w.d)
+    rows = np.sort(np.random.default_rng(2).choice(w.L, 16, replace=False))
+    post = O.posterior(y, om["E"], 1.0, w.seed, n, w.L, rows=rows)
+    diff = gx.reshape(-1)[rows] != post["x0hat"]  # lambda = 1: every position takes its sample
+    assert not np.any(diff & (post["gap_perturbed"] >= GUMBEL_TIE))
+
+
+def test_status_words_are_clean(dgc):
+    dgc.dg_workspace_status(None)
