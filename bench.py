@@ -120,31 +120,38 @@ def traffic_from_profile(kernel_file: str):
 
 # ------------------------------------------------------------------------ oracle arm -----
 
-def oracle_step_sample(w, rows: int, seed_shift: int = 0):
+class OracleSample:
     """One denoising step of the workload by the CPU oracle: the decoder over the whole canvas
-    of one batch element, the posterior and Euler step for `rows` positions.  Returns seconds."""
-    import numpy as np
+    of one batch element, then the posterior and Euler step for `rows` positions.  The seeded
+    inputs are made once; each call returns the seconds of one step."""
 
-    from discrete_diffusion_text_gb300 import synth
-    from oracle import dgoracle as O
+    def __init__(self, w):
+        from discrete_diffusion_text_gb300 import synth
 
-    m = synth.make_model(w)
-    kp, vp = synth.make_prefix_kv(w, B=1)
-    om = {k: (v.double().numpy() if hasattr(v, "double") else v) for k, v in m.items()}
-    kp, vp = kp.double().numpy(), vp.double().numpy()
-    x = O.initial_canvas(1, w.L, w.V, w.seed + seed_shift)
-    _, jump = O.schedule_thresholds(w.schedule, w.T)
-    n = w.T - 1
-    t0 = time.perf_counter()
-    h, q, k, v = O.decoder_front(x, om["E"], om["Wqkv"], w.H, w.Hkv, w.hd)
-    Oa, _ = O.canvas_attention(q, kp, vp, k, v, w.window, w.hd ** -0.5)
-    y = O.decoder_back(h, Oa, om["Wo"]).reshape(w.L, w.d)
-    sel = np.arange(rows)
-    post = O.posterior(y, om["E"], w.inv_tau, w.seed, n, w.L, rows=sel)
-    O.euler_update(x[:, :rows], post["x0hat"][None], post["top1"][None],
-                   post["logp_top1"][None].astype(np.float32), np.zeros((1, rows), np.uint8),
-                   w.seed, n, int(jump[n]), math.inf)
-    return time.perf_counter() - t0
+        self.w = w
+        m = synth.make_model(w)
+        kp, vp = synth.make_prefix_kv(w, B=1)
+        self.om = {k: (v.double().numpy() if hasattr(v, "double") else v) for k, v in m.items()}
+        self.kp, self.vp = kp.double().numpy(), vp.double().numpy()
+
+    def __call__(self, rows: int, seed_shift: int = 0) -> float:
+        import numpy as np
+
+        from oracle import dgoracle as O
+
+        w, om = self.w, self.om
+        x = O.initial_canvas(1, w.L, w.V, w.seed + seed_shift)
+        _, jump = O.schedule_thresholds(w.schedule, w.T)
+        n = w.T - 1
+        t0 = time.perf_counter()
+        h, q, k, v = O.decoder_front(x, om["E"], om["Wqkv"], w.H, w.Hkv, w.hd)
+        Oa, _ = O.canvas_attention(q, self.kp, self.vp, k, v, w.window, w.hd ** -0.5)
+        y = O.decoder_back(h, Oa, om["Wo"]).reshape(w.L, w.d)
+        post = O.posterior(y, om["E"], w.inv_tau, w.seed, n, w.L, rows=np.arange(rows))
+        O.euler_update(x[:, :rows], post["x0hat"][None], post["top1"][None],
+                       post["logp_top1"][None].astype(np.float32), np.zeros((1, rows), np.uint8),
+                       w.seed, n, int(jump[n]), math.inf)
+        return time.perf_counter() - t0
 
 
 def cpu_cores() -> int:
@@ -159,9 +166,10 @@ def run_reference(args, w):
     if rank != 0:
         return
     rows = 32
+    sample_step = OracleSample(w)
     for i in range(args.warmup):
-        oracle_step_sample(w, rows, i)
-    ts = [oracle_step_sample(w, rows, 100 + i) for i in range(args.steps)]
+        sample_step(rows, i)
+    ts = [sample_step(rows, 100 + i) for i in range(args.steps)]
     sec = sum(ts) / len(ts)
     value = rows / sec
     sample = (f"one denoising step of the {w.name} workload per benchmark step: decoder over the "
@@ -187,7 +195,7 @@ def run_ours(args, w):
     import torch
 
     from discrete_diffusion_text_gb300 import dgcanvas as dgc
-    from discrete_diffusion_text_gb300 import synth
+    from discrete_diffusion_text_gb300 import replicas, synth
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -216,7 +224,7 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream(dev)
 
     def step(i):
-        seed = (w.seed << 32) + 1000003 * rank + i
+        seed = replicas.replica_seed(w.seed, rank, i)
         dgc.dg_forward_noise(canvas, canvas, keep0, w.V, seed)        # x_1: uniform prior
         lock.zero_()
         cfg = dgc.make_cfg(w.T, w.schedule, w.inv_tau, lock_thr, seed,
@@ -251,13 +259,12 @@ def run_ours(args, w):
     attn_ms, attn_n = dgc.dg_kernel_timer_read(1)
     dgc.dg_kernel_timer_enable(False)
     dgc.dg_workspace_status(ws)
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = replicas.max_over_ranks(ms)
     ms_per_step = ms / args.steps
+    # denoising steps per canvas in the last benchmark step (all steps alike unless the
+    # workload stops canvases early)
     denoise_steps = steps_done / B if steps_done else w.T
-    value = world * w.L * B * denoise_steps / (ms_per_step / 1000.0)
+    value = replicas.job_throughput(world, w.L, B, denoise_steps, ms_per_step / 1000.0)
 
     # ---- end to end through the public API with host buffers: the prefix KV of the step's
     # requests goes host -> device, the final canvas and step counts come back.
@@ -270,7 +277,7 @@ def run_ours(args, w):
     def e2e_step(i):
         kp_d.copy_(kp_h, non_blocking=True)
         vp_d.copy_(vp_h, non_blocking=True)
-        seed = (w.seed << 32) + 7777 + i
+        seed = replicas.replica_seed(w.seed, rank, 7777 + i)
         dgc.dg_forward_noise(canvas, canvas, keep0, w.V, seed)
         lock.zero_()
         cfg = dgc.make_cfg(w.T, w.schedule, w.inv_tau, lock_thr, seed,
@@ -290,12 +297,9 @@ def run_ours(args, w):
         e2e_step(i)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * w.L * B * w.T / (e2e_ms / args.steps / 1000.0)
+    e2e_ms = replicas.max_over_ranks(e0.elapsed_time(e1))
+    e2e_steps = float(st_h.sum().item()) / B if int(st_h.sum().item()) else w.T
+    e2e_value = replicas.job_throughput(world, w.L, B, e2e_steps, e2e_ms / args.steps / 1000.0)
     h2d = kp.numel() * 2 * 2
     d2h = out_h.numel() * 4 + st_h.numel() * 4
 
@@ -316,7 +320,7 @@ def run_ours(args, w):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rows = 256
-        sec = oracle_step_sample(w, rows)
+        sec = OracleSample(w)(rows)
         cpu = {"value": rows / sec, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                "sample": f"one denoising step of the {w.name} workload (decoder over the canvas, "
                          f"posterior over all 262,144 tokens and Euler step for all {rows} "

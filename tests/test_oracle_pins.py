@@ -244,6 +244,39 @@ def test_attention_is_bidirectional_in_the_canvas():
     assert np.abs(o1[0, 0] - o2[0, 0]).max() > 1e-4
 
 
+# ------------------------------------------------------------- stand-in decoder -----
+
+def test_decoder_front_selects_the_right_segments():
+    """With Wqkv rows that are unit vectors, q / k / v are chosen coordinates of h = E[x]:
+    a transposed weight, a swapped q|k|v segment or a wrong head split fails this."""
+    V, d, H, Hkv, hd, B, L = 32, 64, 2, 1, 8, 2, 4
+    rng = np.random.default_rng(0)
+    E = O.round_bf16(rng.standard_normal((V, d)))
+    cols = rng.permutation(d)[: (H + 2 * Hkv) * hd]
+    Wqkv = np.zeros(((H + 2 * Hkv) * hd, d))
+    Wqkv[np.arange(len(cols)), cols] = 1.0
+    x = rng.integers(0, V, (B, L))
+    h, q, k, v = O.decoder_front(x, E, Wqkv, H, Hkv, hd)
+    assert np.array_equal(h, E[x])
+    hq = h[..., cols[: H * hd]].reshape(B, L, H, hd)
+    hk = h[..., cols[H * hd:(H + Hkv) * hd]].reshape(B, L, Hkv, hd)
+    hv = h[..., cols[(H + Hkv) * hd:]].reshape(B, L, Hkv, hd)
+    assert np.array_equal(q, hq) and np.array_equal(k, hk) and np.array_equal(v, hv)
+
+
+def test_decoder_back_is_residual_plus_projection():
+    B, L, d, H, hd = 1, 3, 16, 2, 8
+    rng = np.random.default_rng(1)
+    h = O.round_bf16(rng.standard_normal((B, L, d)))
+    Oa = O.round_bf16(rng.standard_normal((B, L, H, hd)))
+    assert np.array_equal(O.decoder_back(h, Oa, np.zeros((d, H * hd))), h)
+    Wo = np.zeros((d, H * hd))
+    Wo[np.arange(d), np.arange(d)[::-1]] = 1.0                 # y_j = h_j + O_flat[d - 1 - j]
+    y = O.decoder_back(h, Oa, Wo)
+    ref = O.round_bf16(h + Oa.reshape(B, L, -1)[..., ::-1])
+    assert np.array_equal(y, ref)
+
+
 # ---------------------------------------------------------------------- posterior -----
 
 def test_posterior_uniform_logits():
