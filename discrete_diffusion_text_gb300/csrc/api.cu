@@ -214,6 +214,7 @@ struct LoopWs {
   uint32_t* status;
   uint8_t* active;
   int* n_active;
+  int* counters;  // [2B]: per-canvas unlocked count and CTA tickets of the finalisation
   uint16_t *h, *q, *k, *v, *o, *y;
   void* attn;
   VocabPart* parts;
@@ -232,6 +233,7 @@ LoopWs loop_layout(const dg_model* m, int B, int L, int P, int window, uint8_t* 
   w.status = reinterpret_cast<uint32_t*>(take(kStatusBytes));
   w.active = take(B);
   w.n_active = reinterpret_cast<int*>(take(sizeof(int)));
+  w.counters = reinterpret_cast<int*>(take(2 * sizeof(int) * static_cast<size_t>(B)));
   w.h = reinterpret_cast<uint16_t*>(take(BL * m->d * 2));
   w.q = reinterpret_cast<uint16_t*>(take(BL * m->H * m->hd * 2));
   w.k = reinterpret_cast<uint16_t*>(take(BL * m->Hkv * m->hd * 2));
@@ -401,7 +403,8 @@ dg_status dg_out_proj(const uint16_t* h, const uint16_t* O, const uint16_t* Wo, 
 
 size_t dg_vocab_posterior_workspace(int B, int L, int V) {
   if (B <= 0 || L <= 0 || V < 256) return kStatusBytes;
-  return kStatusBytes + align256(plan_vocab(B * L, V).part_bytes);
+  return kStatusBytes + align256(2 * sizeof(int) * static_cast<size_t>(B)) +
+         align256(plan_vocab(B * L, V).part_bytes);
 }
 
 dg_status dg_vocab_posterior_step(const uint16_t* y, const uint16_t* W, int B, int L, int d, int V,
@@ -426,7 +429,13 @@ dg_status dg_vocab_posterior_step(const uint16_t* y, const uint16_t* W, int B, i
   cudaStream_t st = as_stream(stream);
   uint8_t* w = static_cast<uint8_t*>(ws);
   uint32_t* status = reinterpret_cast<uint32_t*>(w);
-  VocabPart* parts = reinterpret_cast<VocabPart*>(w + kStatusBytes);
+  int* counters = reinterpret_cast<int*>(w + kStatusBytes);
+  VocabPart* parts = reinterpret_cast<VocabPart*>(
+      w + kStatusBytes + align256(2 * sizeof(int) * static_cast<size_t>(B)));
+  {
+    const cudaError_t em = cudaMemsetAsync(counters, 0, 2 * sizeof(int) * B, st);
+    if (em != cudaSuccess) return cuda_fail(em, "vocab_posterior: memset");
+  }
   const VocabPlan vp = plan_vocab(B * L, V);
   cudaError_t e = launch_vocab_pass(y, W, B * L, L, d, V, inv_tau, seed, step, parts, status,
                                     nullptr, st);
@@ -453,6 +462,8 @@ dg_status dg_vocab_posterior_step(const uint16_t* y, const uint16_t* W, int B, i
   fp.k0 = static_cast<uint32_t>(seed);
   fp.k1 = static_cast<uint32_t>(seed >> 32);
   fp.step = static_cast<uint32_t>(step);
+  fp.unlocked = counters;
+  fp.cta_done = counters + B;
   launch_vocab_finalize(fp, B, st);
   return check_launch("vocab finalize launch");
 }
@@ -522,6 +533,7 @@ dg_status dg_denoise_loop(const dg_model* m, const uint16_t* k_pre, const uint16
   const VocabPlan vp = plan_vocab(BL, m->V);
 
   cudaError_t e = cudaMemsetAsync(w.n_active, 0, sizeof(int), st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(w.counters, 0, 2 * sizeof(int) * B, st);
   if (e != cudaSuccess) return cuda_fail(e, "loop: memset");
   launch_loop_init(lock, w.active, w.n_active, steps_taken, B, L, cfg->stop_when_all_locked, st);
   if ((s = check_launch("loop init launch")) != DG_OK) return s;
@@ -577,6 +589,8 @@ dg_status dg_denoise_loop(const dg_model* m, const uint16_t* k_pre, const uint16
     fp.steps_taken = steps_taken;
     fp.n_active = w.n_active;
     fp.stop_when_all_locked = cfg->stop_when_all_locked;
+    fp.unlocked = w.counters;
+    fp.cta_done = w.counters + B;
     launch_vocab_finalize(fp, B, st);
     if ((s = check_launch("loop: finalize launch")) != DG_OK) return s;
   }

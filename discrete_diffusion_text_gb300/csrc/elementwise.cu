@@ -98,25 +98,57 @@ void launch_euler_update(const int32_t* x_in, const int32_t* x0hat, const int32_
 }
 
 // ------------------------------------------------- vocabulary-pass finalisation -------
-// One CTA per canvas, one thread per position.  Merges the position's partial tuples from
-// every vocabulary chunk in a fixed order (deterministic), writes the posterior outputs and
-// applies the Euler step.  In the loop, `active` freezes finished canvases, `steps_taken`
-// counts applied steps and `n_active` counts canvases that have not stopped.
-__global__ void vocab_finalize_kernel(FinalizeParams p) {
+// One warp per position (eight positions per CTA, all of one canvas).  The lanes merge the
+// position's partial tuples from the vocabulary chunks (lane l takes chunks l, l + 32, ...),
+// then a fixed xor-butterfly combines the lanes: the reduction order never changes, so the
+// result is deterministic.  Lane 0 writes the posterior outputs and applies the Euler step.
+// Per canvas, the CTAs count the positions left unlocked; the last CTA of the canvas to
+// finish (an atomic ticket, no waiting) sets `done`, updates the loop bookkeeping and resets
+// the counters for the next call.
+constexpr int kFinRows = 8;
+
+__device__ __forceinline__ VocabPart shfl_xor_part(const VocabPart& a, int off) {
+  VocabPart o;
+  o.m = __shfl_xor_sync(0xFFFFFFFFu, a.m, off);
+  o.s = __shfl_xor_sync(0xFFFFFFFFu, a.s, off);
+  o.top_z = __shfl_xor_sync(0xFFFFFFFFu, a.top_z, off);
+  o.best_score = __shfl_xor_sync(0xFFFFFFFFu, a.best_score, off);
+  o.best_z = __shfl_xor_sync(0xFFFFFFFFu, a.best_z, off);
+  o.top_idx = __shfl_xor_sync(0xFFFFFFFFu, a.top_idx, off);
+  o.best_idx = __shfl_xor_sync(0xFFFFFFFFu, a.best_idx, off);
+  o.pad = 0;
+  return o;
+}
+
+__global__ void __launch_bounds__(kFinRows * 32) vocab_finalize_kernel(FinalizeParams p) {
   if (p.n_active && *p.n_active == 0) return;
-  const int b = blockIdx.x;
-  const int i = threadIdx.x;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kFinRows + warp;  // L is a multiple of kFinRows
+  const int b = row / p.L;
+  const int i = row % p.L;
   const bool is_active = p.active == nullptr || p.active[b] != 0;
-  bool locked_after = true;
-  if (i < p.L) {
-    const int row = b * p.L + i;
-    const int mt = row >> 7;
-    const int row_in = row & 127;
-    VocabPart acc = p.parts[static_cast<int64_t>(mt) * 128 + row_in];
-    for (int c = 1; c < p.S; ++c) {
-      const VocabPart q = p.parts[(static_cast<int64_t>(c) * p.num_mt + mt) * 128 + row_in];
-      merge_part(acc, q);
+
+  const int mt = row >> 7;
+  const int row_in = row & 127;
+  VocabPart acc = empty_part();
+  for (int c = lane; c < p.S; c += 32)
+    merge_part(acc, p.parts[(static_cast<int64_t>(c) * p.num_mt + mt) * 128 + row_in]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const VocabPart o = shfl_xor_part(acc, off);
+    // both lanes of a pair combine (lower lane's tuple first) and get identical results
+    if (lane & off) {
+      VocabPart t = o;
+      merge_part(t, acc);
+      acc = t;
+    } else {
+      merge_part(acc, o);
     }
+  }
+
+  bool locked_after = false;
+  if (lane == 0) {
     const float lse = acc.m + logf(acc.s);
     const float lp_top1 = acc.top_z - lse;
     if (p.out_x0hat) p.out_x0hat[row] = acc.best_idx;
@@ -138,26 +170,33 @@ __global__ void vocab_finalize_kernel(FinalizeParams p) {
       if (p.x_out != p.x_in) p.x_out[row] = p.x_in[row];
       if (p.jump) p.jump[row] = 0;
       locked_after = p.lock != nullptr && p.lock[row] != 0;
-    } else {
-      locked_after = false;
     }
   }
-  const int all = __syncthreads_and(locked_after ? 1 : 0);
-  if (i == 0) {
-    if (p.done) p.done[b] = all ? 1 : 0;
-    if (is_active && p.x_in != nullptr) {
-      if (p.steps_taken) p.steps_taken[b] += 1;
-      if (p.active && p.stop_when_all_locked && all) {
-        p.active[b] = 0;
-        if (p.n_active) atomicSub(p.n_active, 1);
+  const int unlocked = __syncthreads_count(lane == 0 && !locked_after ? 1 : 0);
+  if (threadIdx.x == 0) {
+    if (unlocked) atomicAdd(&p.unlocked[b], unlocked);
+    __threadfence();
+    const int ticket = atomicAdd(&p.cta_done[b], 1);
+    if (ticket == p.L / kFinRows - 1) {  // the last CTA of this canvas
+      __threadfence();
+      const bool all = atomicAdd(&p.unlocked[b], 0) == 0;
+      if (p.done) p.done[b] = all ? 1 : 0;
+      if (is_active && p.x_in != nullptr) {
+        if (p.steps_taken) p.steps_taken[b] += 1;
+        if (p.active && p.stop_when_all_locked && all) {
+          p.active[b] = 0;
+          if (p.n_active) atomicSub(p.n_active, 1);
+        }
       }
+      p.unlocked[b] = 0;
+      p.cta_done[b] = 0;
     }
   }
 }
 
 void launch_vocab_finalize(const FinalizeParams& p, int B, cudaStream_t st) {
-  const int threads = ((p.L + 31) / 32) * 32;
-  vocab_finalize_kernel<<<B, threads, 0, st>>>(p);
+  const int rows = B * p.L;
+  vocab_finalize_kernel<<<rows / kFinRows, kFinRows * 32, 0, st>>>(p);
 }
 
 // Loop bookkeeping: active[b] = 1 unless the canvas is already fully locked and stopping is

@@ -138,10 +138,21 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
       }
-      int sg = 0;
-      while (sg + 1 < p.out.nseg && col >= p.out.seg_begin[sg + 1]) ++sg;
-      uint16_t* dst = p.out.ptr[sg] + static_cast<int64_t>(row) * p.out.ld[sg] +
-                      (col - p.out.seg_begin[sg]);
+      // output segment of this column (static indices only: no local-memory copy of params)
+      uint16_t* base = p.out.ptr[0];
+      int ld = p.out.ld[0];
+      int beg = p.out.seg_begin[0];
+      if (p.out.nseg > 1 && col >= p.out.seg_begin[1]) {
+        base = p.out.ptr[1];
+        ld = p.out.ld[1];
+        beg = p.out.seg_begin[1];
+      }
+      if (p.out.nseg > 2 && col >= p.out.seg_begin[2]) {
+        base = p.out.ptr[2];
+        ld = p.out.ld[2];
+        beg = p.out.seg_begin[2];
+      }
+      uint16_t* dst = base + static_cast<int64_t>(row) * ld + (col - beg);
       uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {

@@ -25,6 +25,8 @@ struct FinalizeParams {
   int32_t* steps_taken;  // loop only
   int* n_active;         // loop only
   int stop_when_all_locked;
+  int* unlocked;  // [B] per-canvas counters, zero before the first call; reset by the kernel
+  int* cta_done;  // [B]
 };
 
 void launch_forward_noise(const int32_t* x0, int32_t* xt, const uint64_t* keep_thr, int B, int L,

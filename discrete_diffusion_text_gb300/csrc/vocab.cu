@@ -3,19 +3,20 @@
 // z = y W^T (rows = canvas positions, columns = vocabulary) is computed on the 5th-generation
 // tensor cores tile by tile; no logit ever leaves the SM.  Each CTA is persistent over "units"
 // = (128-row tile, contiguous vocabulary chunk):
-//   warp 0      TMA: k-blocks of y (128 x 64) and W (256 x 64) into a 4-stage ring;
-//   warp 1      one thread issues tcgen05.mma M=128, N=256, K=16 into one of two TMEM
-//               accumulators (2 x 256 columns), so the next tile's MMA overlaps this epilogue;
-//   warps 2..9  epilogue, one thread per (row, half of the 256 columns): tempered logits
-//               z~ = z / tau, online (max, sum exp) for the log-sum-exp, the top-1 (lowest index on
-//               ties), and the Gumbel-max sample argmax(z~ + g) with g from Philox.
-// Only rows' partial tuples are written; a per-canvas finalisation kernel merges them in a
-// fixed order and applies the Euler step.
+//   warp 0       TMA: k-blocks of y (128 x 64) and W (256 x 64) into a 4-stage ring;
+//   warp 1       one thread issues tcgen05.mma M=128, N=256, K=16 into one of two TMEM
+//                accumulators (2 x 256 columns), so the next tile's MMA overlaps this epilogue;
+//   warps 2..17  epilogue: four groups of four warps, each group one 64-column quarter of the
+//                tile, one thread per row: tempered logits z~ = z / tau, online (max, sum exp)
+//                for the log-sum-exp, the top-1 (lowest index on ties), and the Gumbel-max
+//                sample argmax(z~ + g) with g from Philox.
+// Only rows' partial tuples are written; a finalisation kernel merges them in a fixed order and
+// applies the Euler step.
 //
 // Gumbel candidates: g_v = -log(E_v) with E_v = -log(1 - W_v) >= W_v (W_v the open-unit draw),
 // so entry v can only beat the current best score b if W_v < exp(z~_v - b).  exp(z~_v - m) is
 // already computed for the sum, so the test costs one multiply; the two logarithms are taken
-// only for the rare entries that pass (with a safety margin for rounding).
+// out of line, only for the rare entries that pass (with a safety margin for rounding).
 #include "kernels.cuh"
 #include "sm103.cuh"
 
@@ -26,8 +27,11 @@ constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
 constexpr int kStages = 4;
-constexpr int kThreads = 320;     // 10 warps
-constexpr int kEpiThreads = 256;  // warps 2..9
+constexpr int kEpiWarps = 16;
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kThreads = 64 + kEpiThreads;      // TMA warp + MMA warp + epilogue
+constexpr int kGroups = kEpiWarps / 4;          // column groups of the tile
+constexpr int kGroupCols = kBN / kGroups;       // 64 columns per group
 
 struct VocabParams {
   int R, L, d, V;
@@ -44,13 +48,12 @@ struct VocabLayout {
   static constexpr int kBBytes = kBN * kBK * 2;   // 32 KiB
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kScratchOff = kStages * kStageBytes;
-  static constexpr int kScratchBytes = kBM * sizeof(VocabPart);
+  static constexpr int kScratchBytes = (kGroups - 1) * kBM * sizeof(VocabPart);
   static constexpr int kBarOff = kScratchOff + kScratchBytes;
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
 
 // Running per-row state of one epilogue thread.
 struct RowState {
@@ -69,23 +72,58 @@ __device__ __forceinline__ void refresh_cthr(RowState& st) {
   st.cthr = st.best == -INFINITY ? INFINITY : __expf(st.m - st.best) * 1.001f;
 }
 
-__device__ __forceinline__ void process_chunk(RowState& st, const float (&z)[32], int vbase,
+__device__ __forceinline__ float open_unit(uint32_t u) {
+  // W = (u + 1/2) / 2^32, rounded to fp32 (full relative precision near 0)
+  return fmaf(__uint2float_rn(u), 2.3283064365386963e-10f, 1.1641532182693481e-10f);
+}
+
+struct Best {
+  float score;
+  int idx;
+  float z;
+};
+
+// The rare path: exact Gumbel scores for the candidate entries of one 32-column chunk, in
+// increasing vocabulary order.  Out of line so that the hot loop stays small; it receives a
+// copy of the chunk's logits and returns the best (score, index, logit) by value, so nothing
+// of the hot loop's register state has its address taken.
+__device__ __noinline__ Best gumbel_candidates(Best b, const float* zt, uint32_t cand, int vbase,
+                                               uint32_t pos, uint32_t canvas, uint32_t k0,
+                                               uint32_t k1, uint32_t c3) {
+  while (cand) {
+    const int e = __ffs(cand) - 1;
+    cand &= cand - 1;
+    const Words4 w = philox4x32_10(static_cast<uint32_t>((vbase + e) >> 2), pos, canvas, c3, k0, k1);
+    const int q = e & 3;
+    const uint32_t u = q == 0 ? w.x : (q == 1 ? w.y : (q == 2 ? w.z : w.w));
+    const float E = -log1pf(-open_unit(u));
+    const float sc = zt[e] - logf(E);
+    if (sc > b.score) {
+      b.score = sc;
+      b.idx = vbase + e;
+      b.z = zt[e];
+    }
+  }
+  return b;
+}
+
+__device__ __forceinline__ void process_chunk(RowState& st, float (&zt)[32], int vbase,
                                               float inv_tau, uint32_t pos, uint32_t canvas,
                                               uint32_t k0, uint32_t k1, uint32_t c3) {
-  float zt[32];
   float cm = -INFINITY;
 #pragma unroll
   for (int e = 0; e < 32; ++e) {
-    zt[e] = z[e] * inv_tau;
+    zt[e] *= inv_tau;
     cm = fmaxf(cm, zt[e]);
   }
-  // top-1: strictly greater keeps the lowest index within this thread's increasing order
+  // strictly greater: an equal value seen earlier (a lower index) keeps the top-1; within the
+  // chunk the first position holding the maximum wins
+  if (cm > st.top_z) {
+    uint32_t eq = 0;
 #pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    if (zt[e] > st.top_z) {
-      st.top_z = zt[e];
-      st.top_idx = vbase + e;
-    }
+    for (int e = 0; e < 32; ++e) eq |= (zt[e] == cm ? 1u : 0u) << e;
+    st.top_z = cm;
+    st.top_idx = vbase + __ffs(eq) - 1;
   }
   if (cm > st.m) {
     st.s *= ex2_approx((st.m - cm) * kLog2e);
@@ -93,15 +131,9 @@ __device__ __forceinline__ void process_chunk(RowState& st, const float (&z)[32]
     refresh_cthr(st);
   }
   const float mlog2 = st.m * kLog2e;
+  const float cthr = st.cthr;
   float ssum = 0.f;
-  float pe[32];
-#pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    pe[e] = ex2_approx(fmaf(zt[e], kLog2e, -mlog2));
-    ssum += pe[e];
-  }
-  st.s += ssum;
-  // Gumbel perturbation, 4 vocabulary entries per Philox call.
+  uint32_t cand = 0;
 #pragma unroll
   for (int g4 = 0; g4 < 8; ++g4) {
     const Words4 w = philox4x32_10(static_cast<uint32_t>(vbase >> 2) + g4, pos, canvas, c3, k0,
@@ -110,18 +142,23 @@ __device__ __forceinline__ void process_chunk(RowState& st, const float (&z)[32]
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int e = g4 * 4 + q;
-      // W = (u + 1/2) / 2^32, rounded to fp32 (full relative precision near 0)
-      const float W = fmaf(__uint2float_rn(u[q]), 2.3283064365386963e-10f, 1.1641532182693481e-10f);
-      if (W < pe[e] * st.cthr) {
-        const float E = -log1pf(-W);
-        const float sc = zt[e] - logf(E);
-        if (sc > st.best) {
-          st.best = sc;
-          st.best_idx = vbase + e;
-          st.best_z = zt[e];
-          refresh_cthr(st);
-        }
-      }
+      const float pe = ex2_approx(fmaf(zt[e], kLog2e, -mlog2));
+      ssum += pe;
+      cand |= (open_unit(u[q]) < pe * cthr ? 1u : 0u) << e;
+    }
+  }
+  st.s += ssum;
+  if (cand) {
+    float copy[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) copy[e] = zt[e];
+    const Best b = gumbel_candidates({st.best, st.best_idx, st.best_z}, copy, cand, vbase, pos,
+                                     canvas, k0, k1, c3);
+    if (b.score != st.best || b.idx != st.best_idx) {
+      st.best = b.score;
+      st.best_idx = b.idx;
+      st.best_z = b.z;
+      refresh_cthr(st);
     }
   }
 }
@@ -232,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // --------------------------------------------------------------- epilogue -----
     const int ew = warp - 2;
-    const int half = ew >> 2;                       // which 128 of the 256 columns
+    const int grp = ew >> 2;                        // which 64-column quarter of the tile
     const int row_in = (warp & 3) * 32 + lane;      // TMEM lane quarter of this warp
     const uint32_t lane_base = tmem_lane_base(warp);
     // After an abort the loop structure is kept (every epilogue warp still reaches each
@@ -262,16 +299,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) continue;
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < kGroupCols / 32; ++c) {
           float z[32];
-          tmem_ld32(tmem + lane_base + buf * kBN + half * 128 + c * 32, z);
-          process_chunk(st, z, vt * kBN + half * 128 + c * 32, p.inv_tau, pos, canvas, p.k0,
-                        p.k1, p.c3);
+          const int col = grp * kGroupCols + c * 32;
+          tmem_ld32(tmem + lane_base + buf * kBN + col, z);
+          process_chunk(st, z, vt * kBN + col, p.inv_tau, pos, canvas, p.k0, p.k1, p.c3);
         }
         tc_fence_before();
         mbar_arrive(&tempty[buf]);
       }
-      // Merge the two column halves of each row through shared memory.
+      // Merge the column groups of each row through shared memory, in group order.
       VocabPart mine;
       mine.m = st.m;
       mine.s = st.s;
@@ -282,10 +319,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mine.best_z = st.best_z;
       mine.pad = 0;
       named_bar_sync(1, kEpiThreads);
-      if (half == 1) scratch[row_in] = mine;
+      if (grp > 0) scratch[(grp - 1) * kBM + row_in] = mine;
       named_bar_sync(1, kEpiThreads);
-      if (half == 0) {
-        merge_part(mine, scratch[row_in]);
+      if (grp == 0) {
+#pragma unroll
+        for (int q = 1; q < kGroups; ++q) merge_part(mine, scratch[(q - 1) * kBM + row_in]);
         if (ok && row < p.R) p.parts[static_cast<int64_t>(u) * kBM + row_in] = mine;
       }
     }
