@@ -420,10 +420,11 @@ AttnPlan plan_attention(int B, int L, int P, int H, int hd, int window) {
   const int eff_p = (window > 0 && window < P) ? window + L : P;  // keys a query tile may see
   const int nt_all = (eff_p + kTile - 1) / kTile + n_q;
   const int sms = num_sms();
-  // Minimise waves x tiles-per-split, then prefer fewer splits (less merge traffic).
+  // Minimise waves x tiles-per-split, then prefer fewer splits (less merge traffic).  With
+  // at least one CTA per SM already, keys are not split.
   int best = 1;
   int64_t best_cost = -1;
-  for (int s = 1; s <= nt_all && s <= 64; ++s) {
+  for (int s = 1; s <= nt_all && s <= 64 && (s == 1 || units < sms); ++s) {
     const int per = (nt_all + s - 1) / s;
     const int64_t ctas = static_cast<int64_t>(units) * s;
     const int64_t waves = (ctas + sms - 1) / sms;

@@ -345,17 +345,20 @@ VocabPlan plan_vocab(int R, int V) {
   pl.num_mt = (R + kBM - 1) / kBM;
   pl.nvt = V / kBN;
   const int sms = num_sms();
-  // Choose the number of vocabulary chunks S that minimises (waves x tiles per chunk); ties
-  // go to fewer chunks (less merge work).
+  // Choose the number of vocabulary chunks S: minimise the tiles of the busiest CTA
+  // (waves x tiles per chunk) plus a small cost per chunk for the merge (each row's tuples are
+  // merged by one warp, 32 per round); units stay within 16 waves so the tuple workspace stays
+  // bounded (at most 16 x SMs x 4 KiB unless there are more row tiles than that).
   int bestS = 1, best_per = pl.nvt;
-  int64_t best_cost = -1;
+  double best_cost = -1.0;
   for (int S = 1; S <= pl.nvt; ++S) {
     const int per = (pl.nvt + S - 1) / S;
     const int S2 = (pl.nvt + per - 1) / per;
     if (S2 != S) continue;
     const int64_t units = static_cast<int64_t>(pl.num_mt) * S2;
+    if (S2 > 1 && units > 16ll * sms) break;
     const int64_t waves = (units + sms - 1) / sms;
-    const int64_t cost = waves * per;
+    const double cost = static_cast<double>(waves * per) + S2 / 8.0;
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       bestS = S2;
