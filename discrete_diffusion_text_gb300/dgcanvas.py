@@ -67,6 +67,8 @@ SIGNATURES = {
     "dg_vocab_posterior_workspace": (_SZ, [_I, _I, _I]),
     "dg_vocab_posterior_step": (_I, [_P, _P, _I, _I, _I, _I, _F, _U64, _I, _P, _P, _P, _P, _P,
                                      _U64, _F, _P, _P, _SZ, _P]),
+    "dg_vocab_posterior_step_noalloc": (_I, [_P, _P, _I, _I, _I, _I, _F, _U64, _I, _P, _P, _P,
+                                             _P, _P, _U64, _F, _P, _P]),
     "dg_euler_update": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _U64, _I, _U64, _F, _P]),
     "dg_denoise_loop_workspace": (_SZ, [_P, _I, _I, _I, _I]),
     "dg_denoise_loop_kernel_count": (_I, [_P, _I, _I, _I, _I, _I]),
@@ -224,6 +226,26 @@ def dg_vocab_posterior_step(y, W, B: int, L: int, inv_tau: float, seed: int, ste
         _ptr(jump), _ptr(done), jump_thr, lock_logthr,
         ctypes.addressof(po) if po is not None else None, _ptr(ws), ws.numel(), _stream(stream)),
         "dg_vocab_posterior_step")
+
+
+def dg_vocab_posterior_step_noalloc(y, W, B: int, L: int, inv_tau: float, seed: int, step: int,
+                                    x_in=None, x_out=None, lock=None, jump=None, done=None,
+                                    jump_thr: int = 0, lock_logthr: float = math.inf, out=None,
+                                    stream=None):
+    """dg_vocab_posterior_step without a workspace: the library's fixed device scratch array
+    is used instead (for callers that cannot allocate); same arguments otherwise."""
+    _bf16(y, "y")
+    _bf16(W, "W")
+    V, d = W.shape
+    po = None
+    if out is not None:
+        po = dg_posterior_out(*(_ptr(out.get(k)) for k in
+                                ("x0hat", "top1", "logp_top1", "lse", "logp_x0hat")))
+    _check(load().dg_vocab_posterior_step_noalloc(
+        _ptr(y), _ptr(W), B, L, d, V, inv_tau, seed, step, _ptr(x_in), _ptr(x_out), _ptr(lock),
+        _ptr(jump), _ptr(done), jump_thr, lock_logthr,
+        ctypes.addressof(po) if po is not None else None, _stream(stream)),
+        "dg_vocab_posterior_step_noalloc")
 
 
 def dg_euler_update(x_in, x0hat, top1, logp_top1, x_out, lock, jump, done, seed: int, step: int,

@@ -176,6 +176,32 @@ dg_status dg_vocab_posterior_step(const uint16_t* y, const uint16_t* W, int B, i
                                   const dg_posterior_out* out, void* ws, size_t ws_bytes,
                                   void* stream);
 
+/* Allocation-free variant of dg_vocab_posterior_step.  (The pages have no counterpart: this is
+ * a deployment convenience, not a step of the method.)  It is for callers that cannot supply
+ * a workspace: code that receives only input and output buffers from a host framework with
+ * no handle to its memory pool, processes whose device memory is reserved up front, and
+ * loops that must not risk the device synchronisation of cudaMalloc / cudaFree.
+ *   - Same arguments, layouts, results and errors as dg_vocab_posterior_step, without ws.
+ *   - Scratch lives in one file-scope device array of 16 MiB, held by every GPU that loads the
+ *     library until the process exits.  The call allocates nothing (no cudaMalloc, cudaFree or
+ *     allocating library routine); it clears the part of the array that must start at zero.
+ *   - Sizes whose scratch exceeds 16 MiB (about 2,000 canvases of 256 positions or more at a
+ *     262,144-token vocabulary on a 152-SM GPU; the need is the dg_vocab_posterior_workspace
+ *     size less 256 bytes) return DG_ENOTSUP with a message; use dg_vocab_posterior_step with
+ *     a workspace for those.
+ *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress)
+ *     with that device current; make that first call before any stream capture.
+ *   - Every call shares the one array: calls that may overlap on the GPU (different streams
+ *     without ordering between them) race on it.  Order them on one stream.
+ *   - Kernel timeouts are reported by dg_workspace_status(NULL, stream).
+ */
+dg_status dg_vocab_posterior_step_noalloc(const uint16_t* y, const uint16_t* W, int B, int L,
+                                          int d, int V, float inv_tau, uint64_t seed, int step,
+                                          const int32_t* x_in, int32_t* x_out, uint8_t* lock,
+                                          uint8_t* jump, uint8_t* done, uint64_t jump_thr,
+                                          float lock_logthr, const dg_posterior_out* out,
+                                          void* stream);
+
 /* ----------------------------------------------------- Euler jump + lock + commit ----
  * The reverse Step [TR "Backward Denoising Process"] with optional confidence locking
  * [PBD glossary "Iterative denoising"]: per position of every canvas,
