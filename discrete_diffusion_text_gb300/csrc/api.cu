@@ -240,7 +240,7 @@ LoopWs loop_layout(const dg_model* m, int B, int L, int P, int window, uint8_t* 
   w.v = reinterpret_cast<uint16_t*>(take(BL * m->Hkv * m->hd * 2));
   w.o = reinterpret_cast<uint16_t*>(take(BL * m->H * m->hd * 2));
   w.y = reinterpret_cast<uint16_t*>(take(BL * m->d * 2));
-  const AttnPlan ap = plan_attention(B, L, P, m->H, m->hd, window);
+  const AttnPlan ap = plan_attention(B, L, P, m->H, m->Hkv, m->hd, window);
   w.attn = take(ap.part_bytes > 0 ? ap.part_bytes : 16);
   const VocabPlan vp = plan_vocab(static_cast<int>(BL), m->V);
   w.parts = reinterpret_cast<VocabPart*>(take(vp.part_bytes));
@@ -354,9 +354,9 @@ dg_status dg_embed_qkv(const int32_t* x, const uint16_t* E, const uint16_t* Wqkv
 }
 
 size_t dg_canvas_attn_workspace(int B, int L, int P, int H, int Hkv, int hd, int window) {
-  (void)Hkv;
-  if (B < 0 || L <= 0 || H <= 0 || (hd != 64 && hd != 128)) return kStatusBytes;
-  return kStatusBytes + align256(plan_attention(B, L, P, H, hd, window).part_bytes);
+  if (B < 0 || L <= 0 || H <= 0 || Hkv <= 0 || H % Hkv != 0 || (hd != 64 && hd != 128))
+    return kStatusBytes;
+  return kStatusBytes + align256(plan_attention(B, L, P, H, Hkv, hd, window).part_bytes);
 }
 
 dg_status dg_canvas_attn(const uint16_t* q, const uint16_t* k_pre, const uint16_t* v_pre,
@@ -493,7 +493,7 @@ size_t dg_denoise_loop_workspace(const dg_model* m, int B, int L, int P, int win
 int dg_denoise_loop_kernel_count(const dg_model* m, int B, int L, int P, int window, int steps) {
   if (!m || B <= 0 || L <= 0 || steps < 0 || m->H <= 0 || (m->hd != 64 && m->hd != 128))
     return -1;
-  const AttnPlan ap = plan_attention(B, L, P, m->H, m->hd, window);
+  const AttnPlan ap = plan_attention(B, L, P, m->H, m->Hkv, m->hd, window);
   // loop init, then per step: embedding gather, QKV GEMM, attention (+ split merge),
   // output projection, vocabulary pass, finalisation
   return 1 + steps * (6 + (ap.splits > 1 ? 1 : 0));

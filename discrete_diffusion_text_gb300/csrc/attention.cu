@@ -1,31 +1,44 @@
-// Canvas attention on the 5th-generation tensor cores: 128 canvas queries of one head
-// against the visible prefix keys and all canvas keys, in key tiles of 128.
+// Canvas attention on the 5th-generation tensor cores.
 //
-// Per CTA = (canvas b, query head h, query tile, key split):
-//   warp 0     TMA: the Q tile once, then K/V tiles into a 2-stage ring (128-byte swizzle);
-//   warp 1     one thread issues S_j = Q K_j^T (tcgen05, M=128, N=128) into one of two TMEM
-//              score buffers, and O += P_{j-1} V_{j-1} (M=128, N=hd) once P_{j-1} is ready;
-//   warps 2..5 one thread per query row: read S_j from TMEM, mask, exponentiate against a
-//              running reference max, write P_j (bf16) to shared memory in the swizzled
-//              K-major layout the tensor core reads.
-// The reference max is only raised when a row's max grows by more than 2^8 (log2 units):
-// p <= 256 stays exact in fp32 accumulation and bf16, and O/l use the same reference, so the
-// result is unchanged while O (in TMEM) is rescaled rarely.
-// With several key splits, each writes unnormalised fp32 partials (O, m, l) and a merge
-// kernel combines them with the log-sum-exp rule.
+// One CTA serves two "slots" that read the same keys and values: the two query heads of a GQA
+// group for one 128-query tile (or, when a group has one query head, two query tiles of that
+// head).  Keys and values come in tiles of 64 keys, staged once for both slots.
+//   warp 0       TMA: Q of both slots once, then K_0, V_0, K_1, V_1, ... through a 6-slot ring
+//                (K_{j+1} reuses the slot of K_{j-2}, so loads run two tiles ahead);
+//   warp 1       one thread issues, per key tile j, S_s(j+1) = Q_s K_{j+1}^T (M=128, N=64) into
+//                the free one of two TMEM score buffers of each slot, then O_s += P_s(j) V_j
+//                (M=128, N=hd, V as an MN-major operand) once P_s(j) is written;
+//   warps 4..7   softmax of slot 0, warps 8..11 softmax of slot 1: one thread per query row
+//                reads its 64 scores from TMEM, masks, exponentiates against a running
+//                reference max and writes P (bf16) into one of two shared-memory buffers of its
+//                slot, in the 128-byte-swizzle K-major operand layout.
+//   (warps 2, 3 only complete the first warpgroup, whose registers go to the softmax warps.)
+// Double-buffered scores and P mean no step waits for the MMA it just fed.  The reference max is
+// only raised when a row's max grows by more than 2^8 (log2 units): p <= 256 is exact enough in
+// fp32 accumulation and bf16, and O and l use the same reference, so the result is unchanged
+// while O (in TMEM) is rescaled rarely.
+// With several key splits, each writes unnormalised fp32 partials (O, m, l) and a merge kernel
+// combines them with the log-sum-exp rule.
 #include "kernels.cuh"
 #include "sm103.cuh"
 
 namespace dg {
 namespace {
 
-constexpr int kTile = 128;         // queries per CTA and keys per tile
+constexpr int kQTile = 128;  // queries per slot
+constexpr int kKTile = 64;   // keys per tile
 constexpr float kRescaleLog2 = 8.f;
+constexpr int kRing = 6;     // K/V ring slots (K_j and V_j alternate)
+constexpr int kThreads = 384;      // warpgroup 0: TMA + MMA warps; warpgroups 1, 2: softmax
+constexpr int kRegsControl = 48;   // registers per thread of warpgroup 0 after the split
+constexpr int kRegsSoftmax = 216;  // registers per thread of the softmax warpgroups
+// 128 x 48 + 256 x 216 = 61,440 registers: needs a launch allocation of >= 160 per thread.
 
 struct AttnParams {
   int B, L, P, H, Hkv, hd, window;
   float scale_log2;  // scale * log2(e)
   int n_pre_tiles, n_can_tiles, n_qtiles, splits;
+  int units;         // CTAs per split
   uint16_t* out;
   float* lse;
   float* part_o;   // [splits][B*H*L][hd]
@@ -36,37 +49,52 @@ struct AttnParams {
 
 template <int HD>
 struct AttnLayout {
-  static constexpr int kChunk = kTile * 64 * 2;      // one [128][64] bf16 swizzled chunk
-  static constexpr int kQBytes = (HD / 64) * kChunk;
-  static constexpr int kKVBytes = (HD / 64) * kChunk;  // one of K or V
-  static constexpr int kStageBytes = 2 * kKVBytes;
-  static constexpr int kPBytes = 2 * kChunk;          // [128 queries][128 keys]
+  static constexpr int kQChunk = kQTile * 128;         // [128 rows][64 bf16] swizzled chunk
+  static constexpr int kKVChunk = kKTile * 128;        // [64 rows][64 bf16]
+  static constexpr int kQBytes = (HD / 64) * kQChunk;  // one slot's Q tile
+  static constexpr int kKVBytes = (HD / 64) * kKVChunk;  // one K or V tile
+  static constexpr int kPBytes = kQTile * kKTile * 2;  // [128 queries][64 keys]: one chunk
   static constexpr int kQOff = 0;
-  static constexpr int kKVOff = kQOff + kQBytes;
-  static constexpr int kPOff = kKVOff + 2 * kStageBytes;
-  static constexpr int kBarOff = kPOff + 2 * kPBytes;
+  static constexpr int kKVOff = kQOff + 2 * kQBytes;
+  static constexpr int kPOff = kKVOff + kRing * kKVBytes;
+  static constexpr int kBarOff = kPOff + 4 * kPBytes;  // P: 2 slots x 2 buffers
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;
 };
 
-__device__ __forceinline__ void write_p_row(uint8_t* pbuf, int row, const float* p) {
-  // 128 bf16 of one query row into two [128 rows][64 keys] chunks, 16-byte units swizzled by
-  // (row % 8), matching the 128-byte-swizzle K-major operand layout.
-#pragma unroll
-  for (int u16 = 0; u16 < 16; ++u16) {
-    const int chunk = u16 >> 3;
-    const int u = u16 & 7;
-    const int phys = u ^ (row & 7);
-    uint4 v;
-    v.x = pack_bf16x2(p[u16 * 8 + 0], p[u16 * 8 + 1]);
-    v.y = pack_bf16x2(p[u16 * 8 + 2], p[u16 * 8 + 3]);
-    v.z = pack_bf16x2(p[u16 * 8 + 4], p[u16 * 8 + 5]);
-    v.w = pack_bf16x2(p[u16 * 8 + 6], p[u16 * 8 + 7]);
-    *reinterpret_cast<uint4*>(pbuf + chunk * (kTile * 128) + row * 128 + phys * 16) = v;
+// The two slots of a CTA: (head, query tile) each, sharing one KV head and key range.
+struct Slots {
+  int b, g, h0, h1, qt0, qt1;
+  bool valid1;
+};
+
+__device__ __forceinline__ Slots cta_slots(int u, const AttnParams& p) {
+  Slots s;
+  const int r = p.H / p.Hkv;
+  if ((r & 1) == 0) {  // two query heads of one group, same query tile
+    const int pairs = p.H / 2;
+    const int qt = u % p.n_qtiles;
+    const int pr = (u / p.n_qtiles) % pairs;
+    s.b = u / (p.n_qtiles * pairs);
+    s.h0 = 2 * pr;
+    s.h1 = 2 * pr + 1;
+    s.qt0 = s.qt1 = qt;
+    s.valid1 = true;
+  } else {  // one head, two consecutive query tiles
+    const int nqp = (p.n_qtiles + 1) / 2;
+    const int qp = u % nqp;
+    const int h = (u / nqp) % p.H;
+    s.b = u / (nqp * p.H);
+    s.h0 = s.h1 = h;
+    s.qt0 = 2 * qp;
+    s.qt1 = 2 * qp + 1;
+    s.valid1 = s.qt1 < p.n_qtiles;
   }
+  s.g = (s.h0 * p.Hkv) / p.H;
+  return s;
 }
 
 template <int HD>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     canvas_attn_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmKp,
                        const __grid_constant__ CUtensorMap tmVp,
@@ -79,31 +107,27 @@ __global__ void __launch_bounds__(192, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBarOff);
   uint64_t* q_full = bars + 0;
-  uint64_t* kv_full = bars + 1;   // [2]
-  uint64_t* kv_empty = bars + 3;  // [2]
-  uint64_t* s_full = bars + 5;    // [2]
-  uint64_t* p_full = bars + 7;    // [2]
-  uint64_t* pv_done = bars + 9;   // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11);
+  uint64_t* kv_full = bars + 1;    // [kRing]
+  uint64_t* kv_empty = bars + 7;   // [kRing]
+  uint64_t* s_full = bars + 13;    // [slot * 2 + buffer]
+  uint64_t* s_free = bars + 17;    // [slot * 2 + buffer]
+  uint64_t* p_full = bars + 21;    // [slot * 2 + buffer]
+  uint64_t* pv_done = bars + 25;   // [slot * 2 + buffer]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 29);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  int idx = blockIdx.x;
-  const int qt = idx % p.n_qtiles;
-  idx /= p.n_qtiles;
-  const int h = idx % p.H;
-  const int b = idx / p.H;
-  const int g = (h * p.Hkv) / p.H;
+  const Slots sl = cta_slots(blockIdx.x, p);
   const int split = blockIdx.y;
-  const int q0 = qt * kTile;
+  const int nslots = sl.valid1 ? 2 : 1;
 
-  // Key tiles of this query tile: prefix tiles from the first one any of its queries can see,
-  // then the canvas tiles; this split takes a contiguous share of them.
+  // Key tiles: prefix tiles from the first one any query of either slot can see (slot 0 holds
+  // the lower query tile), then the canvas tiles; this split takes a contiguous share.
   int t_lo = 0;
   if (p.window > 0) {
-    const int kmin = p.P + q0 - p.window + 1;
-    t_lo = kmin > 0 ? kmin / kTile : 0;
+    const int kmin = p.P + sl.qt0 * kQTile - p.window + 1;
+    t_lo = kmin > 0 ? kmin / kKTile : 0;
     if (t_lo > p.n_pre_tiles) t_lo = p.n_pre_tiles;
   }
   const int n_pre = p.n_pre_tiles - t_lo;
@@ -113,16 +137,20 @@ __global__ void __launch_bounds__(192, 1)
   const int t_end = min(nt_all, t_begin + per);
   const int nt = t_end > t_begin ? t_end - t_begin : 0;
 
-  const int row_in = (warp & 3) * 32 + lane;  // softmax warps 2..5 -> quarters 2,3,0,1
-  const int qi = q0 + row_in;
-  const int64_t out_row = (static_cast<int64_t>(b) * p.H + h) * p.L + qi;  // (b, h, i)
+  // softmax role of this thread (warps 4..11)
+  const int slot = warp >= 8 ? 1 : 0;
+  const int row_in = (warp & 3) * 32 + lane;  // TMEM lane quarter of this warp
+  const int qi = (slot ? sl.qt1 : sl.qt0) * kQTile + row_in;
+  const int hq = slot ? sl.h1 : sl.h0;
+  const int64_t out_row = (static_cast<int64_t>(sl.b) * p.H + hq) * p.L + qi;  // (b, h, i)
+  const int64_t part_rows = static_cast<int64_t>(p.B) * p.H * p.L;
 
-  if (nt == 0) {  // nothing to do: an empty partial (only when splits > 1)
-    if (warp >= 2 && qi < p.L) {
-      float* ml = p.part_ml + (static_cast<int64_t>(split) * p.B * p.H * p.L + out_row) * 2;
+  if (nt == 0) {  // nothing to do: empty partials (only when splits > 1)
+    if (warp >= 4 && (slot == 0 || sl.valid1) && qi < p.L) {
+      float* ml = p.part_ml + (split * part_rows + out_row) * 2;
       ml[0] = -INFINITY;
       ml[1] = 0.f;
-      float* po = p.part_o + (static_cast<int64_t>(split) * p.B * p.H * p.L + out_row) * HD;
+      float* po = p.part_o + (split * part_rows + out_row) * HD;
       for (int c = 0; c < HD; ++c) po[c] = 0.f;
     }
     return;
@@ -130,10 +158,13 @@ __global__ void __launch_bounds__(192, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kRing; ++s) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
+    }
+    for (int s = 0; s < 4; ++s) {
       mbar_init(&s_full[s], 1);
+      mbar_init(&s_free[s], 128);
       mbar_init(&p_full[s], 128);
       mbar_init(&pv_done[s], 1);
     }
@@ -148,192 +179,249 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tm_s0 = tmem;         // scores, buffer 0: columns [0, 128)
-  const uint32_t tm_o = tmem + 256;    // output accumulator: columns [256, 256 + HD)
+  // TMEM columns: S of (slot s, buffer b) at [(2s + b) * 64, +64); O of slot s at 256 + 128 s
+  auto tm_s = [&](int s, int b) { return tmem + (2 * s + b) * kKTile; };
+  auto tm_o = [&](int s) { return tmem + 256 + s * 128; };
+  auto q_buf = [&](int s) { return smem + Lay::kQOff + s * Lay::kQBytes; };
+  auto kv_buf = [&](int i) { return smem + Lay::kKVOff + (i % kRing) * Lay::kKVBytes; };
+  auto p_buf = [&](int s, int b) { return smem + Lay::kPOff + (2 * s + b) * Lay::kPBytes; };
 
-  uint8_t* sQ = smem + Lay::kQOff;
-  auto kv_stage = [&](int s) { return smem + Lay::kKVOff + s * Lay::kStageBytes; };
-  auto p_buf = [&](int s) { return smem + Lay::kPOff + s * Lay::kPBytes; };
-
-  if (warp == 0) {
-    if (lane == 0) {
+  // Register split (each warpgroup changes its budget in its own branch): the control
+  // warpgroup (TMA and MMA warps) needs few registers, each softmax thread holds a score row.
+  // 128 x kRegsControl + 256 x kRegsSoftmax fits the launch allocation (checked on the host
+  // before the first launch).
+  if (warp < 4) {
+    regs_decrease<kRegsControl>();
+    if (warp == 0 && lane == 0) {
+      // ------------------------------------------------------------------ producer -----
       tma_prefetch_map(&tmQ);
-      mbar_arrive_expect_tx(q_full, Lay::kQBytes);
-      for (int c = 0; c < HD / 64; ++c)
-        tma_load_4d(sQ + c * Lay::kChunk, &tmQ, q_full, c * 64, h, q0, b);
+      mbar_arrive_expect_tx(q_full, nslots * Lay::kQBytes);
+      for (int s = 0; s < nslots; ++s)
+        for (int c = 0; c < HD / 64; ++c)
+          tma_load_4d(q_buf(s) + c * Lay::kQChunk, &tmQ, q_full, c * 64, s ? sl.h1 : sl.h0,
+                      (s ? sl.qt1 : sl.qt0) * kQTile, sl.b);
+      // load index i: K_j for i = 2j, V_j for i = 2j + 1, into ring slot i % kRing
       int issued = 0;
-      for (int j = 0; j < nt; ++j) {
-        const int s = j & 1;
-        if (!mbar_wait(&kv_empty[s], ((j >> 1) & 1) ^ 1, abort_flag)) break;
-        const int t = t_begin + j;
+      for (int i = 0; i < 2 * nt; ++i) {
+        const int rs = i % kRing;
+        if (!mbar_wait(&kv_empty[rs], ((i / kRing) & 1) ^ 1, abort_flag)) break;
+        const int t = t_begin + (i >> 1);
         const bool pre = t < n_pre;
-        const int kb = pre ? (t_lo + t) * kTile : (t - n_pre) * kTile;
-        const CUtensorMap* mk = pre ? &tmKp : &tmKc;
-        const CUtensorMap* mv = pre ? &tmVp : &tmVc;
-        uint8_t* st = kv_stage(s);
-        mbar_arrive_expect_tx(&kv_full[s], Lay::kStageBytes);
-        for (int c = 0; c < HD / 64; ++c) {
-          tma_load_4d(st + c * Lay::kChunk, mk, &kv_full[s], c * 64, g, kb, b);
-          tma_load_4d(st + Lay::kKVBytes + c * Lay::kChunk, mv, &kv_full[s], c * 64, g, kb, b);
-        }
+        const int kb = pre ? (t_lo + t) * kKTile : (t - n_pre) * kKTile;
+        const CUtensorMap* m = (i & 1) ? (pre ? &tmVp : &tmVc) : (pre ? &tmKp : &tmKc);
+        uint8_t* dst = kv_buf(i);
+        mbar_arrive_expect_tx(&kv_full[rs], Lay::kKVBytes);
+        for (int c = 0; c < HD / 64; ++c)
+          tma_load_4d(dst + c * Lay::kKVChunk, m, &kv_full[rs], c * 64, sl.g, kb, sl.b);
         ++issued;
       }
       if (*abort_flag) {
         mbar_wait_drain(q_full, 0);
-        for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j)
-          mbar_wait_drain(&kv_full[j & 1], (j >> 1) & 1);
+        for (int i = (issued > kRing ? issued - kRing : 0); i < issued; ++i)
+          mbar_wait_drain(&kv_full[i % kRing], (i / kRing) & 1);
       }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16(128, kTile, false);
+    } else if (warp == 1 && lane == 0) {
+      // ---------------------------------------------------------------- MMA issuer -----
+      constexpr uint32_t idesc_s = idesc_bf16(128, kKTile, false);
       constexpr uint32_t idesc_o = idesc_bf16(128, HD, true);
-      const uint32_t q_addr = smem_u32(sQ);
       bool ok = mbar_wait(q_full, 0, abort_flag);
-      auto issue_pv = [&](int jj) -> bool {
-        const int s = jj & 1;
-        if (!mbar_wait(&p_full[s], (jj >> 1) & 1, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t pa = smem_u32(p_buf(s));
-        const uint32_t va = smem_u32(kv_stage(s) + Lay::kKVBytes);
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(pa + (kk >> 2) * Lay::kChunk + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(va + kk * 2048, Lay::kChunk, 1024);
-          mma_bf16_ss(tm_o, ad, bd, idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(&pv_done[s]);
-        mma_commit(&kv_empty[s]);
-        return true;
+      auto wait_kv = [&](int i) {
+        return mbar_wait(&kv_full[i % kRing], (i / kRing) & 1, abort_flag);
       };
-      for (int j = 0; ok && j < nt; ++j) {
-        const int s = j & 1;
-        if (!mbar_wait(&kv_full[s], (j >> 1) & 1, abort_flag)) { ok = false; break; }
-        if (j >= 2 && !mbar_wait(&p_full[s], ((j - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t ka = smem_u32(kv_stage(s));
-        const uint32_t tm_s = tm_s0 + s * kTile;
+      auto issue_s = [&](int s, int j) {  // S_s(j) = Q_s K_j^T into buffer j & 1
+        const uint32_t qa = smem_u32(q_buf(s));
+        const uint32_t ka = smem_u32(kv_buf(2 * j));
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * Lay::kChunk + (kk & 3) * 32;
-          mma_bf16_ss(tm_s, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
+          mma_bf16_ss(tm_s(s, j & 1),
+                      sdesc_sw128(qa + (kk >> 2) * Lay::kQChunk + (kk & 3) * 32, 16, 1024),
+                      sdesc_sw128(ka + (kk >> 2) * Lay::kKVChunk + (kk & 3) * 32, 16, 1024),
                       idesc_s, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&s_full[s]);
-        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+        mma_commit(&s_full[2 * s + (j & 1)]);
+      };
+      auto issue_pv = [&](int s, int j) {  // O_s += P_s(j) V_j
+        const uint32_t pa = smem_u32(p_buf(s, j & 1));
+        const uint32_t va = smem_u32(kv_buf(2 * j + 1));
+#pragma unroll
+        for (int kk = 0; kk < kKTile / 16; ++kk) {
+          mma_bf16_ss(tm_o(s), sdesc_sw128(pa + kk * 32, 16, 1024),
+                      sdesc_sw128(va + kk * 2048, Lay::kKVChunk, 1024), idesc_o,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&pv_done[2 * s + (j & 1)]);
+      };
+      // prologue: S of both slots for tile 0, then K_0's ring slot is released
+      if (ok) ok = wait_kv(0);
+      if (ok) {
+        tc_fence_after();
+        for (int s = 0; s < nslots; ++s) issue_s(s, 0);
+        mma_commit(&kv_empty[0]);
       }
-      if (ok) issue_pv(nt - 1);
+      for (int j = 0; ok && j < nt; ++j) {
+        if (j + 1 < nt) {
+          // scores of the next tile into the other buffer, once its previous scores (tile j-1)
+          // have been read
+          if (!(ok = wait_kv(2 * j + 2))) break;
+          for (int s = 0; ok && s < nslots; ++s) {
+            if (j >= 1 && !(ok = mbar_wait(&s_free[2 * s + ((j + 1) & 1)], ((j - 1) >> 1) & 1,
+                                           abort_flag)))
+              break;
+            tc_fence_after();
+            issue_s(s, j + 1);
+          }
+          if (!ok) break;
+          mma_commit(&kv_empty[(2 * j + 2) % kRing]);  // K_{j+1}: read by both S MMAs
+        }
+        if (!(ok = wait_kv(2 * j + 1))) break;
+        for (int s = 0; ok && s < nslots; ++s) {
+          if (!(ok = mbar_wait(&p_full[2 * s + (j & 1)], (j >> 1) & 1, abort_flag))) break;
+          tc_fence_after();
+          issue_pv(s, j);
+        }
+        if (!ok) break;
+        mma_commit(&kv_empty[(2 * j + 1) % kRing]);  // V_j: read by both PV MMAs
+      }
       if (*abort_flag) {  // make sure no MMA is still writing TMEM before it is released
-        uint64_t* last = &pv_done[0];
-        mma_commit(last);
-        mbar_wait_drain(last, 0);
-        mbar_wait_drain(last, 1);
+        mma_commit(&pv_done[0]);
+        mbar_wait_drain(&pv_done[0], 0);
+        mbar_wait_drain(&pv_done[0], 1);
       }
     }
   } else {
-    // ------------------------------------------------------------ softmax warps -----
-    const uint32_t lane_base = tmem_lane_base(warp);
-    float m_ref = -INFINITY;
-    float l = 0.f;
-    bool ok = true;
-    const int kmin = p.window > 0 ? p.P + qi - p.window + 1 : 0;
-    for (int j = 0; j < nt; ++j) {
-      const int s = j & 1;
-      if (!warp_wait(&s_full[s], (j >> 1) & 1, abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      const int t = t_begin + j;
-      const bool pre = t < n_pre;
-      const int kb = pre ? (t_lo + t) * kTile : (t - n_pre) * kTile;
-      const int klim = pre ? p.P : p.L;
-      const int klo = pre ? kmin : 0;
-      float sv[kTile];
+    regs_increase<kRegsSoftmax>();
+    if (slot == 0 || sl.valid1) {
+      // ------------------------------------------------------------- softmax warps -----
+      const uint32_t lane_base = tmem_lane_base(warp);
+      float m_ref = -INFINITY;
+      float l = 0.f;
+      bool ok = true;
+      const int kmin = p.window > 0 ? p.P + qi - p.window + 1 : 0;
+      const float c = p.scale_log2;
+      for (int j = 0; j < nt; ++j) {
+        const int b = j & 1;
+        if (!warp_wait(&s_full[2 * slot + b], (j >> 1) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const int t = t_begin + j;
+        const bool pre = t < n_pre;
+        const int kb = pre ? (t_lo + t) * kKTile : (t - n_pre) * kKTile;
+        const int klim = pre ? p.P : p.L;
+        const int klo = pre ? kmin : 0;
+        float sv[kKTile];
+        tmem_ld64(tm_s(slot, b) + lane_base, sv);  // the score row in one TMEM round trip
+        tc_fence_before();
+        mbar_arrive(&s_free[2 * slot + b]);  // the MMA warp may reuse this score buffer
+        // raw scores; the scale (> 0) is folded into the exponent, so the max is taken on raw
+        // values (rounding is monotone)
+        if (!(kb >= klo && kb + kKTile <= klim)) {
 #pragma unroll
-      for (int c = 0; c < kTile / 32; ++c) {
-        float v[32];
-        tmem_ld32(tm_s0 + lane_base + s * kTile + c * 32, v);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int key = kb + c * 32 + e;
-          sv[c * 32 + e] = (key < klim && key >= klo) ? v[e] * p.scale_log2 : -INFINITY;
+          for (int e = 0; e < kKTile; ++e) {
+            const int key = kb + e;
+            if (!(key < klim && key >= klo)) sv[e] = -INFINITY;
+          }
         }
-      }
-      float mt = -INFINITY;
+        float mx[8];  // eight partial maxima: short dependency chains
 #pragma unroll
-      for (int e = 0; e < kTile; ++e) mt = fmaxf(mt, sv[e]);
-      const float m_new = fmaxf(m_ref, mt);
-      if (j == 0) {
-        m_ref = m_new;
-      } else {
-        const bool need = m_new > m_ref + kRescaleLog2;
-        if (__any_sync(0xFFFFFFFFu, need)) {
-          if (!warp_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag)) { ok = false; break; }
+        for (int q = 0; q < 8; ++q) mx[q] = sv[q];
+#pragma unroll
+        for (int e = 8; e < kKTile; ++e) mx[e & 7] = fmaxf(mx[e & 7], sv[e]);
+        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        const float m_new = fmaxf(m_ref, mt * c);
+        // raise the reference max only when the row max grew by more than 2^8; f rescales the
+        // accumulated O and l (applied below, once this tile's P is written)
+        const bool need = j > 0 && m_new > m_ref + kRescaleLog2;
+        const float f = need ? ex2_approx(m_ref - m_new) : 1.f;
+        if (j == 0 || need) m_ref = m_new;
+        const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+        // P = exp2(s * c - m), summed with eight partial sums and packed to bf16 pairs
+        float ps[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) ps[q] = 0.f;
+        uint32_t pk[kKTile / 2];
+#pragma unroll
+        for (int e = 0; e < kKTile; e += 2) {
+          const float a = ex2_approx(fmaf(sv[e], c, -m_use));
+          const float bb = ex2_approx(fmaf(sv[e + 1], c, -m_use));
+          ps[e & 7] += a;
+          ps[(e + 1) & 7] += bb;
+          pk[e >> 1] = pack_bf16x2(a, bb);
+        }
+        const float rs =
+            ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+        // P buffer b was last read by PV of tile j - 2
+        if (j >= 2 &&
+            !warp_wait(&pv_done[2 * slot + b], ((j - 2) >> 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        // the 64 keys of this row are one 128-byte row of the swizzled chunk: 16-byte unit u
+        // goes to position u ^ (row % 8)
+        uint8_t* prow = p_buf(slot, b) + row_in * 128;
+#pragma unroll
+        for (int u = 0; u < kKTile / 8; ++u)
+          *reinterpret_cast<uint4*>(prow + ((u ^ (row_in & 7)) * 16)) =
+              make_uint4(pk[u * 4], pk[u * 4 + 1], pk[u * 4 + 2], pk[u * 4 + 3]);
+        l = l * f + rs;
+        if (__any_sync(0xFFFFFFFFu, need)) {  // O *= f once PV of tile j - 1 has completed
+          if (!warp_wait(&pv_done[2 * slot + ((j - 1) & 1)], ((j - 1) >> 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          const float f = need ? ex2_approx(m_ref - m_new) : 1.f;
 #pragma unroll 1
-          for (int c = 0; c < HD / 32; ++c) {
+          for (int cc = 0; cc < HD / 32; ++cc) {
             float o[32];
-            tmem_ld32(tm_o + lane_base + c * 32, o);
+            tmem_ld32(tm_o(slot) + lane_base + cc * 32, o);
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] *= f;
-            tmem_st32(tm_o + lane_base + c * 32, o);
-          }
-          if (need) {
-            l *= f;
-            m_ref = m_new;
+            tmem_st32(tm_o(slot) + lane_base + cc * 32, o);
           }
         }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&p_full[2 * slot + b]);
       }
-      if (j >= 2 && !warp_wait(&pv_done[s], ((j - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
-      const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-      float rs = 0.f;
-#pragma unroll
-      for (int e = 0; e < kTile; ++e) {
-        sv[e] = ex2_approx(sv[e] - m_use);
-        rs += sv[e];
-      }
-      l += rs;
-      write_p_row(p_buf(s), row_in, sv);
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&p_full[s]);
-    }
-    if (ok) ok = warp_wait(&pv_done[(nt - 1) & 1], ((nt - 1) >> 1) & 1, abort_flag);
-    tc_fence_after();
-    const bool write = ok && qi < p.L;
-    if (p.splits == 1) {
-      const float inv_l = 1.f / l;
-      uint16_t* dst = p.out + ((static_cast<int64_t>(b) * p.L + qi) * p.H + h) * HD;
+      if (ok)
+        ok = warp_wait(&pv_done[2 * slot + ((nt - 1) & 1)], ((nt - 1) >> 1) & 1, abort_flag);
+      tc_fence_after();
+      const bool write = ok && qi < p.L;
+      if (p.splits == 1) {
+        const float inv_l = 1.f / l;
+        uint16_t* dst = p.out + ((static_cast<int64_t>(sl.b) * p.L + qi) * p.H + hq) * HD;
 #pragma unroll 1
-      for (int c = 0; c < HD / 32; ++c) {
-        float o[32];
-        tmem_ld32(tm_o + lane_base + c * 32, o);
-        if (write) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+        for (int cc = 0; cc < HD / 32; ++cc) {
+          float o[32];
+          tmem_ld32(tm_o(slot) + lane_base + cc * 32, o);
+          if (write) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            d4[q] = make_uint4(pack_bf16x2(o[q * 8 + 0] * inv_l, o[q * 8 + 1] * inv_l),
-                               pack_bf16x2(o[q * 8 + 2] * inv_l, o[q * 8 + 3] * inv_l),
-                               pack_bf16x2(o[q * 8 + 4] * inv_l, o[q * 8 + 5] * inv_l),
-                               pack_bf16x2(o[q * 8 + 6] * inv_l, o[q * 8 + 7] * inv_l));
+            for (int q = 0; q < 4; ++q)
+              d4[q] = make_uint4(pack_bf16x2(o[q * 8 + 0] * inv_l, o[q * 8 + 1] * inv_l),
+                                 pack_bf16x2(o[q * 8 + 2] * inv_l, o[q * 8 + 3] * inv_l),
+                                 pack_bf16x2(o[q * 8 + 4] * inv_l, o[q * 8 + 5] * inv_l),
+                                 pack_bf16x2(o[q * 8 + 6] * inv_l, o[q * 8 + 7] * inv_l));
+          }
         }
-      }
-      if (write && p.lse) p.lse[out_row] = (m_ref + __log2f(l)) * 0.6931471805599453f;
-    } else {
-      const int64_t prow = static_cast<int64_t>(split) * p.B * p.H * p.L + out_row;
-      float* po = p.part_o + prow * HD;
+        if (write && p.lse) p.lse[out_row] = (m_ref + __log2f(l)) * 0.6931471805599453f;
+      } else {
+        const int64_t prow = split * part_rows + out_row;
+        float* po = p.part_o + prow * HD;
 #pragma unroll 1
-      for (int c = 0; c < HD / 32; ++c) {
-        float o[32];
-        tmem_ld32(tm_o + lane_base + c * 32, o);
-        if (write) {
-          float4* d4 = reinterpret_cast<float4*>(po + c * 32);
+        for (int cc = 0; cc < HD / 32; ++cc) {
+          float o[32];
+          tmem_ld32(tm_o(slot) + lane_base + cc * 32, o);
+          if (write) {
+            float4* d4 = reinterpret_cast<float4*>(po + cc * 32);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) d4[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+            for (int q = 0; q < 8; ++q)
+              d4[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+          }
         }
-      }
-      if (write) {
-        p.part_ml[prow * 2] = m_ref;
-        p.part_ml[prow * 2 + 1] = l;
+        if (write) {
+          p.part_ml[prow * 2] = m_ref;
+          p.part_ml[prow * 2 + 1] = l;
+        }
       }
     }
   }
@@ -371,9 +459,8 @@ __global__ void attn_merge_kernel(AttnParams p) {
 #pragma unroll
     for (int e = 0; e < HD / 32; ++e) acc[e] += w * po[e * 32 + lane];
   }
-  const int64_t hrow = row;  // (b, h, i)
-  const int i = static_cast<int>(hrow % p.L);
-  const int64_t bh = hrow / p.L;
+  const int i = static_cast<int>(row % p.L);
+  const int64_t bh = row / p.L;
   const int h = static_cast<int>(bh % p.H);
   const int64_t b = bh / p.H;
   __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + ((b * p.L + i) * p.H + h) * HD;
@@ -393,12 +480,19 @@ cudaError_t launch_hd(const CUtensorMap* maps, const AttnParams& p, cudaStream_t
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Lay::kSmemBytes);
     if (e != cudaSuccess) return e;
+    // The register split must fit the block's launch allocation, or an increase would never
+    // be granted: refuse to launch a build where it does not.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, canvas_attn_kernel<HD>);
+    if (e != cudaSuccess) return e;
+    if (static_cast<long>(fa.numRegs) * kThreads < 128L * kRegsControl + 256L * kRegsSoftmax)
+      return cudaErrorInvalidConfiguration;
     configured_device = dev;
   }
-  dim3 grid(p.B * p.H * p.n_qtiles, p.splits);
+  dim3 grid(p.units, p.splits);
   timer_begin(1, st);
-  canvas_attn_kernel<HD><<<grid, 192, Lay::kSmemBytes, st>>>(maps[0], maps[1], maps[2], maps[3],
-                                                             maps[4], p);
+  canvas_attn_kernel<HD><<<grid, kThreads, Lay::kSmemBytes, st>>>(maps[0], maps[1], maps[2],
+                                                                  maps[3], maps[4], p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (p.splits > 1) {
@@ -412,13 +506,18 @@ cudaError_t launch_hd(const CUtensorMap* maps, const AttnParams& p, cudaStream_t
   return e;
 }
 
+int attn_units(int B, int L, int H, int Hkv) {
+  const int n_q = (L + kQTile - 1) / kQTile;
+  const int r = H / Hkv;
+  return (r % 2 == 0) ? B * (H / 2) * n_q : B * H * ((n_q + 1) / 2);
+}
+
 }  // namespace
 
-AttnPlan plan_attention(int B, int L, int P, int H, int hd, int window) {
-  const int n_q = (L + kTile - 1) / kTile;
-  const int units = B * H * n_q;
+AttnPlan plan_attention(int B, int L, int P, int H, int Hkv, int hd, int window) {
+  const int units = attn_units(B, L, H, Hkv);
   const int eff_p = (window > 0 && window < P) ? window + L : P;  // keys a query tile may see
-  const int nt_all = (eff_p + kTile - 1) / kTile + n_q;
+  const int nt_all = (eff_p + kKTile - 1) / kKTile + (L + kKTile - 1) / kKTile;
   const int sms = num_sms();
   // Minimise waves x tiles-per-split, then prefer fewer splits (less merge traffic).  With
   // at least one CTA per SM already, keys are not split.
@@ -428,7 +527,7 @@ AttnPlan plan_attention(int B, int L, int P, int H, int hd, int window) {
     const int per = (nt_all + s - 1) / s;
     const int64_t ctas = static_cast<int64_t>(units) * s;
     const int64_t waves = (ctas + sms - 1) / sms;
-    const int64_t cost = waves * (per + 1);  // +1: per-CTA setup, roughly one tile
+    const int64_t cost = waves * (per + 2);  // +2: per-CTA setup, roughly two tiles
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best = s;
@@ -445,16 +544,17 @@ cudaError_t launch_attention(const uint16_t* q, const uint16_t* k_pre, const uin
                              float* lse, int B, int L, int P, int H, int Hkv, int hd, int window,
                              float scale, void* part_ws, uint32_t* status, const int* n_active,
                              cudaStream_t st) {
-  const AttnPlan pl = plan_attention(B, L, P, H, hd, window);
+  const AttnPlan pl = plan_attention(B, L, P, H, Hkv, hd, window);
   CUtensorMap maps[5];
-  const uint32_t box[4] = {64u, 1u, static_cast<uint32_t>(kTile), 1u};
   {
+    const uint32_t box[4] = {64u, 1u, static_cast<uint32_t>(kQTile), 1u};
     const uint64_t dims[4] = {static_cast<uint64_t>(hd), static_cast<uint64_t>(H),
                               static_cast<uint64_t>(L), static_cast<uint64_t>(B)};
     const uint64_t str[3] = {static_cast<uint64_t>(hd) * 2, static_cast<uint64_t>(H) * hd * 2,
                              static_cast<uint64_t>(L) * H * hd * 2};
     if (!make_tmap_bf16(&maps[0], q, 4, dims, str, box)) return cudaErrorInvalidValue;
   }
+  const uint32_t kvbox[4] = {64u, 1u, static_cast<uint32_t>(kKTile), 1u};
   const uint16_t* kv_src[4] = {k_pre, v_pre, k_can, v_can};
   for (int m = 0; m < 4; ++m) {
     const int rows = m < 2 ? (P > 0 ? P : 1) : L;
@@ -464,7 +564,7 @@ cudaError_t launch_attention(const uint16_t* q, const uint16_t* k_pre, const uin
                               static_cast<uint64_t>(rows), static_cast<uint64_t>(B)};
     const uint64_t str[3] = {static_cast<uint64_t>(hd) * 2, static_cast<uint64_t>(Hkv) * hd * 2,
                              static_cast<uint64_t>(m < 2 ? (P > 0 ? P : L) : L) * Hkv * hd * 2};
-    if (!make_tmap_bf16(&maps[1 + m], base, 4, dims, str, box)) return cudaErrorInvalidValue;
+    if (!make_tmap_bf16(&maps[1 + m], base, 4, dims, str, kvbox)) return cudaErrorInvalidValue;
   }
   AttnParams p;
   p.B = B;
@@ -475,10 +575,11 @@ cudaError_t launch_attention(const uint16_t* q, const uint16_t* k_pre, const uin
   p.hd = hd;
   p.window = window;
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.n_pre_tiles = (P + kTile - 1) / kTile;
-  p.n_can_tiles = (L + kTile - 1) / kTile;
-  p.n_qtiles = (L + kTile - 1) / kTile;
+  p.n_pre_tiles = (P + kKTile - 1) / kKTile;
+  p.n_can_tiles = (L + kKTile - 1) / kKTile;
+  p.n_qtiles = (L + kQTile - 1) / kQTile;
   p.splits = pl.splits;
+  p.units = attn_units(B, L, H, Hkv);
   p.out = out;
   p.lse = lse;
   p.part_o = reinterpret_cast<float*>(part_ws);

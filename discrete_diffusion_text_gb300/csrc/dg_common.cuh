@@ -10,7 +10,7 @@
 
 #include <string>
 
-#include "../../include/dgcanvas.h"
+#include "dgcanvas.h"
 
 namespace dg {
 
@@ -37,6 +37,38 @@ __device__ __forceinline__ Words4 philox4x32_10(uint32_t c0, uint32_t c1, uint32
     c3 = lo0;
     k0 += 0x9E3779B9u;
     k1 += 0xBB67AE85u;
+  }
+  return {c0, c1, c2, c3};
+}
+
+// The same generator with the ten round keys computed once (k0 + r*W0, k1 + r*W1) by the
+// caller, for loops that draw many counters under one key.
+struct PhiloxKeys {
+  uint32_t k0[10], k1[10];
+};
+
+__device__ __forceinline__ PhiloxKeys philox_round_keys(uint32_t k0, uint32_t k1) {
+  PhiloxKeys k;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    k.k0[r] = k0 + static_cast<uint32_t>(r) * 0x9E3779B9u;
+    k.k1[r] = k1 + static_cast<uint32_t>(r) * 0xBB67AE85u;
+  }
+  return k;
+}
+
+__device__ __forceinline__ Words4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2,
+                                                uint32_t c3, const PhiloxKeys& k) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
+    const uint32_t n0 = hi1 ^ c1 ^ k.k0[r];
+    const uint32_t n2 = hi0 ^ c3 ^ k.k1[r];
+    c0 = n0;
+    c1 = lo1;
+    c2 = n2;
+    c3 = lo0;
   }
   return {c0, c1, c2, c3};
 }

@@ -60,7 +60,7 @@ struct AttnPlan {
   int splits;
   size_t part_bytes;  // fp32 partials for split > 1
 };
-AttnPlan plan_attention(int B, int L, int P, int H, int hd, int window);
+AttnPlan plan_attention(int B, int L, int P, int H, int Hkv, int hd, int window);
 cudaError_t launch_attention(const uint16_t* q, const uint16_t* k_pre, const uint16_t* v_pre,
                              const uint16_t* k_can, const uint16_t* v_can, uint16_t* out,
                              float* lse, int B, int L, int P, int H, int Hkv, int hd, int window,

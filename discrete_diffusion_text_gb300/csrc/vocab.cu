@@ -83,45 +83,47 @@ struct Best {
   float z;
 };
 
-// The rare path: exact Gumbel scores for the candidate entries of one 32-column chunk, in
-// increasing vocabulary order.  Out of line so that the hot loop stays small; it receives a
-// copy of the chunk's logits and returns the best (score, index, logit) by value, so nothing
-// of the hot loop's register state has its address taken.
-__device__ __noinline__ Best gumbel_candidates(Best b, const float* zt, uint32_t cand, int vbase,
-                                               uint32_t pos, uint32_t canvas, uint32_t k0,
-                                               uint32_t k1, uint32_t c3) {
-  while (cand) {
-    const int e = __ffs(cand) - 1;
-    cand &= cand - 1;
-    const Words4 w = philox4x32_10(static_cast<uint32_t>((vbase + e) >> 2), pos, canvas, c3, k0, k1);
-    const int q = e & 3;
-    const uint32_t u = q == 0 ? w.x : (q == 1 ? w.y : (q == 2 ? w.z : w.w));
-    const float E = -log1pf(-open_unit(u));
-    const float sc = zt[e] - logf(E);
-    if (sc > b.score) {
-      b.score = sc;
-      b.idx = vbase + e;
-      b.z = zt[e];
-    }
+// The rare path: the exact Gumbel score of one candidate entry v with tempered logit z.
+// Out of line so that the hot loop stays small; scalars in and out (nothing of the hot loop's
+// register state has its address taken).
+__device__ __noinline__ Best gumbel_candidate(Best b, float z, int v, uint32_t pos,
+                                              uint32_t canvas, uint32_t k0, uint32_t k1,
+                                              uint32_t c3) {
+  const Words4 w = philox4x32_10(static_cast<uint32_t>(v >> 2), pos, canvas, c3, k0, k1);
+  const int q = v & 3;
+  const uint32_t u = q == 0 ? w.x : (q == 1 ? w.y : (q == 2 ? w.z : w.w));
+  const float E = -log1pf(-open_unit(u));
+  const float sc = z - logf(E);
+  if (sc > b.score) {
+    b.score = sc;
+    b.idx = v;
+    b.z = z;
   }
   return b;
 }
 
-__device__ __forceinline__ void process_chunk(RowState& st, float (&zt)[32], int vbase,
+// One 32-column chunk of raw logits z (tempered here: z~ = z * inv_tau, inv_tau > 0).
+//  - The chunk max is taken on raw z: rounding is monotone, so max(fl(z * c)) = fl(max(z) * c).
+//  - exp(z~ - m) is one FFMA into ex2: exp2(z * c log2 e - m log2 e).
+//  - Candidate filter without an int-to-float conversion: X = 1 + floor(u / 2^9) * 2^-23 lies in
+//    [1, 2) and X - 1 <= W, so W < t implies X < 1 + t, hence X <= fl(1 + t) (rounding is
+//    monotone and X is representable).  With t = exp(z~ - m) * cthr >= exp(z~ - best) this
+//    never drops an entry that could beat the best score; survivors get the exact test.
+__device__ __forceinline__ void process_chunk(RowState& st, const float (&z)[32], int vbase,
                                               float inv_tau, uint32_t pos, uint32_t canvas,
-                                              uint32_t k0, uint32_t k1, uint32_t c3) {
-  float cm = -INFINITY;
+                                              const PhiloxKeys& keys, uint32_t k0, uint32_t k1,
+                                              uint32_t c3) {
+  float mx[4] = {z[0], z[1], z[2], z[3]};  // four partial maxima: short dependency chains
 #pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    zt[e] *= inv_tau;
-    cm = fmaxf(cm, zt[e]);
-  }
+  for (int e = 4; e < 32; ++e) mx[e & 3] = fmaxf(mx[e & 3], z[e]);
+  const float cmr = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+  const float cm = cmr * inv_tau;
   // strictly greater: an equal value seen earlier (a lower index) keeps the top-1; within the
   // chunk the first position holding the maximum wins
   if (cm > st.top_z) {
     uint32_t eq = 0;
 #pragma unroll
-    for (int e = 0; e < 32; ++e) eq |= (zt[e] == cm ? 1u : 0u) << e;
+    for (int e = 0; e < 32; ++e) eq |= (z[e] * inv_tau == cm ? 1u : 0u) << e;
     st.top_z = cm;
     st.top_idx = vbase + __ffs(eq) - 1;
   }
@@ -130,30 +132,35 @@ __device__ __forceinline__ void process_chunk(RowState& st, float (&zt)[32], int
     st.m = cm;
     refresh_cthr(st);
   }
+  const float scale = inv_tau * kLog2e;
   const float mlog2 = st.m * kLog2e;
   const float cthr = st.cthr;
-  float ssum = 0.f;
+  float ps[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums
   uint32_t cand = 0;
 #pragma unroll
   for (int g4 = 0; g4 < 8; ++g4) {
-    const Words4 w = philox4x32_10(static_cast<uint32_t>(vbase >> 2) + g4, pos, canvas, c3, k0,
-                                   k1);
+    const Words4 w = philox4x32_10(static_cast<uint32_t>(vbase >> 2) + g4, pos, canvas, c3, keys);
     const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int e = g4 * 4 + q;
-      const float pe = ex2_approx(fmaf(zt[e], kLog2e, -mlog2));
-      ssum += pe;
-      cand |= (open_unit(u[q]) < pe * cthr ? 1u : 0u) << e;
+      const float pe = ex2_approx(fmaf(z[e], scale, -mlog2));
+      ps[q] += pe;
+      const float X = __uint_as_float(0x3F800000u | (u[q] >> 9));
+      if (X <= fmaf(pe, cthr, 1.0f)) cand |= 1u << e;
     }
   }
-  st.s += ssum;
+  st.s += (ps[0] + ps[1]) + (ps[2] + ps[3]);
   if (cand) {
-    float copy[32];
+    Best b{st.best, st.best_idx, st.best_z};
+    do {  // candidates in increasing vocabulary order
+      const int e = __ffs(cand) - 1;
+      cand &= cand - 1;
+      float ze = z[0];
 #pragma unroll
-    for (int e = 0; e < 32; ++e) copy[e] = zt[e];
-    const Best b = gumbel_candidates({st.best, st.best_idx, st.best_z}, copy, cand, vbase, pos,
-                                     canvas, k0, k1, c3);
+      for (int k = 1; k < 32; ++k) ze = e == k ? z[k] : ze;  // static indices only
+      b = gumbel_candidate(b, ze * inv_tau, vbase + e, pos, canvas, k0, k1, c3);
+    } while (cand);
     if (b.score != st.best || b.idx != st.best_idx) {
       st.best = b.score;
       st.best_idx = b.idx;
@@ -272,6 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int grp = ew >> 2;                        // which 64-column quarter of the tile
     const int row_in = (warp & 3) * 32 + lane;      // TMEM lane quarter of this warp
     const uint32_t lane_base = tmem_lane_base(warp);
+    const PhiloxKeys keys = philox_round_keys(p.k0, p.k1);
     // After an abort the loop structure is kept (every epilogue warp still reaches each
     // unit's named barriers); only the waits, loads and stores are skipped.
     uint32_t j = 0;
@@ -298,15 +306,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) ok = warp_wait(&tfull[buf], (j >> 1) & 1, abort_flag);
         if (!ok) continue;
         tc_fence_after();
-#pragma unroll 1
-        for (int c = 0; c < kGroupCols / 32; ++c) {
-          float z[32];
-          const int col = grp * kGroupCols + c * 32;
-          tmem_ld32(tmem + lane_base + buf * kBN + col, z);
-          process_chunk(st, z, vt * kBN + col, p.inv_tau, pos, canvas, p.k0, p.k1, p.c3);
-        }
+        // this thread's 64 columns in one TMEM round trip; the accumulator buffer is handed
+        // back to the MMA warp before the (longer) posterior work on the registers
+        float z[kGroupCols];
+        const int col = grp * kGroupCols;
+        tmem_ld64(tmem + lane_base + buf * kBN + col, z);
         tc_fence_before();
         mbar_arrive(&tempty[buf]);
+#pragma unroll
+        for (int c = 0; c < kGroupCols / 32; ++c)
+          process_chunk(st, *reinterpret_cast<const float(*)[32]>(&z[c * 32]),
+                        vt * kBN + col + c * 32, p.inv_tau, pos, canvas, keys, p.k0, p.k1, p.c3);
       }
       // Merge the column groups of each row through shared memory, in group order.
       VocabPart mine;
