@@ -2,21 +2,24 @@
 //
 // One CTA serves two "slots" that read the same keys and values: the two query heads of a GQA
 // group for one 128-query tile (or, when a group has one query head, two query tiles of that
-// head).  Keys and values come in tiles of 64 keys, staged once for both slots.
-//   warp 0       TMA: Q of both slots once, then K_0, V_0, K_1, V_1, ... through a 6-slot ring
-//                (K_{j+1} reuses the slot of K_{j-2}, so loads run two tiles ahead);
-//   warp 1       one thread issues, per key tile j, S_s(j+1) = Q_s K_{j+1}^T (M=128, N=64) into
-//                the free one of two TMEM score buffers of each slot, then O_s += P_s(j) V_j
-//                (M=128, N=hd, V as an MN-major operand) once P_s(j) is written;
+// head).  Keys and values come in tiles of 128 keys, staged once for both slots, so every
+// score MMA is M=128 x N=128 (the 128-row MMA costs the same ~45 cycles for any N <= 64, and
+// only reaches full rate from N=128 up).
+//   warp 0       TMA: Q of both slots once, then K_0, V_0, K_1, V_1, ... through a ring of
+//                tiles (five at hd=128);
+//   warp 1       one thread issues, per key tile j and slot s, O_s += P_s(j) V_j with P_s(j)
+//                read straight from TMEM, then -- once that MMA has finished reading P_s(j) --
+//                S_s(j+1) = Q_s K_{j+1}^T into the same TMEM columns;
 //   warps 4..7   softmax of slot 0, warps 8..11 softmax of slot 1: one thread per query row
-//                reads its 64 scores from TMEM, masks, exponentiates against a running
-//                reference max and writes P (bf16) into one of two shared-memory buffers of its
-//                slot, in the 128-byte-swizzle K-major operand layout.
+//                reads its 128 scores from TMEM, masks, exponentiates against a running
+//                reference max and writes P as bf16 pairs over the first 64 score columns.
 //   (warps 2, 3 only complete the first warpgroup, whose registers go to the softmax warps.)
-// Double-buffered scores and P mean no step waits for the MMA it just fed.  The reference max is
-// only raised when a row's max grows by more than 2^8 (log2 units): p <= 256 is exact enough in
-// fp32 accumulation and bf16, and O and l use the same reference, so the result is unchanged
-// while O (in TMEM) is rescaled rarely.
+// TMEM holds S_0, S_1 (128 columns each, P aliased in their first halves) and O_0, O_1.  The
+// MMA order per tile is PV_0, S_0(next), PV_1, S_1(next): each softmax warpgroup has the other
+// slot's two MMAs to hide behind, and the wait for PV_s before S_s(next) overlaps the other
+// slot's work.  The reference max is only raised when a row's max grows by more than 2^8
+// (log2 units): p <= 256 is exact enough in fp32 accumulation and bf16, and O and l use the
+// same reference, so the result is unchanged while O (in TMEM) is rescaled rarely.
 // With several key splits, each writes unnormalised fp32 partials (O, m, l) and a merge kernel
 // combines them with the log-sum-exp rule.
 #include "kernels.cuh"
@@ -26,9 +29,9 @@ namespace dg {
 namespace {
 
 constexpr int kQTile = 128;  // queries per slot
-constexpr int kKTile = 64;   // keys per tile
+constexpr int kKTile = 128;  // keys per tile
 constexpr float kRescaleLog2 = 8.f;
-constexpr int kRing = 6;     // K/V ring slots (K_j and V_j alternate)
+constexpr int kRingMax = 10;
 constexpr int kThreads = 384;      // warpgroup 0: TMA + MMA warps; warpgroups 1, 2: softmax
 constexpr int kRegsControl = 48;   // registers per thread of warpgroup 0 after the split
 constexpr int kRegsSoftmax = 216;  // registers per thread of the softmax warpgroups
@@ -49,16 +52,16 @@ struct AttnParams {
 
 template <int HD>
 struct AttnLayout {
-  static constexpr int kQChunk = kQTile * 128;         // [128 rows][64 bf16] swizzled chunk
-  static constexpr int kKVChunk = kKTile * 128;        // [64 rows][64 bf16]
-  static constexpr int kQBytes = (HD / 64) * kQChunk;  // one slot's Q tile
+  static constexpr int kRing = HD == 128 ? 5 : 10;   // K/V ring slots (K_j and V_j alternate)
+  static constexpr int kQChunk = kQTile * 128;        // [128 rows][64 bf16] swizzled chunk
+  static constexpr int kKVChunk = kKTile * 128;       // [128 keys][64 bf16]
+  static constexpr int kQBytes = (HD / 64) * kQChunk;    // one slot's Q tile
   static constexpr int kKVBytes = (HD / 64) * kKVChunk;  // one K or V tile
-  static constexpr int kPBytes = kQTile * kKTile * 2;  // [128 queries][64 keys]: one chunk
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = kQOff + 2 * kQBytes;
-  static constexpr int kPOff = kKVOff + kRing * kKVBytes;
-  static constexpr int kBarOff = kPOff + 4 * kPBytes;  // P: 2 slots x 2 buffers
-  static constexpr int kSmemBytes = kBarOff + 256 + 1024;
+  static constexpr int kBarOff = kKVOff + kRing * kKVBytes;
+  static constexpr int kSmemBytes = kBarOff + 512 + 1024;
+  static_assert(kRing <= kRingMax, "barrier array");
 };
 
 // The two slots of a CTA: (head, query tile) each, sharing one KV head and key range.
@@ -101,19 +104,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tmKc,
                        const __grid_constant__ CUtensorMap tmVc, AttnParams p) {
   using Lay = AttnLayout<HD>;
+  constexpr int kRing = Lay::kRing;
   if (p.n_active && *p.n_active == 0) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBarOff);
   uint64_t* q_full = bars + 0;
-  uint64_t* kv_full = bars + 1;    // [kRing]
-  uint64_t* kv_empty = bars + 7;   // [kRing]
-  uint64_t* s_full = bars + 13;    // [slot * 2 + buffer]
-  uint64_t* s_free = bars + 17;    // [slot * 2 + buffer]
-  uint64_t* p_full = bars + 21;    // [slot * 2 + buffer]
-  uint64_t* pv_done = bars + 25;   // [slot * 2 + buffer]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 29);
+  uint64_t* kv_full = bars + 1;                  // [kRing]
+  uint64_t* kv_empty = bars + 1 + kRingMax;      // [kRing]
+  uint64_t* s_full = bars + 1 + 2 * kRingMax;    // [slot]
+  uint64_t* p_full = s_full + 2;                 // [slot]
+  uint64_t* pv_done = s_full + 4;                // [slot]
+  uint64_t* drain = s_full + 6;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 7);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -162,12 +166,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    for (int s = 0; s < 4; ++s) {
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&s_full[s], 1);
-      mbar_init(&s_free[s], 128);
       mbar_init(&p_full[s], 128);
       mbar_init(&pv_done[s], 1);
     }
+    mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -179,12 +183,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // TMEM columns: S of (slot s, buffer b) at [(2s + b) * 64, +64); O of slot s at 256 + 128 s
-  auto tm_s = [&](int s, int b) { return tmem + (2 * s + b) * kKTile; };
+  // TMEM columns: S (and P) of slot s at [128 s, +128); O of slot s at 256 + 128 s
+  auto tm_s = [&](int s) { return tmem + s * 128; };
   auto tm_o = [&](int s) { return tmem + 256 + s * 128; };
   auto q_buf = [&](int s) { return smem + Lay::kQOff + s * Lay::kQBytes; };
   auto kv_buf = [&](int i) { return smem + Lay::kKVOff + (i % kRing) * Lay::kKVBytes; };
-  auto p_buf = [&](int s, int b) { return smem + Lay::kPOff + (2 * s + b) * Lay::kPBytes; };
 
   // Register split (each warpgroup changes its budget in its own branch): the control
   // warpgroup (TMA and MMA warps) needs few registers, each softmax thread holds a score row.
@@ -228,28 +231,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto wait_kv = [&](int i) {
         return mbar_wait(&kv_full[i % kRing], (i / kRing) & 1, abort_flag);
       };
-      auto issue_s = [&](int s, int j) {  // S_s(j) = Q_s K_j^T into buffer j & 1
+      auto issue_s = [&](int s, int j) {  // S_s(j) = Q_s K_j^T
         const uint32_t qa = smem_u32(q_buf(s));
         const uint32_t ka = smem_u32(kv_buf(2 * j));
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
-          mma_bf16_ss(tm_s(s, j & 1),
+          mma_bf16_ss(tm_s(s),
                       sdesc_sw128(qa + (kk >> 2) * Lay::kQChunk + (kk & 3) * 32, 16, 1024),
                       sdesc_sw128(ka + (kk >> 2) * Lay::kKVChunk + (kk & 3) * 32, 16, 1024),
                       idesc_s, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&s_full[2 * s + (j & 1)]);
+        mma_commit(&s_full[s]);
       };
-      auto issue_pv = [&](int s, int j) {  // O_s += P_s(j) V_j
-        const uint32_t pa = smem_u32(p_buf(s, j & 1));
+      auto issue_pv = [&](int s, int j) {  // O_s += P_s(j) V_j, P from TMEM (8 columns per 16 keys)
         const uint32_t va = smem_u32(kv_buf(2 * j + 1));
 #pragma unroll
         for (int kk = 0; kk < kKTile / 16; ++kk) {
-          mma_bf16_ss(tm_o(s), sdesc_sw128(pa + kk * 32, 16, 1024),
+          mma_bf16_ts(tm_o(s), tm_s(s) + kk * 8,
                       sdesc_sw128(va + kk * 2048, Lay::kKVChunk, 1024), idesc_o,
                       (j > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&pv_done[2 * s + (j & 1)]);
+        mma_commit(&pv_done[s]);
       };
       // prologue: S of both slots for tile 0, then K_0's ring slot is released
       if (ok) ok = wait_kv(0);
@@ -259,33 +261,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&kv_empty[0]);
       }
       for (int j = 0; ok && j < nt; ++j) {
-        if (j + 1 < nt) {
-          // scores of the next tile into the other buffer, once its previous scores (tile j-1)
-          // have been read
-          if (!(ok = wait_kv(2 * j + 2))) break;
-          for (int s = 0; ok && s < nslots; ++s) {
-            if (j >= 1 && !(ok = mbar_wait(&s_free[2 * s + ((j + 1) & 1)], ((j - 1) >> 1) & 1,
-                                           abort_flag)))
-              break;
-            tc_fence_after();
-            issue_s(s, j + 1);
-          }
-          if (!ok) break;
-          mma_commit(&kv_empty[(2 * j + 2) % kRing]);  // K_{j+1}: read by both S MMAs
-        }
         if (!(ok = wait_kv(2 * j + 1))) break;
-        for (int s = 0; ok && s < nslots; ++s) {
-          if (!(ok = mbar_wait(&p_full[2 * s + (j & 1)], (j >> 1) & 1, abort_flag))) break;
+        const bool next = j + 1 < nt;
+        for (int s = 0; s < nslots; ++s) {
+          if (!(ok = mbar_wait(&p_full[s], j & 1, abort_flag))) break;
           tc_fence_after();
           issue_pv(s, j);
+          if (s == nslots - 1) mma_commit(&kv_empty[(2 * j + 1) % kRing]);  // V_j read
+          if (next) {
+            if (s == 0 && !(ok = wait_kv(2 * j + 2))) break;
+            // S_s(j+1) overwrites the columns P_s(j) occupies: wait until PV_s(j) has read them
+            if (!(ok = mbar_wait(&pv_done[s], j & 1, abort_flag))) break;
+            tc_fence_after();
+            issue_s(s, j + 1);
+            if (s == nslots - 1) mma_commit(&kv_empty[(2 * j + 2) % kRing]);  // K_{j+1} read
+          }
         }
-        if (!ok) break;
-        mma_commit(&kv_empty[(2 * j + 1) % kRing]);  // V_j: read by both PV MMAs
       }
       if (*abort_flag) {  // make sure no MMA is still writing TMEM before it is released
-        mma_commit(&pv_done[0]);
-        mbar_wait_drain(&pv_done[0], 0);
-        mbar_wait_drain(&pv_done[0], 1);
+        mma_commit(drain);
+        mbar_wait_drain(drain, 0);
       }
     }
   } else {
@@ -299,8 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int kmin = p.window > 0 ? p.P + qi - p.window + 1 : 0;
       const float c = p.scale_log2;
       for (int j = 0; j < nt; ++j) {
-        const int b = j & 1;
-        if (!warp_wait(&s_full[2 * slot + b], (j >> 1) & 1, abort_flag)) { ok = false; break; }
+        if (!warp_wait(&s_full[slot], j & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const int t = t_begin + j;
         const bool pre = t < n_pre;
@@ -308,9 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int klim = pre ? p.P : p.L;
         const int klo = pre ? kmin : 0;
         float sv[kKTile];
-        tmem_ld64(tm_s(slot, b) + lane_base, sv);  // the score row in one TMEM round trip
-        tc_fence_before();
-        mbar_arrive(&s_free[2 * slot + b]);  // the MMA warp may reuse this score buffer
+        tmem_ld128(tm_s(slot) + lane_base, sv);  // the score row in one TMEM round trip
         // raw scores; the scale (> 0) is folded into the exponent, so the max is taken on raw
         // values (rounding is monotone)
         if (!(kb >= klo && kb + kKTile <= klim)) {
@@ -334,37 +326,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float f = need ? ex2_approx(m_ref - m_new) : 1.f;
         if (j == 0 || need) m_ref = m_new;
         const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-        // P = exp2(s * c - m), summed with eight partial sums and packed to bf16 pairs
+        // P = exp2(s * c - m), summed with eight partial sums, packed to bf16 pairs and written
+        // over the first 64 score columns, 32 columns (64 keys) at a time
         float ps[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) ps[q] = 0.f;
-        uint32_t pk[kKTile / 2];
 #pragma unroll
-        for (int e = 0; e < kKTile; e += 2) {
-          const float a = ex2_approx(fmaf(sv[e], c, -m_use));
-          const float bb = ex2_approx(fmaf(sv[e + 1], c, -m_use));
-          ps[e & 7] += a;
-          ps[(e + 1) & 7] += bb;
-          pk[e >> 1] = pack_bf16x2(a, bb);
+        for (int h = 0; h < kKTile / 64; ++h) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int e = 0; e < 64; e += 2) {
+            const float a = ex2_approx(fmaf(sv[64 * h + e], c, -m_use));
+            const float bb = ex2_approx(fmaf(sv[64 * h + e + 1], c, -m_use));
+            ps[e & 7] += a;
+            ps[(e + 1) & 7] += bb;
+            pk[e >> 1] = pack_bf16x2(a, bb);
+          }
+          tmem_st32(tm_s(slot) + lane_base + 32 * h, pk);
         }
         const float rs =
             ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-        // P buffer b was last read by PV of tile j - 2
-        if (j >= 2 &&
-            !warp_wait(&pv_done[2 * slot + b], ((j - 2) >> 1) & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        // the 64 keys of this row are one 128-byte row of the swizzled chunk: 16-byte unit u
-        // goes to position u ^ (row % 8)
-        uint8_t* prow = p_buf(slot, b) + row_in * 128;
-#pragma unroll
-        for (int u = 0; u < kKTile / 8; ++u)
-          *reinterpret_cast<uint4*>(prow + ((u ^ (row_in & 7)) * 16)) =
-              make_uint4(pk[u * 4], pk[u * 4 + 1], pk[u * 4 + 2], pk[u * 4 + 3]);
         l = l * f + rs;
         if (__any_sync(0xFFFFFFFFu, need)) {  // O *= f once PV of tile j - 1 has completed
-          if (!warp_wait(&pv_done[2 * slot + ((j - 1) & 1)], ((j - 1) >> 1) & 1, abort_flag)) {
+          if (!warp_wait(&pv_done[slot], (j - 1) & 1, abort_flag)) {
             ok = false;
             break;
           }
@@ -378,12 +362,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32(tm_o(slot) + lane_base + cc * 32, o);
           }
         }
-        fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(&p_full[2 * slot + b]);
+        mbar_arrive(&p_full[slot]);
       }
-      if (ok)
-        ok = warp_wait(&pv_done[2 * slot + ((nt - 1) & 1)], ((nt - 1) >> 1) & 1, abort_flag);
+      if (ok) ok = warp_wait(&pv_done[slot], (nt - 1) & 1, abort_flag);
       tc_fence_after();
       const bool write = ok && qi < p.L;
       if (p.splits == 1) {
