@@ -2,24 +2,28 @@
 //
 // One CTA serves two "slots" that read the same keys and values: the two query heads of a GQA
 // group for one 128-query tile (or, when a group has one query head, two query tiles of that
-// head).  Keys and values come in tiles of 128 keys, staged once for both slots, so every
-// score MMA is M=128 x N=128 (the 128-row MMA costs the same ~45 cycles for any N <= 64, and
-// only reaches full rate from N=128 up).
-//   warp 0       TMA: Q of both slots once, then K_0, V_0, K_1, V_1, ... through a ring of
-//                tiles (five at hd=128);
-//   warp 1       one thread issues, per key tile j and slot s, O_s += P_s(j) V_j with P_s(j)
-//                read straight from TMEM, then -- once that MMA has finished reading P_s(j) --
-//                S_s(j+1) = Q_s K_{j+1}^T into the same TMEM columns;
+// head).  Keys and values come in tiles of 64 keys, staged once for both slots through a deep
+// ring.
+//   warp 0       TMA: Q of both slots once, then K_0, V_0, K_1, V_1, ... (ring of 10 tiles at
+//                hd=128);
+//   warps 1, 2   one thread each issues S_s(j) = Q_s K_j^T (M=128, N=64) of slot s = warp - 1
+//                into one of the slot's two TMEM score buffers;
+//   warp 3       one thread issues O_s += P_s(j) V_j for both slots, with P_s(j) read straight
+//                from TMEM (A operand in tensor memory, V as an MN-major operand);
 //   warps 4..7   softmax of slot 0, warps 8..11 softmax of slot 1: one thread per query row
-//                reads its 128 scores from TMEM, masks, exponentiates against a running
-//                reference max and writes P as bf16 pairs over the first 64 score columns.
-//   (warps 2, 3 only complete the first warpgroup, whose registers go to the softmax warps.)
-// TMEM holds S_0, S_1 (128 columns each, P aliased in their first halves) and O_0, O_1.  The
-// MMA order per tile is PV_0, S_0(next), PV_1, S_1(next): each softmax warpgroup has the other
-// slot's two MMAs to hide behind, and the wait for PV_s before S_s(next) overlaps the other
-// slot's work.  The reference max is only raised when a row's max grows by more than 2^8
-// (log2 units): p <= 256 is exact enough in fp32 accumulation and bf16, and O and l use the
-// same reference, so the result is unchanged while O (in TMEM) is rescaled rarely.
+//                reads its 64 scores from TMEM, masks, exponentiates against a running
+//                reference max and writes P as bf16 pairs over the first 32 columns of the
+//                same score buffer.
+// TMEM: S of (slot s, buffer b) at [(2s + b) * 64, +64), O of slot s at [256 + 128 s, +128).
+// With two score buffers per slot, S_s(j+2) is computed while the softmax of tile j+1 runs, so
+// a slot's softmax warps go from tile to tile without waiting for its P.V or score MMAs; the
+// only ordering is that S_s(j+2) waits for O_s += P_s(j) V_j, which reads the buffer's P.
+// An issuing thread is held in each tcgen05.mma for about the MMA's own duration, so a single
+// issuer leaves the pipe idle during every barrier wait and commit; three issuers with about
+// equal shares (scores of slot 0, scores of slot 1, both P.V) cover each other's waits.
+// The reference max is only raised when a row's max grows by more than 2^8 (log2 units):
+// p <= 256 is exact enough in fp32 accumulation and bf16, and O and l use the same reference,
+// so the result is unchanged while O (in TMEM) is rescaled rarely.
 // With several key splits, each writes unnormalised fp32 partials (O, m, l) and a merge kernel
 // combines them with the log-sum-exp rule.
 #include "kernels.cuh"
@@ -29,13 +33,13 @@ namespace dg {
 namespace {
 
 constexpr int kQTile = 128;  // queries per slot
-constexpr int kKTile = 128;  // keys per tile
+constexpr int kKTile = 64;   // keys per tile
 constexpr float kRescaleLog2 = 8.f;
-constexpr int kRingMax = 10;
+constexpr int kRingMax = 16;
 constexpr int kThreads = 384;      // warpgroup 0: TMA + MMA warps; warpgroups 1, 2: softmax
-constexpr int kRegsControl = 48;   // registers per thread of warpgroup 0 after the split
-constexpr int kRegsSoftmax = 216;  // registers per thread of the softmax warpgroups
-// 128 x 48 + 256 x 216 = 61,440 registers: needs a launch allocation of >= 160 per thread.
+constexpr int kRegsControl = 104;  // registers per thread of warpgroup 0 after the split
+constexpr int kRegsSoftmax = 192;  // registers per thread of the softmax warpgroups
+// 128 x 104 + 256 x 192 = 62,464 registers: needs a launch allocation of >= 163 per thread.
 
 struct AttnParams {
   int B, L, P, H, Hkv, hd, window;
@@ -52,9 +56,9 @@ struct AttnParams {
 
 template <int HD>
 struct AttnLayout {
-  static constexpr int kRing = HD == 128 ? 5 : 10;   // K/V ring slots (K_j and V_j alternate)
+  static constexpr int kRing = HD == 128 ? 10 : 16;  // K/V ring slots (K_j and V_j alternate)
   static constexpr int kQChunk = kQTile * 128;        // [128 rows][64 bf16] swizzled chunk
-  static constexpr int kKVChunk = kKTile * 128;       // [128 keys][64 bf16]
+  static constexpr int kKVChunk = kKTile * 128;       // [64 keys][64 bf16]
   static constexpr int kQBytes = (HD / 64) * kQChunk;    // one slot's Q tile
   static constexpr int kKVBytes = (HD / 64) * kKVChunk;  // one K or V tile
   static constexpr int kQOff = 0;
@@ -96,6 +100,13 @@ __device__ __forceinline__ Slots cta_slots(int u, const AttnParams& p) {
   return s;
 }
 
+// Three-operand maximum (one instruction for two new elements of a running max).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
     canvas_attn_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -113,11 +124,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* q_full = bars + 0;
   uint64_t* kv_full = bars + 1;                  // [kRing]
   uint64_t* kv_empty = bars + 1 + kRingMax;      // [kRing]
-  uint64_t* s_full = bars + 1 + 2 * kRingMax;    // [slot]
-  uint64_t* p_full = s_full + 2;                 // [slot]
-  uint64_t* pv_done = s_full + 4;                // [slot]
-  uint64_t* drain = s_full + 6;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 7);
+  uint64_t* s_full = bars + 1 + 2 * kRingMax;    // [slot * 2 + buffer]
+  uint64_t* p_full = s_full + 4;                 // [slot * 2 + buffer]
+  uint64_t* pv_done = s_full + 8;                // [slot * 2 + buffer]
+  uint64_t* drain = s_full + 12;                 // [issuer]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 15);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -164,14 +175,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(q_full, 1);
     for (int s = 0; s < kRing; ++s) {
       mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&kv_empty[s], (s & 1) ? 1 : nslots);  // K slots: each score thread; V slots: the P.V thread
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < 4; ++s) {
       mbar_init(&s_full[s], 1);
-      mbar_init(&p_full[s], 128);
+      mbar_init(&p_full[s], 4);  // one arrival per softmax warp
       mbar_init(&pv_done[s], 1);
     }
-    mbar_init(drain, 1);
+    for (int s = 0; s < 3; ++s) mbar_init(&drain[s], 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -183,8 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // TMEM columns: S (and P) of slot s at [128 s, +128); O of slot s at 256 + 128 s
-  auto tm_s = [&](int s) { return tmem + s * 128; };
+  auto tm_s = [&](int s, int b) { return tmem + (2 * s + b) * kKTile; };
   auto tm_o = [&](int s) { return tmem + 256 + s * 128; };
   auto q_buf = [&](int s) { return smem + Lay::kQOff + s * Lay::kQBytes; };
   auto kv_buf = [&](int i) { return smem + Lay::kKVOff + (i % kRing) * Lay::kKVBytes; };
@@ -223,64 +233,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = (issued > kRing ? issued - kRing : 0); i < issued; ++i)
           mbar_wait_drain(&kv_full[i % kRing], (i / kRing) & 1);
       }
-    } else if (warp == 1 && lane == 0) {
-      // ---------------------------------------------------------------- MMA issuer -----
+    } else if (lane == 0 && (warp == 3 || warp - 1 < nslots)) {
+      // ------------------------------------------------------------------ MMA issuers -----
+      // warp 1 + s (s < 2): the score MMAs of slot s; warp 3: the P.V MMAs of both slots
       constexpr uint32_t idesc_s = idesc_bf16(128, kKTile, false);
       constexpr uint32_t idesc_o = idesc_bf16(128, HD, true);
       bool ok = mbar_wait(q_full, 0, abort_flag);
       auto wait_kv = [&](int i) {
         return mbar_wait(&kv_full[i % kRing], (i / kRing) & 1, abort_flag);
       };
-      auto issue_s = [&](int s, int j) {  // S_s(j) = Q_s K_j^T
+      if (warp < 3) {
+        const int s = warp - 1;
         const uint32_t qa = smem_u32(q_buf(s));
-        const uint32_t ka = smem_u32(kv_buf(2 * j));
-#pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          mma_bf16_ss(tm_s(s),
-                      sdesc_sw128(qa + (kk >> 2) * Lay::kQChunk + (kk & 3) * 32, 16, 1024),
-                      sdesc_sw128(ka + (kk >> 2) * Lay::kKVChunk + (kk & 3) * 32, 16, 1024),
-                      idesc_s, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&s_full[s]);
-      };
-      auto issue_pv = [&](int s, int j) {  // O_s += P_s(j) V_j, P from TMEM (8 columns per 16 keys)
-        const uint32_t va = smem_u32(kv_buf(2 * j + 1));
-#pragma unroll
-        for (int kk = 0; kk < kKTile / 16; ++kk) {
-          mma_bf16_ts(tm_o(s), tm_s(s) + kk * 8,
-                      sdesc_sw128(va + kk * 2048, Lay::kKVChunk, 1024), idesc_o,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(&pv_done[s]);
-      };
-      // prologue: S of both slots for tile 0, then K_0's ring slot is released
-      if (ok) ok = wait_kv(0);
-      if (ok) {
-        tc_fence_after();
-        for (int s = 0; s < nslots; ++s) issue_s(s, 0);
-        mma_commit(&kv_empty[0]);
-      }
-      for (int j = 0; ok && j < nt; ++j) {
-        if (!(ok = wait_kv(2 * j + 1))) break;
-        const bool next = j + 1 < nt;
-        for (int s = 0; s < nslots; ++s) {
-          if (!(ok = mbar_wait(&p_full[s], j & 1, abort_flag))) break;
+        for (int j = 0; ok && j < nt; ++j) {
+          if (!(ok = wait_kv(2 * j))) break;
+          // S_s(j) overwrites the buffer whose first columns hold P_s(j-2)
+          if (j >= 2 && !(ok = mbar_wait(&pv_done[2 * s + (j & 1)], ((j - 2) >> 1) & 1, abort_flag)))
+            break;
           tc_fence_after();
-          issue_pv(s, j);
-          if (s == nslots - 1) mma_commit(&kv_empty[(2 * j + 1) % kRing]);  // V_j read
-          if (next) {
-            if (s == 0 && !(ok = wait_kv(2 * j + 2))) break;
-            // S_s(j+1) overwrites the columns P_s(j) occupies: wait until PV_s(j) has read them
-            if (!(ok = mbar_wait(&pv_done[s], j & 1, abort_flag))) break;
-            tc_fence_after();
-            issue_s(s, j + 1);
-            if (s == nslots - 1) mma_commit(&kv_empty[(2 * j + 2) % kRing]);  // K_{j+1} read
+          const uint32_t ka = smem_u32(kv_buf(2 * j));
+#pragma unroll
+          for (int kk = 0; kk < HD / 16; ++kk) {
+            mma_bf16_ss(tm_s(s, j & 1),
+                        sdesc_sw128(qa + (kk >> 2) * Lay::kQChunk + (kk & 3) * 32, 16, 1024),
+                        sdesc_sw128(ka + (kk >> 2) * Lay::kKVChunk + (kk & 3) * 32, 16, 1024),
+                        idesc_s, kk > 0 ? 1u : 0u);
           }
+          mma_commit(&s_full[2 * s + (j & 1)]);
+          mma_commit(&kv_empty[(2 * j) % kRing]);  // this slot's read of K_j
+        }
+      } else {
+        for (int j = 0; ok && j < nt; ++j) {
+          if (!(ok = wait_kv(2 * j + 1))) break;
+          const uint32_t va = smem_u32(kv_buf(2 * j + 1));
+          for (int s = 0; ok && s < nslots; ++s) {
+            if (!(ok = mbar_wait(&p_full[2 * s + (j & 1)], (j >> 1) & 1, abort_flag))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < kKTile / 16; ++kk) {
+              mma_bf16_ts(tm_o(s), tm_s(s, j & 1) + kk * 8,
+                          sdesc_sw128(va + kk * 2048, Lay::kKVChunk, 1024), idesc_o,
+                          (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(&pv_done[2 * s + (j & 1)]);
+          }
+          if (!ok) break;
+          mma_commit(&kv_empty[(2 * j + 1) % kRing]);  // V_j read by both slots
         }
       }
       if (*abort_flag) {  // make sure no MMA is still writing TMEM before it is released
-        mma_commit(drain);
-        mbar_wait_drain(drain, 0);
+        mma_commit(&drain[warp - 1]);
+        mbar_wait_drain(&drain[warp - 1], 0);
       }
     }
   } else {
@@ -294,7 +297,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int kmin = p.window > 0 ? p.P + qi - p.window + 1 : 0;
       const float c = p.scale_log2;
       for (int j = 0; j < nt; ++j) {
-        if (!warp_wait(&s_full[slot], j & 1, abort_flag)) { ok = false; break; }
+        const int b = j & 1;
+        if (!warp_wait(&s_full[2 * slot + b], (j >> 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const int t = t_begin + j;
         const bool pre = t < n_pre;
@@ -302,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int klim = pre ? p.P : p.L;
         const int klo = pre ? kmin : 0;
         float sv[kKTile];
-        tmem_ld128(tm_s(slot) + lane_base, sv);  // the score row in one TMEM round trip
+        tmem_ld64(tm_s(slot, b) + lane_base, sv);  // the score row in one TMEM round trip
         // raw scores; the scale (> 0) is folded into the exponent, so the max is taken on raw
         // values (rounding is monotone)
         if (!(kb >= klo && kb + kKTile <= klim)) {
@@ -316,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int q = 0; q < 8; ++q) mx[q] = sv[q];
 #pragma unroll
-        for (int e = 8; e < kKTile; ++e) mx[e & 7] = fmaxf(mx[e & 7], sv[e]);
+        for (int e = 8; e < kKTile; e += 2) mx[(e >> 1) & 7] = fmax3(mx[(e >> 1) & 7], sv[e], sv[e + 1]);
         const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
         const float m_new = fmaxf(m_ref, mt * c);
@@ -327,28 +331,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j == 0 || need) m_ref = m_new;
         const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
         // P = exp2(s * c - m), summed with eight partial sums, packed to bf16 pairs and written
-        // over the first 64 score columns, 32 columns (64 keys) at a time
+        // over the first 32 columns of this score buffer
         float ps[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) ps[q] = 0.f;
+        uint32_t pk[kKTile / 2];
 #pragma unroll
-        for (int h = 0; h < kKTile / 64; ++h) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int e = 0; e < 64; e += 2) {
-            const float a = ex2_approx(fmaf(sv[64 * h + e], c, -m_use));
-            const float bb = ex2_approx(fmaf(sv[64 * h + e + 1], c, -m_use));
-            ps[e & 7] += a;
-            ps[(e + 1) & 7] += bb;
-            pk[e >> 1] = pack_bf16x2(a, bb);
-          }
-          tmem_st32(tm_s(slot) + lane_base + 32 * h, pk);
+        for (int e = 0; e < kKTile; e += 2) {
+          const float a = ex2_approx(fmaf(sv[e], c, -m_use));
+          const float bb = ex2_approx(fmaf(sv[e + 1], c, -m_use));
+          ps[e & 7] += a;
+          ps[(e + 1) & 7] += bb;
+          pk[e >> 1] = pack_bf16x2(a, bb);
         }
+        tmem_st32(tm_s(slot, b) + lane_base, pk);
         const float rs =
             ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
         l = l * f + rs;
         if (__any_sync(0xFFFFFFFFu, need)) {  // O *= f once PV of tile j - 1 has completed
-          if (!warp_wait(&pv_done[slot], (j - 1) & 1, abort_flag)) {
+          if (!warp_wait(&pv_done[2 * slot + ((j - 1) & 1)], ((j - 1) >> 1) & 1, abort_flag)) {
             ok = false;
             break;
           }
@@ -363,9 +364,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(&p_full[slot]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[2 * slot + b]);
       }
-      if (ok) ok = warp_wait(&pv_done[slot], (nt - 1) & 1, abort_flag);
+      if (ok)
+        ok = warp_wait(&pv_done[2 * slot + ((nt - 1) & 1)], ((nt - 1) >> 1) & 1, abort_flag);
       tc_fence_after();
       const bool write = ok && qi < p.L;
       if (p.splits == 1) {
