@@ -147,9 +147,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int n_pre = p.n_pre_tiles - t_lo;
   const int nt_all = n_pre + p.n_can_tiles;
-  const int per = (nt_all + p.splits - 1) / p.splits;
-  const int t_begin = split * per;
-  const int t_end = min(nt_all, t_begin + per);
+  // Even partition: with splits <= nt_all every split gets at least one tile.  (CTAs that
+  // find no work and exit at once were measured to delay the whole launch by ~12 us.)
+  const int t_begin = static_cast<int>(static_cast<int64_t>(split) * nt_all / p.splits);
+  const int t_end = static_cast<int>(static_cast<int64_t>(split + 1) * nt_all / p.splits);
   const int nt = t_end > t_begin ? t_end - t_begin : 0;
 
   // softmax role of this thread (warps 4..11)
@@ -421,7 +422,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Combines split partials: O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.  One warp per
-// (b, h, i) row.
+// (b, h, i) row; lane s holds the (m, l) of splits s and s + 32, so the weights need one load
+// round trip, and the O loads of consecutive splits are independent.
 template <int HD>
 __global__ void attn_merge_kernel(AttnParams p) {
   if (p.n_active && *p.n_active == 0) return;
@@ -429,17 +431,29 @@ __global__ void attn_merge_kernel(AttnParams p) {
   const int64_t row = blockIdx.x * static_cast<int64_t>(blockDim.x / 32) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
-  float M = -INFINITY;
-  for (int s = 0; s < p.splits; ++s) M = fmaxf(M, p.part_ml[(s * rows + row) * 2]);
+  float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
+  if (lane < p.splits) {
+    m0 = p.part_ml[(lane * rows + row) * 2];
+    l0 = p.part_ml[(lane * rows + row) * 2 + 1];
+  }
+  if (lane + 32 < p.splits) {
+    m1 = p.part_ml[((lane + 32) * rows + row) * 2];
+    l1 = p.part_ml[((lane + 32) * rows + row) * 2 + 1];
+  }
+  float M = fmaxf(m0, m1);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+  const float w0 = m0 == -INFINITY ? 0.f : ex2_approx(m0 - M);
+  const float w1 = m1 == -INFINITY ? 0.f : ex2_approx(m1 - M);
+  float l = w0 * l0 + w1 * l1;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, o);
   float acc[HD / 32];
 #pragma unroll
   for (int e = 0; e < HD / 32; ++e) acc[e] = 0.f;
-  float l = 0.f;
+#pragma unroll 4
   for (int s = 0; s < p.splits; ++s) {
-    const float ms = p.part_ml[(s * rows + row) * 2];
-    if (ms == -INFINITY) continue;
-    const float w = ex2_approx(ms - M);
-    l += w * p.part_ml[(s * rows + row) * 2 + 1];
+    const float w = __shfl_sync(0xFFFFFFFFu, s < 32 ? w0 : w1, s & 31);
     const float* po = p.part_o + (s * rows + row) * HD;
 #pragma unroll
     for (int e = 0; e < HD / 32; ++e) acc[e] += w * po[e * 32 + lane];
@@ -504,15 +518,17 @@ AttnPlan plan_attention(int B, int L, int P, int H, int Hkv, int hd, int window)
   const int eff_p = (window > 0 && window < P) ? window + L : P;  // keys a query tile may see
   const int nt_all = (eff_p + kKTile - 1) / kKTile + (L + kKTile - 1) / kKTile;
   const int sms = num_sms();
-  // Minimise waves x tiles-per-split, then prefer fewer splits (less merge traffic).  With
-  // at least one CTA per SM already, keys are not split.
+  // Cost in units of one 64-key tile of a CTA (~0.9 us): waves x (tiles per split + a fixed
+  // ~6 per CTA for start-up, pipeline fill and the partial write), plus ~6 for the merge
+  // kernel when keys are split; ties go to fewer splits.  With at least one CTA per SM
+  // already, keys are not split.
   int best = 1;
   int64_t best_cost = -1;
   for (int s = 1; s <= nt_all && s <= 64 && (s == 1 || units < sms); ++s) {
     const int per = (nt_all + s - 1) / s;
     const int64_t ctas = static_cast<int64_t>(units) * s;
     const int64_t waves = (ctas + sms - 1) / sms;
-    const int64_t cost = waves * (per + 2);  // +2: per-CTA setup, roughly two tiles
+    const int64_t cost = waves * (per + 6) + (s > 1 ? 6 : 0);
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best = s;
