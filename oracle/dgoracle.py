@@ -40,6 +40,19 @@ draw the method makes, so that both implementations see identical random bits:
   noising / canvas init : counter (pos, canvas, 0, 1<<24); word 0 = keep draw, word 1 = token
   Gumbel noise          : counter (v>>2, pos, canvas, (2<<24)|step); vocab v uses word v&3
   Euler jump            : counter (0, pos, canvas, (3<<24)|step); word 0
+  re-noising (entropy-bounded sampler) : counter (pos, canvas, 0, (4<<24)|step); word 0
+
+Entropy-bounded sampler [TR "DiffusionGemma 샘플러"], readings taken where the section is silent:
+  * the entropy of a position is that of the tempered posterior used for sampling at the step,
+    -sum_v p_v log p_v with p = Softmax(z / tau_n);
+  * tau_n = tau_start + (tau_end - tau_start) * n / (T - 1) over steps n = 0..T-1, so the first
+    step uses 0.8 and the last possible step 0.4 (the section's two endpoints);
+  * positions are ordered by (entropy, position); k is the length of the longest prefix of that
+    order whose running float32 sum stays <= gamma (k may be 0); the first k positions take
+    their posterior sample, every other position a fresh uniform token;
+  * a canvas stops after step n when its mean entropy (float32 sum in position order / L) is
+    below the threshold and its top-1 sequence equals that of step n-1; the returned canvas is
+    the top-1 sequence of the last evaluated posterior (also when the cap T is reached).
 """
 
 from __future__ import annotations
@@ -60,6 +73,7 @@ _PHILOX_W1 = np.uint64(0xBB67AE85)
 STREAM_NOISE = 1
 STREAM_GUMBEL = 2
 STREAM_JUMP = 3
+STREAM_RENOISE = 4
 
 SCHED_LINEAR = 0
 SCHED_COSINE = 1
@@ -307,6 +321,7 @@ def posterior(y, E, inv_tau: float, seed: int, step: int, L: int, rows=None, chu
       logp_top1  = z~_top1 - lse
       x0hat      = argmax_v (z~_v + g_v)              (Gumbel-max sample of Softmax(z~))
       logp_x0hat = z~_x0hat - lse
+      entropy    = -sum_v p_v log p_v,  p = Softmax(z~)   (clamped at 0 against rounding)
 
     g_v comes from the Gumbel stream of (step, canvas, position, v).  Also returned, for the
     parity bars: the gap between the two largest perturbed scores and between the two
@@ -322,7 +337,7 @@ def posterior(y, E, inv_tau: float, seed: int, step: int, L: int, rows=None, chu
     k0, k1 = seed_key(seed)
     v = np.arange(V, dtype=np.uint64)
     out = {k: np.zeros(len(rows), np.float64) for k in
-           ("lse", "logp_top1", "logp_x0hat", "gap_perturbed", "gap_logit")}
+           ("lse", "logp_top1", "logp_x0hat", "gap_perturbed", "gap_logit", "entropy")}
     out["top1"] = np.zeros(len(rows), np.int64)
     out["x0hat"] = np.zeros(len(rows), np.int64)
     for s in range(0, len(rows), chunk):
@@ -346,6 +361,8 @@ def posterior(y, E, inv_tau: float, seed: int, step: int, L: int, rows=None, chu
         out["x0hat"][sl] = x0hat
         out["logp_top1"][sl] = z[idx, top1] - lse
         out["logp_x0hat"][sl] = z[idx, x0hat] - lse
+        logp = z - lse[:, None]
+        out["entropy"][sl] = np.maximum(0.0, -(np.exp(logp) * logp).sum(axis=1))
         two = -np.partition(-score, 1, axis=1)[:, :2]
         out["gap_perturbed"][sl] = two[:, 0] - two[:, 1]
         twz = -np.partition(-z, 1, axis=1)[:, :2]
@@ -439,3 +456,136 @@ def denoise_loop(model, k_pre, v_pre, window: int, x, lock, T: int, schedule: in
         if stop_when_all_locked:
             active &= ~done.astype(bool)
     return x, lock, steps
+
+
+# ----------------------------------------------------------------------------------------
+# Entropy-bounded sampler with temperature annealing and adaptive stopping
+# [TR "DiffusionGemma 샘플러": "Entropy-bounded 토큰 정제", "Temperature annealing",
+# "Adaptive stopping"; hyper-parameters T = 48, gamma = 0.1, stop threshold 0.005,
+# tau 0.8 -> 0.4]
+# ----------------------------------------------------------------------------------------
+
+def annealed_temperature(T: int, tau_start: float = 0.8, tau_end: float = 0.4):
+    """tau_n for n = 0..T-1: linear in the step index from tau_start to tau_end."""
+    n = np.arange(T, dtype=np.float64)
+    if T == 1:
+        return np.array([tau_start])
+    return tau_start + (tau_end - tau_start) * n / (T - 1)
+
+
+def entropy_bounded_select(entropy, gamma: float):
+    """Accept positions in increasing (entropy, position) order while the running float32 sum
+    of their entropies stays <= gamma.  entropy: float32 [B, L].  Returns accept (uint8 [B, L])
+    and the accepted count k [B]."""
+    H = np.asarray(entropy, np.float32)
+    B, L = H.shape
+    g = np.float32(gamma)
+    accept = np.zeros((B, L), np.uint8)
+    k = np.zeros(B, np.int64)
+    for b in range(B):
+        order = sorted(range(L), key=lambda i: (H[b, i], i))
+        run = np.float32(0.0)
+        for cnt, i in enumerate(order):
+            run = np.float32(run + H[b, i])
+            if run > g:
+                break
+            accept[b, i] = 1
+            k[b] = cnt + 1
+    return accept, k
+
+
+def renoise_tokens(B: int, L: int, V: int, seed: int, step: int):
+    """A fresh uniform token per position from the re-noising stream of the step."""
+    k0, k1 = seed_key(seed)
+    pos = np.arange(L, dtype=np.uint64)[None, :]
+    canvas = np.arange(B, dtype=np.uint64)[:, None]
+    u, _, _, _ = philox4x32_10(pos, canvas, 0, (STREAM_RENOISE << 24) | int(step), k0, k1)
+    return u32_to_token(u, V)
+
+
+def mean_entropy(entropy):
+    """Per canvas: float32 sum over positions in position order, divided by L in float32."""
+    H = np.asarray(entropy, np.float32)
+    B, L = H.shape
+    out = np.zeros(B, np.float32)
+    for b in range(B):
+        acc = np.float32(0.0)
+        for i in range(L):
+            acc = np.float32(acc + H[b, i])
+        out[b] = np.float32(acc / np.float32(L))
+    return out
+
+
+def entropy_bounded_update(x0hat, top1, entropy, prev_top1, seed: int, step: int, V: int,
+                           gamma: float, stop_entropy: float, final_step: bool = False):
+    """One step of the entropy-bounded sampler on every canvas (arrays [B, L]):
+
+      accepted positions (entropy_bounded_select) -> their posterior sample x0hat
+      all other positions                         -> a fresh uniform token (re-noising)
+      done = mean entropy < stop_entropy  and  top1 == prev_top1 at every position
+             (prev_top1 None: no previous prediction, never done)
+      a canvas that is done, or any canvas at the final step, returns its top-1 sequence.
+
+    Returns x_out, accept (uint8), done (uint8 [B]), mean entropy (float32 [B])."""
+    x0hat = np.asarray(x0hat, np.int64)
+    top1 = np.asarray(top1, np.int64)
+    B, L = x0hat.shape
+    accept, _ = entropy_bounded_select(entropy, gamma)
+    x_out = np.where(accept.astype(bool), x0hat, renoise_tokens(B, L, V, seed, step))
+    mh = mean_entropy(entropy)
+    if prev_top1 is None:
+        stable = np.zeros(B, bool)
+    else:
+        stable = (np.asarray(prev_top1, np.int64) == top1).all(axis=1)
+    done = (mh < np.float32(stop_entropy)) & stable
+    finish = done | bool(final_step)
+    x_out = np.where(finish[:, None], top1, x_out)
+    return x_out, accept, done.astype(np.uint8), mh
+
+
+def eb_denoise_step(model, k_pre, v_pre, window: int, x, n: int, inv_tau: float,
+                    prev_top1, seed: int, gamma: float, stop_entropy: float,
+                    final_step: bool):
+    """logits = Decoder(x_t, KV); p_hat = Softmax(logits / tau_n); entropy-bounded update."""
+    E, H, Hkv, hd = model["E"], model["H"], model["Hkv"], model["hd"]
+    B, L = np.asarray(x).shape
+    h, q, kc, vc = decoder_front(x, E, model["Wqkv"], H, Hkv, hd)
+    O, _ = canvas_attention(q, k_pre, v_pre, kc, vc, window, hd ** -0.5)
+    y = decoder_back(h, O, model["Wo"])
+    post = posterior(y.reshape(B * L, -1), E, inv_tau, seed, n, L)
+    shape = (B, L)
+    x_out, accept, done, mh = entropy_bounded_update(
+        post["x0hat"].reshape(shape), post["top1"].reshape(shape),
+        post["entropy"].reshape(shape).astype(np.float32), prev_top1, seed, n, E.shape[0],
+        gamma, stop_entropy, final_step)
+    return x_out, accept, done, mh, post
+
+
+def eb_inv_tau(T: int, tau_start: float, tau_end: float):
+    """Per-step inverse temperature as handed to the kernels: float32(1 / tau_n)."""
+    return [float(np.float32(1.0 / t)) for t in annealed_temperature(T, tau_start, tau_end)]
+
+
+def eb_denoise_loop(model, k_pre, v_pre, window: int, x, T: int, tau_start: float,
+                    tau_end: float, gamma: float, stop_entropy: float, seed: int):
+    """The entropy-bounded sampler for at most T steps.  Returns the final canvas (the top-1
+    sequence of each canvas's last posterior), the steps taken per canvas and the per-step
+    mean entropies of step 0 (diagnostic)."""
+    x = np.asarray(x, np.int64).copy()
+    B, L = x.shape
+    inv = eb_inv_tau(T, tau_start, tau_end)
+    steps = np.zeros(B, np.int64)
+    active = np.ones(B, bool)
+    prev = None
+    for n in range(T):
+        if not active.any():
+            break
+        x_new, _, done, _, post = eb_denoise_step(model, k_pre, v_pre, window, x, n, inv[n],
+                                                  prev, seed, gamma, stop_entropy, n == T - 1)
+        x[active] = x_new[active]
+        steps[active] += 1
+        top1 = post["top1"].reshape(B, L)
+        prev = top1 if prev is None else np.where(active[:, None], top1, prev)
+        active &= ~done.astype(bool)
+    return x, steps
+

@@ -475,3 +475,144 @@ def test_metrics_match_the_pages():
     assert M.effective_denoising_steps(n, s) == pytest.approx((256 * 12 + 100 * 6) / 356)
     assert M.tokens_per_forward(n, s) == pytest.approx(356 / 19)
     assert M.valid_tokens([5, 7, 1, 9]) == 2 and M.valid_tokens([5, 7]) == 2
+
+
+# ------------------------------------------------------- entropy-bounded sampler -----
+
+def test_posterior_entropy_matches_scipy_and_closed_forms():
+    """Entropy of the tempered posterior: scipy.stats.entropy on random logits, log V for
+    uniform logits, log 4 for four equal dominant logits, and the binary closed form
+    H = -p log p - (1-p) log(1-p) with p = sigmoid(delta / tau)."""
+    V, d, R, L = 300, 300, 24, 8
+    rng = np.random.default_rng(7)
+    E = np.eye(V, d)
+    y = rng.standard_normal((R, d)) * 2.0
+    tau = 0.6
+    post = O.posterior(y, E, 1.0 / tau, seed=1, step=0, L=L)
+    ref = stats.entropy(np.exp((y / tau) - logsumexp(y / tau, axis=1, keepdims=True)), axis=1)
+    assert np.allclose(post["entropy"], ref, atol=1e-10)
+    uni = O.posterior(np.zeros((2, d)), E, 1.0, seed=1, step=0, L=L)
+    assert np.allclose(uni["entropy"], math.log(V), atol=1e-12)
+    four = np.full((1, d), -60.0)
+    four[0, [3, 50, 51, 299]] = 5.0
+    assert abs(O.posterior(four, E, 1.0, seed=1, step=0, L=L)["entropy"][0] - math.log(4)) < 1e-9
+    for delta in (0.0, 0.3, 2.0, 9.0):
+        two = np.full((1, d), -80.0)
+        two[0, 0], two[0, 1] = delta, 0.0
+        p = 1.0 / (1.0 + math.exp(-delta / tau))
+        h = -(p * math.log(p) + (1 - p) * math.log(1 - p))
+        got = O.posterior(two, E, 1.0 / tau, seed=1, step=0, L=L)["entropy"][0]
+        assert abs(got - h) < 1e-9, (delta, got, h)
+
+
+def test_annealed_temperature_endpoints_and_linearity():
+    """0.8 at the first step, 0.4 at the last possible step, equal decrements in between."""
+    for T in (2, 12, 48):
+        tau = O.annealed_temperature(T)
+        assert tau[0] == 0.8 and abs(tau[-1] - 0.4) < 1e-15
+        assert np.allclose(np.diff(tau), -0.4 / (T - 1), atol=1e-15)
+    assert O.annealed_temperature(1)[0] == 0.8
+    inv = O.eb_inv_tau(48, 0.8, 0.4)
+    assert inv[0] == float(np.float32(1.25)) and inv[-1] == float(np.float32(2.5))
+
+
+def test_entropy_bounded_select_hand_examples():
+    """Worked cases: ordering by (entropy, position), a running sum equal to gamma is still
+    accepted, k = 0 when the smallest entropy exceeds gamma, all-zero entropies accept all."""
+    cases = [
+        ([0.05, 0.0, 0.03, 0.04, 0.0], 0.1, [0, 1, 1, 1, 1], 4),
+        ([0.2, 0.3, 0.11], 0.1, [0, 0, 0], 0),
+        ([0.0, 0.0, 0.0, 0.0], 0.1, [1, 1, 1, 1], 4),
+        ([0.05, 0.05, 0.05], 0.1, [1, 1, 0], 2),          # tie broken by position
+        ([0.0625, 0.03125, 0.0625], 0.09375, [1, 1, 0], 2),  # exact dyadic sum == gamma
+        ([0.1, 0.0], 0.1, [1, 1], 2),
+    ]
+    for H, g, want, k in cases:
+        acc, kk = O.entropy_bounded_select(np.array([H], np.float32), g)
+        assert acc[0].tolist() == want and int(kk[0]) == k, (H, g, acc, kk)
+
+
+def test_renoise_stream_is_uniform_and_distinct():
+    """Re-noised tokens are uniform over V (chi-square) and differ from the noising and jump
+    streams of the same counters."""
+    V, B, L = 64, 400, 256
+    tok = O.renoise_tokens(B, L, V, seed=11, step=3)
+    assert stats.chisquare(np.bincount(tok.reshape(-1), minlength=V)).pvalue > 1e-4
+    init = O.initial_canvas(B, L, V, seed=11)
+    assert (tok != init).mean() > 0.9
+    assert (O.renoise_tokens(B, L, V, seed=11, step=4) != tok).mean() > 0.9
+
+
+def test_entropy_bounded_update_decisions():
+    """Accepted positions take x0hat and the rest fresh tokens; done needs both the entropy
+    test and an unchanged top-1 sequence; done canvases and the final step return top-1."""
+    B, L, V = 3, 6, 50
+    x0hat = np.arange(B * L).reshape(B, L) % V
+    top1 = (np.arange(B * L).reshape(B, L) * 7) % V
+    H = np.array([[0.0] * 6, [0.001] * 6, [0.0, 0.5, 0.5, 0.5, 0.5, 0.0]], np.float32)
+    prev = top1.copy()
+    prev[1, 2] += 1  # canvas 1 changed its prediction
+    x_out, acc, done, mh = O.entropy_bounded_update(x0hat, top1, H, prev, 5, 2, V, 0.1, 0.005)
+    assert done.tolist() == [1, 0, 0]
+    assert np.array_equal(x_out[0], top1[0])                      # done -> top-1
+    assert acc[1].tolist() == [1] * 6 and np.array_equal(x_out[1], x0hat[1])
+    rn = O.renoise_tokens(B, L, V, 5, 2)
+    assert acc[2].tolist() == [1, 0, 0, 0, 0, 1]
+    assert np.array_equal(x_out[2], np.where(acc[2] == 1, x0hat[2], rn[2]))
+    assert abs(float(mh[2]) - 2.0 / 6.0) < 1e-7
+    _, _, done0, _ = O.entropy_bounded_update(x0hat, top1, H, None, 5, 2, V, 0.1, 0.005)
+    assert done0.tolist() == [0, 0, 0]                            # no previous prediction
+    xf, _, _, _ = O.entropy_bounded_update(x0hat, top1, H, None, 5, 2, V, 0.1, 0.005, True)
+    assert np.array_equal(xf, top1)                               # final step
+
+
+def _peaked_model(V, d, H, Hkv, hd, scale, seed):
+    rng = np.random.default_rng(seed)
+    E = rng.standard_normal((V, d))
+    E = E / np.linalg.norm(E, axis=1, keepdims=True) * scale
+    E = O.round_bf16(E)
+    Wqkv = O.round_bf16(rng.standard_normal(((H + 2 * Hkv) * hd, d)) * 0.02)
+    Wo = O.round_bf16(rng.standard_normal((d, H * hd)) * 0.02)
+    return {"E": E, "Wqkv": Wqkv, "Wo": Wo, "H": H, "Hkv": Hkv, "hd": hd}
+
+
+def test_entropy_bounded_loop_fixed_point_stops_after_two_steps():
+    """With large, nearly orthogonal embedding rows the posterior at each position is
+    concentrated on the token already there: entropies ~0, every position is accepted with its
+    (identical) sample, the prediction is unchanged at the second step, and the loop stops
+    there returning the initial canvas."""
+    V, d, H, Hkv, hd, B, L, P = 512, 128, 2, 2, 64, 2, 16, 8
+    model = _peaked_model(V, d, H, Hkv, hd, 20.0, 3)
+    rng = np.random.default_rng(4)
+    k_pre = O.round_bf16(rng.standard_normal((B, P, Hkv, hd)))
+    v_pre = O.round_bf16(rng.standard_normal((B, P, Hkv, hd)))
+    x = O.initial_canvas(B, L, V, seed=9)
+    out, steps = O.eb_denoise_loop(model, k_pre, v_pre, 0, x, 48, 0.8, 0.4, 0.1, 0.005, 9)
+    assert steps.tolist() == [2, 2]
+    assert np.array_equal(out, x)
+
+
+def test_entropy_bounded_loop_uninformed_model_runs_to_the_cap():
+    """Near-uniform posteriors (entropy ~ log V > gamma): nothing is accepted, every position is
+    re-noised each step, and the loop runs all T steps, returning the last top-1 sequence."""
+    V, d, H, Hkv, hd, B, L, P, T = 256, 64, 2, 1, 64, 2, 16, 4, 5
+    rng = np.random.default_rng(5)
+    model = {"E": O.round_bf16(rng.standard_normal((V, d)) * 0.02),
+             "Wqkv": O.round_bf16(rng.standard_normal(((H + 2 * Hkv) * hd, d)) * 0.02),
+             "Wo": O.round_bf16(rng.standard_normal((d, H * hd)) * 0.02), "H": H, "Hkv": Hkv, "hd": hd}
+    k_pre = O.round_bf16(rng.standard_normal((B, P, Hkv, hd)))
+    v_pre = O.round_bf16(rng.standard_normal((B, P, Hkv, hd)))
+    x = O.initial_canvas(B, L, V, seed=6)
+    out, steps = O.eb_denoise_loop(model, k_pre, v_pre, 0, x, T, 0.8, 0.4, 0.1, 0.005, 6)
+    assert steps.tolist() == [T, T]
+    # the last step's canvas: re-noised tokens of steps 0..T-2, then top-1 at the last step
+    xs = x.copy()
+    inv = O.eb_inv_tau(T, 0.8, 0.4)
+    for n in range(T - 1):
+        xs, acc, _, _, _ = O.eb_denoise_step(model, k_pre, v_pre, 0, xs, n, inv[n], None, 6,
+                                             0.1, 0.005, False)
+        assert acc.sum() == 0
+        assert np.array_equal(xs, O.renoise_tokens(B, L, V, 6, n))
+    _, _, _, _, post = O.eb_denoise_step(model, k_pre, v_pre, 0, xs, T - 1, inv[T - 1], None, 6,
+                                         0.1, 0.005, True)
+    assert np.array_equal(out, post["top1"].reshape(B, L))
