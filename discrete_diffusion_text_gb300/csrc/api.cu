@@ -218,6 +218,8 @@ struct LoopWs {
   uint16_t *h, *q, *k, *v, *o, *y;
   void* attn;
   VocabPart* parts;
+  int32_t *x0hat, *top1, *prev_top1;  // entropy-bounded sampler
+  float* entropy;
   size_t total;
 };
 
@@ -244,6 +246,10 @@ LoopWs loop_layout(const dg_model* m, int B, int L, int P, int window, uint8_t* 
   w.attn = take(ap.part_bytes > 0 ? ap.part_bytes : 16);
   const VocabPlan vp = plan_vocab(static_cast<int>(BL), m->V);
   w.parts = reinterpret_cast<VocabPart*>(take(vp.part_bytes));
+  w.x0hat = reinterpret_cast<int32_t*>(take(BL * 4));
+  w.top1 = reinterpret_cast<int32_t*>(take(BL * 4));
+  w.prev_top1 = reinterpret_cast<int32_t*>(take(BL * 4));
+  w.entropy = reinterpret_cast<float*>(take(BL * 4));
   w.total = off;
   return w;
 }
@@ -278,7 +284,7 @@ extern "C" {
 
 const char* dg_last_error(void) { return g_last_error.c_str(); }
 
-int dg_abi_version(void) { return 1; }
+int dg_abi_version(void) { return 2; }
 
 dg_status dg_schedule_thresholds(int schedule, int T, uint64_t* keep_thr, uint64_t* jump_thr) {
   if (T < 1) return fail(DG_EINVAL, "schedule: T must be >= 1");
@@ -451,6 +457,7 @@ dg_status dg_vocab_posterior_step(const uint16_t* y, const uint16_t* W, int B, i
     fp.out_logp_top1 = out->logp_top1;
     fp.out_lse = out->lse;
     fp.out_logp_x0hat = out->logp_x0hat;
+    fp.out_entropy = out->entropy;
   }
   fp.x_in = x_in;
   fp.x_out = x_out;
@@ -466,6 +473,42 @@ dg_status dg_vocab_posterior_step(const uint16_t* y, const uint16_t* W, int B, i
   fp.cta_done = counters + B;
   launch_vocab_finalize(fp, B, st);
   return check_launch("vocab finalize launch");
+}
+
+dg_status dg_entropy_bounded_update(const int32_t* x0hat, const int32_t* top1,
+                                    const float* entropy, int32_t* prev_top1, int prev_valid,
+                                    int32_t* x_out, uint8_t* accept, uint8_t* done,
+                                    float* mean_entropy, int B, int L, int V, uint64_t seed,
+                                    int step, float gamma, float stop_entropy, int final_step,
+                                    void* stream) {
+  if (B < 0 || L <= 0 || L > 1024 || V < 1)
+    return fail(DG_EINVAL, "entropy_bounded_update: bad sizes (1 <= L <= 1024, V >= 1)");
+  if (step < 0 || step >= (1 << 24)) return fail(DG_EINVAL, "entropy_bounded_update: bad step");
+  if (std::isnan(gamma) || std::isnan(stop_entropy))
+    return fail(DG_EINVAL, "entropy_bounded_update: NaN threshold");
+  if (B == 0) return DG_OK;
+  if (!x0hat || !top1 || !entropy || !x_out)
+    return fail(DG_EINVAL, "entropy_bounded_update: NULL pointer");
+  EBParams p{};
+  p.x0hat = x0hat;
+  p.top1 = top1;
+  p.entropy = entropy;
+  p.prev_top1 = prev_top1;
+  p.prev_valid = prev_valid;
+  p.x_out = x_out;
+  p.accept = accept;
+  p.done = done;
+  p.mean_out = mean_entropy;
+  p.L = L;
+  p.V = V;
+  p.k0 = static_cast<uint32_t>(seed);
+  p.k1 = static_cast<uint32_t>(seed >> 32);
+  p.step = static_cast<uint32_t>(step);
+  p.gamma = gamma;
+  p.stop_entropy = stop_entropy;
+  p.final_step = final_step;
+  launch_entropy_bounded(p, B, as_stream(stream));
+  return check_launch("entropy_bounded_update launch");
 }
 
 dg_status dg_euler_update(const int32_t* x_in, const int32_t* x0hat, const int32_t* top1,
@@ -509,16 +552,34 @@ dg_status dg_denoise_loop(const dg_model* m, const uint16_t* k_pre, const uint16
   if (s != DG_OK) return s;
   if (!cfg) return fail(DG_EINVAL, "loop: NULL cfg");
   if (cfg->T < 1 || cfg->T >= (1 << 24)) return fail(DG_EINVAL, "loop: T out of range");
-  if (cfg->schedule != DG_SCHED_LINEAR && cfg->schedule != DG_SCHED_COSINE)
+  const bool eb = cfg->sampler == DG_SAMPLER_ENTROPY_BOUNDED;
+  if (!eb && cfg->sampler != DG_SAMPLER_EULER) return fail(DG_EINVAL, "loop: unknown sampler");
+  if (!eb && cfg->schedule != DG_SCHED_LINEAR && cfg->schedule != DG_SCHED_COSINE)
     return fail(DG_EINVAL, "loop: unknown schedule");
-  if (!(cfg->inv_tau > 0.f) || !std::isfinite(cfg->inv_tau)) return fail(DG_EINVAL, "loop: bad inv_tau");
+  if (!eb && (!(cfg->inv_tau > 0.f) || !std::isfinite(cfg->inv_tau)))
+    return fail(DG_EINVAL, "loop: bad inv_tau");
   const int end = cfg->end_step > 0 ? cfg->end_step : cfg->T;
   if (cfg->start_step < 0 || end > cfg->T || cfg->start_step > end)
     return fail(DG_EINVAL, "loop: bad start/end step");
+  std::vector<float> eb_inv_tau;
+  if (eb) {
+    if (cfg->start_step != 0 || end != cfg->T)
+      return fail(DG_ENOTSUP, "loop: the entropy-bounded sampler runs from step 0 to T");
+    if (!(cfg->tau_start > 0.0) || !(cfg->tau_end > 0.0) || !std::isfinite(cfg->tau_start) ||
+        !std::isfinite(cfg->tau_end) || std::isnan(cfg->gamma) || std::isnan(cfg->stop_entropy))
+      return fail(DG_EINVAL, "loop: bad entropy-bounded sampler parameters");
+    for (int n = 0; n < cfg->T; ++n) {
+      const double tau = cfg->T == 1 ? cfg->tau_start
+                                     : cfg->tau_start + (cfg->tau_end - cfg->tau_start) * n /
+                                                            (cfg->T - 1);
+      eb_inv_tau.push_back(static_cast<float>(1.0 / tau));
+    }
+  }
   if (static_cast<int64_t>(B) * L >= (1ll << 31)) return fail(DG_ENOTSUP, "loop: too many rows");
   if (B == 0) return DG_OK;
-  if (bad_ptr(canvas) || bad_ptr(lock) || bad_ptr(steps_taken) || bad_ptr(ws))
+  if (bad_ptr(canvas) || (!eb && bad_ptr(lock)) || bad_ptr(steps_taken) || bad_ptr(ws))
     return fail(DG_EINVAL, "loop: NULL or misaligned canvas/lock/steps/workspace");
+  if (eb) lock = nullptr;
   if (P > 0 && (bad_ptr(k_pre) || bad_ptr(v_pre))) return fail(DG_EINVAL, "loop: bad prefix pointer");
   if (ws_bytes < dg_denoise_loop_workspace(m, B, L, P, window))
     return fail(DG_EINVAL, "loop: workspace too small");
@@ -535,7 +596,8 @@ dg_status dg_denoise_loop(const dg_model* m, const uint16_t* k_pre, const uint16
   cudaError_t e = cudaMemsetAsync(w.n_active, 0, sizeof(int), st);
   if (e == cudaSuccess) e = cudaMemsetAsync(w.counters, 0, 2 * sizeof(int) * B, st);
   if (e != cudaSuccess) return cuda_fail(e, "loop: memset");
-  launch_loop_init(lock, w.active, w.n_active, steps_taken, B, L, cfg->stop_when_all_locked, st);
+  launch_loop_init(lock, w.active, w.n_active, steps_taken, B, L,
+                   eb ? 0 : cfg->stop_when_all_locked, st);
   if ((s = check_launch("loop init launch")) != DG_OK) return s;
 
   GemmOut qkv{};
@@ -569,14 +631,45 @@ dg_status dg_denoise_loop(const dg_model* m, const uint16_t* k_pre, const uint16
     if (e != cudaSuccess) return cuda_fail(e, "loop: attention launch");
     e = launch_gemm(w.o, m->Wo, BL, m->d, Hhd, yo, w.h, m->d, w.status, w.n_active, st);
     if (e != cudaSuccess) return cuda_fail(e, "loop: out_proj gemm launch");
-    e = launch_vocab_pass(w.y, m->E, BL, L, m->d, m->V, cfg->inv_tau, cfg->seed, n, w.parts,
-                          w.status, w.n_active, st);
+    e = launch_vocab_pass(w.y, m->E, BL, L, m->d, m->V, eb ? eb_inv_tau[n] : cfg->inv_tau,
+                          cfg->seed, n, w.parts, w.status, w.n_active, st);
     if (e != cudaSuccess) return cuda_fail(e, "loop: vocab pass launch");
     FinalizeParams fp{};
     fp.parts = w.parts;
     fp.num_mt = vp.num_mt;
     fp.S = vp.S;
     fp.L = L;
+    if (eb) {  // posterior only; the entropy-bounded kernel makes the step
+      fp.out_x0hat = w.x0hat;
+      fp.out_top1 = w.top1;
+      fp.out_entropy = w.entropy;
+      fp.n_active = w.n_active;
+      fp.unlocked = w.counters;
+      fp.cta_done = w.counters + B;
+      launch_vocab_finalize(fp, B, st);
+      if ((s = check_launch("loop: finalize launch")) != DG_OK) return s;
+      EBParams ep{};
+      ep.x0hat = w.x0hat;
+      ep.top1 = w.top1;
+      ep.entropy = w.entropy;
+      ep.prev_top1 = w.prev_top1;
+      ep.prev_valid = n > 0 ? 1 : 0;
+      ep.x_out = canvas;
+      ep.L = L;
+      ep.V = m->V;
+      ep.k0 = static_cast<uint32_t>(cfg->seed);
+      ep.k1 = static_cast<uint32_t>(cfg->seed >> 32);
+      ep.step = static_cast<uint32_t>(n);
+      ep.gamma = cfg->gamma;
+      ep.stop_entropy = cfg->stop_entropy;
+      ep.final_step = n == cfg->T - 1 ? 1 : 0;
+      ep.active = w.active;
+      ep.steps_taken = steps_taken;
+      ep.n_active = w.n_active;
+      launch_entropy_bounded(ep, B, st);
+      if ((s = check_launch("loop: entropy-bounded launch")) != DG_OK) return s;
+      continue;
+    }
     fp.x_in = canvas;
     fp.x_out = canvas;
     fp.lock = lock;

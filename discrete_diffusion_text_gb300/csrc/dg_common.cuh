@@ -77,6 +77,7 @@ __device__ __forceinline__ Words4 philox4x32_10(uint32_t c0, uint32_t c1, uint32
 constexpr uint32_t kStreamNoise = 1u << 24;
 constexpr uint32_t kStreamGumbel = 2u << 24;
 constexpr uint32_t kStreamJump = 3u << 24;
+constexpr uint32_t kStreamRenoise = 4u << 24;
 
 // A draw as a token uniform over [0, V): floor(u * V / 2^32).
 __device__ __forceinline__ int32_t draw_token(uint32_t u, uint32_t V) {
@@ -110,22 +111,33 @@ __device__ __forceinline__ uint32_t jump_draw(uint32_t pos, uint32_t canvas, uin
 
 // ------------------------------------------------- split-vocabulary partial tuple -----
 // What one CTA knows about one row after scanning a contiguous range of the vocabulary:
-// running max m and sum of exp(z - m) of the tempered logits, the top-1 logit and index,
-// and the best Gumbel-perturbed score with its index and logit.  Ties go to the lower index.
+// running max m, s = sum of exp(z - m) and t = sum of exp(z - m) (z - m) of the tempered
+// logits (the entropy of the row is log s - t / s), the top-1 logit and index, and the best
+// Gumbel-perturbed score with its index and logit.  Ties go to the lower index.
 
 struct alignas(16) VocabPart {
   float m, s, top_z, best_score;
   float best_z;
-  int32_t top_idx, best_idx, pad;
+  int32_t top_idx, best_idx;
+  float t;
 };
 
 __device__ __forceinline__ void merge_part(VocabPart& a, const VocabPart& b) {
   const float M = fmaxf(a.m, b.m);
-  float s = 0.f;
-  if (a.m != -INFINITY) s += a.s * __expf(a.m - M);
-  if (b.m != -INFINITY) s += b.s * __expf(b.m - M);
+  float s = 0.f, t = 0.f;
+  if (a.m != -INFINITY) {  // re-reference to M: (z - M) = (z - m_a) + (m_a - M)
+    const float f = __expf(a.m - M);
+    s += a.s * f;
+    t += f * fmaf(a.s, a.m - M, a.t);
+  }
+  if (b.m != -INFINITY) {
+    const float f = __expf(b.m - M);
+    s += b.s * f;
+    t += f * fmaf(b.s, b.m - M, b.t);
+  }
   a.m = M;
   a.s = s;
+  a.t = t;
   if (b.top_z > a.top_z || (b.top_z == a.top_z && b.top_idx < a.top_idx)) {
     a.top_z = b.top_z;
     a.top_idx = b.top_idx;
@@ -147,7 +159,7 @@ __device__ __forceinline__ VocabPart empty_part() {
   p.best_z = -INFINITY;
   p.top_idx = 0x7FFFFFFF;
   p.best_idx = 0x7FFFFFFF;
-  p.pad = 0;
+  p.t = 0.f;
   return p;
 }
 

@@ -116,7 +116,7 @@ __device__ __forceinline__ VocabPart shfl_xor_part(const VocabPart& a, int off) 
   o.best_z = __shfl_xor_sync(0xFFFFFFFFu, a.best_z, off);
   o.top_idx = __shfl_xor_sync(0xFFFFFFFFu, a.top_idx, off);
   o.best_idx = __shfl_xor_sync(0xFFFFFFFFu, a.best_idx, off);
-  o.pad = 0;
+  o.t = __shfl_xor_sync(0xFFFFFFFFu, a.t, off);
   return o;
 }
 
@@ -156,6 +156,8 @@ __global__ void __launch_bounds__(kFinRows * 32) vocab_finalize_kernel(FinalizeP
     if (p.out_logp_top1) p.out_logp_top1[row] = lp_top1;
     if (p.out_lse) p.out_lse[row] = lse;
     if (p.out_logp_x0hat) p.out_logp_x0hat[row] = acc.best_z - lse;
+    // entropy = log s - t / s (both relative to the max), clamped at 0 against rounding
+    if (p.out_entropy) p.out_entropy[row] = fmaxf(0.f, logf(acc.s) - acc.t / acc.s);
     if (p.x_in != nullptr && is_active) {
       const bool was_locked = p.lock != nullptr && p.lock[row] != 0;
       const uint32_t u = jump_draw(static_cast<uint32_t>(i), static_cast<uint32_t>(b), p.step,
@@ -194,6 +196,88 @@ __global__ void __launch_bounds__(kFinRows * 32) vocab_finalize_kernel(FinalizeP
   }
 }
 
+// Entropy-bounded step [TR "DiffusionGemma 샘플러"]: one CTA per canvas, one thread per
+// position.  Each position's rank in (entropy, position) order is counted against the
+// canvas's entropies in shared memory; one thread then forms the running float32 sum in that
+// order and the mean in position order, exactly as the definition states them (no parallel
+// reduction, so the acceptance count and the stop test are bit-reproducible).
+__global__ void __launch_bounds__(1024) entropy_bounded_kernel(EBParams p) {
+  if (p.n_active && *p.n_active == 0) return;
+  const int b = blockIdx.x;
+  if (p.active && p.active[b] == 0) return;  // uniform over the CTA
+  __shared__ float sH[1024];
+  __shared__ float sSorted[1024];
+  __shared__ int s_k;
+  __shared__ float s_mean;
+  const int i = threadIdx.x;
+  const bool valid = i < p.L;
+  const int64_t r = static_cast<int64_t>(b) * p.L + i;
+  const bool have_prev = p.prev_top1 != nullptr && p.prev_valid != 0;
+  float Hi = 0.f;
+  int32_t t1 = 0, prev = 0;
+  if (valid) {
+    Hi = p.entropy[r];
+    sH[i] = Hi;
+    t1 = p.top1[r];
+    if (have_prev) prev = p.prev_top1[r];
+  }
+  __syncthreads();
+  int rank = 0;
+  if (valid) {
+    for (int j = 0; j < p.L; ++j) {
+      const float Hj = sH[j];
+      rank += (Hj < Hi || (Hj == Hi && j < i)) ? 1 : 0;
+    }
+    sSorted[rank] = Hi;
+  }
+  const int all_same = __syncthreads_and((!valid || (have_prev && prev == t1)) ? 1 : 0);
+  if (i == 0) {
+    float run = 0.f;
+    int k = 0;
+    for (int j = 0; j < p.L; ++j) {
+      run = __fadd_rn(run, sSorted[j]);
+      if (run > p.gamma) break;
+      k = j + 1;
+    }
+    float acc = 0.f;
+    for (int j = 0; j < p.L; ++j) acc = __fadd_rn(acc, sH[j]);
+    s_k = k;
+    s_mean = __fdiv_rn(acc, static_cast<float>(p.L));
+  }
+  __syncthreads();
+  const bool done = s_mean < p.stop_entropy && have_prev && all_same != 0;
+  if (valid) {
+    const bool acc_i = rank < s_k;
+    int32_t x;
+    if (done || p.final_step) {
+      x = t1;
+    } else if (acc_i) {
+      x = p.x0hat[r];
+    } else {
+      const uint32_t u = philox4x32_10(static_cast<uint32_t>(i), static_cast<uint32_t>(b), 0u,
+                                       kStreamRenoise | p.step, p.k0, p.k1).x;
+      x = draw_token(u, static_cast<uint32_t>(p.V));
+    }
+    p.x_out[r] = x;
+    if (p.accept) p.accept[r] = acc_i ? 1 : 0;
+    if (p.prev_top1) p.prev_top1[r] = t1;
+  }
+  if (i == 0) {
+    if (p.done) p.done[b] = done ? 1 : 0;
+    if (p.mean_out) p.mean_out[b] = s_mean;
+    if (p.steps_taken) p.steps_taken[b] += 1;
+    if (p.active && done) {
+      p.active[b] = 0;
+      if (p.n_active) atomicSub(p.n_active, 1);
+    }
+  }
+}
+
+void launch_entropy_bounded(const EBParams& p, int B, cudaStream_t st) {
+  const int threads = (p.L + 31) / 32 * 32;
+  entropy_bounded_kernel<<<B, threads, 0, st>>>(p);
+}
+
 void launch_vocab_finalize(const FinalizeParams& p, int B, cudaStream_t st) {
   const int rows = B * p.L;
   vocab_finalize_kernel<<<rows / kFinRows, kFinRows * 32, 0, st>>>(p);
@@ -204,9 +288,9 @@ void launch_vocab_finalize(const FinalizeParams& p, int B, cudaStream_t st) {
 __global__ void loop_init_kernel(const uint8_t* lock, uint8_t* active, int* n_active,
                                  int32_t* steps_taken, int L, int stop_when_all_locked) {
   const int b = blockIdx.x;
-  bool locked = true;
-  for (int i = threadIdx.x; i < L; i += blockDim.x)
-    locked = locked && lock[static_cast<int64_t>(b) * L + i] != 0;
+  bool locked = lock != nullptr;  // no lock state: nothing is locked
+  for (int i = threadIdx.x; locked && i < L; i += blockDim.x)
+    locked = lock[static_cast<int64_t>(b) * L + i] != 0;
   const int all = __syncthreads_and(locked ? 1 : 0);
   if (threadIdx.x == 0) {
     const bool act = !(stop_when_all_locked && all);

@@ -13,6 +13,7 @@ struct FinalizeParams {
   float* out_logp_top1;
   float* out_lse;
   float* out_logp_x0hat;
+  float* out_entropy;
   const int32_t* x_in;  // NULL: posterior only
   int32_t* x_out;
   uint8_t* lock;
@@ -28,6 +29,27 @@ struct FinalizeParams {
   int* unlocked;  // [B] per-canvas counters, zero before the first call; reset by the kernel
   int* cta_done;  // [B]
 };
+
+// One step of the entropy-bounded sampler for every canvas (one CTA per canvas).
+struct EBParams {
+  const int32_t* x0hat;
+  const int32_t* top1;
+  const float* entropy;
+  int32_t* prev_top1;  // NULL: no previous prediction
+  int prev_valid;
+  int32_t* x_out;
+  uint8_t* accept;
+  uint8_t* done;
+  float* mean_out;
+  int L, V;
+  uint32_t k0, k1, step;
+  float gamma, stop_entropy;
+  int final_step;
+  uint8_t* active;       // loop only
+  int32_t* steps_taken;  // loop only
+  int* n_active;         // loop only
+};
+void launch_entropy_bounded(const EBParams& p, int B, cudaStream_t st);
 
 void launch_forward_noise(const int32_t* x0, int32_t* xt, const uint64_t* keep_thr, int B, int L,
                           int V, uint64_t seed, cudaStream_t st);

@@ -101,6 +101,7 @@ extern "C" dg_status dg_vocab_posterior_step_noalloc(
     fp.out_logp_top1 = out->logp_top1;
     fp.out_lse = out->lse;
     fp.out_logp_x0hat = out->logp_x0hat;
+    fp.out_entropy = out->entropy;
   }
   fp.x_in = x_in;
   fp.x_out = x_out;

@@ -59,6 +59,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 struct RowState {
   float m;       // running max of z~ (natural units)
   float s;       // sum of exp(z~ - m)
+  float t;       // sum of exp(z~ - m) * (z~ - m): entropy = log s - t / s
   float top_z;
   int top_idx;
   float best;    // best perturbed score z~ + g
@@ -128,14 +129,17 @@ __device__ __forceinline__ void process_chunk(RowState& st, const float (&z)[32]
     st.top_idx = vbase + __ffs(eq) - 1;
   }
   if (cm > st.m) {
-    st.s *= ex2_approx((st.m - cm) * kLog2e);
+    const float f = ex2_approx((st.m - cm) * kLog2e);
+    st.t = st.s > 0.f ? f * fmaf(st.s, st.m - cm, st.t) : 0.f;  // re-reference (z~ - m)
+    st.s *= f;
     st.m = cm;
     refresh_cthr(st);
   }
   const float scale = inv_tau * kLog2e;
   const float mlog2 = st.m * kLog2e;
   const float cthr = st.cthr;
-  float ps[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums
+  float ps[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums of exp(z~ - m)
+  float pt[4] = {0.f, 0.f, 0.f, 0.f};  // and of exp(z~ - m) (z~ - m) log2(e)
   uint32_t cand = 0;
 #pragma unroll
   for (int g4 = 0; g4 < 8; ++g4) {
@@ -144,13 +148,16 @@ __device__ __forceinline__ void process_chunk(RowState& st, const float (&z)[32]
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int e = g4 * 4 + q;
-      const float pe = ex2_approx(fmaf(z[e], scale, -mlog2));
+      const float a = fmaf(z[e], scale, -mlog2);  // (z~ - m) log2(e)
+      const float pe = ex2_approx(a);
       ps[q] += pe;
+      pt[q] = fmaf(pe, a, pt[q]);
       const float X = __uint_as_float(0x3F800000u | (u[q] >> 9));
       if (X <= fmaf(pe, cthr, 1.0f)) cand |= 1u << e;
     }
   }
   st.s += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+  st.t += ((pt[0] + pt[1]) + (pt[2] + pt[3])) * 0.6931471805599453f;
   if (cand) {
     Best b{st.best, st.best_idx, st.best_z};
     do {  // candidates in increasing vocabulary order
@@ -295,6 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       RowState st;
       st.m = -INFINITY;
       st.s = 0.f;
+      st.t = 0.f;
       st.top_z = -INFINITY;
       st.top_idx = 0x7FFFFFFF;
       st.best = -INFINITY;
@@ -327,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mine.best_score = st.best;
       mine.best_idx = st.best_idx;
       mine.best_z = st.best_z;
-      mine.pad = 0;
+      mine.t = st.t;
       named_bar_sync(1, kEpiThreads);
       if (grp > 0) scratch[(grp - 1) * kBM + row_in] = mine;
       named_bar_sync(1, kEpiThreads);

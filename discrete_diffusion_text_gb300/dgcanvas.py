@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(_HERE, "libdgcanvas.so")
 
 DG_OK, DG_EINVAL, DG_ENOTSUP, DG_ECUDA, DG_EKERNEL, DG_ETIMEOUT = range(6)
 DG_SCHED_LINEAR, DG_SCHED_COSINE = 0, 1
+DG_SAMPLER_EULER, DG_SAMPLER_ENTROPY_BOUNDED = 0, 1
 _STATUS_NAMES = {0: "DG_OK", 1: "DG_EINVAL", 2: "DG_ENOTSUP", 3: "DG_ECUDA", 4: "DG_EKERNEL",
                  5: "DG_ETIMEOUT"}
 
@@ -28,6 +29,7 @@ _P = ctypes.c_void_p
 _I = ctypes.c_int
 _U64 = ctypes.c_uint64
 _F = ctypes.c_float
+_D = ctypes.c_double
 _SZ = ctypes.c_size_t
 
 
@@ -45,12 +47,16 @@ class dg_model(ctypes.Structure):
 class dg_sampler_cfg(ctypes.Structure):
     _fields_ = [("T", _I), ("schedule", _I), ("inv_tau", _F), ("lock_logthr", _F),
                 ("seed", _U64), ("start_step", _I), ("end_step", _I),
-                ("stop_when_all_locked", _I)]
+                ("stop_when_all_locked", _I), ("sampler", _I), ("tau_start", _D),
+                ("tau_end", _D), ("gamma", _F), ("stop_entropy", _F)]
 
 
 class dg_posterior_out(ctypes.Structure):
     _fields_ = [("x0hat", _P), ("top1", _P), ("logp_top1", _P), ("lse", _P),
-                ("logp_x0hat", _P)]
+                ("logp_x0hat", _P), ("entropy", _P)]
+
+
+_POST_FIELDS = ("x0hat", "top1", "logp_top1", "lse", "logp_x0hat", "entropy")
 
 
 SIGNATURES = {
@@ -70,6 +76,8 @@ SIGNATURES = {
     "dg_vocab_posterior_step_noalloc": (_I, [_P, _P, _I, _I, _I, _I, _F, _U64, _I, _P, _P, _P,
                                              _P, _P, _U64, _F, _P, _P]),
     "dg_euler_update": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _U64, _I, _U64, _F, _P]),
+    "dg_entropy_bounded_update": (_I, [_P, _P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _U64, _I,
+                                       _F, _F, _I, _P]),
     "dg_denoise_loop_workspace": (_SZ, [_P, _I, _I, _I, _I]),
     "dg_denoise_loop_kernel_count": (_I, [_P, _I, _I, _I, _I, _I]),
     "dg_denoise_loop": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -211,16 +219,13 @@ def dg_vocab_posterior_step(y, W, B: int, L: int, inv_tau: float, seed: int, ste
                             ws=None, stream=None):
     """y [B*L, d] bf16; W [V, d] bf16; x_in/x_out int32 [B*L] or None; lock/jump uint8 [B*L];
     done uint8 [B]; out: dict with optional int32/fp32 [B*L] tensors x0hat, top1, logp_top1,
-    lse, logp_x0hat."""
+    lse, logp_x0hat, entropy."""
     _bf16(y, "y")
     _bf16(W, "W")
     V, d = W.shape
     po = None
-    keep = []
     if out is not None:
-        po = dg_posterior_out(*(_ptr(out.get(k)) for k in
-                                ("x0hat", "top1", "logp_top1", "lse", "logp_x0hat")))
-        keep.append(po)
+        po = dg_posterior_out(*(_ptr(out.get(k)) for k in _POST_FIELDS))
     _check(load().dg_vocab_posterior_step(
         _ptr(y), _ptr(W), B, L, d, V, inv_tau, seed, step, _ptr(x_in), _ptr(x_out), _ptr(lock),
         _ptr(jump), _ptr(done), jump_thr, lock_logthr,
@@ -239,8 +244,7 @@ def dg_vocab_posterior_step_noalloc(y, W, B: int, L: int, inv_tau: float, seed: 
     V, d = W.shape
     po = None
     if out is not None:
-        po = dg_posterior_out(*(_ptr(out.get(k)) for k in
-                                ("x0hat", "top1", "logp_top1", "lse", "logp_x0hat")))
+        po = dg_posterior_out(*(_ptr(out.get(k)) for k in _POST_FIELDS))
     _check(load().dg_vocab_posterior_step_noalloc(
         _ptr(y), _ptr(W), B, L, d, V, inv_tau, seed, step, _ptr(x_in), _ptr(x_out), _ptr(lock),
         _ptr(jump), _ptr(done), jump_thr, lock_logthr,
@@ -257,6 +261,19 @@ def dg_euler_update(x_in, x0hat, top1, logp_top1, x_out, lock, jump, done, seed:
            "dg_euler_update")
 
 
+def dg_entropy_bounded_update(x0hat, top1, entropy, x_out, seed: int, step: int, V: int,
+                              gamma: float, stop_entropy: float, prev_top1=None,
+                              prev_valid: bool = True, accept=None, done=None,
+                              mean_entropy=None, final_step: bool = False, stream=None):
+    """x0hat, top1, x_out, prev_top1 int32 [B, L]; entropy fp32 [B, L]; accept uint8 [B, L];
+    done uint8 [B]; mean_entropy fp32 [B]."""
+    B, L = x0hat.shape
+    _check(load().dg_entropy_bounded_update(
+        _ptr(x0hat), _ptr(top1), _ptr(entropy), _ptr(prev_top1), 1 if prev_valid else 0,
+        _ptr(x_out), _ptr(accept), _ptr(done), _ptr(mean_entropy), B, L, V, seed, step, gamma,
+        stop_entropy, 1 if final_step else 0, _stream(stream)), "dg_entropy_bounded_update")
+
+
 def make_model(E, Wqkv, Wo, H: int, Hkv: int, hd: int) -> dg_model:
     for t, n in ((E, "E"), (Wqkv, "Wqkv"), (Wo, "Wo")):
         _bf16(t, n)
@@ -268,9 +285,12 @@ def make_model(E, Wqkv, Wo, H: int, Hkv: int, hd: int) -> dg_model:
 
 def make_cfg(T: int, schedule: int, inv_tau: float = 1.0, lock_logthr: float = math.inf,
              seed: int = 0, start_step: int = 0, end_step: int = 0,
-             stop_when_all_locked: bool = False) -> dg_sampler_cfg:
+             stop_when_all_locked: bool = False, sampler: int = DG_SAMPLER_EULER,
+             tau_start: float = 0.8, tau_end: float = 0.4, gamma: float = 0.1,
+             stop_entropy: float = 0.005) -> dg_sampler_cfg:
     return dg_sampler_cfg(T, schedule, inv_tau, lock_logthr, seed, start_step, end_step,
-                          1 if stop_when_all_locked else 0)
+                          1 if stop_when_all_locked else 0, sampler, tau_start, tau_end, gamma,
+                          stop_entropy)
 
 
 def dg_denoise_loop_workspace(m: dg_model, B, L, P, window) -> int:
@@ -283,9 +303,11 @@ def dg_denoise_loop_kernel_count(m: dg_model, B, L, P, window, steps) -> int:
 
 def dg_denoise_loop(m: dg_model, k_pre, v_pre, window: int, canvas, lock, steps_taken,
                     cfg: dg_sampler_cfg, ws, stream=None):
-    """canvas int32 [B, L] (in/out); lock uint8 [B, L] (in/out); steps_taken int32 [B] (out)."""
+    """canvas int32 [B, L] (in/out); lock uint8 [B, L] (in/out; may be None with the
+    entropy-bounded sampler); steps_taken int32 [B] (out)."""
     _dev(canvas, torch.int32, "canvas")
-    _dev(lock, torch.uint8, "lock")
+    if lock is not None:
+        _dev(lock, torch.uint8, "lock")
     _dev(steps_taken, torch.int32, "steps_taken")
     B, L = canvas.shape
     P = k_pre.shape[1]

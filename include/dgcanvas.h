@@ -149,6 +149,9 @@ dg_status dg_out_proj(const uint16_t* h, const uint16_t* O, const uint16_t* Wo, 
  *     top1       = argmax_v z~_v (lowest index on ties);   logp_top1 = z~_top1 - lse
  *     x0hat      = argmax_v (z~_v + g_v)  (Gumbel-max sample; g from the Gumbel stream at `step`;
  *                  lowest index on ties);                  logp_x0hat = z~_x0hat - lse
+ *     entropy    = -sum_v p_v log p_v of p = Softmax(z~) [TR "DiffusionGemma 샘플러"], accumulated
+ *                  online in the same pass (log s - t / s with s = sum exp(z~ - m),
+ *                  t = sum exp(z~ - m) (z~ - m)), clamped at 0
  * and, when x_in != NULL, the Euler step of dg_euler_update at `step`.  No [rows, V] logit
  * tensor is written to memory.
  *
@@ -166,6 +169,7 @@ typedef struct {
   float* logp_top1;
   float* lse;
   float* logp_x0hat;
+  float* entropy; /* -sum_v p_v log p_v of Softmax(z~), clamped at 0 */
 } dg_posterior_out;
 
 size_t dg_vocab_posterior_workspace(int B, int L, int V);
@@ -220,6 +224,30 @@ dg_status dg_euler_update(const int32_t* x_in, const int32_t* x0hat, const int32
                           uint8_t* done, int B, int L, uint64_t seed, int step, uint64_t jump_thr,
                           float lock_logthr, void* stream);
 
+/* ------------------------------------------------------ entropy-bounded update ----
+ * One step of the entropy-bounded sampler [TR "DiffusionGemma 샘플러": "Entropy-bounded 토큰
+ * 정제", "Adaptive stopping"], per canvas b:
+ *   - positions taken in increasing (entropy, position) order are accepted while the running
+ *     float32 sum of their entropies stays <= gamma (possibly none); accepted positions take
+ *     x0hat, every other position a fresh uniform token (Philox counter (pos, canvas, 0,
+ *     4<<24 | step), word 0, mapped to [0, V) by multiply-shift);
+ *   - done[b] = mean entropy < stop_entropy, and prev_top1 != NULL with prev_valid != 0 and
+ *     top1 == prev_top1 at every position; the mean is the float32 sum in position order,
+ *     divided by L;
+ *   - when done[b], or when final_step != 0, the canvas's x_out is its top1 sequence instead;
+ *   - prev_top1 (when not NULL) is overwritten with top1 for the next step.
+ *
+ *   x0hat, top1 [B, L] int32; entropy [B, L] fp32; prev_top1 [B, L] int32 in/out or NULL;
+ *   x_out [B, L] int32 (may alias x0hat or top1); accept [B, L] uint8 out or NULL; done [B]
+ *   uint8 out or NULL; mean_entropy [B] fp32 out or NULL.  Limits: 1 <= L <= 1024, V >= 1.
+ */
+dg_status dg_entropy_bounded_update(const int32_t* x0hat, const int32_t* top1,
+                                    const float* entropy, int32_t* prev_top1, int prev_valid,
+                                    int32_t* x_out, uint8_t* accept, uint8_t* done,
+                                    float* mean_entropy, int B, int L, int V, uint64_t seed,
+                                    int step, float gamma, float stop_entropy, int final_step,
+                                    void* stream);
+
 /* -------------------------------------------------------------------- denoising loop ----
  * Steps n = start_step .. end_step-1 of at most T [TR "디노이징 반복과 self-conditioning";
  * "DiffusionGemma 샘플러": cap T] of
@@ -229,6 +257,10 @@ dg_status dg_euler_update(const int32_t* x_in, const int32_t* x0hat, const int32
  * 제거"].  When stop_when_all_locked is set, a canvas whose positions are all locked stops
  * (its later steps are skipped), and once every canvas has stopped the remaining kernels
  * return at once.
+ * With cfg->sampler = DG_SAMPLER_ENTROPY_BOUNDED the step is instead the posterior at the
+ * annealed temperature tau_n followed by dg_entropy_bounded_update; a canvas stops at the first
+ * step whose stop test holds, and every canvas ends holding its last top-1 sequence (lock is
+ * not used and may be NULL; the run must start at step 0 and cover all T steps).
  *
  *   m: device pointers to the weights (E [V, d] also serves as the LM head) and the sizes;
  *   k_pre, v_pre [B, P, Hkv, hd]; canvas [B, L] int32 in: x_1 (or the state at start_step),
@@ -243,15 +275,26 @@ typedef struct {
   int V, d, H, Hkv, hd;
 } dg_model;
 
+typedef enum {
+  DG_SAMPLER_EULER = 0,           /* Euler step with optional locking (the fields above) */
+  DG_SAMPLER_ENTROPY_BOUNDED = 1  /* entropy-bounded sampler with annealing and stopping */
+} dg_sampler;
+
 typedef struct {
-  int T;                    /* number of steps of the schedule (h = 1/T) */
-  int schedule;             /* dg_schedule */
-  float inv_tau;            /* 1 / temperature */
-  float lock_logthr;        /* log(theta) as float; +INFINITY disables locking */
+  int T;                    /* number of steps of the schedule (h = 1/T); the cap for EB */
+  int schedule;             /* dg_schedule (Euler) */
+  float inv_tau;            /* 1 / temperature (Euler) */
+  float lock_logthr;        /* log(theta) as float; +INFINITY disables locking (Euler) */
   uint64_t seed;
-  int start_step;           /* first step to run (resume) */
+  int start_step;           /* first step to run (resume; 0 for the entropy-bounded sampler) */
   int end_step;             /* one past the last step to run; <= 0 means T */
-  int stop_when_all_locked; /* nonzero: a fully locked canvas stops */
+  int stop_when_all_locked; /* nonzero: a fully locked canvas stops (Euler) */
+  int sampler;              /* dg_sampler */
+  double tau_start;         /* entropy-bounded: temperature of step 0 ... */
+  double tau_end;           /* ... and of step T-1; tau_n = tau_start + (tau_end - tau_start) * n
+                               / (T - 1) in double, handed to the kernels as float(1 / tau_n) */
+  float gamma;              /* entropy budget of the accepted positions */
+  float stop_entropy;       /* adaptive-stopping threshold on the mean entropy */
 } dg_sampler_cfg;
 
 size_t dg_denoise_loop_workspace(const dg_model* m, int B, int L, int P, int window);
