@@ -43,6 +43,9 @@ def parse():
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sampler", default="euler", choices=["euler", "eb"],
+                    help="euler: the workload's Euler step; eb: entropy-bounded sampler with "
+                         "annealing 0.8->0.4, gamma 0.1, stop at mean entropy 0.005, cap T")
     return ap.parse_args()
 
 
@@ -222,14 +225,20 @@ def run_ours(args, w):
     steps_taken = torch.zeros(B, dtype=torch.int32, device=dev)
     keep0 = torch.zeros(B, dtype=torch.int64, device=dev)
     stream = torch.cuda.current_stream(dev)
+    eb = args.sampler == "eb"
+
+    def make_cfg(seed):
+        if eb:
+            return dgc.make_cfg(w.T, w.schedule, seed=seed, sampler=dgc.DG_SAMPLER_ENTROPY_BOUNDED,
+                                tau_start=0.8, tau_end=0.4, gamma=0.1, stop_entropy=0.005)
+        return dgc.make_cfg(w.T, w.schedule, w.inv_tau, lock_thr, seed,
+                            stop_when_all_locked=w.stop_when_all_locked)
 
     def step(i):
         seed = replicas.replica_seed(w.seed, rank, i)
         dgc.dg_forward_noise(canvas, canvas, keep0, w.V, seed)        # x_1: uniform prior
         lock.zero_()
-        cfg = dgc.make_cfg(w.T, w.schedule, w.inv_tau, lock_thr, seed,
-                           stop_when_all_locked=w.stop_when_all_locked)
-        dgc.dg_denoise_loop(model, kp, vp, w.window, canvas, lock, steps_taken, cfg, ws)
+        dgc.dg_denoise_loop(model, kp, vp, w.window, canvas, lock, steps_taken, make_cfg(seed), ws)
 
     for i in range(args.warmup):
         step(i)
@@ -280,9 +289,8 @@ def run_ours(args, w):
         seed = replicas.replica_seed(w.seed, rank, 7777 + i)
         dgc.dg_forward_noise(canvas, canvas, keep0, w.V, seed)
         lock.zero_()
-        cfg = dgc.make_cfg(w.T, w.schedule, w.inv_tau, lock_thr, seed,
-                           stop_when_all_locked=w.stop_when_all_locked)
-        dgc.dg_denoise_loop(model, kp_d, vp_d, w.window, canvas, lock, steps_taken, cfg, ws)
+        dgc.dg_denoise_loop(model, kp_d, vp_d, w.window, canvas, lock, steps_taken, make_cfg(seed),
+                            ws)
         out_h.copy_(canvas, non_blocking=True)
         st_h.copy_(steps_taken, non_blocking=True)
 
@@ -314,8 +322,9 @@ def run_ours(args, w):
                 "launches": vocab_n, "avg_ms": vocab_avg_s * 1000.0,
                 "hbm_frac": (2.0 * w.V * w.d + 2.0 * B * w.L * w.d) / vocab_avg_s / 1e9 / hbm,
                 "attention_avg_ms": attn_ms / max(attn_n, 1)}
+    # the entropy-bounded sampler launches one more kernel (its update) per denoising step
     launches = args.steps * (1 + dgc.dg_denoise_loop_kernel_count(model, B, w.L, w.P, w.window,
-                                                                  w.T))
+                                                                  w.T) + (w.T if eb else 0))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -332,7 +341,10 @@ def run_ours(args, w):
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16", "data": "synthetic (seeded N(0,0.02) weights, N(0,1) prefix KV, "
                                          "uniform-prior canvases)",
-                "config": {"workload": w.describe(), "global_batch": B * world, "seq_len": w.L,
+                "config": {"workload": w.describe() + (
+                               "; entropy-bounded sampler (tau 0.8->0.4, gamma 0.1, stop at mean "
+                               "entropy 0.005, cap T)" if eb else ""),
+                           "global_batch": B * world, "seq_len": w.L,
                            "prefix": w.P, "denoise_steps": w.T,
                            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                            "l2": "inputs larger than L2: the 1 GiB LM-head weight and the prefix "
