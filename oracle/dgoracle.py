@@ -589,3 +589,43 @@ def eb_denoise_loop(model, k_pre, v_pre, window: int, x, T: int, tau_start: floa
         active &= ~done.astype(bool)
     return x, steps
 
+
+
+# ----------------------------------------------------------------------------------------
+# Fused SFT cross-entropy on noised canvases [TR "1단계: Supervised Finetuning":
+# canvases noised at t ~ Unif[0, 1] (each token replaced by a uniform draw with probability t),
+# loss L = - sum_i log p_theta(x_0^i | x_t, c)]
+# ----------------------------------------------------------------------------------------
+
+def cross_entropy(y, E, inv_tau: float, targets, chunk=None):
+    """Per row r of y [R, d] (logits z = y E^T, tempered z~ = z * inv_tau):
+    loss_r = -log Softmax(z~)[target_r] = lse_r - z~_r[target_r].  Returns (loss, lse)."""
+    y = np.asarray(y, np.float64)
+    E64 = np.asarray(E, np.float64)
+    tgt = np.asarray(targets, np.int64)
+    R, V = y.shape[0], E64.shape[0]
+    if chunk is None:
+        chunk = max(1, (1 << 24) // V)
+    loss = np.zeros(R)
+    lse = np.zeros(R)
+    for s in range(0, R, chunk):
+        z = (y[s:s + chunk] @ E64.T) * inv_tau
+        m = z.max(axis=1, keepdims=True)
+        l = (m + np.log(np.exp(z - m).sum(axis=1, keepdims=True)))[:, 0]
+        lse[s:s + chunk] = l
+        loss[s:s + chunk] = l - z[np.arange(len(l)), tgt[s:s + chunk]]
+    return loss, lse
+
+
+def sft_loss(model, k_pre, v_pre, window: int, x0, keep_thr, seed: int, inv_tau: float = 1.0):
+    """Noise x0 [B, L] with per-canvas keep thresholds (forward process), run the stand-in decoder
+    on x_t and return the per-position loss [B, L] = -log p(x_0 | x_t, KV) and x_t."""
+    E, H, Hkv, hd = model["E"], model["H"], model["Hkv"], model["hd"]
+    x0 = np.asarray(x0, np.int64)
+    B, L = x0.shape
+    xt = forward_noise(x0, keep_thr, E.shape[0], seed)
+    h, q, kc, vc = decoder_front(xt, E, model["Wqkv"], H, Hkv, hd)
+    O, _ = canvas_attention(q, k_pre, v_pre, kc, vc, window, hd ** -0.5)
+    y = decoder_back(h, O, model["Wo"])
+    loss, _ = cross_entropy(y.reshape(B * L, -1), E, inv_tau, x0.reshape(-1))
+    return loss.reshape(B, L), xt

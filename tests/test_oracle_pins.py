@@ -616,3 +616,52 @@ def test_entropy_bounded_loop_uninformed_model_runs_to_the_cap():
     _, _, _, _, post = O.eb_denoise_step(model, k_pre, v_pre, 0, xs, T - 1, inv[T - 1], None, 6,
                                          0.1, 0.005, True)
     assert np.array_equal(out, post["top1"].reshape(B, L))
+
+
+# --------------------------------------------------------------- SFT cross-entropy -----
+
+def test_cross_entropy_matches_torch_and_closed_forms():
+    """Against torch.nn.functional.cross_entropy in float64 (an independent implementation), log V
+    for uniform logits, and ~0 for a dominant correct logit."""
+    V, d, R = 500, 64, 40
+    rng = np.random.default_rng(21)
+    E = rng.standard_normal((V, d)) * 0.3
+    y = rng.standard_normal((R, d))
+    tgt = rng.integers(0, V, R)
+    loss, lse = O.cross_entropy(y, E, 1.7, tgt)
+    z = torch.tensor((y @ E.T) * 1.7)
+    ref = torch.nn.functional.cross_entropy(z, torch.tensor(tgt), reduction="none").numpy()
+    assert np.allclose(loss, ref, atol=1e-10)
+    assert np.allclose(lse, torch.logsumexp(z, dim=1).numpy(), atol=1e-10)
+    uni, _ = O.cross_entropy(np.zeros((3, d)), E, 1.0, [0, 7, 499])
+    assert np.allclose(uni, math.log(V), atol=1e-12)
+    Ei = np.eye(V, d)
+    yy = np.zeros((2, d))
+    yy[0, 5], yy[1, 9] = 60.0, 60.0
+    sharp, _ = O.cross_entropy(yy, Ei, 1.0, [5, 9])
+    assert np.all(sharp < 1e-20)
+    wrong, _ = O.cross_entropy(yy, Ei, 1.0, [6, 10])
+    assert np.allclose(wrong, 60.0, atol=1e-9)
+
+
+def test_sft_loss_is_the_cross_entropy_of_the_noised_canvas():
+    """keep = 1 (t = 0) leaves x_0 unchanged; the loss equals the cross-entropy of the decoder on
+    x_0; with t = 1 every token is redrawn; per-canvas thresholds act per canvas."""
+    V, d, H, Hkv, hd, B, L, P = 256, 64, 2, 1, 64, 2, 16, 4
+    rng = np.random.default_rng(22)
+    model = {"E": O.round_bf16(rng.standard_normal((V, d)) * 0.5),
+             "Wqkv": O.round_bf16(rng.standard_normal(((H + 2 * Hkv) * hd, d)) * 0.02),
+             "Wo": O.round_bf16(rng.standard_normal((d, H * hd)) * 0.02), "H": H, "Hkv": Hkv, "hd": hd}
+    k_pre = O.round_bf16(rng.standard_normal((B, P, Hkv, hd)))
+    v_pre = O.round_bf16(rng.standard_normal((B, P, Hkv, hd)))
+    x0 = rng.integers(0, V, (B, L))
+    full = np.array([1 << 32, 0], np.uint64)  # canvas 0 kept (kappa = 1), canvas 1 fully noised
+    loss, xt = O.sft_loss(model, k_pre, v_pre, 0, x0, full, seed=3)
+    assert np.array_equal(xt[0], x0[0])
+    assert np.mean(xt[1] != x0[1]) > 0.9
+    h, q, kc, vc = O.decoder_front(x0, model["E"], model["Wqkv"], H, Hkv, hd)
+    Oa, _ = O.canvas_attention(q, k_pre, v_pre, kc, vc, 0, hd ** -0.5)
+    y = O.decoder_back(h, Oa, model["Wo"])
+    ref, _ = O.cross_entropy(y.reshape(B * L, -1)[:L], model["E"], 1.0, x0[0])
+    # canvas 0's decoder input is x_0 itself, but its attention sees canvas 0 only: compare it
+    assert np.allclose(loss[0], ref, atol=1e-9)
