@@ -475,6 +475,117 @@ dg_status dg_vocab_posterior_step(const uint16_t* y, const uint16_t* W, int B, i
   return check_launch("vocab finalize launch");
 }
 
+dg_status dg_cross_entropy_step(const uint16_t* y, const uint16_t* W, int B, int L, int d, int V,
+                                float inv_tau, const int32_t* targets, float* loss, float* lse,
+                                void* ws, size_t ws_bytes, void* stream) {
+  if (B < 0 || L <= 0 || d <= 0 || V <= 0) return fail(DG_EINVAL, "cross_entropy: bad sizes");
+  if (d % 64 != 0) return fail(DG_ENOTSUP, "cross_entropy: d must be a multiple of 64");
+  if (V % 256 != 0) return fail(DG_ENOTSUP, "cross_entropy: V must be a multiple of 256");
+  if (L > 256 || L % 64 != 0) return fail(DG_ENOTSUP, "cross_entropy: L must be 64..256, multiple of 64");
+  if (!(inv_tau > 0.f) || !std::isfinite(inv_tau)) return fail(DG_EINVAL, "cross_entropy: bad inv_tau");
+  if (static_cast<int64_t>(B) * L >= (1ll << 31)) return fail(DG_ENOTSUP, "cross_entropy: too many rows");
+  if (B == 0) return DG_OK;
+  if (bad_ptr(y) || bad_ptr(W) || bad_ptr(ws) || bad_ptr(targets) || !loss)
+    return fail(DG_EINVAL, "cross_entropy: NULL or misaligned pointer");
+  if (ws_bytes < dg_vocab_posterior_workspace(B, L, V))
+    return fail(DG_EINVAL, "cross_entropy: workspace too small");
+  cudaStream_t st = as_stream(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  uint32_t* status = reinterpret_cast<uint32_t*>(w);
+  int* counters = reinterpret_cast<int*>(w + kStatusBytes);
+  VocabPart* parts = reinterpret_cast<VocabPart*>(
+      w + kStatusBytes + align256(2 * sizeof(int) * static_cast<size_t>(B)));
+  const cudaError_t em = cudaMemsetAsync(counters, 0, 2 * sizeof(int) * B, st);
+  if (em != cudaSuccess) return cuda_fail(em, "cross_entropy: memset");
+  const VocabPlan vp = plan_vocab(B * L, V);
+  cudaError_t e = launch_vocab_pass(y, W, B * L, L, d, V, inv_tau, 0, 0, parts, status, nullptr,
+                                    st, targets);
+  if (e != cudaSuccess) return cuda_fail(e, "cross_entropy: vocab pass launch");
+  FinalizeParams fp{};
+  fp.parts = parts;
+  fp.num_mt = vp.num_mt;
+  fp.S = vp.S;
+  fp.L = L;
+  fp.out_lse = lse;
+  fp.out_loss = loss;
+  fp.unlocked = counters;
+  fp.cta_done = counters + B;
+  launch_vocab_finalize(fp, B, st);
+  return check_launch("cross_entropy: finalize launch");
+}
+
+dg_status dg_sft_loss(const dg_model* m, const uint16_t* k_pre, const uint16_t* v_pre, int B,
+                      int L, int P, int window, const int32_t* x0, const uint64_t* keep_thr,
+                      uint64_t seed, float inv_tau, int32_t* xt, float* loss, void* ws,
+                      size_t ws_bytes, void* stream) {
+  dg_status s = check_model(m);
+  if (s != DG_OK) return s;
+  s = check_attn_dims(B, L, P, m->H, m->Hkv, m->hd, window);
+  if (s != DG_OK) return s;
+  if (!(inv_tau > 0.f) || !std::isfinite(inv_tau)) return fail(DG_EINVAL, "sft_loss: bad inv_tau");
+  if (static_cast<int64_t>(B) * L >= (1ll << 31)) return fail(DG_ENOTSUP, "sft_loss: too many rows");
+  if (B == 0) return DG_OK;
+  if (bad_ptr(x0) || bad_ptr(xt) || bad_ptr(ws) || !loss || keep_thr == nullptr ||
+      (reinterpret_cast<uintptr_t>(keep_thr) & 7))
+    return fail(DG_EINVAL, "sft_loss: NULL or misaligned pointer");
+  if (P > 0 && (bad_ptr(k_pre) || bad_ptr(v_pre))) return fail(DG_EINVAL, "sft_loss: bad prefix pointer");
+  if (ws_bytes < dg_denoise_loop_workspace(m, B, L, P, window))
+    return fail(DG_EINVAL, "sft_loss: workspace too small");
+  cudaStream_t st = as_stream(stream);
+  const LoopWs w = loop_layout(m, B, L, P, window, static_cast<uint8_t*>(ws));
+  const int BL = B * L;
+  const int Hhd = m->H * m->hd;
+  const int KVhd = m->Hkv * m->hd;
+  cudaError_t e = cudaMemsetAsync(w.counters, 0, 2 * sizeof(int) * B, st);
+  if (e != cudaSuccess) return cuda_fail(e, "sft_loss: memset");
+  // x_t = forward noising of x_0 at each canvas's keep threshold
+  launch_forward_noise(x0, xt, keep_thr, B, L, m->V, seed, st);
+  if ((s = check_launch("sft_loss: noise launch")) != DG_OK) return s;
+  launch_embed_gather(xt, m->E, w.h, BL, m->V, m->d, nullptr, st);
+  if ((s = check_launch("sft_loss: embed launch")) != DG_OK) return s;
+  GemmOut qkv{};
+  qkv.nseg = 3;
+  qkv.seg_begin[0] = 0;
+  qkv.seg_begin[1] = Hhd;
+  qkv.seg_begin[2] = Hhd + KVhd;
+  qkv.seg_begin[3] = Hhd + 2 * KVhd;
+  qkv.ptr[0] = w.q;
+  qkv.ptr[1] = w.k;
+  qkv.ptr[2] = w.v;
+  qkv.ld[0] = Hhd;
+  qkv.ld[1] = KVhd;
+  qkv.ld[2] = KVhd;
+  e = launch_gemm(w.h, m->Wqkv, BL, Hhd + 2 * KVhd, m->d, qkv, nullptr, 0, w.status, nullptr, st);
+  if (e != cudaSuccess) return cuda_fail(e, "sft_loss: qkv gemm launch");
+  e = launch_attention(w.q, k_pre, v_pre, w.k, w.v, w.o, nullptr, B, L, P, m->H, m->Hkv, m->hd,
+                       window, 1.0f / std::sqrt(static_cast<float>(m->hd)), w.attn, w.status,
+                       nullptr, st);
+  if (e != cudaSuccess) return cuda_fail(e, "sft_loss: attention launch");
+  GemmOut yo{};
+  yo.nseg = 1;
+  yo.seg_begin[0] = 0;
+  yo.seg_begin[1] = m->d;
+  yo.ptr[0] = w.y;
+  yo.ld[0] = m->d;
+  e = launch_gemm(w.o, m->Wo, BL, m->d, Hhd, yo, w.h, m->d, w.status, nullptr, st);
+  if (e != cudaSuccess) return cuda_fail(e, "sft_loss: out_proj gemm launch");
+  // fused LM head + cross-entropy against x_0
+  e = launch_vocab_pass(w.y, m->E, BL, L, m->d, m->V, inv_tau, 0, 0, w.parts, w.status, nullptr,
+                        st, x0);
+  if (e != cudaSuccess) return cuda_fail(e, "sft_loss: vocab pass launch");
+  const VocabPlan vp = plan_vocab(BL, m->V);
+  FinalizeParams fp{};
+  fp.parts = w.parts;
+  fp.num_mt = vp.num_mt;
+  fp.S = vp.S;
+  fp.L = L;
+  fp.out_loss = loss;
+  fp.unlocked = w.counters;
+  fp.cta_done = w.counters + B;
+  launch_vocab_finalize(fp, B, st);
+  return check_launch("sft_loss: finalize launch");
+}
+
 dg_status dg_entropy_bounded_update(const int32_t* x0hat, const int32_t* top1,
                                     const float* entropy, int32_t* prev_top1, int prev_valid,
                                     int32_t* x_out, uint8_t* accept, uint8_t* done,

@@ -158,6 +158,8 @@ __global__ void __launch_bounds__(kFinRows * 32) vocab_finalize_kernel(FinalizeP
     if (p.out_logp_x0hat) p.out_logp_x0hat[row] = acc.best_z - lse;
     // entropy = log s - t / s (both relative to the max), clamped at 0 against rounding
     if (p.out_entropy) p.out_entropy[row] = fmaxf(0.f, logf(acc.s) - acc.t / acc.s);
+    // cross-entropy mode: the best-sample fields carry the target's tempered logit
+    if (p.out_loss) p.out_loss[row] = acc.best_idx != 0x7FFFFFFF ? lse - acc.best_z : NAN;
     if (p.x_in != nullptr && is_active) {
       const bool was_locked = p.lock != nullptr && p.lock[row] != 0;
       const uint32_t u = jump_draw(static_cast<uint32_t>(i), static_cast<uint32_t>(b), p.step,

@@ -14,6 +14,7 @@ struct FinalizeParams {
   float* out_lse;
   float* out_logp_x0hat;
   float* out_entropy;
+  float* out_loss;      // cross-entropy mode: lse - z~[target]
   const int32_t* x_in;  // NULL: posterior only
   int32_t* x_out;
   uint8_t* lock;
@@ -95,9 +96,11 @@ struct VocabPlan {
   size_t part_bytes;
 };
 VocabPlan plan_vocab(int R, int V);
+// targets != NULL: cross-entropy mode (no Gumbel draws; the tuples carry the target's logit).
 cudaError_t launch_vocab_pass(const uint16_t* y, const uint16_t* W, int R, int L, int d, int V,
                               float inv_tau, uint64_t seed, int step, VocabPart* parts,
-                              uint32_t* status, const int* n_active, cudaStream_t st);
+                              uint32_t* status, const int* n_active, cudaStream_t st,
+                              const int32_t* targets = nullptr);
 
 // Optional CUDA-event timing around the heavy kernels (kind 0: vocabulary pass,
 // kind 1: attention).

@@ -38,6 +38,7 @@ struct VocabParams {
   int num_mt, nvt, per, S, units;
   float inv_tau;
   uint32_t k0, k1, c3;  // Philox key and counter word 3 (stream tag | step)
+  const int32_t* targets;  // cross-entropy mode: the target token of each row
   VocabPart* parts;
   uint32_t* status;
   const int* n_active;
@@ -110,10 +111,13 @@ __device__ __noinline__ Best gumbel_candidate(Best b, float z, int v, uint32_t p
 //    [1, 2) and X - 1 <= W, so W < t implies X < 1 + t, hence X <= fl(1 + t) (rounding is
 //    monotone and X is representable).  With t = exp(z~ - m) * cthr >= exp(z~ - best) this
 //    never drops an entry that could beat the best score; survivors get the exact test.
+// kCE (cross-entropy mode): no Gumbel draws; instead the tempered logit of the row's target
+// token is captured (in the best-sample fields, which that mode does not otherwise use).
+template <bool kCE>
 __device__ __forceinline__ void process_chunk(RowState& st, const float (&z)[32], int vbase,
                                               float inv_tau, uint32_t pos, uint32_t canvas,
                                               const PhiloxKeys& keys, uint32_t k0, uint32_t k1,
-                                              uint32_t c3) {
+                                              uint32_t c3, int target) {
   float mx[4] = {z[0], z[1], z[2], z[3]};  // four partial maxima: short dependency chains
 #pragma unroll
   for (int e = 4; e < 32; ++e) mx[e & 3] = fmaxf(mx[e & 3], z[e]);
@@ -140,6 +144,27 @@ __device__ __forceinline__ void process_chunk(RowState& st, const float (&z)[32]
   const float cthr = st.cthr;
   float ps[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums of exp(z~ - m)
   float pt[4] = {0.f, 0.f, 0.f, 0.f};  // and of exp(z~ - m) (z~ - m) log2(e)
+  if (kCE) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const float a = fmaf(z[e], scale, -mlog2);
+      const float pe = ex2_approx(a);
+      ps[e & 3] += pe;
+      pt[e & 3] = fmaf(pe, a, pt[e & 3]);
+    }
+    st.s += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+    st.t += ((pt[0] + pt[1]) + (pt[2] + pt[3])) * 0.6931471805599453f;
+    const int e = target - vbase;
+    if (e >= 0 && e < 32) {
+      float ze = z[0];
+#pragma unroll
+      for (int k = 1; k < 32; ++k) ze = e == k ? z[k] : ze;  // static indices only
+      st.best = 0.f;
+      st.best_idx = target;
+      st.best_z = ze * inv_tau;
+    }
+    return;
+  }
   uint32_t cand = 0;
 #pragma unroll
   for (int g4 = 0; g4 < 8; ++g4) {
@@ -177,6 +202,7 @@ __device__ __forceinline__ void process_chunk(RowState& st, const float (&z)[32]
   }
 }
 
+template <bool kCE>
 __global__ void __launch_bounds__(kThreads, 1)
     vocab_posterior_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB, VocabParams p) {
@@ -299,6 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = mt * kBM + row_in;
       const uint32_t canvas = static_cast<uint32_t>(row / p.L);
       const uint32_t pos = static_cast<uint32_t>(row % p.L);
+      const int target = kCE && row < p.R ? p.targets[row] : -1;
       RowState st;
       st.m = -INFINITY;
       st.s = 0.f;
@@ -323,8 +350,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&tempty[buf]);
 #pragma unroll
         for (int c = 0; c < kGroupCols / 32; ++c)
-          process_chunk(st, *reinterpret_cast<const float(*)[32]>(&z[c * 32]),
-                        vt * kBN + col + c * 32, p.inv_tau, pos, canvas, keys, p.k0, p.k1, p.c3);
+          process_chunk<kCE>(st, *reinterpret_cast<const float(*)[32]>(&z[c * 32]),
+                             vt * kBN + col + c * 32, p.inv_tau, pos, canvas, keys, p.k0, p.k1,
+                             p.c3, target);
       }
       // Merge the column groups of each row through shared memory, in group order.
       VocabPart mine;
@@ -393,7 +421,8 @@ VocabPlan plan_vocab(int R, int V) {
 
 cudaError_t launch_vocab_pass(const uint16_t* y, const uint16_t* W, int R, int L, int d, int V,
                               float inv_tau, uint64_t seed, int step, VocabPart* parts,
-                              uint32_t* status, const int* n_active, cudaStream_t st) {
+                              uint32_t* status, const int* n_active, cudaStream_t st,
+                              const int32_t* targets) {
   const VocabPlan pl = plan_vocab(R, V);
   CUtensorMap ta, tb;
   const uint64_t dA[2] = {static_cast<uint64_t>(d), static_cast<uint64_t>(R)};
@@ -418,6 +447,7 @@ cudaError_t launch_vocab_pass(const uint16_t* y, const uint16_t* W, int R, int L
   p.k0 = static_cast<uint32_t>(seed);
   p.k1 = static_cast<uint32_t>(seed >> 32);
   p.c3 = kStreamGumbel | (static_cast<uint32_t>(step) & 0xFFFFFFu);
+  p.targets = targets;
   p.parts = parts;
   p.status = status;
   p.n_active = n_active;
@@ -425,14 +455,21 @@ cudaError_t launch_vocab_pass(const uint16_t* y, const uint16_t* W, int R, int L
   static int configured_device = -1;
   const int dev = device_id();
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(vocab_posterior_kernel,
+    cudaError_t e = cudaFuncSetAttribute(vocab_posterior_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          VocabLayout::kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(vocab_posterior_kernel<true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               VocabLayout::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
   timer_begin(0, st);
-  vocab_posterior_kernel<<<pl.grid, kThreads, VocabLayout::kSmemBytes, st>>>(ta, tb, p);
+  if (targets)
+    vocab_posterior_kernel<true><<<pl.grid, kThreads, VocabLayout::kSmemBytes, st>>>(ta, tb, p);
+  else
+    vocab_posterior_kernel<false><<<pl.grid, kThreads, VocabLayout::kSmemBytes, st>>>(ta, tb, p);
   cudaError_t e = cudaGetLastError();
   timer_end(0, st);
   return e;

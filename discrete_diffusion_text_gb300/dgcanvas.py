@@ -76,6 +76,8 @@ SIGNATURES = {
     "dg_vocab_posterior_step_noalloc": (_I, [_P, _P, _I, _I, _I, _I, _F, _U64, _I, _P, _P, _P,
                                              _P, _P, _U64, _F, _P, _P]),
     "dg_euler_update": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _U64, _I, _U64, _F, _P]),
+    "dg_cross_entropy_step": (_I, [_P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P, _SZ, _P]),
+    "dg_sft_loss": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _U64, _F, _P, _P, _P, _SZ, _P]),
     "dg_entropy_bounded_update": (_I, [_P, _P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _U64, _I,
                                        _F, _F, _I, _P]),
     "dg_denoise_loop_workspace": (_SZ, [_P, _I, _I, _I, _I]),
@@ -259,6 +261,33 @@ def dg_euler_update(x_in, x0hat, top1, logp_top1, x_out, lock, jump, done, seed:
                                   _ptr(x_out), _ptr(lock), _ptr(jump), _ptr(done), B, L, seed,
                                   step, jump_thr, lock_logthr, _stream(stream)),
            "dg_euler_update")
+
+
+def dg_cross_entropy_step(y, W, B: int, L: int, inv_tau: float, targets, loss, lse=None,
+                          ws=None, stream=None):
+    """y [B*L, d] bf16; W [V, d] bf16; targets int32 [B*L]; loss (and lse) fp32 [B*L] out."""
+    _bf16(y, "y")
+    _bf16(W, "W")
+    V, d = W.shape
+    _dev(targets, torch.int32, "targets")
+    _dev(loss, torch.float32, "loss")
+    _check(load().dg_cross_entropy_step(_ptr(y), _ptr(W), B, L, d, V, inv_tau, _ptr(targets),
+                                        _ptr(loss), _ptr(lse), _ptr(ws), ws.numel(),
+                                        _stream(stream)), "dg_cross_entropy_step")
+
+
+def dg_sft_loss(m, k_pre, v_pre, window: int, x0, keep_thr, seed: int, xt, loss,
+                inv_tau: float = 1.0, ws=None, stream=None):
+    """x0, xt int32 [B, L]; keep_thr int64/uint64 [B] (device); loss fp32 [B, L] out."""
+    _dev(x0, torch.int32, "x0")
+    _dev(xt, torch.int32, "xt")
+    _dev(loss, torch.float32, "loss")
+    B, L = x0.shape
+    P = k_pre.shape[1]
+    _check(load().dg_sft_loss(ctypes.byref(m), _ptr(k_pre) if P > 0 else None,
+                              _ptr(v_pre) if P > 0 else None, B, L, P, window, _ptr(x0),
+                              _ptr(keep_thr), seed, inv_tau, _ptr(xt), _ptr(loss), _ptr(ws),
+                              ws.numel(), _stream(stream)), "dg_sft_loss")
 
 
 def dg_entropy_bounded_update(x0hat, top1, entropy, x_out, seed: int, step: int, V: int,

@@ -224,6 +224,19 @@ dg_status dg_euler_update(const int32_t* x_in, const int32_t* x0hat, const int32
                           uint8_t* done, int B, int L, uint64_t seed, int step, uint64_t jump_thr,
                           float lock_logthr, void* stream);
 
+/* ------------------------------------------------------- fused SFT cross-entropy ----
+ * The training-side twin of the fused LM head [TR "1단계: Supervised Finetuning": L(theta) =
+ * - sum_i log p_theta(x_0^i | x_t, c)]: per row r, with z~ = (y W^T) * inv_tau,
+ *     loss[r] = lse_r - z~_r[targets[r]]   (= -log Softmax(z~_r)[targets[r]])
+ * in one pass over the vocabulary (no Gumbel draws, no [rows, V] logit tensor).
+ *   y [B*L, d] bf16; W [V, d] bf16; targets [B*L] int32 in [0, V) (a target outside gives NaN);
+ *   loss [B*L] fp32 out; lse [B*L] fp32 out or NULL.  ws: at least
+ *   dg_vocab_posterior_workspace(B, L, V) bytes.  Limits: those of dg_vocab_posterior_step.
+ */
+dg_status dg_cross_entropy_step(const uint16_t* y, const uint16_t* W, int B, int L, int d, int V,
+                                float inv_tau, const int32_t* targets, float* loss, float* lse,
+                                void* ws, size_t ws_bytes, void* stream);
+
 /* ------------------------------------------------------ entropy-bounded update ----
  * One step of the entropy-bounded sampler [TR "DiffusionGemma 샘플러": "Entropy-bounded 토큰
  * 정제", "Adaptive stopping"], per canvas b:
@@ -306,6 +319,19 @@ dg_status dg_denoise_loop(const dg_model* m, const uint16_t* k_pre, const uint16
                           int L, int P, int window, int32_t* canvas, uint8_t* lock,
                           int32_t* steps_taken, const dg_sampler_cfg* cfg, void* ws,
                           size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------- SFT loss on noised canvases ----
+ * The SFT loss on noised canvases: x_t = dg_forward_noise(x_0, keep_thr, seed) (per-canvas keep
+ * thresholds floor(kappa(t_b) * 2^32); the report draws t_b ~ Unif[0, 1]), the stand-in decoder
+ * on x_t with the prefix KV, and loss = dg_cross_entropy_step against x_0.
+ *   x0 [B, L] int32; keep_thr [B] uint64 (device); xt [B, L] int32 out; loss [B, L] fp32 out.
+ *   ws: at least dg_denoise_loop_workspace(m, B, L, P, window) bytes.  Limits: those of
+ *   dg_denoise_loop.
+ */
+dg_status dg_sft_loss(const dg_model* m, const uint16_t* k_pre, const uint16_t* v_pre, int B,
+                      int L, int P, int window, const int32_t* x0, const uint64_t* keep_thr,
+                      uint64_t seed, float inv_tau, int32_t* xt, float* loss, void* ws,
+                      size_t ws_bytes, void* stream);
 
 /* ----------------------------------------------------------------- status and timing ----
  * dg_workspace_status: synchronises `stream`, reads and clears the status word at the start
