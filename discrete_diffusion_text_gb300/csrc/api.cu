@@ -444,7 +444,7 @@ dg_status dg_vocab_posterior_step(const uint16_t* y, const uint16_t* W, int B, i
   }
   const VocabPlan vp = plan_vocab(B * L, V);
   cudaError_t e = launch_vocab_pass(y, W, B * L, L, d, V, inv_tau, seed, step, parts, status,
-                                    nullptr, st);
+                                    nullptr, st, nullptr, out && out->entropy);
   if (e != cudaSuccess) return cuda_fail(e, "vocab pass launch");
   FinalizeParams fp{};
   fp.parts = parts;
@@ -743,7 +743,7 @@ dg_status dg_denoise_loop(const dg_model* m, const uint16_t* k_pre, const uint16
     e = launch_gemm(w.o, m->Wo, BL, m->d, Hhd, yo, w.h, m->d, w.status, w.n_active, st);
     if (e != cudaSuccess) return cuda_fail(e, "loop: out_proj gemm launch");
     e = launch_vocab_pass(w.y, m->E, BL, L, m->d, m->V, eb ? eb_inv_tau[n] : cfg->inv_tau,
-                          cfg->seed, n, w.parts, w.status, w.n_active, st);
+                          cfg->seed, n, w.parts, w.status, w.n_active, st, nullptr, eb);
     if (e != cudaSuccess) return cuda_fail(e, "loop: vocab pass launch");
     FinalizeParams fp{};
     fp.parts = w.parts;

@@ -97,10 +97,11 @@ struct VocabPlan {
 };
 VocabPlan plan_vocab(int R, int V);
 // targets != NULL: cross-entropy mode (no Gumbel draws; the tuples carry the target's logit).
+// entropy: the tuples also carry the entropy accumulator (otherwise it stays 0).
 cudaError_t launch_vocab_pass(const uint16_t* y, const uint16_t* W, int R, int L, int d, int V,
                               float inv_tau, uint64_t seed, int step, VocabPart* parts,
                               uint32_t* status, const int* n_active, cudaStream_t st,
-                              const int32_t* targets = nullptr);
+                              const int32_t* targets = nullptr, bool entropy = false);
 
 // Optional CUDA-event timing around the heavy kernels (kind 0: vocabulary pass,
 // kind 1: attention).

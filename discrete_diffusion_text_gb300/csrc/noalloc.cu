@@ -88,7 +88,8 @@ extern "C" dg_status dg_vocab_posterior_step_noalloc(
   cudaError_t e = cudaMemsetAsync(counters, 0, 2 * sizeof(int) * static_cast<size_t>(B), st);
   if (e != cudaSuccess) return cuda_fail(e, "vocab_posterior_noalloc: clearing counters");
   uint32_t* status = status_or_fallback(nullptr);
-  e = launch_vocab_pass(y, W, B * L, L, d, V, inv_tau, seed, step, parts, status, nullptr, st);
+  e = launch_vocab_pass(y, W, B * L, L, d, V, inv_tau, seed, step, parts, status, nullptr, st,
+                        nullptr, out && out->entropy);
   if (e != cudaSuccess) return cuda_fail(e, "vocab_posterior_noalloc: vocab pass launch");
   FinalizeParams fp{};
   fp.parts = parts;

@@ -113,7 +113,8 @@ __device__ __noinline__ Best gumbel_candidate(Best b, float z, int v, uint32_t p
 //    never drops an entry that could beat the best score; survivors get the exact test.
 // kCE (cross-entropy mode): no Gumbel draws; instead the tempered logit of the row's target
 // token is captured (in the best-sample fields, which that mode does not otherwise use).
-template <bool kCE>
+// kEnt: also accumulate t = sum exp(z~ - m)(z~ - m) for the entropy (one FMA per logit).
+template <bool kCE, bool kEnt>
 __device__ __forceinline__ void process_chunk(RowState& st, const float (&z)[32], int vbase,
                                               float inv_tau, uint32_t pos, uint32_t canvas,
                                               const PhiloxKeys& keys, uint32_t k0, uint32_t k1,
@@ -134,7 +135,7 @@ __device__ __forceinline__ void process_chunk(RowState& st, const float (&z)[32]
   }
   if (cm > st.m) {
     const float f = ex2_approx((st.m - cm) * kLog2e);
-    st.t = st.s > 0.f ? f * fmaf(st.s, st.m - cm, st.t) : 0.f;  // re-reference (z~ - m)
+    if (kEnt) st.t = st.s > 0.f ? f * fmaf(st.s, st.m - cm, st.t) : 0.f;  // re-reference
     st.s *= f;
     st.m = cm;
     refresh_cthr(st);
@@ -150,10 +151,10 @@ __device__ __forceinline__ void process_chunk(RowState& st, const float (&z)[32]
       const float a = fmaf(z[e], scale, -mlog2);
       const float pe = ex2_approx(a);
       ps[e & 3] += pe;
-      pt[e & 3] = fmaf(pe, a, pt[e & 3]);
+      if (kEnt) pt[e & 3] = fmaf(pe, a, pt[e & 3]);
     }
     st.s += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-    st.t += ((pt[0] + pt[1]) + (pt[2] + pt[3])) * 0.6931471805599453f;
+    if (kEnt) st.t += ((pt[0] + pt[1]) + (pt[2] + pt[3])) * 0.6931471805599453f;
     const int e = target - vbase;
     if (e >= 0 && e < 32) {
       float ze = z[0];
@@ -176,13 +177,13 @@ __device__ __forceinline__ void process_chunk(RowState& st, const float (&z)[32]
       const float a = fmaf(z[e], scale, -mlog2);  // (z~ - m) log2(e)
       const float pe = ex2_approx(a);
       ps[q] += pe;
-      pt[q] = fmaf(pe, a, pt[q]);
+      if (kEnt) pt[q] = fmaf(pe, a, pt[q]);
       const float X = __uint_as_float(0x3F800000u | (u[q] >> 9));
       if (X <= fmaf(pe, cthr, 1.0f)) cand |= 1u << e;
     }
   }
   st.s += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-  st.t += ((pt[0] + pt[1]) + (pt[2] + pt[3])) * 0.6931471805599453f;
+  if (kEnt) st.t += ((pt[0] + pt[1]) + (pt[2] + pt[3])) * 0.6931471805599453f;
   if (cand) {
     Best b{st.best, st.best_idx, st.best_z};
     do {  // candidates in increasing vocabulary order
@@ -202,7 +203,7 @@ __device__ __forceinline__ void process_chunk(RowState& st, const float (&z)[32]
   }
 }
 
-template <bool kCE>
+template <bool kCE, bool kEnt>
 __global__ void __launch_bounds__(kThreads, 1)
     vocab_posterior_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB, VocabParams p) {
@@ -350,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&tempty[buf]);
 #pragma unroll
         for (int c = 0; c < kGroupCols / 32; ++c)
-          process_chunk<kCE>(st, *reinterpret_cast<const float(*)[32]>(&z[c * 32]),
+          process_chunk<kCE, kEnt>(st, *reinterpret_cast<const float(*)[32]>(&z[c * 32]),
                              vt * kBN + col + c * 32, p.inv_tau, pos, canvas, keys, p.k0, p.k1,
                              p.c3, target);
       }
@@ -422,7 +423,7 @@ VocabPlan plan_vocab(int R, int V) {
 cudaError_t launch_vocab_pass(const uint16_t* y, const uint16_t* W, int R, int L, int d, int V,
                               float inv_tau, uint64_t seed, int step, VocabPart* parts,
                               uint32_t* status, const int* n_active, cudaStream_t st,
-                              const int32_t* targets) {
+                              const int32_t* targets, bool entropy) {
   const VocabPlan pl = plan_vocab(R, V);
   CUtensorMap ta, tb;
   const uint64_t dA[2] = {static_cast<uint64_t>(d), static_cast<uint64_t>(R)};
@@ -455,21 +456,20 @@ cudaError_t launch_vocab_pass(const uint16_t* y, const uint16_t* W, int R, int L
   static int configured_device = -1;
   const int dev = device_id();
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(vocab_posterior_kernel<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         VocabLayout::kSmemBytes);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(vocab_posterior_kernel<true>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               VocabLayout::kSmemBytes);
+    cudaError_t e = cudaSuccess;
+    for (auto fn : {vocab_posterior_kernel<false, false>, vocab_posterior_kernel<false, true>,
+                    vocab_posterior_kernel<true, false>})
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 VocabLayout::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
   timer_begin(0, st);
-  if (targets)
-    vocab_posterior_kernel<true><<<pl.grid, kThreads, VocabLayout::kSmemBytes, st>>>(ta, tb, p);
-  else
-    vocab_posterior_kernel<false><<<pl.grid, kThreads, VocabLayout::kSmemBytes, st>>>(ta, tb, p);
+  auto fn = targets ? vocab_posterior_kernel<true, false>
+                    : (entropy ? vocab_posterior_kernel<false, true>
+                               : vocab_posterior_kernel<false, false>);
+  fn<<<pl.grid, kThreads, VocabLayout::kSmemBytes, st>>>(ta, tb, p);
   cudaError_t e = cudaGetLastError();
   timer_end(0, st);
   return e;
