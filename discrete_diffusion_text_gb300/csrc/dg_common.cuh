@@ -23,18 +23,25 @@ struct Words4 {
   uint32_t x, y, z, w;
 };
 
+// One 32 x 32 -> 64-bit product (its high and low words in one multiply).
+__device__ __forceinline__ uint64_t mul_wide_u32(uint32_t a, uint32_t b) {
+  uint64_t p;
+  asm("mul.wide.u32 %0, %1, %2;" : "=l"(p) : "r"(a), "r"(b));
+  return p;
+}
+
 __device__ __forceinline__ Words4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2,
                                                 uint32_t c3, uint32_t k0, uint32_t k1) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    const uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
-    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
-    const uint32_t n0 = hi1 ^ c1 ^ k0;
-    const uint32_t n2 = hi0 ^ c3 ^ k1;
+    const uint64_t p0 = mul_wide_u32(0xD2511F53u, c0);
+    const uint64_t p1 = mul_wide_u32(0xCD9E8D57u, c2);
+    const uint32_t n0 = static_cast<uint32_t>(p1 >> 32) ^ c1 ^ k0;
+    const uint32_t n2 = static_cast<uint32_t>(p0 >> 32) ^ c3 ^ k1;
     c0 = n0;
-    c1 = lo1;
+    c1 = static_cast<uint32_t>(p1);
     c2 = n2;
-    c3 = lo0;
+    c3 = static_cast<uint32_t>(p0);
     k0 += 0x9E3779B9u;
     k1 += 0xBB67AE85u;
   }
@@ -61,14 +68,14 @@ __device__ __forceinline__ Words4 philox4x32_10(uint32_t c0, uint32_t c1, uint32
                                                 uint32_t c3, const PhiloxKeys& k) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    const uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
-    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
-    const uint32_t n0 = hi1 ^ c1 ^ k.k0[r];
-    const uint32_t n2 = hi0 ^ c3 ^ k.k1[r];
+    const uint64_t p0 = mul_wide_u32(0xD2511F53u, c0);
+    const uint64_t p1 = mul_wide_u32(0xCD9E8D57u, c2);
+    const uint32_t n0 = static_cast<uint32_t>(p1 >> 32) ^ c1 ^ k.k0[r];
+    const uint32_t n2 = static_cast<uint32_t>(p0 >> 32) ^ c3 ^ k.k1[r];
     c0 = n0;
-    c1 = lo1;
+    c1 = static_cast<uint32_t>(p1);
     c2 = n2;
-    c3 = lo0;
+    c3 = static_cast<uint32_t>(p0);
   }
   return {c0, c1, c2, c3};
 }
