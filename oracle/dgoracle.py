@@ -629,3 +629,78 @@ def sft_loss(model, k_pre, v_pre, window: int, x0, keep_thr, seed: int, inv_tau:
     y = decoder_back(h, O, model["Wo"])
     loss, _ = cross_entropy(y.reshape(B * L, -1), E, inv_tau, x0.reshape(-1))
     return loss.reshape(B, L), xt
+
+
+# ----------------------------------------------------------------------------------------
+# Encode-append and the block-autoregressive outer loop [TR "블록 자기회귀(Block-AR) 생성":
+# context encoding -> denoising loop over a 256-token canvas -> the finished canvas passes
+# through the causal encoder and is appended to the KV cache; repeat until the end-of-turn
+# token; the response is the concatenation of the canvases]
+# ----------------------------------------------------------------------------------------
+
+def encode_append(model, canvas, k_cache, v_cache, P: int, rows=None):
+    """For the one-layer stand-in, the keys and values a token contributes to later attention are
+    its own projections (bf16): k = E[x] Wk^T, v = E[x] Wv^T; a causal encoder over the canvas
+    therefore reduces to them.  They are written at cache rows P .. P+L-1 of each canvas (or of
+    the canvases in ``rows``).  k_cache, v_cache: float64 [B, P_cap, Hkv, hd], modified."""
+    E, H, Hkv, hd = model["E"], model["H"], model["Hkv"], model["hd"]
+    canvas = np.asarray(canvas, np.int64)
+    B, L = canvas.shape
+    _, _, k, v = decoder_front(canvas, E, model["Wqkv"], H, Hkv, hd)
+    sel = np.arange(B) if rows is None else np.asarray(rows, np.int64)
+    k_cache[sel, P:P + L] = k[sel]
+    v_cache[sel, P:P + L] = v[sel]
+    return k_cache, v_cache
+
+
+def block_generate(model, k_ctx, v_ctx, window: int, L: int, NB: int, eos: int, seed: int,
+                   T: int, schedule: int = SCHED_LINEAR, inv_tau: float = 1.0,
+                   lock_logthr: float = math.inf, stop_when_all_locked: bool = False,
+                   sampler: str = "euler", tau_start: float = 0.8, tau_end: float = 0.4,
+                   gamma: float = 0.1, stop_entropy: float = 0.005):
+    """Blocks j = 0 .. NB-1: the canvas starts from the uniform prior of seed + j, the denoising
+    loop (Euler or entropy-bounded, with seed + j) runs with the context plus every earlier
+    canvas as prefix KV, the finished canvas is recorded and encode-appended.  A canvas stops
+    at the first block whose canvas contains `eos` (its response length counts the tokens up to
+    and including it) or after NB blocks.  Returns out [B, NB, L] (-1 where never generated),
+    blocks [B], n_tokens [B], steps [B] (denoising steps summed over blocks) and the caches."""
+    k_ctx = np.asarray(k_ctx, np.float64)
+    v_ctx = np.asarray(v_ctx, np.float64)
+    B, P0 = k_ctx.shape[:2]
+    V = model["E"].shape[0]
+    cap = P0 + NB * L
+    k_cache = np.zeros((B, cap) + k_ctx.shape[2:])
+    v_cache = np.zeros((B, cap) + v_ctx.shape[2:])
+    k_cache[:, :P0] = k_ctx
+    v_cache[:, :P0] = v_ctx
+    out = np.full((B, NB, L), -1, np.int64)
+    blocks = np.zeros(B, np.int64)
+    n_tokens = np.zeros(B, np.int64)
+    steps = np.zeros(B, np.int64)
+    active = np.ones(B, bool)
+    for j in range(NB):
+        if not active.any():
+            break
+        P = P0 + j * L
+        x = initial_canvas(B, L, V, seed + j)
+        kp, vp = k_cache[:, :P], v_cache[:, :P]
+        if sampler == "euler":
+            xf, _, st = denoise_loop(model, kp, vp, window, x, np.zeros((B, L), np.uint8), T,
+                                     schedule, inv_tau, lock_logthr, seed + j,
+                                     stop_when_all_locked=stop_when_all_locked)
+        else:
+            xf, st = eb_denoise_loop(model, kp, vp, window, x, T, tau_start, tau_end, gamma,
+                                     stop_entropy, seed + j)
+        rows = np.nonzero(active)[0]
+        out[rows, j] = xf[rows]
+        steps[rows] += st[rows]
+        blocks[rows] = j + 1
+        encode_append(model, xf, k_cache, v_cache, P, rows)
+        for b in rows:
+            hit = np.nonzero(xf[b] == eos)[0]
+            if len(hit):
+                n_tokens[b] = j * L + int(hit[0]) + 1
+                active[b] = False
+            else:
+                n_tokens[b] = (j + 1) * L
+    return out, blocks, n_tokens, steps, k_cache, v_cache

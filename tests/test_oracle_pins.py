@@ -665,3 +665,62 @@ def test_sft_loss_is_the_cross_entropy_of_the_noised_canvas():
     ref, _ = O.cross_entropy(y.reshape(B * L, -1)[:L], model["E"], 1.0, x0[0])
     # canvas 0's decoder input is x_0 itself, but its attention sees canvas 0 only: compare it
     assert np.allclose(loss[0], ref, atol=1e-9)
+
+
+# ------------------------------------------------------ encode-append + block-AR loop -----
+
+def _delta_model(V, d, H, Hkv, hd, seed):
+    """Embedding 8 * I (V = d): the posterior is a delta at the token already there, so every
+    denoising loop returns its initial canvas."""
+    rng = np.random.default_rng(seed)
+    return {"E": np.eye(V, d) * 8.0,
+            "Wqkv": O.round_bf16(rng.standard_normal(((H + 2 * Hkv) * hd, d)) * 0.02),
+            "Wo": np.zeros((d, H * hd)), "H": H, "Hkv": Hkv, "hd": hd}
+
+
+def test_encode_append_writes_the_key_and_value_projections():
+    """Rows P..P+L-1 become E[x] Wk^T and E[x] Wv^T (Wk, Wv: the key and value row blocks of
+    Wqkv, rounded to bf16); other rows and other canvases are untouched."""
+    V, d, H, Hkv, hd, B, L, P = 64, 64, 2, 1, 64, 3, 8, 5
+    m = _delta_model(V, d, H, Hkv, hd, 1)
+    rng = np.random.default_rng(2)
+    canvas = rng.integers(0, V, (B, L))
+    kc = rng.standard_normal((B, P + L + 4, Hkv, hd))
+    vc = rng.standard_normal((B, P + L + 4, Hkv, hd))
+    k0, v0 = kc.copy(), vc.copy()
+    O.encode_append(m, canvas, kc, vc, P, rows=[0, 2])
+    Wk = m["Wqkv"][H * hd:(H + Hkv) * hd]
+    Wv = m["Wqkv"][(H + Hkv) * hd:]
+    for b in (0, 2):
+        emb = m["E"][canvas[b]]
+        assert np.allclose(kc[b, P:P + L], O.round_bf16(emb @ Wk.T).reshape(L, Hkv, hd), atol=0)
+        assert np.allclose(vc[b, P:P + L], O.round_bf16(emb @ Wv.T).reshape(L, Hkv, hd), atol=0)
+    assert np.array_equal(kc[1], k0[1]) and np.array_equal(vc[1], v0[1])
+    assert np.array_equal(kc[:, :P], k0[:, :P]) and np.array_equal(kc[:, P + L:], k0[:, P + L:])
+
+
+def test_block_generate_with_delta_posterior_and_eos():
+    """Each block returns its own uniform-prior canvas (seed + j); a canvas stops at the first
+    block containing the end-of-turn token, with the response length counted up to it; the KV
+    cache grows by one canvas per generated block."""
+    V, d, H, Hkv, hd, B, L, P0, NB, T = 256, 256, 2, 1, 64, 3, 16, 8, 4, 3
+    m = _delta_model(V, d, H, Hkv, hd, 3)
+    rng = np.random.default_rng(4)
+    k_ctx = O.round_bf16(rng.standard_normal((B, P0, Hkv, hd)))
+    v_ctx = O.round_bf16(rng.standard_normal((B, P0, Hkv, hd)))
+    seed = 10
+    inits = [O.initial_canvas(B, L, V, seed + j) for j in range(NB)]
+    eos = int(inits[1][0, 5])  # canvas 0 meets it in block 1 (if not already in block 0)
+    out, blocks, n_tok, steps, kc, vc = O.block_generate(m, k_ctx, v_ctx, 0, L, NB, eos, seed, T)
+    for b in range(B):
+        stop = next((j for j in range(NB) if eos in inits[j][b]), None)
+        nb = NB if stop is None else stop + 1
+        assert blocks[b] == nb
+        for j in range(nb):
+            assert np.array_equal(out[b, j], inits[j][b])
+        assert np.all(out[b, nb:] == -1)
+        n_exp = NB * L if stop is None else stop * L + int(np.nonzero(inits[stop][b] == eos)[0][0]) + 1
+        assert n_tok[b] == n_exp
+        assert steps[b] == nb * T
+        assert np.array_equal(kc[b, :P0], k_ctx[b])
+    assert blocks[0] <= 2
