@@ -2,6 +2,7 @@
 // loop.  Every step of the path runs in the library's own kernels.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -653,14 +654,13 @@ int dg_denoise_loop_kernel_count(const dg_model* m, int B, int L, int P, int win
   return 1 + steps * (6 + (ap.splits > 1 ? 1 : 0));
 }
 
-dg_status dg_denoise_loop(const dg_model* m, const uint16_t* k_pre, const uint16_t* v_pre, int B,
-                          int L, int P, int window, int32_t* canvas, uint8_t* lock,
-                          int32_t* steps_taken, const dg_sampler_cfg* cfg, void* ws,
-                          size_t ws_bytes, void* stream) {
-  dg_status s = check_model(m);
-  if (s != DG_OK) return s;
-  s = check_attn_dims(B, L, P, m->H, m->Hkv, m->hd, window);
-  if (s != DG_OK) return s;
+}  // extern "C"
+
+namespace {
+
+// Checks a sampler configuration; on success *end is the last step + 1 and, for the
+// entropy-bounded sampler, eb_inv_tau holds 1/tau_n for every step (double, then rounded).
+dg_status check_cfg(const dg_sampler_cfg* cfg, int* end, std::vector<float>* eb_inv_tau) {
   if (!cfg) return fail(DG_EINVAL, "loop: NULL cfg");
   if (cfg->T < 1 || cfg->T >= (1 << 24)) return fail(DG_EINVAL, "loop: T out of range");
   const bool eb = cfg->sampler == DG_SAMPLER_ENTROPY_BOUNDED;
@@ -669,12 +669,12 @@ dg_status dg_denoise_loop(const dg_model* m, const uint16_t* k_pre, const uint16
     return fail(DG_EINVAL, "loop: unknown schedule");
   if (!eb && (!(cfg->inv_tau > 0.f) || !std::isfinite(cfg->inv_tau)))
     return fail(DG_EINVAL, "loop: bad inv_tau");
-  const int end = cfg->end_step > 0 ? cfg->end_step : cfg->T;
-  if (cfg->start_step < 0 || end > cfg->T || cfg->start_step > end)
+  *end = cfg->end_step > 0 ? cfg->end_step : cfg->T;
+  if (cfg->start_step < 0 || *end > cfg->T || cfg->start_step > *end)
     return fail(DG_EINVAL, "loop: bad start/end step");
-  std::vector<float> eb_inv_tau;
+  eb_inv_tau->clear();
   if (eb) {
-    if (cfg->start_step != 0 || end != cfg->T)
+    if (cfg->start_step != 0 || *end != cfg->T)
       return fail(DG_ENOTSUP, "loop: the entropy-bounded sampler runs from step 0 to T");
     if (!(cfg->tau_start > 0.0) || !(cfg->tau_end > 0.0) || !std::isfinite(cfg->tau_start) ||
         !std::isfinite(cfg->tau_end) || std::isnan(cfg->gamma) || std::isnan(cfg->stop_entropy))
@@ -683,32 +683,45 @@ dg_status dg_denoise_loop(const dg_model* m, const uint16_t* k_pre, const uint16
       const double tau = cfg->T == 1 ? cfg->tau_start
                                      : cfg->tau_start + (cfg->tau_end - cfg->tau_start) * n /
                                                             (cfg->T - 1);
-      eb_inv_tau.push_back(static_cast<float>(1.0 / tau));
+      eb_inv_tau->push_back(static_cast<float>(1.0 / tau));
     }
   }
-  if (static_cast<int64_t>(B) * L >= (1ll << 31)) return fail(DG_ENOTSUP, "loop: too many rows");
-  if (B == 0) return DG_OK;
-  if (bad_ptr(canvas) || (!eb && bad_ptr(lock)) || bad_ptr(steps_taken) || bad_ptr(ws))
-    return fail(DG_EINVAL, "loop: NULL or misaligned canvas/lock/steps/workspace");
-  if (eb) lock = nullptr;
-  if (P > 0 && (bad_ptr(k_pre) || bad_ptr(v_pre))) return fail(DG_EINVAL, "loop: bad prefix pointer");
-  if (ws_bytes < dg_denoise_loop_workspace(m, B, L, P, window))
-    return fail(DG_EINVAL, "loop: workspace too small");
+  return DG_OK;
+}
 
-  std::vector<uint64_t> jump(cfg->T);
-  dg_schedule_thresholds(cfg->schedule, cfg->T, nullptr, jump.data());
-  cudaStream_t st = as_stream(stream);
-  const LoopWs w = loop_layout(m, B, L, P, window, static_cast<uint8_t*>(ws));
+// One canvas denoising run on the stream: loop bookkeeping, then steps start .. end-1 of the
+// sampler.  The prefix holds P rows per canvas at a stride of pre_stride rows; gen_active (or
+// NULL) leaves canvases out; seed is the run's key.  Arguments are already checked.
+struct RunArgs {
+  const dg_model* m;
+  const uint16_t* k_pre;
+  const uint16_t* v_pre;
+  int B, L, P, pre_stride, window;
+  int32_t* canvas;
+  uint8_t* lock;  // NULL for the entropy-bounded sampler
+  int32_t* steps_taken;
+  const uint8_t* gen_active;
+  uint64_t seed;
+  int start, end;
+};
+
+dg_status run_denoise(const RunArgs& a, const dg_sampler_cfg* cfg,
+                      const std::vector<float>& eb_inv_tau, const std::vector<uint64_t>& jump,
+                      const LoopWs& w, cudaStream_t st) {
+  const dg_model* m = a.m;
+  const bool eb = cfg->sampler == DG_SAMPLER_ENTROPY_BOUNDED;
+  const int B = a.B, L = a.L;
   const int BL = B * L;
   const int Hhd = m->H * m->hd;
   const int KVhd = m->Hkv * m->hd;
   const VocabPlan vp = plan_vocab(BL, m->V);
+  dg_status s;
 
   cudaError_t e = cudaMemsetAsync(w.n_active, 0, sizeof(int), st);
   if (e == cudaSuccess) e = cudaMemsetAsync(w.counters, 0, 2 * sizeof(int) * B, st);
   if (e != cudaSuccess) return cuda_fail(e, "loop: memset");
-  launch_loop_init(lock, w.active, w.n_active, steps_taken, B, L,
-                   eb ? 0 : cfg->stop_when_all_locked, st);
+  launch_loop_init_masked(a.lock, a.gen_active, w.active, w.n_active, a.steps_taken, B, L,
+                          eb ? 0 : cfg->stop_when_all_locked, st);
   if ((s = check_launch("loop init launch")) != DG_OK) return s;
 
   GemmOut qkv{};
@@ -730,20 +743,21 @@ dg_status dg_denoise_loop(const dg_model* m, const uint16_t* k_pre, const uint16
   yo.ptr[0] = w.y;
   yo.ld[0] = m->d;
   const float scale = 1.0f / std::sqrt(static_cast<float>(m->hd));
+  const uint32_t k0 = static_cast<uint32_t>(a.seed), k1 = static_cast<uint32_t>(a.seed >> 32);
 
-  for (int n = cfg->start_step; n < end; ++n) {
-    launch_embed_gather(canvas, m->E, w.h, BL, m->V, m->d, w.n_active, st);
+  for (int n = a.start; n < a.end; ++n) {
+    launch_embed_gather(a.canvas, m->E, w.h, BL, m->V, m->d, w.n_active, st);
     if ((s = check_launch("loop: embed launch")) != DG_OK) return s;
     e = launch_gemm(w.h, m->Wqkv, BL, Hhd + 2 * KVhd, m->d, qkv, nullptr, 0, w.status, w.n_active,
                     st);
     if (e != cudaSuccess) return cuda_fail(e, "loop: qkv gemm launch");
-    e = launch_attention(w.q, k_pre, v_pre, w.k, w.v, w.o, nullptr, B, L, P, m->H, m->Hkv, m->hd,
-                         window, scale, w.attn, w.status, w.n_active, st);
+    e = launch_attention(w.q, a.k_pre, a.v_pre, w.k, w.v, w.o, nullptr, B, L, a.P, m->H, m->Hkv,
+                         m->hd, a.window, scale, w.attn, w.status, w.n_active, st, a.pre_stride);
     if (e != cudaSuccess) return cuda_fail(e, "loop: attention launch");
     e = launch_gemm(w.o, m->Wo, BL, m->d, Hhd, yo, w.h, m->d, w.status, w.n_active, st);
     if (e != cudaSuccess) return cuda_fail(e, "loop: out_proj gemm launch");
     e = launch_vocab_pass(w.y, m->E, BL, L, m->d, m->V, eb ? eb_inv_tau[n] : cfg->inv_tau,
-                          cfg->seed, n, w.parts, w.status, w.n_active, st, nullptr, eb);
+                          a.seed, n, w.parts, w.status, w.n_active, st, nullptr, eb);
     if (e != cudaSuccess) return cuda_fail(e, "loop: vocab pass launch");
     FinalizeParams fp{};
     fp.parts = w.parts;
@@ -765,38 +779,290 @@ dg_status dg_denoise_loop(const dg_model* m, const uint16_t* k_pre, const uint16
       ep.entropy = w.entropy;
       ep.prev_top1 = w.prev_top1;
       ep.prev_valid = n > 0 ? 1 : 0;
-      ep.x_out = canvas;
+      ep.x_out = a.canvas;
       ep.L = L;
       ep.V = m->V;
-      ep.k0 = static_cast<uint32_t>(cfg->seed);
-      ep.k1 = static_cast<uint32_t>(cfg->seed >> 32);
+      ep.k0 = k0;
+      ep.k1 = k1;
       ep.step = static_cast<uint32_t>(n);
       ep.gamma = cfg->gamma;
       ep.stop_entropy = cfg->stop_entropy;
       ep.final_step = n == cfg->T - 1 ? 1 : 0;
       ep.active = w.active;
-      ep.steps_taken = steps_taken;
+      ep.steps_taken = a.steps_taken;
       ep.n_active = w.n_active;
       launch_entropy_bounded(ep, B, st);
       if ((s = check_launch("loop: entropy-bounded launch")) != DG_OK) return s;
       continue;
     }
-    fp.x_in = canvas;
-    fp.x_out = canvas;
-    fp.lock = lock;
+    fp.x_in = a.canvas;
+    fp.x_out = a.canvas;
+    fp.lock = a.lock;
     fp.jump_thr = jump[n];
     fp.lock_logthr = cfg->lock_logthr;
-    fp.k0 = static_cast<uint32_t>(cfg->seed);
-    fp.k1 = static_cast<uint32_t>(cfg->seed >> 32);
+    fp.k0 = k0;
+    fp.k1 = k1;
     fp.step = static_cast<uint32_t>(n);
     fp.active = w.active;
-    fp.steps_taken = steps_taken;
+    fp.steps_taken = a.steps_taken;
     fp.n_active = w.n_active;
     fp.stop_when_all_locked = cfg->stop_when_all_locked;
     fp.unlocked = w.counters;
     fp.cta_done = w.counters + B;
     launch_vocab_finalize(fp, B, st);
     if ((s = check_launch("loop: finalize launch")) != DG_OK) return s;
+  }
+  return DG_OK;
+}
+
+// Encode-append scratch: status word, embeddings, K and V of the canvas.
+struct AppendWs {
+  uint32_t* status;
+  uint16_t *h, *k, *v;
+  size_t total;
+};
+
+AppendWs append_layout(const dg_model* m, int B, int L, uint8_t* base) {
+  AppendWs w{};
+  const size_t BL = static_cast<size_t>(B) * L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    uint8_t* p = base ? base + off : nullptr;
+    off += align256(bytes);
+    return p;
+  };
+  w.status = reinterpret_cast<uint32_t*>(take(kStatusBytes));
+  w.h = reinterpret_cast<uint16_t*>(take(BL * m->d * 2));
+  w.k = reinterpret_cast<uint16_t*>(take(BL * m->Hkv * m->hd * 2));
+  w.v = reinterpret_cast<uint16_t*>(take(BL * m->Hkv * m->hd * 2));
+  w.total = off;
+  return w;
+}
+
+// K and V of the canvas tokens (embedding gather, then the K/V rows of the fused projection
+// only), copied to cache rows P .. P+L-1 of every canvas with active[b] != 0 (all if NULL).
+// n_run (or NULL) lets the kernels skip the pass when no canvas is generating.
+dg_status run_encode_append(const dg_model* m, const int32_t* canvas, uint16_t* k_cache,
+                            uint16_t* v_cache, int B, int L, int P, int P_cap,
+                            const uint8_t* active, const int* n_run, uint16_t* h, uint16_t* k,
+                            uint16_t* v, uint32_t* status, cudaStream_t st) {
+  const int BL = B * L;
+  const int Hhd = m->H * m->hd;
+  const int KVhd = m->Hkv * m->hd;
+  dg_status s;
+  launch_embed_gather(canvas, m->E, h, BL, m->V, m->d, n_run, st);
+  if ((s = check_launch("encode-append: embed launch")) != DG_OK) return s;
+  GemmOut kv{};
+  kv.nseg = 2;
+  kv.seg_begin[0] = 0;
+  kv.seg_begin[1] = KVhd;
+  kv.seg_begin[2] = 2 * KVhd;
+  kv.ptr[0] = k;
+  kv.ptr[1] = v;
+  kv.ld[0] = KVhd;
+  kv.ld[1] = KVhd;
+  const cudaError_t e = launch_gemm(h, m->Wqkv + static_cast<size_t>(Hhd) * m->d, BL, 2 * KVhd,
+                                    m->d, kv, nullptr, 0, status, n_run, st);
+  if (e != cudaSuccess) return cuda_fail(e, "encode-append: kv gemm launch");
+  launch_kv_append(k, v, k_cache, v_cache, active, B, L, P, P_cap, KVhd, st);
+  return check_launch("encode-append: copy launch");
+}
+
+// Block-autoregressive generation scratch: the denoising loop's workspace first (so that its
+// status word is the workspace's first word), sized for the longest prefix, then the block
+// state.
+struct BlockWs {
+  LoopWs loop;
+  size_t loop_bytes;
+  int32_t *canvas, *zeros, *steps_taken;
+  uint64_t* keep_zero;
+  uint8_t *lock, *gen_active;
+  int* gen_count;
+  size_t total;
+};
+
+BlockWs block_layout(const dg_model* m, int B, int L, int P0, int NB, int window, uint8_t* base) {
+  BlockWs w{};
+  size_t loop_bytes = 0;
+  for (int j = 0; j < NB; ++j)
+    loop_bytes = std::max(loop_bytes,
+                          loop_layout(m, B, L, P0 + j * L, window, nullptr).total);
+  const size_t app = append_layout(m, B, L, nullptr).total;
+  loop_bytes = std::max(loop_bytes, app);
+  w.loop_bytes = loop_bytes;
+  const size_t BL = static_cast<size_t>(B) * L;
+  size_t off = loop_bytes;
+  auto take = [&](size_t bytes) {
+    uint8_t* p = base ? base + off : nullptr;
+    off += align256(bytes);
+    return p;
+  };
+  w.canvas = reinterpret_cast<int32_t*>(take(BL * 4));
+  w.zeros = reinterpret_cast<int32_t*>(take(BL * 4));
+  w.steps_taken = reinterpret_cast<int32_t*>(take(static_cast<size_t>(B) * 4));
+  w.keep_zero = reinterpret_cast<uint64_t*>(take(static_cast<size_t>(B) * 8));
+  w.lock = take(BL);
+  w.gen_active = take(B);
+  w.gen_count = reinterpret_cast<int*>(take(sizeof(int)));
+  w.total = off;
+  return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+dg_status dg_denoise_loop(const dg_model* m, const uint16_t* k_pre, const uint16_t* v_pre, int B,
+                          int L, int P, int window, int32_t* canvas, uint8_t* lock,
+                          int32_t* steps_taken, const dg_sampler_cfg* cfg, void* ws,
+                          size_t ws_bytes, void* stream) {
+  dg_status s = check_model(m);
+  if (s != DG_OK) return s;
+  s = check_attn_dims(B, L, P, m->H, m->Hkv, m->hd, window);
+  if (s != DG_OK) return s;
+  int end = 0;
+  std::vector<float> eb_inv_tau;
+  if ((s = check_cfg(cfg, &end, &eb_inv_tau)) != DG_OK) return s;
+  const bool eb = cfg->sampler == DG_SAMPLER_ENTROPY_BOUNDED;
+  if (static_cast<int64_t>(B) * L >= (1ll << 31)) return fail(DG_ENOTSUP, "loop: too many rows");
+  if (B == 0) return DG_OK;
+  if (bad_ptr(canvas) || (!eb && bad_ptr(lock)) || bad_ptr(steps_taken) || bad_ptr(ws))
+    return fail(DG_EINVAL, "loop: NULL or misaligned canvas/lock/steps/workspace");
+  if (eb) lock = nullptr;
+  if (P > 0 && (bad_ptr(k_pre) || bad_ptr(v_pre))) return fail(DG_EINVAL, "loop: bad prefix pointer");
+  if (ws_bytes < dg_denoise_loop_workspace(m, B, L, P, window))
+    return fail(DG_EINVAL, "loop: workspace too small");
+
+  std::vector<uint64_t> jump(cfg->T);
+  dg_schedule_thresholds(cfg->schedule, cfg->T, nullptr, jump.data());
+  RunArgs a{};
+  a.m = m;
+  a.k_pre = k_pre;
+  a.v_pre = v_pre;
+  a.B = B;
+  a.L = L;
+  a.P = P;
+  a.pre_stride = P;
+  a.window = window;
+  a.canvas = canvas;
+  a.lock = lock;
+  a.steps_taken = steps_taken;
+  a.gen_active = nullptr;
+  a.seed = cfg->seed;
+  a.start = cfg->start_step;
+  a.end = end;
+  return run_denoise(a, cfg, eb_inv_tau, jump, loop_layout(m, B, L, P, window,
+                                                           static_cast<uint8_t*>(ws)),
+                     as_stream(stream));
+}
+
+size_t dg_encode_append_workspace(const dg_model* m, int B, int L) {
+  if (!m || B <= 0 || L <= 0 || m->d <= 0 || m->Hkv <= 0 || m->hd <= 0) return kStatusBytes;
+  return append_layout(m, B, L, nullptr).total;
+}
+
+dg_status dg_encode_append(const dg_model* m, const int32_t* canvas, uint16_t* k_cache,
+                           uint16_t* v_cache, int B, int L, int P, int P_cap,
+                           const uint8_t* active, void* ws, size_t ws_bytes, void* stream) {
+  dg_status s = check_model(m);
+  if (s != DG_OK) return s;
+  if (B < 0 || L <= 0 || P < 0 || P_cap < P + L)
+    return fail(DG_EINVAL, "encode-append: bad sizes (need P + L <= P_cap)");
+  if (static_cast<int64_t>(B) * L >= (1ll << 31) || static_cast<int64_t>(B) * P_cap >= (1ll << 31))
+    return fail(DG_ENOTSUP, "encode-append: too many rows");
+  if (B == 0) return DG_OK;
+  if (bad_ptr(canvas) || bad_ptr(k_cache) || bad_ptr(v_cache) || bad_ptr(ws))
+    return fail(DG_EINVAL, "encode-append: NULL or misaligned canvas/cache/workspace");
+  if (ws_bytes < dg_encode_append_workspace(m, B, L))
+    return fail(DG_EINVAL, "encode-append: workspace too small");
+  const AppendWs w = append_layout(m, B, L, static_cast<uint8_t*>(ws));
+  return run_encode_append(m, canvas, k_cache, v_cache, B, L, P, P_cap, active, nullptr, w.h, w.k,
+                           w.v, w.status, as_stream(stream));
+}
+
+size_t dg_block_generate_workspace(const dg_model* m, int B, int L, int P0, int NB, int window) {
+  if (!m || B <= 0 || L <= 0 || P0 < 0 || NB <= 0 || m->d <= 0 || m->H <= 0 || m->Hkv <= 0 ||
+      (m->hd != 64 && m->hd != 128) || m->V < 256)
+    return kStatusBytes;
+  return block_layout(m, B, L, P0, NB, window, nullptr).total;
+}
+
+dg_status dg_block_generate(const dg_model* m, uint16_t* k_cache, uint16_t* v_cache, int B, int P0,
+                            int P_cap, int L, int NB, int window, int32_t eos,
+                            const dg_sampler_cfg* cfg, int32_t* out, int32_t* blocks,
+                            int32_t* n_tokens, int32_t* steps, void* ws, size_t ws_bytes,
+                            void* stream) {
+  dg_status s = check_model(m);
+  if (s != DG_OK) return s;
+  if (NB < 0 || P0 < 0) return fail(DG_EINVAL, "block generate: negative size");
+  if (static_cast<int64_t>(P0) + static_cast<int64_t>(NB) * L > P_cap)
+    return fail(DG_EINVAL, "block generate: cache too small (need P0 + NB * L <= P_cap)");
+  s = check_attn_dims(B, L, P0, m->H, m->Hkv, m->hd, window);
+  if (s != DG_OK) return s;
+  int end = 0;
+  std::vector<float> eb_inv_tau;
+  if ((s = check_cfg(cfg, &end, &eb_inv_tau)) != DG_OK) return s;
+  if (cfg->start_step != 0 || end != cfg->T)
+    return fail(DG_ENOTSUP, "block generate: every block runs steps 0 .. T-1");
+  const bool eb = cfg->sampler == DG_SAMPLER_ENTROPY_BOUNDED;
+  if (static_cast<int64_t>(B) * P_cap >= (1ll << 31) ||
+      static_cast<int64_t>(B) * NB * L >= (1ll << 31))
+    return fail(DG_ENOTSUP, "block generate: too many rows");
+  if (B == 0 || NB == 0) return DG_OK;
+  if (bad_ptr(k_cache) || bad_ptr(v_cache) || bad_ptr(out) || bad_ptr(blocks) ||
+      bad_ptr(n_tokens) || bad_ptr(steps) || bad_ptr(ws))
+    return fail(DG_EINVAL, "block generate: NULL or misaligned pointer");
+  if (ws_bytes < dg_block_generate_workspace(m, B, L, P0, NB, window))
+    return fail(DG_EINVAL, "block generate: workspace too small");
+
+  std::vector<uint64_t> jump(cfg->T);
+  dg_schedule_thresholds(cfg->schedule, cfg->T, nullptr, jump.data());
+  cudaStream_t st = as_stream(stream);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  const BlockWs bw = block_layout(m, B, L, P0, NB, window, base);
+  const int BL = B * L;
+  cudaError_t e = cudaMemsetAsync(out, 0xFF, static_cast<size_t>(BL) * NB * 4, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(bw.zeros, 0, static_cast<size_t>(BL) * 4, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(bw.keep_zero, 0, static_cast<size_t>(B) * 8, st);
+  if (e != cudaSuccess) return cuda_fail(e, "block generate: memset");
+  launch_block_init(bw.gen_active, bw.gen_count, blocks, n_tokens, steps, B, st);
+  if ((s = check_launch("block generate: init launch")) != DG_OK) return s;
+
+  for (int j = 0; j < NB; ++j) {
+    const int P = P0 + j * L;
+    const uint64_t seed = cfg->seed + static_cast<uint64_t>(j);
+    // x_1 of block j: the uniform prior under the block's own key
+    launch_forward_noise(bw.zeros, bw.canvas, bw.keep_zero, B, L, m->V, seed, st);
+    if ((s = check_launch("block generate: prior launch")) != DG_OK) return s;
+    if (!eb) {
+      e = cudaMemsetAsync(bw.lock, 0, BL, st);
+      if (e != cudaSuccess) return cuda_fail(e, "block generate: lock memset");
+    }
+    RunArgs a{};
+    a.m = m;
+    a.k_pre = k_cache;
+    a.v_pre = v_cache;
+    a.B = B;
+    a.L = L;
+    a.P = P;
+    a.pre_stride = P_cap;
+    a.window = window;
+    a.canvas = bw.canvas;
+    a.lock = eb ? nullptr : bw.lock;
+    a.steps_taken = bw.steps_taken;
+    a.gen_active = bw.gen_active;
+    a.seed = seed;
+    a.start = 0;
+    a.end = cfg->T;
+    const LoopWs lw = loop_layout(m, B, L, P, window, base);
+    if ((s = run_denoise(a, cfg, eb_inv_tau, jump, lw, st)) != DG_OK) return s;
+    const AppendWs aw = append_layout(m, B, L, base);
+    if ((s = run_encode_append(m, bw.canvas, k_cache, v_cache, B, L, P, P_cap, bw.gen_active,
+                               bw.gen_count, aw.h, aw.k, aw.v, aw.status, st)) != DG_OK)
+      return s;
+    launch_block_record(bw.canvas, bw.steps_taken, out, bw.gen_active, bw.gen_count, blocks,
+                        n_tokens, steps, B, L, NB, j, eos, st);
+    if ((s = check_launch("block generate: record launch")) != DG_OK) return s;
   }
   return DG_OK;
 }

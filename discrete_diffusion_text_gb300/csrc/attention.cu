@@ -544,7 +544,8 @@ cudaError_t launch_attention(const uint16_t* q, const uint16_t* k_pre, const uin
                              const uint16_t* k_can, const uint16_t* v_can, uint16_t* out,
                              float* lse, int B, int L, int P, int H, int Hkv, int hd, int window,
                              float scale, void* part_ws, uint32_t* status, const int* n_active,
-                             cudaStream_t st) {
+                             cudaStream_t st, int pre_stride) {
+  if (pre_stride < 0) pre_stride = P;
   const AttnPlan pl = plan_attention(B, L, P, H, Hkv, hd, window);
   CUtensorMap maps[5];
   {
@@ -564,7 +565,8 @@ cudaError_t launch_attention(const uint16_t* q, const uint16_t* k_pre, const uin
     const uint64_t dims[4] = {static_cast<uint64_t>(hd), static_cast<uint64_t>(Hkv),
                               static_cast<uint64_t>(rows), static_cast<uint64_t>(B)};
     const uint64_t str[3] = {static_cast<uint64_t>(hd) * 2, static_cast<uint64_t>(Hkv) * hd * 2,
-                             static_cast<uint64_t>(m < 2 ? (P > 0 ? P : L) : L) * Hkv * hd * 2};
+                             static_cast<uint64_t>(m < 2 ? (P > 0 ? pre_stride : L) : L) * Hkv *
+                                 hd * 2};
     if (!make_tmap_bf16(&maps[1 + m], base, 4, dims, str, kvbox)) return cudaErrorInvalidValue;
   }
   AttnParams p;

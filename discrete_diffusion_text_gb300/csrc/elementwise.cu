@@ -286,16 +286,18 @@ void launch_vocab_finalize(const FinalizeParams& p, int B, cudaStream_t st) {
 }
 
 // Loop bookkeeping: active[b] = 1 unless the canvas is already fully locked and stopping is
-// on; n_active = number of active canvases; steps_taken = 0.
-__global__ void loop_init_kernel(const uint8_t* lock, uint8_t* active, int* n_active,
-                                 int32_t* steps_taken, int L, int stop_when_all_locked) {
+// on, or it is not generating any more (gen_active[b] == 0); n_active = number of active
+// canvases; steps_taken = 0.
+__global__ void loop_init_kernel(const uint8_t* lock, const uint8_t* gen_active, uint8_t* active,
+                                 int* n_active, int32_t* steps_taken, int L,
+                                 int stop_when_all_locked) {
   const int b = blockIdx.x;
   bool locked = lock != nullptr;  // no lock state: nothing is locked
   for (int i = threadIdx.x; locked && i < L; i += blockDim.x)
     locked = lock[static_cast<int64_t>(b) * L + i] != 0;
   const int all = __syncthreads_and(locked ? 1 : 0);
   if (threadIdx.x == 0) {
-    const bool act = !(stop_when_all_locked && all);
+    const bool act = !(stop_when_all_locked && all) && (gen_active == nullptr || gen_active[b]);
     active[b] = act ? 1 : 0;
     steps_taken[b] = 0;
     if (act) atomicAdd(n_active, 1);
@@ -304,8 +306,97 @@ __global__ void loop_init_kernel(const uint8_t* lock, uint8_t* active, int* n_ac
 
 void launch_loop_init(const uint8_t* lock, uint8_t* active, int* n_active, int32_t* steps_taken,
                       int B, int L, int stop_when_all_locked, cudaStream_t st) {
-  loop_init_kernel<<<B, 256, 0, st>>>(lock, active, n_active, steps_taken, L,
+  loop_init_kernel<<<B, 256, 0, st>>>(lock, nullptr, active, n_active, steps_taken, L,
                                       stop_when_all_locked);
+}
+
+void launch_loop_init_masked(const uint8_t* lock, const uint8_t* gen_active, uint8_t* active,
+                             int* n_active, int32_t* steps_taken, int B, int L,
+                             int stop_when_all_locked, cudaStream_t st) {
+  loop_init_kernel<<<B, 256, 0, st>>>(lock, gen_active, active, n_active, steps_taken, L,
+                                      stop_when_all_locked);
+}
+
+// Encode-append: the canvas's K and V rows (kv_row_elems bf16 each) into cache rows P .. P+L-1
+// of every active canvas; cache [B, P_cap, row].  16 bytes per thread.
+__global__ void kv_append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                                 uint4* __restrict__ kc, uint4* __restrict__ vc,
+                                 const uint8_t* active, int L, int P, int P_cap, int row16) {
+  const int r = blockIdx.x;  // canvas row b * L + i
+  const int b = r / L, i = r % L;
+  if (active && active[b] == 0) return;
+  const int64_t src = static_cast<int64_t>(r) * row16;
+  const int64_t dst = (static_cast<int64_t>(b) * P_cap + P + i) * row16;
+  for (int c = threadIdx.x; c < row16; c += blockDim.x) {
+    kc[dst + c] = k[src + c];
+    vc[dst + c] = v[src + c];
+  }
+}
+
+void launch_kv_append(const uint16_t* k, const uint16_t* v, uint16_t* k_cache, uint16_t* v_cache,
+                      const uint8_t* active, int B, int L, int P, int P_cap, int kv_row_elems,
+                      cudaStream_t st) {
+  kv_append_kernel<<<B * L, 128, 0, st>>>(reinterpret_cast<const uint4*>(k),
+                                          reinterpret_cast<const uint4*>(v),
+                                          reinterpret_cast<uint4*>(k_cache),
+                                          reinterpret_cast<uint4*>(v_cache), active, L, P, P_cap,
+                                          kv_row_elems / 8);
+}
+
+// A finished block j of every generating canvas: out[b, j, :] = canvas, steps added, blocks =
+// j + 1; the first end-of-turn token (if any) fixes the response length and ends the canvas.
+__global__ void block_init_kernel(uint8_t* gen_active, int* gen_count, int32_t* blocks,
+                                  int32_t* n_tokens, int32_t* steps_total, int B) {
+  for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < B; b += gridDim.x * blockDim.x) {
+    gen_active[b] = 1;
+    blocks[b] = 0;
+    n_tokens[b] = 0;
+    steps_total[b] = 0;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) *gen_count = B;
+}
+
+void launch_block_init(uint8_t* gen_active, int* gen_count, int32_t* blocks, int32_t* n_tokens,
+                       int32_t* steps_total, int B, cudaStream_t st) {
+  const int blocks_n = std::min((B + 255) / 256, 1024);
+  block_init_kernel<<<blocks_n, 256, 0, st>>>(gen_active, gen_count, blocks, n_tokens,
+                                              steps_total, B);
+}
+
+__global__ void block_record_kernel(const int32_t* canvas, const int32_t* steps_taken,
+                                    int32_t* out, uint8_t* active, int* gen_count,
+                                    int32_t* blocks, int32_t* n_tokens, int32_t* steps_total,
+                                    int L, int NB, int j, int32_t eos) {
+  const int b = blockIdx.x;
+  if (active[b] == 0) return;  // uniform over the CTA
+  __shared__ int first;
+  if (threadIdx.x == 0) first = 0x7FFFFFFF;
+  __syncthreads();
+  for (int i = threadIdx.x; i < L; i += blockDim.x) {
+    const int32_t x = canvas[static_cast<int64_t>(b) * L + i];
+    out[(static_cast<int64_t>(b) * NB + j) * L + i] = x;
+    if (x == eos) atomicMin(&first, i);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    blocks[b] = j + 1;
+    steps_total[b] += steps_taken[b];
+    if (first != 0x7FFFFFFF) {
+      n_tokens[b] = j * L + first + 1;
+      active[b] = 0;
+      atomicSub(gen_count, 1);
+    } else {
+      n_tokens[b] = (j + 1) * L;
+    }
+  }
+}
+
+void launch_block_record(const int32_t* canvas, const int32_t* steps_taken, int32_t* out,
+                         uint8_t* active, int* gen_count, int32_t* blocks, int32_t* n_tokens,
+                         int32_t* steps_total, int B, int L, int NB, int j, int32_t eos,
+                         cudaStream_t st) {
+  block_record_kernel<<<B, 256, 0, st>>>(canvas, steps_taken, out, active, gen_count, blocks,
+                                         n_tokens, steps_total, L, NB, j, eos);
 }
 
 // h[r, :] = E[x[r], :]; ids outside [0, V) give a zero row.  16 bytes per thread.

@@ -52,6 +52,21 @@ struct EBParams {
 };
 void launch_entropy_bounded(const EBParams& p, int B, cudaStream_t st);
 
+// Block-AR helpers: K/V of the canvas into cache rows [P, P + L) of each active canvas, and
+// the record of a finished block (output, end-of-turn test, counts).
+void launch_kv_append(const uint16_t* k, const uint16_t* v, uint16_t* k_cache, uint16_t* v_cache,
+                      const uint8_t* active, int B, int L, int P, int P_cap, int kv_row_elems,
+                      cudaStream_t st);
+void launch_block_init(uint8_t* gen_active, int* gen_count, int32_t* blocks, int32_t* n_tokens,
+                       int32_t* steps_total, int B, cudaStream_t st);
+void launch_block_record(const int32_t* canvas, const int32_t* steps_taken, int32_t* out,
+                         uint8_t* active, int* gen_count, int32_t* blocks, int32_t* n_tokens,
+                         int32_t* steps_total, int B, int L, int NB, int j, int32_t eos,
+                         cudaStream_t st);
+void launch_loop_init_masked(const uint8_t* lock, const uint8_t* gen_active, uint8_t* active,
+                             int* n_active, int32_t* steps_taken, int B, int L,
+                             int stop_when_all_locked, cudaStream_t st);
+
 void launch_forward_noise(const int32_t* x0, int32_t* xt, const uint64_t* keep_thr, int B, int L,
                           int V, uint64_t seed, cudaStream_t st);
 void launch_euler_update(const int32_t* x_in, const int32_t* x0hat, const int32_t* top1,
@@ -84,11 +99,12 @@ struct AttnPlan {
   size_t part_bytes;  // fp32 partials for split > 1
 };
 AttnPlan plan_attention(int B, int L, int P, int H, int Hkv, int hd, int window);
+// pre_stride: prefix rows allocated per canvas in k_pre / v_pre (-1: P).
 cudaError_t launch_attention(const uint16_t* q, const uint16_t* k_pre, const uint16_t* v_pre,
                              const uint16_t* k_can, const uint16_t* v_can, uint16_t* out,
                              float* lse, int B, int L, int P, int H, int Hkv, int hd, int window,
                              float scale, void* part_ws, uint32_t* status, const int* n_active,
-                             cudaStream_t st);
+                             cudaStream_t st, int pre_stride = -1);
 
 // -------------------------------------------------------------- vocabulary pass -----
 struct VocabPlan {

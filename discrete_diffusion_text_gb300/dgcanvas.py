@@ -83,6 +83,11 @@ SIGNATURES = {
     "dg_denoise_loop_workspace": (_SZ, [_P, _I, _I, _I, _I]),
     "dg_denoise_loop_kernel_count": (_I, [_P, _I, _I, _I, _I, _I]),
     "dg_denoise_loop": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+    "dg_encode_append_workspace": (_SZ, [_P, _I, _I]),
+    "dg_encode_append": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "dg_block_generate_workspace": (_SZ, [_P, _I, _I, _I, _I, _I]),
+    "dg_block_generate": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P,
+                               _SZ, _P]),
     "dg_workspace_status": (_I, [_P, _P]),
     "dg_kernel_timer_enable": (_I, [_I]),
     "dg_kernel_timer_read": (_I, [_I, _P, _P]),
@@ -344,6 +349,45 @@ def dg_denoise_loop(m: dg_model, k_pre, v_pre, window: int, canvas, lock, steps_
                                   _ptr(v_pre) if P > 0 else None, B, L, P, window, _ptr(canvas),
                                   _ptr(lock), _ptr(steps_taken), ctypes.byref(cfg), _ptr(ws),
                                   ws.numel(), _stream(stream)), "dg_denoise_loop")
+
+
+def dg_encode_append_workspace(m: dg_model, B, L) -> int:
+    return load().dg_encode_append_workspace(ctypes.byref(m), B, L)
+
+
+def dg_encode_append(m: dg_model, canvas, k_cache, v_cache, P: int, ws, active=None,
+                     stream=None):
+    """canvas int32 [B, L]; k_cache, v_cache bf16 [B, P_cap, Hkv, hd] (rows P .. P+L-1 written
+    for canvases with active[b] != 0, all if active is None)."""
+    _dev(canvas, torch.int32, "canvas")
+    if active is not None:
+        _dev(active, torch.uint8, "active")
+    B, L = canvas.shape
+    P_cap = k_cache.shape[1]
+    _check(load().dg_encode_append(ctypes.byref(m), _ptr(canvas), _ptr(k_cache), _ptr(v_cache),
+                                   B, L, P, P_cap, _ptr(active), _ptr(ws), ws.numel(),
+                                   _stream(stream)), "dg_encode_append")
+
+
+def dg_block_generate_workspace(m: dg_model, B, L, P0, NB, window) -> int:
+    return load().dg_block_generate_workspace(ctypes.byref(m), B, L, P0, NB, window)
+
+
+def dg_block_generate(m: dg_model, k_cache, v_cache, P0: int, L: int, window: int, eos: int,
+                      cfg: dg_sampler_cfg, out, blocks, n_tokens, steps, ws, stream=None):
+    """k_cache, v_cache bf16 [B, P_cap, Hkv, hd] (rows 0 .. P0-1 the context; generated canvases
+    appended); out int32 [B, NB, L]; blocks, n_tokens, steps int32 [B] (all outputs)."""
+    _dev(out, torch.int32, "out")
+    for t, name in ((blocks, "blocks"), (n_tokens, "n_tokens"), (steps, "steps")):
+        _dev(t, torch.int32, name)
+    B, NB, Lo = out.shape
+    if Lo != L:
+        raise ValueError("out must be [B, NB, L]")
+    P_cap = k_cache.shape[1]
+    _check(load().dg_block_generate(ctypes.byref(m), _ptr(k_cache), _ptr(v_cache), B, P0, P_cap,
+                                    L, NB, window, eos, ctypes.byref(cfg), _ptr(out),
+                                    _ptr(blocks), _ptr(n_tokens), _ptr(steps), _ptr(ws),
+                                    ws.numel(), _stream(stream)), "dg_block_generate")
 
 
 def dg_workspace_status(ws=None, stream=None):

@@ -333,9 +333,55 @@ dg_status dg_sft_loss(const dg_model* m, const uint16_t* k_pre, const uint16_t* 
                       uint64_t seed, float inv_tau, int32_t* xt, float* loss, void* ws,
                       size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------- encode-append and block-AR loop ----
+ * [TR "블록 자기회귀(Block-AR) 생성": context encoding, denoising loop, encode-append, repeated
+ * until the end-of-turn token; "추론 효율 지표": one extra forward between canvases.]
+ *
+ * dg_encode_append: the finished canvas goes through the causal encoder and its keys and
+ * values are appended to the prefix cache.  For the one-layer stand-in decoder a token's key
+ * and value are its own projections, k = E[x] Wk^T, v = E[x] Wv^T (bf16; Wk, Wv are the K and
+ * V row blocks of Wqkv), so the causal pass is the K/V part of the fused projection.  They are
+ * written at cache rows P .. P+L-1 of every canvas b with active[b] != 0 (all when active is
+ * NULL); other rows are not touched.
+ *   canvas [B, L] int32 (device); k_cache, v_cache [B, P_cap, Hkv, hd] bf16 in/out; active [B]
+ *   uint8 or NULL.  ws: at least dg_encode_append_workspace(m, B, L) bytes, status word first.
+ *   Limits: P + L <= P_cap; B * P_cap < 2^31; the model limits of dg_denoise_loop.
+ *
+ * dg_block_generate: block-AR generation for B independent conversations.  On entry cache rows
+ * 0 .. P0-1 hold the encoded context.  For block j = 0 .. NB-1, while the conversation has not
+ * ended:
+ *   - the canvas starts from the uniform prior x_1 drawn with key cfg->seed + j (dg_forward_noise
+ *     with keep threshold 0);
+ *   - dg_denoise_loop runs all T steps of cfg (either sampler, key cfg->seed + j, lock cleared)
+ *     with the P0 + j*L cache rows as prefix;
+ *   - the finished canvas is written to out[b, j, :] and encode-appended at rows P0 + j*L;
+ *   - if it holds the end-of-turn token `eos`, the conversation ends: its response is the
+ *     tokens up to and including the first `eos`.
+ * Outputs: out [B, NB, L] int32 (-1 in blocks never generated); blocks [B] = canvases
+ * generated; n_tokens [B] = response length (j*L + i + 1 for the first eos at position i of
+ * block j, else blocks * L); steps [B] = denoising steps summed over the canvases (the
+ * sum s_k of the throughput metrics).  All device, int32.  Everything stays on the device;
+ * the host enqueues NB blocks and does not wait: blocks after every conversation ended
+ * return at once.
+ *   k_cache, v_cache [B, P_cap, Hkv, hd] bf16 in/out (rows P0 .. P0 + blocks*L - 1 written).
+ *   ws: at least dg_block_generate_workspace(m, B, L, P0, NB, window) bytes, status word first.
+ *   Limits: P0 + NB*L <= P_cap; cfg runs steps 0 .. T-1; those of dg_denoise_loop.
+ */
+size_t dg_encode_append_workspace(const dg_model* m, int B, int L);
+dg_status dg_encode_append(const dg_model* m, const int32_t* canvas, uint16_t* k_cache,
+                           uint16_t* v_cache, int B, int L, int P, int P_cap,
+                           const uint8_t* active, void* ws, size_t ws_bytes, void* stream);
+size_t dg_block_generate_workspace(const dg_model* m, int B, int L, int P0, int NB, int window);
+dg_status dg_block_generate(const dg_model* m, uint16_t* k_cache, uint16_t* v_cache, int B, int P0,
+                            int P_cap, int L, int NB, int window, int32_t eos,
+                            const dg_sampler_cfg* cfg, int32_t* out, int32_t* blocks,
+                            int32_t* n_tokens, int32_t* steps, void* ws, size_t ws_bytes,
+                            void* stream);
+
 /* ----------------------------------------------------------------- status and timing ----
  * dg_workspace_status: synchronises `stream`, reads and clears the status word at the start
- * of a workspace used by dg_canvas_attn, dg_vocab_posterior_step or dg_denoise_loop, and
+ * of a workspace used by dg_canvas_attn, dg_vocab_posterior_step, dg_denoise_loop,
+ * dg_encode_append or dg_block_generate, and
  * returns DG_OK, DG_ETIMEOUT or DG_EKERNEL accordingly (DG_ECUDA if the stream failed).
  *
  * dg_kernel_timer_enable(1) makes the library record CUDA events on the launching stream
