@@ -33,7 +33,12 @@ Readings taken where the pages are silent (each listed in the design notes):
   * the decoder is a one-layer stand-in: embedding, one bidirectional attention layer over
     [prefix KV ; canvas] with GQA and an optional sliding window, output projection with a
     residual, and an LM head tied to the embedding; no norm, no RoPE, no time input;
-  * intermediate activations (q, k, v, attention output, y) are rounded to bfloat16.
+  * intermediate activations (q, k, v, attention output, y) are rounded to bfloat16;
+  * self-conditioning (when the model carries Wsc1, Wsc2): the expected embedding
+    e = p_hat_0 E under the step's tempered posterior, rounded to bfloat16, goes through a
+    two-layer feed-forward s = Wsc2 gelu(Wsc1 e) (tanh-form GELU, bfloat16 after each layer);
+    s is added to the token embeddings of the next step, h = bf16(E[x] + s), and is zero at
+    the first step of a canvas.
 
 Counter-based random numbers (Philox4x32-10 keyed by the 64-bit seed) replace every random
 draw the method makes, so that both implementations see identical random bits:
@@ -284,14 +289,18 @@ def canvas_attention(q, k_pre, v_pre, k_can, v_can, window: int, scale: float):
     return O, lse
 
 
-def decoder_front(x, E, Wqkv, H: int, Hkv: int, hd: int):
-    """h = E[x_t]; [q | k_c | v_c] = h Wqkv^T, each rounded to bfloat16.
+def decoder_front(x, E, Wqkv, H: int, Hkv: int, hd: int, s=None):
+    """h = E[x_t] (+ s_t, rounded to bfloat16, when a self-conditioning signal is given);
+    [q | k_c | v_c] = h Wqkv^T, each rounded to bfloat16.
 
-    x [B, L] int; E [V, d]; Wqkv [(H + 2 Hkv) hd, d] (rows: q heads, then k heads, then v).
+    x [B, L] int; E [V, d]; Wqkv [(H + 2 Hkv) hd, d] (rows: q heads, then k heads, then v);
+    s [B, L, d] or None.
     """
     x = np.asarray(x, np.int64)
     B, L = x.shape
     h = np.asarray(E, np.float64)[x]                       # [B, L, d]
+    if s is not None:
+        h = round_bf16(h + np.asarray(s, np.float64).reshape(h.shape))
     qkv = round_bf16(h.reshape(B * L, -1) @ np.asarray(Wqkv, np.float64).T)
     q = qkv[:, : H * hd].reshape(B, L, H, hd)
     k = qkv[:, H * hd:(H + Hkv) * hd].reshape(B, L, Hkv, hd)
@@ -371,6 +380,49 @@ def posterior(y, E, inv_tau: float, seed: int, step: int, L: int, rows=None, chu
 
 
 # ----------------------------------------------------------------------------------------
+# Self-conditioning [TR "디노이징 반복과 self-conditioning": s_(t-h) = FFW(p_hat_0 . E)]
+# ----------------------------------------------------------------------------------------
+
+def gelu_tanh(x):
+    """GELU in its tanh form: x/2 * (1 + tanh(sqrt(2/pi) * (x + 0.044715 x^3)))."""
+    x = np.asarray(x, np.float64)
+    return 0.5 * x * (1.0 + np.tanh(math.sqrt(2.0 / math.pi) * (x + 0.044715 * x ** 3)))
+
+
+def expected_embedding(y, E, inv_tau: float, chunk=None):
+    """e = p_hat_0 . E per row: sum_v Softmax(y E^T * inv_tau)_v E[v].  y [R, d]; returns
+    float64 [R, d] (not rounded)."""
+    y = np.asarray(y, np.float64)
+    E64 = np.asarray(E, np.float64)
+    R, V = y.shape[0], E64.shape[0]
+    if chunk is None:
+        chunk = max(1, (1 << 24) // V)
+    e = np.zeros((R, E64.shape[1]))
+    for s0 in range(0, R, chunk):
+        z = (y[s0:s0 + chunk] @ E64.T) * inv_tau
+        m = z.max(axis=1, keepdims=True)
+        w = np.exp(z - m)
+        p = w / w.sum(axis=1, keepdims=True)
+        e[s0:s0 + chunk] = p @ E64
+    return e
+
+
+def self_condition(y, E, inv_tau: float, Wsc1, Wsc2, chunk=None):
+    """s = FFW(p_hat_0 . E): e = bf16(p_hat_0 E), u = bf16(gelu(e Wsc1^T)), s = bf16(u Wsc2^T).
+    y [R, d]; Wsc1 [d_sc, d]; Wsc2 [d, d_sc].  Returns a dict with e_exact (float64, not
+    rounded), e, u and s."""
+    e_exact = expected_embedding(y, E, inv_tau, chunk)
+    e = round_bf16(e_exact)
+    u = round_bf16(gelu_tanh(e @ np.asarray(Wsc1, np.float64).T))
+    s = round_bf16(u @ np.asarray(Wsc2, np.float64).T)
+    return {"e_exact": e_exact, "e": e, "u": u, "s": s}
+
+
+def has_self_cond(model) -> bool:
+    return model.get("Wsc1") is not None
+
+
+# ----------------------------------------------------------------------------------------
 # Discrete Euler step with optional confidence locking
 # [TR "Backward Denoising Process": x_(t-h) ~ Step(x_t, p_theta(.|x_t)), factorised per
 # position; PBD glossary "Iterative denoising": confident tokens are locked in]
@@ -406,22 +458,37 @@ def euler_update(x_in, x0hat, top1, logp_top1, lock, seed: int, step: int, jump_
 
 
 # ----------------------------------------------------------------------------------------
-# One denoising step and the loop [TR "디노이징 반복과 self-conditioning", without s_t]
+# One denoising step and the loop [TR "디노이징 반복과 self-conditioning"]
 # ----------------------------------------------------------------------------------------
 
-def denoise_step(model, k_pre, v_pre, window: int, x, lock, n: int, jump_thr: int,
-                 inv_tau: float, lock_logthr: float, seed: int):
-    """logits = Decoder(x_t, KV); p_hat_0 = Softmax(logits / tau); x_(t-h) ~ Step(x_t, p_hat_0).
-
-    model: dict with E [V, d], Wqkv, Wo, H, Hkv, hd.  Returns (x_out, lock_out, jump, done,
-    diagnostics) where diagnostics holds the posterior tuple per row.
-    """
+def decoder_posterior(model, k_pre, v_pre, window: int, x, n: int, inv_tau: float, seed: int,
+                      s=None):
+    """logits = Decoder(x_t, KV, s_t); the posterior tuple of every row at inverse temperature
+    inv_tau; with self-conditioning weights in the model, also s_(t-h) = FFW(p_hat_0 . E) in
+    post["s"] ([B, L, d]).  s: this step's signal (None = zero)."""
     E, H, Hkv, hd = model["E"], model["H"], model["Hkv"], model["hd"]
     B, L = np.asarray(x).shape
-    h, q, kc, vc = decoder_front(x, E, model["Wqkv"], H, Hkv, hd)
+    h, q, kc, vc = decoder_front(x, E, model["Wqkv"], H, Hkv, hd, s)
     O, _ = canvas_attention(q, k_pre, v_pre, kc, vc, window, hd ** -0.5)
     y = decoder_back(h, O, model["Wo"])
     post = posterior(y.reshape(B * L, -1), E, inv_tau, seed, n, L)
+    if has_self_cond(model):
+        post["s"] = self_condition(y.reshape(B * L, -1), E, inv_tau, model["Wsc1"],
+                                   model["Wsc2"])["s"].reshape(B, L, -1)
+    return post
+
+
+def denoise_step(model, k_pre, v_pre, window: int, x, lock, n: int, jump_thr: int,
+                 inv_tau: float, lock_logthr: float, seed: int, s=None):
+    """logits = Decoder(x_t, KV, s_t); p_hat_0 = Softmax(logits / tau); x_(t-h) ~ Step(x_t,
+    p_hat_0); s_(t-h) = FFW(p_hat_0 . E) when the model self-conditions.
+
+    model: dict with E [V, d], Wqkv, Wo, H, Hkv, hd (and optionally Wsc1, Wsc2).  Returns
+    (x_out, lock_out, jump, done, diagnostics) where diagnostics holds the posterior tuple per
+    row (and the next signal under "s").
+    """
+    B, L = np.asarray(x).shape
+    post = decoder_posterior(model, k_pre, v_pre, window, x, n, inv_tau, seed, s)
     shape = (B, L)
     x_out, lock_out, jump, done = euler_update(
         x, post["x0hat"].reshape(shape), post["top1"].reshape(shape),
@@ -432,13 +499,20 @@ def denoise_step(model, k_pre, v_pre, window: int, x, lock, n: int, jump_thr: in
 
 def denoise_loop(model, k_pre, v_pre, window: int, x, lock, T: int, schedule: int,
                  inv_tau: float, lock_logthr: float, seed: int, start_step: int = 0,
-                 stop_when_all_locked: bool = False, end_step: int | None = None):
+                 stop_when_all_locked: bool = False, end_step: int | None = None,
+                 state: dict | None = None):
     """Steps n = start_step .. end_step-1 (default T-1) of at most T [TR "DiffusionGemma 샘플러":
     cap T].  A canvas whose positions are all locked stops when ``stop_when_all_locked``.
-    Returns the final canvas, the lock mask and the number of steps applied per canvas."""
+    Returns the final canvas, the lock mask and the number of steps applied per canvas.
+    With self-conditioning, the signal starts at zero at step 0; ``state`` (a dict) carries
+    it across calls that split the run (read as state["s"] when start_step > 0, written at
+    the end)."""
     x = np.asarray(x, np.int64).copy()
     lock = np.asarray(lock, np.uint8).copy()
     B = x.shape[0]
+    s = None
+    if start_step > 0 and state is not None:
+        s = state.get("s")
     _, jump_thr = schedule_thresholds(schedule, T)
     steps = np.zeros(B, np.int64)
     active = np.ones(B, bool)
@@ -448,13 +522,18 @@ def denoise_loop(model, k_pre, v_pre, window: int, x, lock, T: int, schedule: in
     for n in range(start_step, end):
         if not active.any():
             break
-        x_new, lock_new, _, done, _ = denoise_step(model, k_pre, v_pre, window, x, lock, n,
-                                                   int(jump_thr[n]), inv_tau, lock_logthr, seed)
+        x_new, lock_new, _, done, post = denoise_step(model, k_pre, v_pre, window, x, lock, n,
+                                                      int(jump_thr[n]), inv_tau, lock_logthr,
+                                                      seed, s)
         x[active] = x_new[active]
         lock[active] = lock_new[active]
         steps[active] += 1
+        if "s" in post:
+            s = post["s"] if s is None else np.where(active[:, None, None], post["s"], s)
         if stop_when_all_locked:
             active &= ~done.astype(bool)
+    if state is not None:
+        state["s"] = s
     return x, lock, steps
 
 
@@ -545,14 +624,12 @@ def entropy_bounded_update(x0hat, top1, entropy, prev_top1, seed: int, step: int
 
 def eb_denoise_step(model, k_pre, v_pre, window: int, x, n: int, inv_tau: float,
                     prev_top1, seed: int, gamma: float, stop_entropy: float,
-                    final_step: bool):
-    """logits = Decoder(x_t, KV); p_hat = Softmax(logits / tau_n); entropy-bounded update."""
-    E, H, Hkv, hd = model["E"], model["H"], model["Hkv"], model["hd"]
+                    final_step: bool, s=None):
+    """logits = Decoder(x_t, KV, s_t); p_hat = Softmax(logits / tau_n); entropy-bounded
+    update (and the next self-conditioning signal in post["s"] when the model has one)."""
+    E = model["E"]
     B, L = np.asarray(x).shape
-    h, q, kc, vc = decoder_front(x, E, model["Wqkv"], H, Hkv, hd)
-    O, _ = canvas_attention(q, k_pre, v_pre, kc, vc, window, hd ** -0.5)
-    y = decoder_back(h, O, model["Wo"])
-    post = posterior(y.reshape(B * L, -1), E, inv_tau, seed, n, L)
+    post = decoder_posterior(model, k_pre, v_pre, window, x, n, inv_tau, seed, s)
     shape = (B, L)
     x_out, accept, done, mh = entropy_bounded_update(
         post["x0hat"].reshape(shape), post["top1"].reshape(shape),
@@ -577,13 +654,17 @@ def eb_denoise_loop(model, k_pre, v_pre, window: int, x, T: int, tau_start: floa
     steps = np.zeros(B, np.int64)
     active = np.ones(B, bool)
     prev = None
+    s = None
     for n in range(T):
         if not active.any():
             break
         x_new, _, done, _, post = eb_denoise_step(model, k_pre, v_pre, window, x, n, inv[n],
-                                                  prev, seed, gamma, stop_entropy, n == T - 1)
+                                                  prev, seed, gamma, stop_entropy, n == T - 1,
+                                                  s)
         x[active] = x_new[active]
         steps[active] += 1
+        if "s" in post:
+            s = post["s"] if s is None else np.where(active[:, None, None], post["s"], s)
         top1 = post["top1"].reshape(B, L)
         prev = top1 if prev is None else np.where(active[:, None], top1, prev)
         active &= ~done.astype(bool)

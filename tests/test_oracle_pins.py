@@ -724,3 +724,141 @@ def test_block_generate_with_delta_posterior_and_eos():
         assert steps[b] == nb * T
         assert np.array_equal(kc[b, :P0], k_ctx[b])
     assert blocks[0] <= 2
+
+
+# ------------------------------------------------------------- self-conditioning -----
+
+def test_gelu_tanh_matches_torch_and_its_symmetry():
+    """The tanh-form GELU against torch's independent implementation, its values at 0 and in
+    the tails, and gelu(x) - gelu(-x) = x (the gate and its mirror add up to one)."""
+    x = np.linspace(-12.0, 12.0, 4001)
+    ref = torch.nn.functional.gelu(torch.tensor(x), approximate="tanh").numpy()
+    assert np.abs(O.gelu_tanh(x) - ref).max() <= 1e-15
+    assert O.gelu_tanh(0.0) == 0.0
+    assert abs(O.gelu_tanh(12.0) - 12.0) < 1e-12 and abs(O.gelu_tanh(-12.0)) < 1e-12
+    assert np.abs(O.gelu_tanh(x) - O.gelu_tanh(-x) - x).max() <= 1e-13
+
+
+def test_expected_embedding_closed_forms():
+    """p_hat . E for (a) E = c I: the softmax itself scaled by c (scipy); (b) y = 0: the mean
+    embedding row; (c) one logit ahead by 60 nats: that row of E; (d) brute force over a
+    5-token vocabulary with explicit loops."""
+    from scipy.special import softmax
+
+    rng = np.random.default_rng(11)
+    V = d = 32
+    c = 1.7
+    E = c * np.eye(V)
+    y = rng.standard_normal((6, d))
+    e = O.expected_embedding(y, E, 0.8)
+    assert np.abs(e - c * softmax(y @ E.T * 0.8, axis=1)).max() <= 1e-14
+    E2 = rng.standard_normal((50, 8))
+    assert np.abs(O.expected_embedding(np.zeros((3, 8)), E2, 1.3) - E2.mean(axis=0)).max() < 1e-14
+    y3 = np.zeros((1, 8))
+    y3[0, 2] = 1.0
+    E3 = rng.standard_normal((50, 8)) * 0.01
+    E3[17, 2] = 60.0
+    assert np.abs(O.expected_embedding(y3, E3, 1.0)[0] - E3[17]).max() < 1e-20 + 1e-24 * 60
+    E4 = rng.standard_normal((5, 3))
+    y4 = rng.standard_normal((2, 3))
+    for r in range(2):
+        w = [math.exp(0.5 * sum(y4[r, k] * E4[v, k] for k in range(3))) for v in range(5)]
+        tot = sum(w)
+        want = [sum(w[v] / tot * E4[v, j] for v in range(5)) for j in range(3)]
+        assert np.allclose(O.expected_embedding(y4[r:r + 1], E4, 0.5)[0], want, rtol=1e-13,
+                           atol=1e-15)
+
+
+def test_expected_embedding_is_invariant_to_vocabulary_order():
+    """Relabelling the vocabulary (a permutation of E's rows) changes nothing."""
+    rng = np.random.default_rng(12)
+    E = rng.standard_normal((300, 16))
+    y = rng.standard_normal((4, 16))
+    perm = rng.permutation(300)
+    a = O.expected_embedding(y, E, 1.25)
+    b = O.expected_embedding(y, E[perm], 1.25)
+    assert np.abs(a - b).max() < 1e-13
+
+
+def test_self_condition_feed_forward_layers():
+    """With identity layers s = bf16(gelu(bf16(e))) (torch's GELU); a zero second layer gives
+    s = 0; the first layer acts on e, the second on gelu of the first (a swapped order or a
+    transposed weight fails the rectangular case, checked with torch matmuls)."""
+    rng = np.random.default_rng(13)
+    V, d = 64, 16
+    E = O.round_bf16(rng.standard_normal((V, d)))
+    y = O.round_bf16(rng.standard_normal((5, d)))
+    r = O.self_condition(y, E, 1.0, np.eye(d), np.eye(d))
+    e_b = O.round_bf16(O.expected_embedding(y, E, 1.0))
+    g = torch.nn.functional.gelu(torch.tensor(e_b), approximate="tanh").numpy()
+    assert np.array_equal(r["e"], e_b)
+    assert np.array_equal(r["s"], O.round_bf16(O.round_bf16(g)))
+    assert not O.self_condition(y, E, 1.0, np.eye(d), np.zeros((d, d)))["s"].any()
+    W1 = O.round_bf16(rng.standard_normal((24, d)) * 0.3)
+    W2 = O.round_bf16(rng.standard_normal((d, 24)) * 0.3)
+    r = O.self_condition(y, E, 0.7, W1, W2)
+    tu = torch.nn.functional.gelu(torch.tensor(r["e"]) @ torch.tensor(W1).T, approximate="tanh")
+    u = O.round_bf16(tu.numpy())
+    assert np.array_equal(r["u"], u)
+    assert np.array_equal(r["s"], O.round_bf16((torch.tensor(u) @ torch.tensor(W2).T).numpy()))
+    assert r["s"].shape == (5, d) and r["u"].shape == (5, 24)
+
+
+def _sc_model(V, d, H, Hkv, hd, dsc, seed, w2_scale=0.5):
+    rng = np.random.default_rng(seed)
+    return {"E": O.round_bf16(rng.standard_normal((V, d)) * 0.3),
+            "Wqkv": O.round_bf16(rng.standard_normal(((H + 2 * Hkv) * hd, d)) * 0.2),
+            "Wo": O.round_bf16(rng.standard_normal((d, H * hd)) * 0.2), "H": H, "Hkv": Hkv,
+            "hd": hd, "Wsc1": O.round_bf16(rng.standard_normal((dsc, d)) * 0.3),
+            "Wsc2": O.round_bf16(rng.standard_normal((d, dsc)) * w2_scale)}
+
+
+def test_self_conditioning_signal_enters_the_embedding():
+    """With zero attention weights the decoder output is h itself, so the step's logits are
+    bf16(E[x] + s) E^T: the posterior of a step given s equals the posterior of that y."""
+    V, d, H, Hkv, hd, B, L, P = 128, 32, 2, 1, 16, 2, 8, 4
+    m = _sc_model(V, d, H, Hkv, hd, 32, 14)
+    m["Wqkv"] = np.zeros_like(m["Wqkv"])
+    m["Wo"] = np.zeros_like(m["Wo"])
+    rng = np.random.default_rng(15)
+    kp, vp = rng.standard_normal((2, B, P, Hkv, hd))
+    x = rng.integers(0, V, (B, L))
+    s = O.round_bf16(rng.standard_normal((B, L, d)))
+    post = O.decoder_posterior(m, kp, vp, 0, x, 3, 1.1, 5, s)
+    y = O.round_bf16(m["E"][x] + s).reshape(B * L, d)
+    ref = O.posterior(y, m["E"], 1.1, 5, 3, L)
+    assert np.array_equal(post["x0hat"], ref["x0hat"]) and np.allclose(post["lse"], ref["lse"])
+    want_s = O.self_condition(y, m["E"], 1.1, m["Wsc1"], m["Wsc2"])["s"].reshape(B, L, d)
+    assert np.array_equal(post["s"], want_s)
+    post0 = O.decoder_posterior(m, kp, vp, 0, x, 3, 1.1, 5, None)
+    assert not np.allclose(post0["lse"], post["lse"])
+
+
+def test_self_conditioning_loop_wiring():
+    """A zero second layer makes every signal zero, so the loop equals the loop of the model
+    without self-conditioning; with a real signal the loop differs from it, and splitting the
+    run at step 4 (carrying the signal) reproduces the whole run, for both samplers."""
+    V, d, H, Hkv, hd, B, L, P, T = 256, 32, 2, 1, 16, 2, 16, 8, 8
+    m = _sc_model(V, d, H, Hkv, hd, 32, 16)
+    rng = np.random.default_rng(17)
+    kp, vp = O.round_bf16(rng.standard_normal((2, B, P, Hkv, hd)))
+    x1 = O.initial_canvas(B, L, V, 3)
+    lock = np.zeros((B, L), np.uint8)
+    plain = {k: v for k, v in m.items() if k not in ("Wsc1", "Wsc2")}
+    zero2 = dict(m, Wsc2=np.zeros_like(m["Wsc2"]))
+    args = (kp, vp, 0, x1, lock, T, O.SCHED_LINEAR, 1.0, float("inf"), 3)
+    xp, _, _ = O.denoise_loop(plain, *args)
+    xz, _, _ = O.denoise_loop(zero2, *args)
+    xs, _, ss = O.denoise_loop(m, *args)
+    assert np.array_equal(xp, xz)
+    assert (xs != xp).mean() > 0.05
+    st = {}
+    xh, lh, sh = O.denoise_loop(m, *args, end_step=4, state=st)
+    assert st["s"] is not None and st["s"].any()
+    xb, _, sb = O.denoise_loop(m, kp, vp, 0, xh, lh, T, O.SCHED_LINEAR, 1.0, float("inf"), 3,
+                               start_step=4, state=st)
+    assert np.array_equal(xb, xs) and np.array_equal(sh + sb, ss)
+    ep, _ = O.eb_denoise_loop(plain, kp, vp, 0, x1, T, 0.8, 0.4, 0.1, 0.005, 3)
+    ez, _ = O.eb_denoise_loop(zero2, kp, vp, 0, x1, T, 0.8, 0.4, 0.1, 0.005, 3)
+    es, _ = O.eb_denoise_loop(m, kp, vp, 0, x1, T, 0.8, 0.4, 0.1, 0.005, 3)
+    assert np.array_equal(ep, ez) and not np.array_equal(ep, es)
