@@ -49,6 +49,9 @@ def parse():
                          "blockar: one step = block-AR generation of --blocks canvases after "
                          "the workload's context (denoising loops + encode-append)")
     ap.add_argument("--blocks", type=int, default=4, help="canvases per blockar step")
+    ap.add_argument("--selfcond", type=int, default=0, metavar="D_SC",
+                    help="denoise mode: add a self-conditioning feed-forward of width D_SC "
+                         "(N(0, 0.02) weights; 1920 gives the pages' 7.8M parameters at d 2048)")
     ap.add_argument("--sampler", default="euler", choices=["euler", "eb"],
                     help="euler: the workload's Euler step; eb: entropy-bounded sampler with "
                          "annealing 0.8->0.4, gamma 0.1, stop at mean entropy 0.005, cap T")
@@ -222,7 +225,12 @@ def run_ours(args, w):
     B = w.B
     m = synth.make_model(w, dev)
     kp, vp = synth.make_prefix_kv(w, dev)
-    model = dgc.make_model(m["E"], m["Wqkv"], m["Wo"], w.H, w.Hkv, w.hd)
+    sc = args.selfcond
+    if sc:
+        m["Wsc1"] = synth.normal_bf16((sc, w.d), 0.02, 1000 * w.seed + 6, dev)
+        m["Wsc2"] = synth.normal_bf16((w.d, sc), 0.02, 1000 * w.seed + 7, dev)
+    model = dgc.make_model(m["E"], m["Wqkv"], m["Wo"], w.H, w.Hkv, w.hd, m.get("Wsc1"),
+                           m.get("Wsc2"))
     lock_thr = math.log(w.lock_theta) if w.lock_theta else math.inf
     lock_thr = float(np.float32(lock_thr))
     ws = dgc.workspace(dgc.dg_denoise_loop_workspace(model, B, w.L, w.P, w.window), dev)
@@ -272,6 +280,7 @@ def run_ours(args, w):
     ms = ev0.elapsed_time(ev1)
     vocab_ms, vocab_n = dgc.dg_kernel_timer_read(0)
     attn_ms, attn_n = dgc.dg_kernel_timer_read(1)
+    sc_ms, sc_n = dgc.dg_kernel_timer_read(2)
     dgc.dg_kernel_timer_enable(False)
     dgc.dg_workspace_status(ws)
     ms = replicas.max_over_ranks(ms)
@@ -328,6 +337,13 @@ def run_ours(args, w):
                 "launches": vocab_n, "avg_ms": vocab_avg_s * 1000.0,
                 "hbm_frac": (2.0 * w.V * w.d + 2.0 * B * w.L * w.d) / vocab_avg_s / 1e9 / hbm,
                 "attention_avg_ms": attn_ms / max(attn_n, 1)}
+    if sc:  # the self-conditioning contraction p_hat E: the same FLOPs as the LM head
+        sc_avg_s = sc_ms / max(sc_n, 1) / 1000.0
+        roofline["selfcond_contraction"] = {
+            "kernel": "sc_gemm_kernel", "avg_ms": sc_avg_s * 1000.0, "launches": sc_n,
+            "achieved_tflops": flops_per_launch / sc_avg_s / 1e12 if sc_n else None,
+            "hbm_gbs_algorithmic": (2.0 * w.V * w.d + 2.0 * B * w.L * w.V) / sc_avg_s / 1e9
+            if sc_n else None}
     # the entropy-bounded sampler launches one more kernel (its update) per denoising step
     launches = args.steps * (1 + dgc.dg_denoise_loop_kernel_count(model, B, w.L, w.P, w.window,
                                                                   w.T) + (w.T if eb else 0))
@@ -349,7 +365,8 @@ def run_ours(args, w):
                                          "uniform-prior canvases)",
                 "config": {"workload": w.describe() + (
                                "; entropy-bounded sampler (tau 0.8->0.4, gamma 0.1, stop at mean "
-                               "entropy 0.005, cap T)" if eb else ""),
+                               "entropy 0.005, cap T)" if eb else "") + (
+                               f"; self-conditioning FFW d_sc {sc}" if sc else ""),
                            "global_batch": B * world, "seq_len": w.L,
                            "prefix": w.P, "denoise_steps": w.T,
                            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",

@@ -110,7 +110,7 @@ std::mutex g_timer_mu;
 bool g_timer_on = false;
 std::vector<cudaEvent_t> g_timer_pool;
 std::vector<TimerRec> g_timer_recs;
-cudaEvent_t g_timer_open[2] = {nullptr, nullptr};
+cudaEvent_t g_timer_open[3] = {nullptr, nullptr, nullptr};
 
 cudaEvent_t timer_event() {
   if (!g_timer_pool.empty()) {
@@ -221,8 +221,16 @@ struct LoopWs {
   VocabPart* parts;
   int32_t *x0hat, *top1, *prev_top1;  // entropy-bounded sampler
   float* entropy;
+  // self-conditioning (empty without it): bf16 exp(z~ - m_ref) [BL, V], m_ref [BL, V/32],
+  // lse [BL], split partials, e [BL, d], u [BL, d_sc] and the signal s [BL, d], which stays
+  // in the workspace between calls so that a split run resumes with it
+  uint16_t* sc_p;
+  float *sc_m, *sc_lse, *sc_part;
+  uint16_t *sc_e, *sc_u, *sc_s;
   size_t total;
 };
+
+bool has_sc(const dg_model* m) { return m->Wsc1 != nullptr; }
 
 LoopWs loop_layout(const dg_model* m, int B, int L, int P, int window, uint8_t* base) {
   LoopWs w{};
@@ -251,6 +259,16 @@ LoopWs loop_layout(const dg_model* m, int B, int L, int P, int window, uint8_t* 
   w.top1 = reinterpret_cast<int32_t*>(take(BL * 4));
   w.prev_top1 = reinterpret_cast<int32_t*>(take(BL * 4));
   w.entropy = reinterpret_cast<float*>(take(BL * 4));
+  if (has_sc(m)) {
+    const ScPlan sp = plan_selfcond(static_cast<int>(BL), m->V, m->d);
+    w.sc_s = reinterpret_cast<uint16_t*>(take(BL * m->d * 2));
+    w.sc_p = reinterpret_cast<uint16_t*>(take(BL * m->V * 2));
+    w.sc_m = reinterpret_cast<float*>(take(BL * (m->V / 32) * 4));
+    w.sc_lse = reinterpret_cast<float*>(take(BL * 4));
+    w.sc_part = reinterpret_cast<float*>(take(sp.part_bytes));
+    w.sc_e = reinterpret_cast<uint16_t*>(take(BL * m->d * 2));
+    w.sc_u = reinterpret_cast<uint16_t*>(take(BL * m->d_sc * 2));
+  }
   w.total = off;
   return w;
 }
@@ -276,6 +294,13 @@ dg_status check_model(const dg_model* m) {
   if (m->V % 256 != 0) return fail(DG_ENOTSUP, "model: V must be a multiple of 256");
   if (m->hd != 64 && m->hd != 128) return fail(DG_ENOTSUP, "model: hd must be 64 or 128");
   if (m->H % m->Hkv != 0) return fail(DG_EINVAL, "model: H must be a multiple of Hkv");
+  if (m->Wsc1 != nullptr || m->Wsc2 != nullptr || m->d_sc != 0) {
+    if (bad_ptr(m->Wsc1) || bad_ptr(m->Wsc2) || m->d_sc <= 0)
+      return fail(DG_EINVAL, "model: self-conditioning needs Wsc1, Wsc2 and d_sc > 0");
+    if (m->d_sc % 64 != 0) return fail(DG_ENOTSUP, "model: d_sc must be a multiple of 64");
+    if (m->d % 256 != 0)
+      return fail(DG_ENOTSUP, "model: self-conditioning needs d to be a multiple of 256");
+  }
   return DG_OK;
 }
 
@@ -285,7 +310,7 @@ extern "C" {
 
 const char* dg_last_error(void) { return g_last_error.c_str(); }
 
-int dg_abi_version(void) { return 2; }
+int dg_abi_version(void) { return 3; }
 
 dg_status dg_schedule_thresholds(int schedule, int T, uint64_t* keep_thr, uint64_t* jump_thr) {
   if (T < 1) return fail(DG_EINVAL, "schedule: T must be >= 1");
@@ -650,8 +675,11 @@ int dg_denoise_loop_kernel_count(const dg_model* m, int B, int L, int P, int win
     return -1;
   const AttnPlan ap = plan_attention(B, L, P, m->H, m->Hkv, m->hd, window);
   // loop init, then per step: embedding gather, QKV GEMM, attention (+ split merge),
-  // output projection, vocabulary pass, finalisation
-  return 1 + steps * (6 + (ap.splits > 1 ? 1 : 0));
+  // output projection, vocabulary pass, finalisation; with self-conditioning, every step but
+  // the run's last (counted here as the last of these `steps`) adds the rescale, the
+  // contraction, its reduction and the two feed-forward GEMMs
+  const int sc_steps = m->Wsc1 != nullptr && steps > 0 ? steps - 1 : 0;
+  return 1 + steps * (6 + (ap.splits > 1 ? 1 : 0)) + 5 * sc_steps;
 }
 
 }  // extern "C"
@@ -745,8 +773,12 @@ dg_status run_denoise(const RunArgs& a, const dg_sampler_cfg* cfg,
   const float scale = 1.0f / std::sqrt(static_cast<float>(m->hd));
   const uint32_t k0 = static_cast<uint32_t>(a.seed), k1 = static_cast<uint32_t>(a.seed >> 32);
 
+  const bool sc = has_sc(m);
   for (int n = a.start; n < a.end; ++n) {
-    launch_embed_gather(a.canvas, m->E, w.h, BL, m->V, m->d, w.n_active, st);
+    // the signal of the previous step (none at step 0; a resumed run reads the one its
+    // previous call left in the workspace)
+    launch_embed_gather(a.canvas, m->E, w.h, BL, m->V, m->d, w.n_active, st,
+                        sc && n > 0 ? w.sc_s : nullptr);
     if ((s = check_launch("loop: embed launch")) != DG_OK) return s;
     e = launch_gemm(w.h, m->Wqkv, BL, Hhd + 2 * KVhd, m->d, qkv, nullptr, 0, w.status, w.n_active,
                     st);
@@ -756,14 +788,18 @@ dg_status run_denoise(const RunArgs& a, const dg_sampler_cfg* cfg,
     if (e != cudaSuccess) return cuda_fail(e, "loop: attention launch");
     e = launch_gemm(w.o, m->Wo, BL, m->d, Hhd, yo, w.h, m->d, w.status, w.n_active, st);
     if (e != cudaSuccess) return cuda_fail(e, "loop: out_proj gemm launch");
-    e = launch_vocab_pass(w.y, m->E, BL, L, m->d, m->V, eb ? eb_inv_tau[n] : cfg->inv_tau,
-                          a.seed, n, w.parts, w.status, w.n_active, st, nullptr, eb);
+    const bool sc_next = sc && n < cfg->T - 1;  // the last step's signal is never used
+    const float inv_tau = eb ? eb_inv_tau[n] : cfg->inv_tau;
+    e = launch_vocab_pass(w.y, m->E, BL, L, m->d, m->V, inv_tau, a.seed, n, w.parts, w.status,
+                          w.n_active, st, nullptr, eb, sc_next ? w.sc_p : nullptr,
+                          sc_next ? w.sc_m : nullptr);
     if (e != cudaSuccess) return cuda_fail(e, "loop: vocab pass launch");
     FinalizeParams fp{};
     fp.parts = w.parts;
     fp.num_mt = vp.num_mt;
     fp.S = vp.S;
     fp.L = L;
+    if (sc_next) fp.out_lse = w.sc_lse;
     if (eb) {  // posterior only; the entropy-bounded kernel makes the step
       fp.out_x0hat = w.x0hat;
       fp.out_top1 = w.top1;
@@ -793,24 +829,30 @@ dg_status run_denoise(const RunArgs& a, const dg_sampler_cfg* cfg,
       ep.n_active = w.n_active;
       launch_entropy_bounded(ep, B, st);
       if ((s = check_launch("loop: entropy-bounded launch")) != DG_OK) return s;
-      continue;
+    } else {
+      fp.x_in = a.canvas;
+      fp.x_out = a.canvas;
+      fp.lock = a.lock;
+      fp.jump_thr = jump[n];
+      fp.lock_logthr = cfg->lock_logthr;
+      fp.k0 = k0;
+      fp.k1 = k1;
+      fp.step = static_cast<uint32_t>(n);
+      fp.active = w.active;
+      fp.steps_taken = a.steps_taken;
+      fp.n_active = w.n_active;
+      fp.stop_when_all_locked = cfg->stop_when_all_locked;
+      fp.unlocked = w.counters;
+      fp.cta_done = w.counters + B;
+      launch_vocab_finalize(fp, B, st);
+      if ((s = check_launch("loop: finalize launch")) != DG_OK) return s;
     }
-    fp.x_in = a.canvas;
-    fp.x_out = a.canvas;
-    fp.lock = a.lock;
-    fp.jump_thr = jump[n];
-    fp.lock_logthr = cfg->lock_logthr;
-    fp.k0 = k0;
-    fp.k1 = k1;
-    fp.step = static_cast<uint32_t>(n);
-    fp.active = w.active;
-    fp.steps_taken = a.steps_taken;
-    fp.n_active = w.n_active;
-    fp.stop_when_all_locked = cfg->stop_when_all_locked;
-    fp.unlocked = w.counters;
-    fp.cta_done = w.counters + B;
-    launch_vocab_finalize(fp, B, st);
-    if ((s = check_launch("loop: finalize launch")) != DG_OK) return s;
+    if (sc_next) {
+      e = launch_self_condition(w.sc_p, w.sc_m, w.sc_lse, m->E, m->Wsc1, m->Wsc2, BL, m->V,
+                                m->d, m->d_sc, w.sc_part, w.sc_e, w.sc_u, w.sc_s, w.status,
+                                w.n_active, st);
+      if (e != cudaSuccess) return cuda_fail(e, "loop: self-conditioning launch");
+    }
   }
   return DG_OK;
 }
@@ -956,6 +998,82 @@ dg_status dg_denoise_loop(const dg_model* m, const uint16_t* k_pre, const uint16
                      as_stream(stream));
 }
 
+size_t dg_self_condition_workspace(int B, int L, int d, int V, int d_sc) {
+  if (B <= 0 || L <= 0 || d <= 0 || V < 256 || d_sc <= 0) return kStatusBytes;
+  const size_t BL = static_cast<size_t>(B) * L;
+  const VocabPlan vp = plan_vocab(static_cast<int>(BL), V);
+  const ScPlan sp = plan_selfcond(static_cast<int>(BL), V, d);
+  return kStatusBytes + align256(2 * sizeof(int) * static_cast<size_t>(B)) +
+         align256(vp.part_bytes) + align256(BL * V * 2) +
+         align256(BL * (V / 32) * 4) + align256(BL * 4) + align256(sp.part_bytes) +
+         align256(BL * d * 2) + align256(BL * d_sc * 2);
+}
+
+dg_status dg_self_condition(const uint16_t* y, const uint16_t* E, const uint16_t* Wsc1,
+                            const uint16_t* Wsc2, int B, int L, int d, int V, int d_sc,
+                            float inv_tau, uint16_t* s_out, uint16_t* e_out, void* ws,
+                            size_t ws_bytes, void* stream) {
+  if (B < 0 || L <= 0 || d <= 0 || V <= 0 || d_sc <= 0)
+    return fail(DG_EINVAL, "self-condition: bad sizes");
+  if (d % 256 != 0 || V % 256 != 0 || d_sc % 64 != 0)
+    return fail(DG_ENOTSUP, "self-condition: needs d % 256 == 0, V % 256 == 0, d_sc % 64 == 0");
+  if (L > 256 || L % 64 != 0)
+    return fail(DG_ENOTSUP, "self-condition: L must be 64..256, multiple of 64");
+  if (!(inv_tau > 0.f) || !std::isfinite(inv_tau))
+    return fail(DG_EINVAL, "self-condition: bad inv_tau");
+  if (static_cast<int64_t>(B) * L >= (1ll << 31) / 128)
+    return fail(DG_ENOTSUP, "self-condition: too many rows");
+  if (B == 0) return DG_OK;
+  if (bad_ptr(y) || bad_ptr(E) || bad_ptr(Wsc1) || bad_ptr(Wsc2) || bad_ptr(s_out) ||
+      bad_ptr(ws) || (e_out && !aligned16(e_out)))
+    return fail(DG_EINVAL, "self-condition: NULL or misaligned pointer");
+  if (ws_bytes < dg_self_condition_workspace(B, L, d, V, d_sc))
+    return fail(DG_EINVAL, "self-condition: workspace too small");
+  cudaStream_t st = as_stream(stream);
+  const int BL = B * L;
+  const VocabPlan vp = plan_vocab(BL, V);
+  const ScPlan sp = plan_selfcond(BL, V, d);
+  uint8_t* p = static_cast<uint8_t*>(ws);
+  uint32_t* status = reinterpret_cast<uint32_t*>(p);
+  p += kStatusBytes;
+  int* counters = reinterpret_cast<int*>(p);
+  p += align256(2 * sizeof(int) * static_cast<size_t>(B));
+  VocabPart* parts = reinterpret_cast<VocabPart*>(p);
+  p += align256(vp.part_bytes);
+  uint16_t* sc_p = reinterpret_cast<uint16_t*>(p);
+  p += align256(static_cast<size_t>(BL) * V * 2);
+  float* sc_m = reinterpret_cast<float*>(p);
+  p += align256(static_cast<size_t>(BL) * (V / 32) * 4);
+  float* lse = reinterpret_cast<float*>(p);
+  p += align256(static_cast<size_t>(BL) * 4);
+  float* part = reinterpret_cast<float*>(p);
+  p += align256(sp.part_bytes);
+  uint16_t* e_ws = reinterpret_cast<uint16_t*>(p);
+  p += align256(static_cast<size_t>(BL) * d * 2);
+  uint16_t* u = reinterpret_cast<uint16_t*>(p);
+  // the LM head pass without sampling (lse only), storing the exponentials
+  cudaError_t e = launch_vocab_pass(y, E, BL, L, d, V, inv_tau, 0, 0, parts, status, nullptr, st,
+                                    nullptr, false, sc_p, sc_m, true);
+  if (e != cudaSuccess) return cuda_fail(e, "self-condition: vocab pass launch");
+  FinalizeParams fp{};
+  fp.parts = parts;
+  fp.num_mt = vp.num_mt;
+  fp.S = vp.S;
+  fp.L = L;
+  fp.out_lse = lse;
+  dg_status s;
+  e = cudaMemsetAsync(counters, 0, 2 * sizeof(int) * B, st);  // finalisation counters
+  if (e != cudaSuccess) return cuda_fail(e, "self-condition: memset");
+  fp.unlocked = counters;
+  fp.cta_done = counters + B;
+  launch_vocab_finalize(fp, B, st);
+  if ((s = check_launch("self-condition: finalize launch")) != DG_OK) return s;
+  e = launch_self_condition(sc_p, sc_m, lse, E, Wsc1, Wsc2, BL, V, d, d_sc, part,
+                            e_out ? e_out : e_ws, u, s_out, status, nullptr, st);
+  if (e != cudaSuccess) return cuda_fail(e, "self-condition: launch");
+  return DG_OK;
+}
+
 size_t dg_encode_append_workspace(const dg_model* m, int B, int L) {
   if (!m || B <= 0 || L <= 0 || m->d <= 0 || m->Hkv <= 0 || m->hd <= 0) return kStatusBytes;
   return append_layout(m, B, L, nullptr).total;
@@ -1089,7 +1207,7 @@ dg_status dg_kernel_timer_enable(int enable) {
 }
 
 dg_status dg_kernel_timer_read(int kind, double* total_ms, int* launches) {
-  if (!total_ms || !launches || kind < 0 || kind > 1) return fail(DG_EINVAL, "timer: bad arguments");
+  if (!total_ms || !launches || kind < 0 || kind > 2) return fail(DG_EINVAL, "timer: bad arguments");
   std::lock_guard<std::mutex> lk(g_timer_mu);
   double tot = 0.0;
   int n = 0;

@@ -2,6 +2,7 @@
 // finalisation of the fused vocabulary pass (split merge + posterior outputs + Euler step).
 #include "dg_common.cuh"
 #include "kernels.cuh"
+#include "sm103.cuh"
 
 namespace dg {
 
@@ -400,22 +401,38 @@ void launch_block_record(const int32_t* canvas, const int32_t* steps_taken, int3
 }
 
 // h[r, :] = E[x[r], :]; ids outside [0, V) give a zero row.  16 bytes per thread.
+// h = E[x] (+ s, the self-conditioning signal, summed in fp32 and rounded to bf16).
 __global__ void embed_gather_kernel(const int32_t* __restrict__ x, const uint4* __restrict__ E,
-                                    uint4* __restrict__ h, int V, int d16, const int* n_active) {
+                                    const uint4* __restrict__ s, uint4* __restrict__ h, int V,
+                                    int d16, const int* n_active) {
   if (n_active && *n_active == 0) return;
   const int r = blockIdx.x;
   const int id = x[r];
   const bool ok = id >= 0 && id < V;
-  for (int c = threadIdx.x; c < d16; c += blockDim.x)
-    h[static_cast<int64_t>(r) * d16 + c] =
-        ok ? E[static_cast<int64_t>(id) * d16 + c] : make_uint4(0, 0, 0, 0);
+  for (int c = threadIdx.x; c < d16; c += blockDim.x) {
+    uint4 w = ok ? E[static_cast<int64_t>(id) * d16 + c] : make_uint4(0, 0, 0, 0);
+    if (s) {
+      const uint4 a = s[static_cast<int64_t>(r) * d16 + c];
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+      uint32_t ew[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aw[e]));
+        const float2 fe = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ew[e]));
+        ew[e] = pack_bf16x2(fe.x + fa.x, fe.y + fa.y);
+      }
+      w = make_uint4(ew[0], ew[1], ew[2], ew[3]);
+    }
+    h[static_cast<int64_t>(r) * d16 + c] = w;
+  }
 }
 
 void launch_embed_gather(const int32_t* x, const uint16_t* E, uint16_t* h, int BL, int V, int d,
-                         const int* n_active, cudaStream_t st) {
+                         const int* n_active, cudaStream_t st, const uint16_t* s) {
   const int d16 = d / 8;
   const int threads = d16 < 256 ? ((d16 + 31) / 32) * 32 : 256;
   embed_gather_kernel<<<BL, threads, 0, st>>>(x, reinterpret_cast<const uint4*>(E),
+                                              reinterpret_cast<const uint4*>(s),
                                               reinterpret_cast<uint4*>(h), V, d16, n_active);
 }
 

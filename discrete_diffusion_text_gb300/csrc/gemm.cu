@@ -22,7 +22,14 @@ struct GemmParams {
   int ld_res;
   uint32_t* status;
   const int* n_active;
+  int act;  // kActNone or kActGeluTanh, applied after the residual
 };
+
+// GELU, tanh form: x/2 (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
+__device__ __forceinline__ float gelu_tanh(float x) {
+  const float k = 0.7978845608028654f;
+  return 0.5f * x * (1.f + tanhf(k * fmaf(0.044715f * x, x * x, x)));
+}
 
 template <int BN>
 struct GemmLayout {
@@ -138,6 +145,10 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
       }
+      if (p.act == kActGeluTanh) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = gelu_tanh(v[e]);
+      }
       // output segment of this column (static indices only: no local-memory copy of params)
       uint16_t* base = p.out.ptr[0];
       int ld = p.out.ld[0];
@@ -195,7 +206,7 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmPa
 
 cudaError_t launch_gemm(const uint16_t* A, const uint16_t* W, int M, int N, int K,
                         const GemmOut& out, const uint16_t* residual, int ld_res,
-                        uint32_t* status, const int* n_active, cudaStream_t st) {
+                        uint32_t* status, const int* n_active, cudaStream_t st, int act) {
   // Largest N tile that divides every output-segment boundary (a tile never straddles two
   // outputs) and still gives at least two CTAs per SM; 64 otherwise.
   if (N % 64 != 0 || K % kBK != 0) return cudaErrorInvalidValue;
@@ -229,6 +240,7 @@ cudaError_t launch_gemm(const uint16_t* A, const uint16_t* W, int M, int N, int 
   p.ld_res = ld_res;
   p.status = status;
   p.n_active = n_active;
+  p.act = act;
   switch (BN) {
     case 256: return launch_bn<256>(ta, tb, p, st);
     case 128: return launch_bn<128>(ta, tb, p, st);

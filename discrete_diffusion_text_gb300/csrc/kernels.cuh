@@ -76,8 +76,9 @@ void launch_euler_update(const int32_t* x_in, const int32_t* x0hat, const int32_
 void launch_vocab_finalize(const FinalizeParams& p, int B, cudaStream_t st);
 void launch_loop_init(const uint8_t* lock, uint8_t* active, int* n_active, int32_t* steps_taken,
                       int B, int L, int stop_when_all_locked, cudaStream_t st);
+// h = E[x] (+ s when s != NULL: the self-conditioning signal, bf16 [BL, d]).
 void launch_embed_gather(const int32_t* x, const uint16_t* E, uint16_t* h, int BL, int V, int d,
-                         const int* n_active, cudaStream_t st);
+                         const int* n_active, cudaStream_t st, const uint16_t* s = nullptr);
 
 // ---------------------------------------------------------------- projection GEMM -----
 // C[M, N] = A[M, K] W[N, K]^T (+ R[M, N]) in bf16 with fp32 accumulation; the N columns are
@@ -89,9 +90,27 @@ struct GemmOut {
   int ld[3];
 };
 
+constexpr int kActNone = 0;
+constexpr int kActGeluTanh = 1;
 cudaError_t launch_gemm(const uint16_t* A, const uint16_t* W, int M, int N, int K,
                         const GemmOut& out, const uint16_t* residual, int ld_res,
-                        uint32_t* status, const int* n_active, cudaStream_t st);
+                        uint32_t* status, const int* n_active, cudaStream_t st,
+                        int act = kActNone);
+
+// ------------------------------------------------------------ self-conditioning -----
+struct ScPlan {
+  int mt, nt, nkb, per, S;
+  size_t part_bytes;  // fp32 partials [S, R, d]
+};
+ScPlan plan_selfcond(int R, int V, int d);
+// From the vocabulary pass's bf16 exp(z~ - m_ref) [R, V] (rescaled in place to the normalised
+// posterior), m_ref [R, V/32] and lse [R]: e = p_hat E (bf16 [R, d]), u = gelu(e W1^T) (bf16
+// [R, dsc]), s = u W2^T (bf16 [R, d]).  d % 256 == 0, V % 64 == 0, dsc % 64 == 0.
+cudaError_t launch_self_condition(uint16_t* p_til, const float* m_ref, const float* lse,
+                                  const uint16_t* E, const uint16_t* W1, const uint16_t* W2,
+                                  int R, int V, int d, int dsc, float* part, uint16_t* e,
+                                  uint16_t* u, uint16_t* s, uint32_t* status,
+                                  const int* n_active, cudaStream_t st);
 
 // ------------------------------------------------------------------- attention -----
 struct AttnPlan {
@@ -114,10 +133,14 @@ struct VocabPlan {
 VocabPlan plan_vocab(int R, int V);
 // targets != NULL: cross-entropy mode (no Gumbel draws; the tuples carry the target's logit).
 // entropy: the tuples also carry the entropy accumulator (otherwise it stays 0).
+// sc_p, sc_m != NULL: also store bf16 exp(z~ - m_ref) [R, V] and m_ref [R, V / 32] for the
+// self-conditioning contraction.  ce_only: no sampling even without targets (lse only).
 cudaError_t launch_vocab_pass(const uint16_t* y, const uint16_t* W, int R, int L, int d, int V,
                               float inv_tau, uint64_t seed, int step, VocabPart* parts,
                               uint32_t* status, const int* n_active, cudaStream_t st,
-                              const int32_t* targets = nullptr, bool entropy = false);
+                              const int32_t* targets = nullptr, bool entropy = false,
+                              uint16_t* sc_p = nullptr, float* sc_m = nullptr,
+                              bool ce_only = false);
 
 // Optional CUDA-event timing around the heavy kernels (kind 0: vocabulary pass,
 // kind 1: attention).

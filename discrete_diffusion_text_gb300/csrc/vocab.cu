@@ -38,7 +38,9 @@ struct VocabParams {
   int num_mt, nvt, per, S, units;
   float inv_tau;
   uint32_t k0, k1, c3;  // Philox key and counter word 3 (stream tag | step)
-  const int32_t* targets;  // cross-entropy mode: the target token of each row
+  const int32_t* targets;  // cross-entropy mode: the target token of each row (or NULL)
+  uint16_t* sc_p;          // self-conditioning: bf16 exp(z~ - m_ref) [R, V]
+  float* sc_m;             // and m_ref per row and 32-column chunk [R, V / 32]
   VocabPart* parts;
   uint32_t* status;
   const int* n_active;
@@ -114,11 +116,16 @@ __device__ __noinline__ Best gumbel_candidate(Best b, float z, int v, uint32_t p
 // kCE (cross-entropy mode): no Gumbel draws; instead the tempered logit of the row's target
 // token is captured (in the best-sample fields, which that mode does not otherwise use).
 // kEnt: also accumulate t = sum exp(z~ - m)(z~ - m) for the entropy (one FMA per logit).
-template <bool kCE, bool kEnt>
+// kSC: also store the chunk's exp(z~ - m) as bf16 (32 values, 64 bytes at sc_dst) with the
+// reference m it was taken against (at *sc_mdst); NULL pointers for rows past the end.  The
+// normalised posterior of the self-conditioning contraction is that value times
+// exp(m - lse), applied once lse is known.
+template <bool kCE, bool kEnt, bool kSC>
 __device__ __forceinline__ void process_chunk(RowState& st, const float (&z)[32], int vbase,
                                               float inv_tau, uint32_t pos, uint32_t canvas,
                                               const PhiloxKeys& keys, uint32_t k0, uint32_t k1,
-                                              uint32_t c3, int target) {
+                                              uint32_t c3, int target, uint16_t* sc_dst,
+                                              float* sc_mdst) {
   float mx[4] = {z[0], z[1], z[2], z[3]};  // four partial maxima: short dependency chains
 #pragma unroll
   for (int e = 4; e < 32; ++e) mx[e & 3] = fmaxf(mx[e & 3], z[e]);
@@ -145,13 +152,22 @@ __device__ __forceinline__ void process_chunk(RowState& st, const float (&z)[32]
   const float cthr = st.cthr;
   float ps[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums of exp(z~ - m)
   float pt[4] = {0.f, 0.f, 0.f, 0.f};  // and of exp(z~ - m) (z~ - m) log2(e)
+  if (kSC && sc_mdst) *sc_mdst = st.m;
   if (kCE) {
+    uint32_t pk[4];
+    float prev = 0.f;
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
       const float a = fmaf(z[e], scale, -mlog2);
       const float pe = ex2_approx(a);
       ps[e & 3] += pe;
       if (kEnt) pt[e & 3] = fmaf(pe, a, pt[e & 3]);
+      if (kSC) {  // eight values (16 bytes) per store
+        if (e & 1) pk[(e >> 1) & 3] = pack_bf16x2(prev, pe);
+        prev = pe;
+        if ((e & 7) == 7 && sc_dst)
+          *reinterpret_cast<uint4*>(sc_dst + (e - 7)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
     }
     st.s += (ps[0] + ps[1]) + (ps[2] + ps[3]);
     if (kEnt) st.t += ((pt[0] + pt[1]) + (pt[2] + pt[3])) * 0.6931471805599453f;
@@ -167,19 +183,28 @@ __device__ __forceinline__ void process_chunk(RowState& st, const float (&z)[32]
     return;
   }
   uint32_t cand = 0;
+  uint32_t pk[4];
 #pragma unroll
   for (int g4 = 0; g4 < 8; ++g4) {
     const Words4 w = philox4x32_10(static_cast<uint32_t>(vbase >> 2) + g4, pos, canvas, c3, keys);
     const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+    float pv[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int e = g4 * 4 + q;
       const float a = fmaf(z[e], scale, -mlog2);  // (z~ - m) log2(e)
       const float pe = ex2_approx(a);
+      pv[q] = pe;
       ps[q] += pe;
       if (kEnt) pt[q] = fmaf(pe, a, pt[q]);
       const float X = __uint_as_float(0x3F800000u | (u[q] >> 9));
       if (X <= fmaf(pe, cthr, 1.0f)) cand |= 1u << e;
+    }
+    if (kSC) {  // eight values (16 bytes) per store
+      pk[(g4 & 1) * 2] = pack_bf16x2(pv[0], pv[1]);
+      pk[(g4 & 1) * 2 + 1] = pack_bf16x2(pv[2], pv[3]);
+      if ((g4 & 1) && sc_dst)
+        *reinterpret_cast<uint4*>(sc_dst + (g4 - 1) * 4) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
     }
   }
   st.s += (ps[0] + ps[1]) + (ps[2] + ps[3]);
@@ -203,7 +228,7 @@ __device__ __forceinline__ void process_chunk(RowState& st, const float (&z)[32]
   }
 }
 
-template <bool kCE, bool kEnt>
+template <bool kCE, bool kEnt, bool kSC>
 __global__ void __launch_bounds__(kThreads, 1)
     vocab_posterior_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB, VocabParams p) {
@@ -326,7 +351,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = mt * kBM + row_in;
       const uint32_t canvas = static_cast<uint32_t>(row / p.L);
       const uint32_t pos = static_cast<uint32_t>(row % p.L);
-      const int target = kCE && row < p.R ? p.targets[row] : -1;
+      const int target = kCE && p.targets && row < p.R ? p.targets[row] : -1;
+      uint16_t* sc_row = kSC && row < p.R ? p.sc_p + static_cast<int64_t>(row) * p.V : nullptr;
+      float* scm_row = kSC && row < p.R ? p.sc_m + static_cast<int64_t>(row) * (p.V / 32)
+                                        : nullptr;
       RowState st;
       st.m = -INFINITY;
       st.s = 0.f;
@@ -350,10 +378,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(&tempty[buf]);
 #pragma unroll
-        for (int c = 0; c < kGroupCols / 32; ++c)
-          process_chunk<kCE, kEnt>(st, *reinterpret_cast<const float(*)[32]>(&z[c * 32]),
-                             vt * kBN + col + c * 32, p.inv_tau, pos, canvas, keys, p.k0, p.k1,
-                             p.c3, target);
+        for (int c = 0; c < kGroupCols / 32; ++c) {
+          const int vb = vt * kBN + col + c * 32;
+          process_chunk<kCE, kEnt, kSC>(st, *reinterpret_cast<const float(*)[32]>(&z[c * 32]),
+                                        vb, p.inv_tau, pos, canvas, keys, p.k0, p.k1, p.c3,
+                                        target, sc_row ? sc_row + vb : nullptr,
+                                        scm_row ? scm_row + (vb >> 5) : nullptr);
+        }
       }
       // Merge the column groups of each row through shared memory, in group order.
       VocabPart mine;
@@ -423,7 +454,8 @@ VocabPlan plan_vocab(int R, int V) {
 cudaError_t launch_vocab_pass(const uint16_t* y, const uint16_t* W, int R, int L, int d, int V,
                               float inv_tau, uint64_t seed, int step, VocabPart* parts,
                               uint32_t* status, const int* n_active, cudaStream_t st,
-                              const int32_t* targets, bool entropy) {
+                              const int32_t* targets, bool entropy, uint16_t* sc_p,
+                              float* sc_m, bool ce_only) {
   const VocabPlan pl = plan_vocab(R, V);
   CUtensorMap ta, tb;
   const uint64_t dA[2] = {static_cast<uint64_t>(d), static_cast<uint64_t>(R)};
@@ -449,6 +481,8 @@ cudaError_t launch_vocab_pass(const uint16_t* y, const uint16_t* W, int R, int L
   p.k1 = static_cast<uint32_t>(seed >> 32);
   p.c3 = kStreamGumbel | (static_cast<uint32_t>(step) & 0xFFFFFFu);
   p.targets = targets;
+  p.sc_p = sc_p;
+  p.sc_m = sc_m;
   p.parts = parts;
   p.status = status;
   p.n_active = n_active;
@@ -457,8 +491,12 @@ cudaError_t launch_vocab_pass(const uint16_t* y, const uint16_t* W, int R, int L
   const int dev = device_id();
   if (configured_device != dev) {
     cudaError_t e = cudaSuccess;
-    for (auto fn : {vocab_posterior_kernel<false, false>, vocab_posterior_kernel<false, true>,
-                    vocab_posterior_kernel<true, false>})
+    for (auto fn : {vocab_posterior_kernel<false, false, false>,
+                    vocab_posterior_kernel<false, true, false>,
+                    vocab_posterior_kernel<true, false, false>,
+                    vocab_posterior_kernel<false, false, true>,
+                    vocab_posterior_kernel<false, true, true>,
+                    vocab_posterior_kernel<true, false, true>})
       if (e == cudaSuccess)
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  VocabLayout::kSmemBytes);
@@ -466,9 +504,17 @@ cudaError_t launch_vocab_pass(const uint16_t* y, const uint16_t* W, int R, int L
     configured_device = dev;
   }
   timer_begin(0, st);
-  auto fn = targets ? vocab_posterior_kernel<true, false>
-                    : (entropy ? vocab_posterior_kernel<false, true>
-                               : vocab_posterior_kernel<false, false>);
+  // cross-entropy mode (targets, or the self-conditioning pass alone: no sampling), or
+  // sampling with or without the entropy accumulator; each with or without the
+  // self-conditioning store
+  const bool sc = sc_p != nullptr;
+  const bool ce = targets != nullptr || ce_only;
+  auto fn = ce ? (sc ? vocab_posterior_kernel<true, false, true>
+                     : vocab_posterior_kernel<true, false, false>)
+               : entropy ? (sc ? vocab_posterior_kernel<false, true, true>
+                               : vocab_posterior_kernel<false, true, false>)
+                         : (sc ? vocab_posterior_kernel<false, false, true>
+                               : vocab_posterior_kernel<false, false, false>);
   fn<<<pl.grid, kThreads, VocabLayout::kSmemBytes, st>>>(ta, tb, p);
   cudaError_t e = cudaGetLastError();
   timer_end(0, st);

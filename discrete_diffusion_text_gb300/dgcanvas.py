@@ -41,7 +41,7 @@ class DGError(RuntimeError):
 
 class dg_model(ctypes.Structure):
     _fields_ = [("E", _P), ("Wqkv", _P), ("Wo", _P), ("V", _I), ("d", _I), ("H", _I),
-                ("Hkv", _I), ("hd", _I)]
+                ("Hkv", _I), ("hd", _I), ("Wsc1", _P), ("Wsc2", _P), ("d_sc", _I)]
 
 
 class dg_sampler_cfg(ctypes.Structure):
@@ -83,6 +83,8 @@ SIGNATURES = {
     "dg_denoise_loop_workspace": (_SZ, [_P, _I, _I, _I, _I]),
     "dg_denoise_loop_kernel_count": (_I, [_P, _I, _I, _I, _I, _I]),
     "dg_denoise_loop": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+    "dg_self_condition_workspace": (_SZ, [_I, _I, _I, _I, _I]),
+    "dg_self_condition": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _SZ, _P]),
     "dg_encode_append_workspace": (_SZ, [_P, _I, _I]),
     "dg_encode_append": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "dg_block_generate_workspace": (_SZ, [_P, _I, _I, _I, _I, _I]),
@@ -308,12 +310,21 @@ def dg_entropy_bounded_update(x0hat, top1, entropy, x_out, seed: int, step: int,
         stop_entropy, 1 if final_step else 0, _stream(stream)), "dg_entropy_bounded_update")
 
 
-def make_model(E, Wqkv, Wo, H: int, Hkv: int, hd: int) -> dg_model:
+def make_model(E, Wqkv, Wo, H: int, Hkv: int, hd: int, Wsc1=None, Wsc2=None) -> dg_model:
+    """Weights of the stand-in decoder (device bf16); Wsc1 [d_sc, d] and Wsc2 [d, d_sc] turn on
+    self-conditioning."""
     for t, n in ((E, "E"), (Wqkv, "Wqkv"), (Wo, "Wo")):
         _bf16(t, n)
+    if (Wsc1 is None) != (Wsc2 is None):
+        raise ValueError("Wsc1 and Wsc2 go together")
+    d_sc = 0
+    if Wsc1 is not None:
+        _bf16(Wsc1, "Wsc1")
+        _bf16(Wsc2, "Wsc2")
+        d_sc = Wsc1.shape[0]
     V, d = E.shape
-    m = dg_model(_ptr(E), _ptr(Wqkv), _ptr(Wo), V, d, H, Hkv, hd)
-    m._keep = (E, Wqkv, Wo)
+    m = dg_model(_ptr(E), _ptr(Wqkv), _ptr(Wo), V, d, H, Hkv, hd, _ptr(Wsc1), _ptr(Wsc2), d_sc)
+    m._keep = (E, Wqkv, Wo, Wsc1, Wsc2)
     return m
 
 
@@ -349,6 +360,24 @@ def dg_denoise_loop(m: dg_model, k_pre, v_pre, window: int, canvas, lock, steps_
                                   _ptr(v_pre) if P > 0 else None, B, L, P, window, _ptr(canvas),
                                   _ptr(lock), _ptr(steps_taken), ctypes.byref(cfg), _ptr(ws),
                                   ws.numel(), _stream(stream)), "dg_denoise_loop")
+
+
+def dg_self_condition_workspace(B, L, d, V, d_sc) -> int:
+    return load().dg_self_condition_workspace(B, L, d, V, d_sc)
+
+
+def dg_self_condition(y, E, Wsc1, Wsc2, B: int, L: int, inv_tau: float, s_out, ws, e_out=None,
+                      stream=None):
+    """y bf16 [B*L, d]; E bf16 [V, d]; Wsc1 bf16 [d_sc, d]; Wsc2 bf16 [d, d_sc]; s_out bf16
+    [B*L, d] (out); e_out bf16 [B*L, d] (out, optional: the expected embedding p_hat . E)."""
+    for t, n in ((y, "y"), (E, "E"), (Wsc1, "Wsc1"), (Wsc2, "Wsc2"), (s_out, "s_out")):
+        _bf16(t, n)
+    if e_out is not None:
+        _bf16(e_out, "e_out")
+    V, d = E.shape
+    _check(load().dg_self_condition(_ptr(y), _ptr(E), _ptr(Wsc1), _ptr(Wsc2), B, L, d, V,
+                                    Wsc1.shape[0], inv_tau, _ptr(s_out), _ptr(e_out), _ptr(ws),
+                                    ws.numel(), _stream(stream)), "dg_self_condition")
 
 
 def dg_encode_append_workspace(m: dg_model, B, L) -> int:

@@ -286,6 +286,14 @@ typedef struct {
   const uint16_t* Wqkv;
   const uint16_t* Wo;
   int V, d, H, Hkv, hd;
+  /* Self-conditioning feed-forward [TR "디노이징 반복과 self-conditioning"]: Wsc1 [d_sc, d],
+   * Wsc2 [d, d_sc] bf16, or both NULL (and d_sc = 0) for a decoder without it.  With it, each
+   * step's tempered posterior p_hat gives s = bf16(bf16(gelu(bf16(p_hat E) Wsc1^T)) Wsc2^T)
+   * (tanh-form GELU), and the next step's embeddings are h = bf16(E[x] + s); s is zero at
+   * step 0.  Needs d % 256 == 0 and d_sc % 64 == 0. */
+  const uint16_t* Wsc1;
+  const uint16_t* Wsc2;
+  int d_sc;
 } dg_model;
 
 typedef enum {
@@ -332,6 +340,25 @@ dg_status dg_sft_loss(const dg_model* m, const uint16_t* k_pre, const uint16_t* 
                       int L, int P, int window, const int32_t* x0, const uint64_t* keep_thr,
                       uint64_t seed, float inv_tau, int32_t* xt, float* loss, void* ws,
                       size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------ self-conditioning ----
+ * s_(t-h) = FFW(p_hat_0 . E) [TR "디노이징 반복과 self-conditioning"], alone (the denoising loop
+ * runs the same kernels when the model carries Wsc1/Wsc2):
+ *   p_hat = Softmax(y E^T * inv_tau) per row; e = bf16(p_hat E); u = bf16(gelu(e Wsc1^T))
+ *   (tanh-form GELU); s = bf16(u Wsc2^T).
+ * The LM-head pass stores bf16 exp(z~ - m) (m: its running maximum, recorded per 32 entries),
+ * rescales it by exp(m - lse) once lse is known, and contracts it with E on the tensor cores
+ * (split over the vocabulary, partial sums added in a fixed order: deterministic).
+ *   y [B*L, d], E [V, d], Wsc1 [d_sc, d], Wsc2 [d, d_sc] bf16 (device); s_out [B*L, d] bf16
+ *   out; e_out [B*L, d] bf16 out or NULL.  ws: at least dg_self_condition_workspace(B, L, d,
+ *   V, d_sc) bytes (status word first; it holds B*L*V*2 bytes of posterior).
+ *   Limits: d % 256 == 0, V % 256 == 0, d_sc % 64 == 0, L a multiple of 64 up to 256.
+ */
+size_t dg_self_condition_workspace(int B, int L, int d, int V, int d_sc);
+dg_status dg_self_condition(const uint16_t* y, const uint16_t* E, const uint16_t* Wsc1,
+                            const uint16_t* Wsc2, int B, int L, int d, int V, int d_sc,
+                            float inv_tau, uint16_t* s_out, uint16_t* e_out, void* ws,
+                            size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------- encode-append and block-AR loop ----
  * [TR "블록 자기회귀(Block-AR) 생성": context encoding, denoising loop, encode-append, repeated
@@ -381,11 +408,12 @@ dg_status dg_block_generate(const dg_model* m, uint16_t* k_cache, uint16_t* v_ca
 /* ----------------------------------------------------------------- status and timing ----
  * dg_workspace_status: synchronises `stream`, reads and clears the status word at the start
  * of a workspace used by dg_canvas_attn, dg_vocab_posterior_step, dg_denoise_loop,
- * dg_encode_append or dg_block_generate, and
+ * dg_encode_append, dg_block_generate or dg_self_condition, and
  * returns DG_OK, DG_ETIMEOUT or DG_EKERNEL accordingly (DG_ECUDA if the stream failed).
  *
  * dg_kernel_timer_enable(1) makes the library record CUDA events on the launching stream
- * around every launch of its LM-head/posterior kernel (kind 0) and attention kernels (kind 1);
+ * around every launch of its LM-head/posterior kernel (kind 0), attention kernels (kind 1)
+ * and self-conditioning contraction (kind 2);
  * dg_kernel_timer_read synchronises those events and returns the summed milliseconds and the
  * number of launches since the last reset; dg_kernel_timer_enable(0) stops and resets.
  */

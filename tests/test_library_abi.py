@@ -48,7 +48,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert lib.dg_abi_version() == 2
+    assert lib.dg_abi_version() == 3
 
 
 @pytest.mark.parametrize("T", [1, 2, 12, 48])
