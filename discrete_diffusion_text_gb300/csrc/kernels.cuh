@@ -103,10 +103,11 @@ struct ScPlan {
   size_t part_bytes;  // fp32 partials [S, R, d]
 };
 ScPlan plan_selfcond(int R, int V, int d);
-// From the vocabulary pass's bf16 exp(z~ - m_ref) [R, V] (rescaled in place to the normalised
-// posterior), m_ref [R, V/32] and lse [R]: e = p_hat E (bf16 [R, d]), u = gelu(e W1^T) (bf16
-// [R, dsc]), s = u W2^T (bf16 [R, d]).  d % 256 == 0, V % 64 == 0, dsc % 64 == 0.
-cudaError_t launch_self_condition(uint16_t* p_til, const float* m_ref, const float* lse,
+// From the vocabulary pass's bf16 exp(z~ - m_ref) [R, V] (normalised to the posterior on its
+// way through shared memory), m_ref [R, V/32] and lse [R]: e = p_hat E (bf16 [R, d]),
+// u = gelu(e W1^T) (bf16 [R, dsc]), s = u W2^T (bf16 [R, d]).  d % 256 == 0, V % 64 == 0,
+// dsc % 64 == 0.
+cudaError_t launch_self_condition(const uint16_t* p_til, const float* m_ref, const float* lse,
                                   const uint16_t* E, const uint16_t* W1, const uint16_t* W2,
                                   int R, int V, int d, int dsc, float* part, uint16_t* e,
                                   uint16_t* u, uint16_t* s, uint32_t* status,

@@ -4,13 +4,18 @@
 // The vocabulary pass (vocab.cu, self-conditioning instantiation) leaves, for every row r and
 // vocabulary entry v, P~[r, v] = bf16(exp(z~ - m_ref)) together with the reference m_ref of
 // each 32-entry chunk; its finalisation gives lse[r].  Here:
-//   1. sc_rescale_kernel   P_hat = bf16(P~ * exp(m_ref - lse)) in place (HBM-bound stream);
-//   2. sc_gemm_kernel      fp32 partials of e = P_hat E over vocabulary splits: a 128 x 256
+//   1. sc_gemm_kernel      fp32 partials of e = P_hat E over vocabulary splits: a 128 x 256
 //                          tile per CTA on the tensor cores (tcgen05.mma, TMEM accumulator),
-//                          A = P_hat rows (K-major), B = E rows read MN-major (E is [V, d],
-//                          so a 64-row slab of E is the K x N operand as stored);
-//   3. sc_reduce_kernel    e = bf16(sum of the partials, in split order);
-//   4. two projection GEMMs: u = bf16(gelu(e Wsc1^T)), s = bf16(u Wsc2^T).
+//                          A = P~ rows (K-major), B = E rows read MN-major (E is [V, d], so a
+//                          64-row slab of E is the K x N operand as stored).  Each A stage is
+//                          normalised on its way from shared to tensor memory: the four
+//                          epilogue warps (idle until the accumulator is done) read row r's
+//                          64 entries, multiply them by exp(m_ref - lse[r]), re-round to bf16
+//                          and store them into a TMEM ring that the MMA reads as its A operand
+//                          (row r in lane r), so P_hat = bf16(P~ exp(m_ref - lse)) never goes
+//                          back to HBM or to shared memory;
+//   2. sc_reduce_kernel    e = bf16(sum of the partials, in split order);
+//   3. two projection GEMMs: u = bf16(gelu(e Wsc1^T)), s = bf16(u Wsc2^T).
 // The contraction over the 262,144-entry vocabulary is split across CTAs (split-K) so that
 // one canvas still fills the GPU; the CTAs of one split are adjacent in launch order (n tile
 // fastest, then m tile), so the slab of E they share and the rows of P_hat each n tile
@@ -31,37 +36,17 @@ constexpr int kScBBytes = kScBChunk * (kScBN / 64);   // 32 KiB
 constexpr int kScStageBytes = kScABytes + kScBBytes;
 constexpr int kScBarOff = kScStages * kScStageBytes;
 constexpr int kScSmemBytes = kScBarOff + 256 + 1024;
+static_assert(kScStageBytes % 1024 == 0, "stages must keep the 1 KiB swizzle alignment");
 constexpr float kScLog2e = 1.4426950408889634f;
 
 struct ScGemmParams {
-  int R, d, nkb, per;
-  float* part;  // [S, R, d]
+  int R, d, V, nkb, per;
+  const float* m_ref;  // [R, V / 32]
+  const float* lse;    // [R]
+  float* part;         // [S, R, d]
   uint32_t* status;
   const int* n_active;
 };
-
-__global__ void sc_rescale_kernel(uint4* __restrict__ p, const float* __restrict__ m_ref,
-                                  const float* __restrict__ lse, int R, int V,
-                                  const int* n_active) {
-  if (n_active && *n_active == 0) return;
-  const int v8 = V / 8;
-  const int64_t n = static_cast<int64_t>(R) * v8;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int r = static_cast<int>(i / v8);
-    const int c = static_cast<int>(i - static_cast<int64_t>(r) * v8);
-    const float f =
-        ex2_approx((m_ref[static_cast<int64_t>(r) * (V / 32) + (c >> 2)] - lse[r]) * kScLog2e);
-    uint4 w = p[i];
-    uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[e]));
-      ws[e] = pack_bf16x2(x.x * f, x.y * f);
-    }
-    p[i] = make_uint4(ws[0], ws[1], ws[2], ws[3]);
-  }
-}
 
 __global__ void __launch_bounds__(192, 1)
     sc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -72,7 +57,8 @@ __global__ void __launch_bounds__(192, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kScBarOff);
   uint64_t* empty = full + kScStages;
-  uint64_t* acc_full = empty + kScStages;
+  uint64_t* scaled = empty + kScStages;  // [kScStages]: A slot in TMEM written, MMA may read
+  uint64_t* acc_full = scaled + kScStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -87,13 +73,16 @@ __global__ void __launch_bounds__(192, 1)
     for (int s = 0; s < kScStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      mbar_init(&scaled[s], 4);  // one arrival per transform warp
     }
     mbar_init(acc_full, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
+  // TMEM: the fp32 accumulator in columns [0, 256); the normalised A operand in a ring of
+  // kScStages slots of 32 columns (64 bf16 per lane) from column 256.
   if (warp == 1) {
-    tmem_alloc(tmem_slot, kScBN);
+    tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -128,23 +117,64 @@ __global__ void __launch_bounds__(192, 1)
       int q = 0;
       for (int kb = kb0; kb < kb1; ++kb, ++q) {
         const int s = q % kScStages;
-        if (!mbar_wait(&full[s], (q / kScStages) & 1, abort_flag)) break;
+        if (!mbar_wait(&scaled[s], (q / kScStages) & 1, abort_flag)) break;
         tc_fence_after();
-        const uint32_t sa = smem_u32(smem + s * kScStageBytes);
-        const uint32_t sb = sa + kScABytes;
+        const uint32_t sb = smem_u32(smem + s * kScStageBytes) + kScABytes;
+        const uint32_t ta = tmem + kScBN + s * 32;
 #pragma unroll
         for (int k = 0; k < kScBK / 16; ++k)
-          mma_bf16_ss(tmem, sdesc_sw128(sa + k * 32, 16, 1024),
-                      sdesc_sw128(sb + k * 2048, kScBChunk, 1024), idesc, (q | k) != 0);
+          mma_bf16_ts(tmem, ta + k * 8, sdesc_sw128(sb + k * 2048, kScBChunk, 1024), idesc,
+                      (q | k) != 0);
         mma_commit(&empty[s]);
       }
       mma_commit(acc_full);
       if (*abort_flag) mbar_wait_drain(acc_full, 0);
     }
   } else {
-    const bool ok = warp_wait(acc_full, 0, abort_flag);
+    // Normalise each A stage: row r's 64 entries (128 bytes in shared memory, its eight
+    // 16-byte chunks permuted by the 128-byte swizzle: logical chunk j sits at j ^ (r & 7))
+    // times exp(m_ref - lse) of their 32-entry chunk, packed in k order into this lane's slot
+    // of the TMEM ring.  The reference maxima are fetched one k-block ahead.
+    const int r_in = (warp & 3) * 32 + lane;
+    const int row = m0 + r_in;
+    const bool live = row < p.R;  // rows past the end are zero-filled by TMA; scaled by 0
+    const float lse = live ? p.lse[row] : 0.f;
+    const float* mrow = p.m_ref + static_cast<int64_t>(live ? row : 0) * (p.V / 32);
+    const uint32_t sw = static_cast<uint32_t>(r_in & 7);
+    const uint32_t lane_base = tmem_lane_base(warp);
+    bool ok = true;
+    float2 mr_next = live ? *reinterpret_cast<const float2*>(mrow + kb0 * 2) : make_float2(0, 0);
+    int q = 0;
+    for (int kb = kb0; kb < kb1; ++kb, ++q) {
+      const int s = q % kScStages;
+      const float2 mr = mr_next;
+      if (live && kb + 1 < kb1) mr_next = *reinterpret_cast<const float2*>(mrow + kb * 2 + 2);
+      if (ok) ok = warp_wait(&full[s], (q / kScStages) & 1, abort_flag);
+      if (ok) {
+        const float c0 = live ? ex2_approx((mr.x - lse) * kScLog2e) : 0.f;
+        const float c1 = live ? ex2_approx((mr.y - lse) * kScLog2e) : 0.f;
+        const uint4* rowp = reinterpret_cast<const uint4*>(
+            smem + s * kScStageBytes + (r_in >> 3) * 1024 + (r_in & 7) * 128);
+        uint32_t pk[32];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float c = j < 4 ? c0 : c1;
+          const uint4 w = rowp[j ^ sw];
+          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[e]));
+            pk[j * 4 + e] = pack_bf16x2(x.x * c, x.y * c);
+          }
+        }
+        tmem_st32(tmem + lane_base + kScBN + s * 32, pk);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&scaled[s]);
+    }
+    ok = ok && warp_wait(acc_full, 0, abort_flag);
     tc_fence_after();
-    const int row = m0 + (warp & 3) * 32 + lane;
     float* dst = p.part + (static_cast<int64_t>(blockIdx.z) * p.R + row) * p.d + n0;
 #pragma unroll 1
     for (int c = 0; c < kScBN / 32; ++c) {
@@ -162,7 +192,7 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kScBN);
+    tmem_dealloc(tmem, 512);
   }
   if (threadIdx.x == 0 && *abort_flag) atomicOr(p.status, kStatusTimeout);
 }
@@ -222,7 +252,7 @@ ScPlan plan_selfcond(int R, int V, int d) {
   return pl;
 }
 
-cudaError_t launch_self_condition(uint16_t* p_til, const float* m_ref, const float* lse,
+cudaError_t launch_self_condition(const uint16_t* p_til, const float* m_ref, const float* lse,
                                   const uint16_t* E, const uint16_t* W1, const uint16_t* W2,
                                   int R, int V, int d, int dsc, float* part, uint16_t* e,
                                   uint16_t* u, uint16_t* s, uint32_t* status,
@@ -230,13 +260,6 @@ cudaError_t launch_self_condition(uint16_t* p_til, const float* m_ref, const flo
   if (d % kScBN != 0 || V % kScBK != 0 || V % 32 != 0 || dsc % 64 != 0)
     return cudaErrorInvalidValue;
   const ScPlan pl = plan_selfcond(R, V, d);
-  {
-    const int64_t n = static_cast<int64_t>(R) * (V / 8);
-    sc_rescale_kernel<<<stream_grid(n, 256), 256, 0, st>>>(reinterpret_cast<uint4*>(p_til),
-                                                           m_ref, lse, R, V, n_active);
-    const cudaError_t err = cudaGetLastError();
-    if (err != cudaSuccess) return err;
-  }
   CUtensorMap ta, tb;
   const uint64_t dA[2] = {static_cast<uint64_t>(V), static_cast<uint64_t>(R)};
   const uint64_t sA[1] = {static_cast<uint64_t>(V) * 2};
@@ -257,6 +280,9 @@ cudaError_t launch_self_condition(uint16_t* p_til, const float* m_ref, const flo
   ScGemmParams gp;
   gp.R = R;
   gp.d = d;
+  gp.V = V;
+  gp.m_ref = m_ref;
+  gp.lse = lse;
   gp.nkb = pl.nkb;
   gp.per = pl.per;
   gp.part = part;
