@@ -116,6 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tmVc, AttnParams p) {
   using Lay = AttnLayout<HD>;
   constexpr int kRing = Lay::kRing;
+  pdl_wait();
   if (p.n_active && *p.n_active == 0) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -412,6 +413,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  // this CTA's work is done: the next kernel in the stream may be scheduled
+  pdl_trigger();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -426,6 +429,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // round trip, and the O loads of consecutive splits are independent.
 template <int HD>
 __global__ void attn_merge_kernel(AttnParams p) {
+  pdl_wait();
+  pdl_trigger();
   if (p.n_active && *p.n_active == 0) return;
   const int64_t rows = static_cast<int64_t>(p.B) * p.H * p.L;
   const int64_t row = blockIdx.x * static_cast<int64_t>(blockDim.x / 32) + (threadIdx.x >> 5);
@@ -490,16 +495,16 @@ cudaError_t launch_hd(const CUtensorMap* maps, const AttnParams& p, cudaStream_t
   }
   dim3 grid(p.units, p.splits);
   timer_begin(1, st);
-  canvas_attn_kernel<HD><<<grid, kThreads, Lay::kSmemBytes, st>>>(maps[0], maps[1], maps[2],
-                                                                  maps[3], maps[4], p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_dependent(canvas_attn_kernel<HD>, grid, dim3(kThreads),
+                                   Lay::kSmemBytes, st, maps[0], maps[1], maps[2], maps[3],
+                                   maps[4], p);
   if (e != cudaSuccess) return e;
   if (p.splits > 1) {
     const int64_t rows = static_cast<int64_t>(p.B) * p.H * p.L;
     const int warps_per_block = 8;
-    attn_merge_kernel<HD><<<static_cast<int>((rows + warps_per_block - 1) / warps_per_block),
-                            32 * warps_per_block, 0, st>>>(p);
-    e = cudaGetLastError();
+    e = launch_dependent(attn_merge_kernel<HD>,
+                         dim3(static_cast<int>((rows + warps_per_block - 1) / warps_per_block)),
+                         dim3(32 * warps_per_block), 0, st, p);
   }
   timer_end(1, st);
   return e;

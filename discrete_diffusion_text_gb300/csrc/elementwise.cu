@@ -122,6 +122,8 @@ __device__ __forceinline__ VocabPart shfl_xor_part(const VocabPart& a, int off) 
 }
 
 __global__ void __launch_bounds__(kFinRows * 32) vocab_finalize_kernel(FinalizeParams p) {
+  pdl_wait();
+  pdl_trigger();
   if (p.n_active && *p.n_active == 0) return;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -205,6 +207,8 @@ __global__ void __launch_bounds__(kFinRows * 32) vocab_finalize_kernel(FinalizeP
 // order and the mean in position order, exactly as the definition states them (no parallel
 // reduction, so the acceptance count and the stop test are bit-reproducible).
 __global__ void __launch_bounds__(1024) entropy_bounded_kernel(EBParams p) {
+  pdl_wait();
+  pdl_trigger();
   if (p.n_active && *p.n_active == 0) return;
   const int b = blockIdx.x;
   if (p.active && p.active[b] == 0) return;  // uniform over the CTA
@@ -278,11 +282,13 @@ __global__ void __launch_bounds__(1024) entropy_bounded_kernel(EBParams p) {
 
 void launch_entropy_bounded(const EBParams& p, int B, cudaStream_t st) {
   const int threads = (p.L + 31) / 32 * 32;
-  entropy_bounded_kernel<<<B, threads, 0, st>>>(p);
+  launch_dependent(entropy_bounded_kernel, dim3(B), dim3(threads), 0, st, p);
 }
 
 void launch_vocab_finalize(const FinalizeParams& p, int B, cudaStream_t st) {
   const int rows = B * p.L;
+  // an ordinary launch: scheduled as a dependent, its CTAs slowed the LM-head kernel's tail
+  // by more than the launch latency they would hide
   vocab_finalize_kernel<<<rows / kFinRows, kFinRows * 32, 0, st>>>(p);
 }
 
@@ -405,6 +411,8 @@ void launch_block_record(const int32_t* canvas, const int32_t* steps_taken, int3
 __global__ void embed_gather_kernel(const int32_t* __restrict__ x, const uint4* __restrict__ E,
                                     const uint4* __restrict__ s, uint4* __restrict__ h, int V,
                                     int d16, const int* n_active) {
+  pdl_wait();
+  pdl_trigger();
   if (n_active && *n_active == 0) return;
   const int r = blockIdx.x;
   const int id = x[r];
@@ -431,9 +439,9 @@ void launch_embed_gather(const int32_t* x, const uint16_t* E, uint16_t* h, int B
                          const int* n_active, cudaStream_t st, const uint16_t* s) {
   const int d16 = d / 8;
   const int threads = d16 < 256 ? ((d16 + 31) / 32) * 32 : 256;
-  embed_gather_kernel<<<BL, threads, 0, st>>>(x, reinterpret_cast<const uint4*>(E),
-                                              reinterpret_cast<const uint4*>(s),
-                                              reinterpret_cast<uint4*>(h), V, d16, n_active);
+  launch_dependent(embed_gather_kernel, dim3(BL), dim3(threads), 0, st, x,
+                   reinterpret_cast<const uint4*>(E), reinterpret_cast<const uint4*>(s),
+                   reinterpret_cast<uint4*>(h), V, d16, n_active);
 }
 
 }  // namespace dg

@@ -13,7 +13,6 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
-constexpr int kStages = 4;
 
 struct GemmParams {
   int M, N, K;
@@ -31,11 +30,14 @@ __device__ __forceinline__ float gelu_tanh(float x) {
   return 0.5f * x * (1.f + tanhf(k * fmaf(0.044715f * x, x * x, x)));
 }
 
+// As many pipeline stages as fit in ~192 KiB: with one or two waves of CTAs that each run a
+// few dozen k-blocks, the copies in flight per SM (not the MMA) set the GEMM's speed.
 template <int BN>
 struct GemmLayout {
   static constexpr int kABytes = kBM * kBK * 2;
   static constexpr int kBBytes = BN * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = (192 * 1024) / kStageBytes;
   static constexpr int kBarOff = kStages * kStageBytes;
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers + 1 KiB alignment slack
 };
@@ -45,13 +47,14 @@ __global__ void __launch_bounds__(192, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, GemmParams p) {
   using Lay = GemmLayout<BN>;
+  pdl_wait();
   if (p.n_active && *p.n_active == 0) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lay::kBarOff);
-  uint64_t* empty = full + kStages;
-  uint64_t* acc_full = empty + kStages;
+  uint64_t* empty = full + Lay::kStages;
+  uint64_t* acc_full = empty + Lay::kStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -62,7 +65,7 @@ __global__ void __launch_bounds__(192, 1)
   const int nkb = p.K / kBK;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < Lay::kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -85,8 +88,8 @@ __global__ void __launch_bounds__(192, 1)
       tma_prefetch_map(&tmB);
       int issued = 0;
       for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % kStages;
-        const uint32_t r = kb / kStages;
+        const int s = kb % Lay::kStages;
+        const uint32_t r = kb / Lay::kStages;
         if (!mbar_wait(&empty[s], (r & 1) ^ 1, abort_flag)) break;
         uint8_t* sa = smem + s * Lay::kStageBytes;
         mbar_arrive_expect_tx(&full[s], Lay::kStageBytes);
@@ -95,16 +98,16 @@ __global__ void __launch_bounds__(192, 1)
         ++issued;
       }
       if (*abort_flag) {  // let copies already in flight land before the CTA exits
-        for (int kb = (issued > kStages ? issued - kStages : 0); kb < issued; ++kb)
-          mbar_wait_drain(&full[kb % kStages], (kb / kStages) & 1);
+        for (int kb = (issued > Lay::kStages ? issued - Lay::kStages : 0); kb < issued; ++kb)
+          mbar_wait_drain(&full[kb % Lay::kStages], (kb / Lay::kStages) & 1);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16(kBM, BN, false);
       for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % kStages;
-        const uint32_t r = kb / kStages;
+        const int s = kb % Lay::kStages;
+        const uint32_t r = kb / Lay::kStages;
         if (!mbar_wait(&full[s], r & 1, abort_flag)) break;
         tc_fence_after();
         const uint32_t sa = smem_u32(smem + s * Lay::kStageBytes);
@@ -175,6 +178,8 @@ __global__ void __launch_bounds__(192, 1)
     }
   }
 
+  // this CTA's work is done: the next kernel in the stream may be scheduled
+  pdl_trigger();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -198,8 +203,7 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmPa
     configured_device = dev;
   }
   dim3 grid(p.N / BN, (p.M + kBM - 1) / kBM);
-  gemm_bf16_kernel<BN><<<grid, 192, Lay::kSmemBytes, st>>>(ta, tb, p);
-  return cudaGetLastError();
+  return launch_dependent(gemm_bf16_kernel<BN>, grid, dim3(192), Lay::kSmemBytes, st, ta, tb, p);
 }
 
 }  // namespace

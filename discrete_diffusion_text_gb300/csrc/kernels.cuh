@@ -1,6 +1,8 @@
 // Launch interfaces of the library's kernels (host side of each translation unit).
 #pragma once
 
+#include <utility>
+
 #include "dg_common.cuh"
 
 namespace dg {
@@ -79,6 +81,25 @@ void launch_loop_init(const uint8_t* lock, uint8_t* active, int* n_active, int32
 // h = E[x] (+ s when s != NULL: the self-conditioning signal, bf16 [BL, d]).
 void launch_embed_gather(const int32_t* x, const uint16_t* E, uint16_t* h, int BL, int V, int d,
                          const int* n_active, cudaStream_t st, const uint16_t* s = nullptr);
+
+// Launch with programmatic stream serialisation: the kernel may be scheduled while the
+// previous kernel in the stream finishes (its launch latency hidden behind that kernel); it
+// must call pdl_wait() before touching global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---------------------------------------------------------------- projection GEMM -----
 // C[M, N] = A[M, K] W[N, K]^T (+ R[M, N]) in bf16 with fp32 accumulation; the N columns are

@@ -51,6 +51,7 @@ struct ScGemmParams {
 __global__ void __launch_bounds__(192, 1)
     sc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    ScGemmParams p) {
+  pdl_wait();
   if (p.n_active && *p.n_active == 0) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -188,6 +189,8 @@ __global__ void __launch_bounds__(192, 1)
     }
   }
 
+  // this CTA's work is done: the next kernel in the stream may be scheduled
+  pdl_trigger();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -200,6 +203,8 @@ __global__ void __launch_bounds__(192, 1)
 // e = bf16(sum_z part[z]) with the splits added in order (deterministic).
 __global__ void sc_reduce_kernel(const float4* __restrict__ part, uint2* __restrict__ e, int S,
                                  int64_t n4, const int* n_active) {
+  pdl_wait();
+  pdl_trigger();
   if (n_active && *n_active == 0) return;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -289,15 +294,15 @@ cudaError_t launch_self_condition(const uint16_t* p_til, const float* m_ref, con
   gp.status = status;
   gp.n_active = n_active;
   timer_begin(2, st);
-  sc_gemm_kernel<<<dim3(pl.nt, pl.mt, pl.S), 192, kScSmemBytes, st>>>(ta, tb, gp);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_dependent(sc_gemm_kernel, dim3(pl.nt, pl.mt, pl.S), dim3(192),
+                                     kScSmemBytes, st, ta, tb, gp);
   timer_end(2, st);
   if (err != cudaSuccess) return err;
   {
     const int64_t n4 = static_cast<int64_t>(R) * d / 4;
-    sc_reduce_kernel<<<stream_grid(n4, 256), 256, 0, st>>>(
-        reinterpret_cast<const float4*>(part), reinterpret_cast<uint2*>(e), pl.S, n4, n_active);
-    err = cudaGetLastError();
+    err = launch_dependent(sc_reduce_kernel, dim3(stream_grid(n4, 256)), dim3(256), 0, st,
+                           reinterpret_cast<const float4*>(part), reinterpret_cast<uint2*>(e),
+                           pl.S, n4, n_active);
     if (err != cudaSuccess) return err;
   }
   GemmOut o1{};

@@ -113,6 +113,17 @@ __device__ __forceinline__ void regs_increase() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// ------------------------------------------------------- programmatic dependent launch ----
+// A kernel launched as a programmatic dependent (launch_dependent below) may start while the
+// previous kernel in the stream is still running; pdl_wait blocks until that kernel has
+// completed and its writes are visible (a no-op for an ordinary launch), and must precede
+// every global-memory access.  pdl_trigger lets the next dependent kernel be scheduled once
+// every CTA of this grid has issued it (or exited); it carries no memory ordering.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------------------- TMA -----
 
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {

@@ -233,6 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     vocab_posterior_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB, VocabParams p) {
   using Lay = VocabLayout;
+  pdl_wait();
   if (p.n_active && *p.n_active == 0) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -407,6 +408,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  // this CTA's work is done: the next kernel in the stream may be scheduled
+  pdl_trigger();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -515,8 +518,8 @@ cudaError_t launch_vocab_pass(const uint16_t* y, const uint16_t* W, int R, int L
                                : vocab_posterior_kernel<false, true, false>)
                          : (sc ? vocab_posterior_kernel<false, false, true>
                                : vocab_posterior_kernel<false, false, false>);
-  fn<<<pl.grid, kThreads, VocabLayout::kSmemBytes, st>>>(ta, tb, p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_dependent(fn, dim3(pl.grid), dim3(kThreads), VocabLayout::kSmemBytes, st,
+                                   ta, tb, p);
   timer_end(0, st);
   return e;
 }
