@@ -371,19 +371,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) ok = warp_wait(&tfull[buf], (j >> 1) & 1, abort_flag);
         if (!ok) continue;
         tc_fence_after();
-        // this thread's 64 columns in one TMEM round trip; the accumulator buffer is handed
-        // back to the MMA warp before the (longer) posterior work on the registers
-        float z[kGroupCols];
+        // this thread's 64 columns, 32 at a time (fewer live registers); the accumulator
+        // buffer goes back to the MMA warp after the second read, which leaves it a whole tile
+        // of slack (the MMA needs this buffer again only after the other one)
         const int col = grp * kGroupCols;
-        tmem_ld64(tmem + lane_base + buf * kBN + col, z);
-        tc_fence_before();
-        mbar_arrive(&tempty[buf]);
-#pragma unroll
+#pragma unroll 1
         for (int c = 0; c < kGroupCols / 32; ++c) {
+          float z[32];
+          tmem_ld32(tmem + lane_base + buf * kBN + col + c * 32, z);
+          if (c == kGroupCols / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(&tempty[buf]);
+          }
           const int vb = vt * kBN + col + c * 32;
-          process_chunk<kCE, kEnt, kSC>(st, *reinterpret_cast<const float(*)[32]>(&z[c * 32]),
-                                        vb, p.inv_tau, pos, canvas, keys, p.k0, p.k1, p.c3,
-                                        target, sc_row ? sc_row + vb : nullptr,
+          process_chunk<kCE, kEnt, kSC>(st, z, vb, p.inv_tau, pos, canvas, keys, p.k0, p.k1,
+                                        p.c3, target, sc_row ? sc_row + vb : nullptr,
                                         scm_row ? scm_row + (vb >> 5) : nullptr);
         }
       }
