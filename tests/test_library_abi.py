@@ -111,3 +111,48 @@ def test_workspace_sizes_are_host_only_and_monotone(lib):
     a = lib.dg_vocab_posterior_workspace(1, 256, 4096)
     assert a >= 256
     assert lib.dg_canvas_attn_workspace(1, 256, 1024, 16, 8, 128, 1024) >= 256
+
+
+def test_argument_validation_of_the_later_rows_without_gpu(lib):
+    """Self-conditioning, encode-append and block-AR generation refuse bad arguments before
+    any device work."""
+    so = lib.load()
+    # self-conditioning: d not a multiple of 256, then NULL pointers
+    assert so.dg_self_condition(None, None, None, None, 1, 256, 192, 4096, 64, 1.0, None, None,
+                                None, 0, None) == lib.DG_ENOTSUP
+    assert so.dg_self_condition(None, None, None, None, 1, 256, 256, 4096, 64, 1.0, None, None,
+                                None, 0, None) == lib.DG_EINVAL
+    assert so.dg_self_condition(None, None, None, None, 1, 256, 256, 4096, 64, 0.0, None, None,
+                                None, 0, None) == lib.DG_EINVAL
+    # a model that names one self-conditioning layer but not the other
+    m = lib.dg_model(None, None, None, 4096, 256, 4, 4, 64, None, None, 128)
+    cfg = lib.make_cfg(12, 0)
+    assert so.dg_denoise_loop(ctypes.byref(m), None, None, 1, 256, 0, 0, None, None, None,
+                              ctypes.byref(cfg), None, 0, None) == lib.DG_EINVAL
+    # encode-append: the appended rows must fit the cache
+    m = lib.dg_model(16, 16, 16, 4096, 256, 4, 4, 64, None, None, 0)
+    assert so.dg_encode_append(ctypes.byref(m), None, None, None, 1, 256, 100, 300, None, None, 0,
+                               None) == lib.DG_EINVAL
+    # block generation: the cache must hold P0 + NB * L rows; every block runs steps 0 .. T-1
+    assert so.dg_block_generate(ctypes.byref(m), None, None, 1, 64, 64 + 3 * 256 - 1, 256, 3, 0,
+                                2, ctypes.byref(cfg), None, None, None, None, None, 0,
+                                None) == lib.DG_EINVAL
+    part = lib.make_cfg(12, 0, start_step=2)
+    assert so.dg_block_generate(ctypes.byref(m), None, None, 1, 64, 64 + 3 * 256, 256, 3, 0, 2,
+                                ctypes.byref(part), None, None, None, None, None, 0,
+                                None) == lib.DG_ENOTSUP
+
+
+def test_later_rows_workspace_sizes_are_host_only(lib):
+    m = lib.dg_model(16, 16, 16, 4096, 256, 4, 4, 64, 16, 16, 128)
+    B, L, V, d = 2, 256, 4096, 256
+    loop = lib.dg_denoise_loop_workspace(m, B, L, 512, 0)
+    plain = lib.dg_denoise_loop_workspace(lib.dg_model(16, 16, 16, 4096, 256, 4, 4, 64, None,
+                                                       None, 0), B, L, 512, 0)
+    # the self-conditioning buffers: at least the bf16 exponentials, B * L * V * 2 bytes
+    assert loop - plain >= B * L * V * 2
+    assert lib.dg_self_condition_workspace(B, L, d, V, 128) >= B * L * V * 2
+    assert lib.dg_encode_append_workspace(m, B, L) >= B * L * d * 2
+    one = lib.dg_block_generate_workspace(m, B, L, 512, 1, 0)
+    four = lib.dg_block_generate_workspace(m, B, L, 512, 4, 0)
+    assert four >= one >= loop
