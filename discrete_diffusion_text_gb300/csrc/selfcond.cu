@@ -95,6 +95,7 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0) {
       tma_prefetch_map(&tmA);
       tma_prefetch_map(&tmB);
+      const uint64_t stream_once = l2_policy_evict_first();
       int issued = 0;
       for (int kb = kb0; kb < kb1; ++kb, ++issued) {
         const int s = issued % kScStages;
@@ -105,7 +106,8 @@ __global__ void __launch_bounds__(192, 1)
         tma_load_2d(sa, &tmA, &full[s], kb * kScBK, m0);
 #pragma unroll
         for (int c = 0; c < kScBN / 64; ++c)
-          tma_load_2d(sa + kScABytes + c * kScBChunk, &tmB, &full[s], n0 + c * 64, kb * kScBK);
+          tma_load_2d_hint(sa + kScABytes + c * kScBChunk, &tmB, &full[s], n0 + c * 64,
+                           kb * kScBK, stream_once);
       }
       if (*abort_flag) {  // let copies already in flight land before the CTA exits
         for (int q = (issued > kScStages ? issued - kScStages : 0); q < issued; ++q)

@@ -275,6 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       tma_prefetch_map(&tmA);
       tma_prefetch_map(&tmB);
+      const uint64_t stream_once = l2_policy_evict_first();
       uint32_t g = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
@@ -289,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t* sa = smem + s * Lay::kStageBytes;
             mbar_arrive_expect_tx(&full[s], Lay::kStageBytes);
             tma_load_2d(sa, &tmA, &full[s], kb * kBK, mt * kBM);
-            tma_load_2d(sa + Lay::kABytes, &tmB, &full[s], kb * kBK, vt * kBN);
+            tma_load_2d_hint(sa + Lay::kABytes, &tmB, &full[s], kb * kBK, vt * kBN, stream_once);
           }
         }
       }
