@@ -110,7 +110,7 @@ std::mutex g_timer_mu;
 bool g_timer_on = false;
 std::vector<cudaEvent_t> g_timer_pool;
 std::vector<TimerRec> g_timer_recs;
-cudaEvent_t g_timer_open[3] = {nullptr, nullptr, nullptr};
+cudaEvent_t g_timer_open[kTimerKinds] = {};
 
 cudaEvent_t timer_event() {
   if (!g_timer_pool.empty()) {
@@ -1207,7 +1207,7 @@ dg_status dg_kernel_timer_enable(int enable) {
 }
 
 dg_status dg_kernel_timer_read(int kind, double* total_ms, int* launches) {
-  if (!total_ms || !launches || kind < 0 || kind > 2) return fail(DG_EINVAL, "timer: bad arguments");
+  if (!total_ms || !launches || kind < 0 || kind >= kTimerKinds) return fail(DG_EINVAL, "timer: bad arguments");
   std::lock_guard<std::mutex> lk(g_timer_mu);
   double tot = 0.0;
   int n = 0;

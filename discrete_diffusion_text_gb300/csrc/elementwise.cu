@@ -287,9 +287,9 @@ void launch_entropy_bounded(const EBParams& p, int B, cudaStream_t st) {
 
 void launch_vocab_finalize(const FinalizeParams& p, int B, cudaStream_t st) {
   const int rows = B * p.L;
-  // an ordinary launch: scheduled as a dependent, its CTAs slowed the LM-head kernel's tail
-  // by more than the launch latency they would hide
-  vocab_finalize_kernel<<<rows / kFinRows, kFinRows * 32, 0, st>>>(p);
+  timer_begin(4, st);
+  launch_dependent(vocab_finalize_kernel, dim3(rows / kFinRows), dim3(kFinRows * 32), 0, st, p);
+  timer_end(4, st);
 }
 
 // Loop bookkeeping: active[b] = 1 unless the canvas is already fully locked and stopping is

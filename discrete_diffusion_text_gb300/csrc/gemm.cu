@@ -245,11 +245,15 @@ cudaError_t launch_gemm(const uint16_t* A, const uint16_t* W, int M, int N, int 
   p.status = status;
   p.n_active = n_active;
   p.act = act;
+  timer_begin(3, st);
+  cudaError_t e;
   switch (BN) {
-    case 256: return launch_bn<256>(ta, tb, p, st);
-    case 128: return launch_bn<128>(ta, tb, p, st);
-    default: return launch_bn<64>(ta, tb, p, st);
+    case 256: e = launch_bn<256>(ta, tb, p, st); break;
+    case 128: e = launch_bn<128>(ta, tb, p, st); break;
+    default: e = launch_bn<64>(ta, tb, p, st); break;
   }
+  timer_end(3, st);
+  return e;
 }
 
 }  // namespace dg

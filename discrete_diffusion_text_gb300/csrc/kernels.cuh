@@ -164,8 +164,9 @@ cudaError_t launch_vocab_pass(const uint16_t* y, const uint16_t* W, int R, int L
                               uint16_t* sc_p = nullptr, float* sc_m = nullptr,
                               bool ce_only = false);
 
-// Optional CUDA-event timing around the heavy kernels (kind 0: vocabulary pass,
-// kind 1: attention).
+// Optional CUDA-event timing around kernels (kind 0: vocabulary pass, 1: attention with its
+// merge, 2: self-conditioning contraction, 3: projection GEMM, 4: finalisation).
+constexpr int kTimerKinds = 5;
 void timer_begin(int kind, cudaStream_t st);
 void timer_end(int kind, cudaStream_t st);
 

@@ -411,10 +411,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  // this CTA's work is done: the next kernel in the stream may be scheduled
-  pdl_trigger();
   tc_fence_before();
   __syncthreads();
+  // every warp of this CTA is done: the next kernel in the stream may be scheduled (not
+  // earlier: its waiting CTAs would share the SM with this kernel's epilogue)
+  pdl_trigger();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);

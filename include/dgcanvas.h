@@ -412,8 +412,9 @@ dg_status dg_block_generate(const dg_model* m, uint16_t* k_cache, uint16_t* v_ca
  * returns DG_OK, DG_ETIMEOUT or DG_EKERNEL accordingly (DG_ECUDA if the stream failed).
  *
  * dg_kernel_timer_enable(1) makes the library record CUDA events on the launching stream
- * around every launch of its LM-head/posterior kernel (kind 0), attention kernels (kind 1)
- * and self-conditioning contraction (kind 2);
+ * around every launch of its LM-head/posterior kernel (kind 0), attention kernels (kind 1),
+ * self-conditioning contraction (kind 2), projection GEMMs (kind 3) and posterior
+ * finalisation (kind 4);
  * dg_kernel_timer_read synchronises those events and returns the summed milliseconds and the
  * number of launches since the last reset; dg_kernel_timer_enable(0) stops and resets.
  */
