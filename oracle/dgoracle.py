@@ -43,9 +43,15 @@ Readings taken where the pages are silent (each listed in the design notes):
 Counter-based random numbers (Philox4x32-10 keyed by the 64-bit seed) replace every random
 draw the method makes, so that both implementations see identical random bits:
   noising / canvas init : counter (pos, canvas, 0, 1<<24); word 0 = keep draw, word 1 = token
-  Gumbel noise          : counter (v>>2, pos, canvas, (2<<24)|step); vocab v uses word v&3
+  chunk Gumbel noise    : counter (c>>2, pos, canvas, (2<<24)|step); chunk c uses word c&3
   Euler jump            : counter (0, pos, canvas, (3<<24)|step); word 0
   re-noising (entropy-bounded sampler) : counter (pos, canvas, 0, (4<<24)|step); word 0
+  within-chunk pick     : counter (c, pos, canvas, (5<<24)|step); word 0
+
+Posterior sample x_hat_0 ~ p_hat_0 (exact, two levels): the vocabulary is cut into aligned
+chunks of 32 entries; a chunk is chosen by Gumbel-max over the chunks' log-sum-exps (so chunk
+c is chosen with probability sum_{v in c} p_v), then an entry of that chunk by inverse CDF in
+vocabulary order (probability p_v / sum_{v' in c} p_v').  The product is p_v.
 
 Entropy-bounded sampler [TR "DiffusionGemma 샘플러"], readings taken where the section is silent:
   * the entropy of a position is that of the tempered posterior used for sampling at the step,
@@ -79,6 +85,8 @@ STREAM_NOISE = 1
 STREAM_GUMBEL = 2
 STREAM_JUMP = 3
 STREAM_RENOISE = 4
+STREAM_PICK = 5
+SAMPLE_CHUNK = 32  # entries per chunk of the two-level posterior sample
 
 SCHED_LINEAR = 0
 SCHED_COSINE = 1
@@ -317,9 +325,54 @@ def decoder_back(h, O, Wo):
 
 
 # ----------------------------------------------------------------------------------------
-# Posterior, Gumbel-max sample, top-1 [TR "디노이징 반복과 self-conditioning":
-# p_hat_0 = Softmax(logits / tau)]
+# Posterior, sample, top-1 [TR "디노이징 반복과 self-conditioning": p_hat_0 = Softmax(logits /
+# tau); x_(t-h) ~ Step(x_t, p_hat_0) draws from p_hat_0]
 # ----------------------------------------------------------------------------------------
+
+def two_level_sample(z, pos, canvas, step: int, seed: int):
+    """One exact draw from Softmax(z) per row of tempered logits z [c, V] (float64):
+
+      lse_c  = log sum_{v in c} exp(z_v)          for the aligned 32-entry chunks c
+      c*     = argmax_c (lse_c + g_c)             (Gumbel-max over chunks, lowest c on ties)
+      x0hat  = the first v of c* with sum_{v' <= v, v' in c*} exp(z_v' - lse_c*) > U
+
+    g_c comes from the chunk Gumbel stream (word c&3 of counter (c>>2, pos, canvas, 2<<24 |
+    step)), U from the pick stream (word 0 of (c*, pos, canvas, 5<<24 | step)).  Returns x0hat
+    and, for the parity bars, the smaller of the gap between the two largest chunk scores and
+    the distance of U from the chunk's cumulative boundaries."""
+    n, V = z.shape
+    nc = (V + SAMPLE_CHUNK - 1) // SAMPLE_CHUNK
+    pad = np.full((n, nc * SAMPLE_CHUNK), -np.inf)
+    pad[:, :V] = z
+    zc = pad.reshape(n, nc, SAMPLE_CHUNK)
+    mc = zc.max(axis=2, keepdims=True)
+    lse_c = (mc + np.log(np.exp(zc - mc).sum(axis=2, keepdims=True)))[:, :, 0]
+    k0, k1 = seed_key(seed)
+    c = np.arange(nc, dtype=np.uint64)
+    words = philox4x32_10(c[None, :] >> np.uint64(2), pos, canvas,
+                          (STREAM_GUMBEL << 24) | int(step), k0, k1)
+    sel = (c & np.uint64(3)).astype(np.int64)[None, :]
+    u = np.choose(np.broadcast_to(sel, (n, nc)), words)
+    score = lse_c + gumbel_from_u32(u)
+    cstar = np.argmax(score, axis=1)
+    if nc > 1:
+        two = -np.partition(-score, 1, axis=1)[:, :2]
+        gap = two[:, 0] - two[:, 1]
+    else:
+        gap = np.full(n, np.inf)
+    w = philox4x32_10(cstar.astype(np.uint64)[:, None], pos, canvas,
+                      (STREAM_PICK << 24) | int(step), k0, k1)[0][:, 0]
+    U = u32_to_open_unit(w)
+    idx = np.arange(n)
+    p = np.exp(zc[idx, cstar] - lse_c[idx, cstar][:, None])   # [n, 32], sums to 1
+    cum = np.cumsum(p, axis=1)
+    # (rounding can leave the last cumulative value a hair below U: the last real entry then)
+    j = np.minimum((cum <= U[:, None]).sum(axis=1),
+                   np.minimum(SAMPLE_CHUNK - 1, V - 1 - cstar * SAMPLE_CHUNK))
+    lo = np.where(j > 0, cum[idx, np.maximum(j - 1, 0)], 0.0)
+    margin = np.minimum(U - lo, cum[idx, j] - U)
+    return cstar * SAMPLE_CHUNK + j, np.minimum(gap, margin)
+
 
 def posterior(y, E, inv_tau: float, seed: int, step: int, L: int, rows=None, chunk=None):
     """Per row r (canvas r // L, position r % L) of y [R, d], with logits z = y E^T
@@ -328,13 +381,13 @@ def posterior(y, E, inv_tau: float, seed: int, step: int, L: int, rows=None, chu
       lse        = log sum_v exp(z~_v)
       top1       = argmax_v z~_v                     (lowest index on ties)
       logp_top1  = z~_top1 - lse
-      x0hat      = argmax_v (z~_v + g_v)              (Gumbel-max sample of Softmax(z~))
+      x0hat      = two_level_sample(z~)                (an exact sample of Softmax(z~))
       logp_x0hat = z~_x0hat - lse
       entropy    = -sum_v p_v log p_v,  p = Softmax(z~)   (clamped at 0 against rounding)
 
-    g_v comes from the Gumbel stream of (step, canvas, position, v).  Also returned, for the
-    parity bars: the gap between the two largest perturbed scores and between the two
-    largest logits.  ``rows`` selects a subset of rows (default: all).
+    Also returned, for the parity bars: the sample's margin (gap_perturbed: see
+    two_level_sample) and the gap between the two largest logits.  ``rows`` selects a subset
+    of rows (default: all).
     """
     y = np.asarray(y, np.float64)
     E64 = np.asarray(E, np.float64)
@@ -343,8 +396,6 @@ def posterior(y, E, inv_tau: float, seed: int, step: int, L: int, rows=None, chu
     rows = np.arange(R) if rows is None else np.asarray(rows, np.int64)
     if chunk is None:  # rows per batch, so that one [rows, V] float64 block stays ~128 MiB
         chunk = max(1, (1 << 24) // V)
-    k0, k1 = seed_key(seed)
-    v = np.arange(V, dtype=np.uint64)
     out = {k: np.zeros(len(rows), np.float64) for k in
            ("lse", "logp_top1", "logp_x0hat", "gap_perturbed", "gap_logit", "entropy")}
     out["top1"] = np.zeros(len(rows), np.int64)
@@ -356,13 +407,8 @@ def posterior(y, E, inv_tau: float, seed: int, step: int, L: int, rows=None, chu
         lse = (m + np.log(np.exp(z - m).sum(axis=1, keepdims=True)))[:, 0]
         canvas = (rr // L).astype(np.uint64)[:, None]
         pos = (rr % L).astype(np.uint64)[:, None]
-        words = philox4x32_10(v[None, :] >> np.uint64(2), pos, canvas,
-                              (STREAM_GUMBEL << 24) | int(step), k0, k1)
-        sel = (v & np.uint64(3)).astype(np.int64)[None, :]
-        u = np.choose(np.broadcast_to(sel, (len(rr), V)), words)
-        score = z + gumbel_from_u32(u)
+        x0hat, margin = two_level_sample(z, pos, canvas, step, seed)
         top1 = np.argmax(z, axis=1)
-        x0hat = np.argmax(score, axis=1)
         idx = np.arange(len(rr))
         sl = slice(s, s + len(rr))
         out["lse"][sl] = lse
@@ -372,8 +418,7 @@ def posterior(y, E, inv_tau: float, seed: int, step: int, L: int, rows=None, chu
         out["logp_x0hat"][sl] = z[idx, x0hat] - lse
         logp = z - lse[:, None]
         out["entropy"][sl] = np.maximum(0.0, -(np.exp(logp) * logp).sum(axis=1))
-        two = -np.partition(-score, 1, axis=1)[:, :2]
-        out["gap_perturbed"][sl] = two[:, 0] - two[:, 1]
+        out["gap_perturbed"][sl] = margin
         twz = -np.partition(-z, 1, axis=1)[:, :2]
         out["gap_logit"][sl] = twz[:, 0] - twz[:, 1]
     return out

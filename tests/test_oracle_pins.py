@@ -281,7 +281,7 @@ def test_decoder_back_is_residual_plus_projection():
 
 def test_posterior_uniform_logits():
     """All logits equal: lse = log V, top-1 is the lowest index, log p = -log V, and the
-    Gumbel-max sample is uniform over the vocabulary."""
+    posterior sample is uniform over the vocabulary."""
     V, d, R, L = 64, 8, 4096, 256
     E = np.random.default_rng(0).standard_normal((V, d))
     y = np.zeros((R, d))
@@ -312,9 +312,10 @@ def test_posterior_normalisation_and_temperature():
     assert np.all(p1["logp_x0hat"] <= p1["logp_top1"] + 1e-12)
 
 
-def test_gumbel_max_samples_the_softmax():
-    """Gumbel-max over 10^6 rows with distinct counters is a categorical draw from
-    Softmax(z / tau): chi-square against the exact probabilities."""
+def test_posterior_sample_is_the_softmax():
+    """The posterior sample over 10^6 rows with distinct counters (one chunk: the inverse-CDF
+    pick alone) is a categorical draw from Softmax(z / tau): chi-square against the exact
+    probabilities."""
     V, d = 16, 16
     z_target = np.linspace(-1.5, 1.0, V)
     E = np.eye(V, d)
@@ -325,6 +326,49 @@ def test_gumbel_max_samples_the_softmax():
     counts = np.bincount(post["x0hat"], minlength=V)
     p = np.exp(z_target / tau - logsumexp(z_target / tau))
     assert stats.chisquare(counts, p * R).pvalue > 1e-3
+
+
+def test_two_level_sample_over_many_chunks_is_the_softmax():
+    """With 8 chunks of different masses (and uneven probabilities inside them), 4 x 10^5
+    draws with distinct counters follow Softmax(z / tau): chi-square against the exact
+    probabilities, per entry and per chunk."""
+    V = 256
+    rng = np.random.default_rng(77)
+    z_target = rng.standard_normal(V) * 1.2
+    z_target[64:96] += 1.5          # one heavy chunk
+    z_target[160:192] -= 2.0        # one light chunk
+    tau = 0.8
+    R, L = 400_000, 1000
+    y = np.broadcast_to(z_target, (R, V))
+    post = O.posterior(y, np.eye(V), 1.0 / tau, seed=99, step=7, L=L, chunk=20000)
+    p = np.exp(z_target / tau - logsumexp(z_target / tau))
+    counts = np.bincount(post["x0hat"], minlength=V)
+    assert stats.chisquare(counts, p * R).pvalue > 1e-3
+    chunk_counts = counts.reshape(8, 32).sum(axis=1)
+    assert stats.chisquare(chunk_counts, p.reshape(8, 32).sum(axis=1) * R).pvalue > 1e-3
+
+
+def test_two_level_sample_hand_cases():
+    """(a) All mass on one entry: always that entry.
+    (b) Two equal entries in different chunks: the chunk whose Gumbel is larger wins (the
+    lower chunk on an exact tie); the pick inside a one-entry chunk is that entry."""
+    V, L = 64, 16
+    z = np.full((6, V), -1e4)
+    z[:, 21] = 3.0
+    x, _ = O.two_level_sample(z, np.arange(6, dtype=np.uint64)[:, None] % L,
+                              np.arange(6, dtype=np.uint64)[:, None] // L, 4, 8)
+    assert np.all(x == 21)
+    z = np.full((40, V), -1e4)
+    z[:, 5] = 0.0
+    z[:, 40] = 0.0
+    pos = np.arange(40, dtype=np.uint64)[:, None] % L
+    can = np.arange(40, dtype=np.uint64)[:, None] // L
+    x, _ = O.two_level_sample(z, pos, can, 2, 31)
+    k0, k1 = O.seed_key(31)
+    w = O.philox4x32_10(0, pos[:, 0], can[:, 0], (O.STREAM_GUMBEL << 24) | 2, k0, k1)
+    g0, g1 = O.gumbel_from_u32(w[0]), O.gumbel_from_u32(w[1])   # chunks 0 and 1: words 0, 1
+    assert np.array_equal(x, np.where(g0 >= g1, 5, 40))
+    assert 5 < (x == 5).sum() < 35
 
 
 def test_posterior_rows_subset_equals_full():
