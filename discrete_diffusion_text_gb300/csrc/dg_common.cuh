@@ -85,6 +85,7 @@ constexpr uint32_t kStreamNoise = 1u << 24;
 constexpr uint32_t kStreamGumbel = 2u << 24;
 constexpr uint32_t kStreamJump = 3u << 24;
 constexpr uint32_t kStreamRenoise = 4u << 24;
+constexpr uint32_t kStreamPick = 5u << 24;
 
 // A draw as a token uniform over [0, V): floor(u * V / 2^32).
 __device__ __forceinline__ int32_t draw_token(uint32_t u, uint32_t V) {

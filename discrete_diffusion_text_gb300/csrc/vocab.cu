@@ -8,15 +8,11 @@
 //                accumulators (2 x 256 columns), so the next tile's MMA overlaps this epilogue;
 //   warps 2..17  epilogue: four groups of four warps, each group one 64-column quarter of the
 //                tile, one thread per row: tempered logits z~ = z / tau, online (max, sum exp)
-//                for the log-sum-exp, the top-1 (lowest index on ties), and the Gumbel-max
-//                sample argmax(z~ + g) with g from Philox.
+//                for the log-sum-exp, the top-1 (lowest index on ties), and the exact
+//                two-level posterior sample: Gumbel-max over aligned 32-entry chunks scored
+//                by their log-sum-exps, then an inverse-CDF pick inside the winning chunk.
 // Only rows' partial tuples are written; a finalisation kernel merges them in a fixed order and
-// applies the Euler step.
-//
-// Gumbel candidates: g_v = -log(E_v) with E_v = -log(1 - W_v) >= W_v (W_v the open-unit draw),
-// so entry v can only beat the current best score b if W_v < exp(z~_v - b).  exp(z~_v - m) is
-// already computed for the sum, so the test costs one multiply; the two logarithms are taken
-// out of line, only for the rare entries that pass (with a safety margin for rounding).
+// applies the Euler step (the chunk scores merge like any Gumbel-max scores).
 #include "kernels.cuh"
 #include "sm103.cuh"
 
@@ -37,7 +33,8 @@ struct VocabParams {
   int R, L, d, V;
   int num_mt, nvt, per, S, units;
   float inv_tau;
-  uint32_t k0, k1, c3;  // Philox key and counter word 3 (stream tag | step)
+  uint32_t k0, k1, c3, c3_pick;  // Philox key; counter word 3 (stream tag | step) of the
+                                 // chunk Gumbel and of the within-chunk pick
   const int32_t* targets;  // cross-entropy mode: the target token of each row (or NULL)
   uint16_t* sc_p;          // self-conditioning: bf16 exp(z~ - m_ref) [R, V]
   float* sc_m;             // and m_ref per row and 32-column chunk [R, V / 32]
@@ -65,56 +62,29 @@ struct RowState {
   float t;       // sum of exp(z~ - m) * (z~ - m): entropy = log s - t / s
   float top_z;
   int top_idx;
-  float best;    // best perturbed score z~ + g
-  int best_idx;
-  float best_z;
-  float cthr;    // exp(m - best) * (1 + margin): candidate test is W < exp(z~ - m) * cthr
+  float best;    // best chunk score lse_c + g_c
+  int best_idx;  // the entry picked inside that chunk
+  float best_z;  // and its tempered logit
 };
-
-__device__ __forceinline__ void refresh_cthr(RowState& st) {
-  // best == -inf: everything is a candidate.
-  st.cthr = st.best == -INFINITY ? INFINITY : __expf(st.m - st.best) * 1.001f;
-}
 
 __device__ __forceinline__ float open_unit(uint32_t u) {
   // W = (u + 1/2) / 2^32, rounded to fp32 (full relative precision near 0)
   return fmaf(__uint2float_rn(u), 2.3283064365386963e-10f, 1.1641532182693481e-10f);
 }
 
-struct Best {
-  float score;
-  int idx;
-  float z;
-};
-
-// The rare path: the exact Gumbel score of one candidate entry v with tempered logit z.
-// Out of line so that the hot loop stays small; scalars in and out (nothing of the hot loop's
-// register state has its address taken).
-__device__ __noinline__ Best gumbel_candidate(Best b, float z, int v, uint32_t pos,
-                                              uint32_t canvas, uint32_t k0, uint32_t k1,
-                                              uint32_t c3) {
-  const Words4 w = philox4x32_10(static_cast<uint32_t>(v >> 2), pos, canvas, c3, k0, k1);
-  const int q = v & 3;
-  const uint32_t u = q == 0 ? w.x : (q == 1 ? w.y : (q == 2 ? w.z : w.w));
-  const float E = -log1pf(-open_unit(u));
-  const float sc = z - logf(E);
-  if (sc > b.score) {
-    b.score = sc;
-    b.idx = v;
-    b.z = z;
-  }
-  return b;
-}
-
-// One 32-column chunk of raw logits z (tempered here: z~ = z * inv_tau, inv_tau > 0).
+// One 32-column chunk of raw logits z (tempered here: z~ = z * inv_tau, inv_tau > 0); the
+// chunk is one of the aligned 32-entry chunks of the two-level posterior sample.
 //  - The chunk max is taken on raw z: rounding is monotone, so max(fl(z * c)) = fl(max(z) * c).
-//  - exp(z~ - m) is one FFMA into ex2: exp2(z * c log2 e - m log2 e).
-//  - Candidate filter without an int-to-float conversion: X = 1 + floor(u / 2^9) * 2^-23 lies in
-//    [1, 2) and X - 1 <= W, so W < t implies X < 1 + t, hence X <= fl(1 + t) (rounding is
-//    monotone and X is representable).  With t = exp(z~ - m) * cthr >= exp(z~ - best) this
-//    never drops an entry that could beat the best score; survivors get the exact test.
-// kCE (cross-entropy mode): no Gumbel draws; instead the tempered logit of the row's target
-// token is captured (in the best-sample fields, which that mode does not otherwise use).
+//  - exp(z~ - m) is one FFMA into ex2: exp2(z * c log2 e - m log2 e); the sum of the chunk's 32
+//    values, sc, is also the chunk's mass relative to the running max.
+//  - Sampling (not kCE): the chunk's score is lse_c + g_c = m + log(sc) + g_c with g_c the chunk
+//    Gumbel (word c&3 of counter (c>>2, pos, canvas, c3)); a chunk that beats the row's best so
+//    far (strictly: an earlier chunk keeps ties) picks its entry at once by inverse CDF in
+//    vocabulary order with one uniform U from the pick stream: the first j whose running sum
+//    of exp(z~ - m) exceeds U sc (the last entry if rounding leaves the sum short).  The draws
+//    cost one Philox call and three logarithms per 32 logits, plus a rare pick.
+// kCE (cross-entropy mode): no draws; instead the tempered logit of the row's target token is
+// captured (in the best-sample fields, which that mode does not otherwise use).
 // kEnt: also accumulate t = sum exp(z~ - m)(z~ - m) for the entropy (one FMA per logit).
 // kSC: also store the chunk's exp(z~ - m) as bf16 (32 values, 64 bytes at sc_dst) with the
 // reference m it was taken against (at *sc_mdst); NULL pointers for rows past the end.  The
@@ -123,8 +93,8 @@ __device__ __noinline__ Best gumbel_candidate(Best b, float z, int v, uint32_t p
 template <bool kCE, bool kEnt, bool kSC>
 __device__ __forceinline__ void process_chunk(RowState& st, const float (&z)[32], int vbase,
                                               float inv_tau, uint32_t pos, uint32_t canvas,
-                                              const PhiloxKeys& keys, uint32_t k0, uint32_t k1,
-                                              uint32_t c3, int target, uint16_t* sc_dst,
+                                              const PhiloxKeys& keys, uint32_t c3,
+                                              uint32_t c3_pick, int target, uint16_t* sc_dst,
                                               float* sc_mdst) {
   float mx[4] = {z[0], z[1], z[2], z[3]};  // four partial maxima: short dependency chains
 #pragma unroll
@@ -145,32 +115,31 @@ __device__ __forceinline__ void process_chunk(RowState& st, const float (&z)[32]
     if (kEnt) st.t = st.s > 0.f ? f * fmaf(st.s, st.m - cm, st.t) : 0.f;  // re-reference
     st.s *= f;
     st.m = cm;
-    refresh_cthr(st);
   }
   const float scale = inv_tau * kLog2e;
   const float mlog2 = st.m * kLog2e;
-  const float cthr = st.cthr;
   float ps[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums of exp(z~ - m)
   float pt[4] = {0.f, 0.f, 0.f, 0.f};  // and of exp(z~ - m) (z~ - m) log2(e)
   if (kSC && sc_mdst) *sc_mdst = st.m;
-  if (kCE) {
-    uint32_t pk[4];
-    float prev = 0.f;
+  uint32_t pk[4];
+  float prev = 0.f;
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      const float a = fmaf(z[e], scale, -mlog2);
-      const float pe = ex2_approx(a);
-      ps[e & 3] += pe;
-      if (kEnt) pt[e & 3] = fmaf(pe, a, pt[e & 3]);
-      if (kSC) {  // eight values (16 bytes) per store
-        if (e & 1) pk[(e >> 1) & 3] = pack_bf16x2(prev, pe);
-        prev = pe;
-        if ((e & 7) == 7 && sc_dst)
-          *reinterpret_cast<uint4*>(sc_dst + (e - 7)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      }
+  for (int e = 0; e < 32; ++e) {
+    const float a = fmaf(z[e], scale, -mlog2);
+    const float pe = ex2_approx(a);
+    ps[e & 3] += pe;
+    if (kEnt) pt[e & 3] = fmaf(pe, a, pt[e & 3]);
+    if (kSC) {  // eight values (16 bytes) per store
+      if (e & 1) pk[(e >> 1) & 3] = pack_bf16x2(prev, pe);
+      prev = pe;
+      if ((e & 7) == 7 && sc_dst)
+        *reinterpret_cast<uint4*>(sc_dst + (e - 7)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
     }
-    st.s += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-    if (kEnt) st.t += ((pt[0] + pt[1]) + (pt[2] + pt[3])) * 0.6931471805599453f;
+  }
+  const float sc = (ps[0] + ps[1]) + (ps[2] + ps[3]);
+  st.s += sc;
+  if (kEnt) st.t += ((pt[0] + pt[1]) + (pt[2] + pt[3])) * 0.6931471805599453f;
+  if (kCE) {
     const int e = target - vbase;
     if (e >= 0 && e < 32) {
       float ze = z[0];
@@ -182,49 +151,26 @@ __device__ __forceinline__ void process_chunk(RowState& st, const float (&z)[32]
     }
     return;
   }
-  uint32_t cand = 0;
-  uint32_t pk[4];
+  const uint32_t c = static_cast<uint32_t>(vbase) >> 5;
+  const Words4 w = philox4x32_10(c >> 2, pos, canvas, c3, keys);
+  const uint32_t q = c & 3;
+  const uint32_t u = q == 0 ? w.x : (q == 1 ? w.y : (q == 2 ? w.z : w.w));
+  const float score = st.m + logf(sc) - logf(-log1pf(-open_unit(u)));
+  if (score > st.best) {
+    const float target_mass = open_unit(philox4x32_10(c, pos, canvas, c3_pick, keys).x) * sc;
+    float cum = 0.f;
+    int j = 31;
 #pragma unroll
-  for (int g4 = 0; g4 < 8; ++g4) {
-    const Words4 w = philox4x32_10(static_cast<uint32_t>(vbase >> 2) + g4, pos, canvas, c3, keys);
-    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-    float pv[4];
+    for (int e = 0; e < 31; ++e) {
+      cum += ex2_approx(fmaf(z[e], scale, -mlog2));
+      if (j == 31 && cum > target_mass) j = e;
+    }
+    float zj = z[0];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int e = g4 * 4 + q;
-      const float a = fmaf(z[e], scale, -mlog2);  // (z~ - m) log2(e)
-      const float pe = ex2_approx(a);
-      pv[q] = pe;
-      ps[q] += pe;
-      if (kEnt) pt[q] = fmaf(pe, a, pt[q]);
-      const float X = __uint_as_float(0x3F800000u | (u[q] >> 9));
-      if (X <= fmaf(pe, cthr, 1.0f)) cand |= 1u << e;
-    }
-    if (kSC) {  // eight values (16 bytes) per store
-      pk[(g4 & 1) * 2] = pack_bf16x2(pv[0], pv[1]);
-      pk[(g4 & 1) * 2 + 1] = pack_bf16x2(pv[2], pv[3]);
-      if ((g4 & 1) && sc_dst)
-        *reinterpret_cast<uint4*>(sc_dst + (g4 - 1) * 4) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-    }
-  }
-  st.s += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-  if (kEnt) st.t += ((pt[0] + pt[1]) + (pt[2] + pt[3])) * 0.6931471805599453f;
-  if (cand) {
-    Best b{st.best, st.best_idx, st.best_z};
-    do {  // candidates in increasing vocabulary order
-      const int e = __ffs(cand) - 1;
-      cand &= cand - 1;
-      float ze = z[0];
-#pragma unroll
-      for (int k = 1; k < 32; ++k) ze = e == k ? z[k] : ze;  // static indices only
-      b = gumbel_candidate(b, ze * inv_tau, vbase + e, pos, canvas, k0, k1, c3);
-    } while (cand);
-    if (b.score != st.best || b.idx != st.best_idx) {
-      st.best = b.score;
-      st.best_idx = b.idx;
-      st.best_z = b.z;
-      refresh_cthr(st);
-    }
+    for (int k = 1; k < 32; ++k) zj = j == k ? z[k] : zj;  // static indices only
+    st.best = score;
+    st.best_idx = vbase + j;
+    st.best_z = zj * inv_tau;
   }
 }
 
@@ -366,7 +312,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       st.best = -INFINITY;
       st.best_idx = 0x7FFFFFFF;
       st.best_z = -INFINITY;
-      st.cthr = INFINITY;
       for (int vt = vt0; vt < vt1; ++vt, ++j) {
         const int buf = j & 1;
         if (ok) ok = warp_wait(&tfull[buf], (j >> 1) & 1, abort_flag);
@@ -385,8 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&tempty[buf]);
           }
           const int vb = vt * kBN + col + c * 32;
-          process_chunk<kCE, kEnt, kSC>(st, z, vb, p.inv_tau, pos, canvas, keys, p.k0, p.k1,
-                                        p.c3, target, sc_row ? sc_row + vb : nullptr,
+          process_chunk<kCE, kEnt, kSC>(st, z, vb, p.inv_tau, pos, canvas, keys, p.c3,
+                                        p.c3_pick, target, sc_row ? sc_row + vb : nullptr,
                                         scm_row ? scm_row + (vb >> 5) : nullptr);
         }
       }
@@ -487,6 +432,7 @@ cudaError_t launch_vocab_pass(const uint16_t* y, const uint16_t* W, int R, int L
   p.k0 = static_cast<uint32_t>(seed);
   p.k1 = static_cast<uint32_t>(seed >> 32);
   p.c3 = kStreamGumbel | (static_cast<uint32_t>(step) & 0xFFFFFFu);
+  p.c3_pick = kStreamPick | (static_cast<uint32_t>(step) & 0xFFFFFFu);
   p.targets = targets;
   p.sc_p = sc_p;
   p.sc_m = sc_m;
