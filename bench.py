@@ -337,7 +337,7 @@ def run_ours(args, w):
     flops_per_launch = 2.0 * B * w.L * w.d * w.V
     vocab_avg_s = vocab_ms / max(vocab_n, 1) / 1000.0
     achieved = flops_per_launch / vocab_avg_s / 1e12
-    roofline = {"kernel": "vocab_posterior_kernel (fused LM head + posterior + Gumbel-max)",
+    roofline = {"kernel": "vocab_posterior_kernel (fused LM head + posterior + exact two-level sample)",
                 "bound": "tensor", "achieved": achieved, "peak": tf_sust, "unit": "TFLOP/s",
                 "frac": achieved / tf_sust, "traffic": traffic_from_profile("vocab.cu"),
                 "peak_kind": f"{peak_kind} sustained bf16",
