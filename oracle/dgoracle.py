@@ -338,8 +338,10 @@ def two_level_sample(z, pos, canvas, step: int, seed: int):
 
     g_c comes from the chunk Gumbel stream (word c&3 of counter (c>>2, pos, canvas, 2<<24 |
     step)), U from the pick stream (word 0 of (c*, pos, canvas, 5<<24 | step)).  Returns x0hat
-    and, for the parity bars, the smaller of the gap between the two largest chunk scores and
-    the distance of U from the chunk's cumulative boundaries."""
+    and, for the parity bars, the decision's margin in logit units: the smaller of the gap
+    between the two largest chunk scores and, for the cumulative boundaries C next to U, the
+    logit change that would move C onto U, |U - C| / (2 C (1 - C)) (a shift of every logit by at
+    most delta moves a boundary by at most 2 delta C (1 - C))."""
     n, V = z.shape
     nc = (V + SAMPLE_CHUNK - 1) // SAMPLE_CHUNK
     pad = np.full((n, nc * SAMPLE_CHUNK), -np.inf)
@@ -369,8 +371,14 @@ def two_level_sample(z, pos, canvas, step: int, seed: int):
     # (rounding can leave the last cumulative value a hair below U: the last real entry then)
     j = np.minimum((cum <= U[:, None]).sum(axis=1),
                    np.minimum(SAMPLE_CHUNK - 1, V - 1 - cstar * SAMPLE_CHUNK))
-    lo = np.where(j > 0, cum[idx, np.maximum(j - 1, 0)], 0.0)
-    margin = np.minimum(U - lo, cum[idx, j] - U)
+    def logit_margin(C, present):
+        m = np.abs(U - C) / np.maximum(2.0 * C * (1.0 - C), 1e-300)
+        return np.where(present, m, np.inf)
+
+    lo = cum[idx, np.maximum(j - 1, 0)]
+    hi = cum[idx, j]
+    last = np.minimum(SAMPLE_CHUNK - 1, V - 1 - cstar * SAMPLE_CHUNK)
+    margin = np.minimum(logit_margin(lo, j > 0), logit_margin(hi, j < last))
     return cstar * SAMPLE_CHUNK + j, np.minimum(gap, margin)
 
 
