@@ -218,6 +218,8 @@ struct LoopWs {
   int* counters;  // [2B]: per-canvas unlocked count and CTA tickets of the finalisation
   uint16_t *h, *q, *k, *v, *o, *y;
   void* attn;
+  void* gemm_part;  // fp32 split-K partials of the projections
+  size_t gemm_part_bytes;
   VocabPart* parts;
   int32_t *x0hat, *top1, *prev_top1;  // entropy-bounded sampler
   float* entropy;
@@ -231,6 +233,27 @@ struct LoopWs {
 };
 
 bool has_sc(const dg_model* m) { return m->Wsc1 != nullptr; }
+
+GemmOut qkv_segments(const dg_model* m) {
+  GemmOut o{};
+  o.nseg = 3;
+  o.seg_begin[0] = 0;
+  o.seg_begin[1] = m->H * m->hd;
+  o.seg_begin[2] = (m->H + m->Hkv) * m->hd;
+  o.seg_begin[3] = (m->H + 2 * m->Hkv) * m->hd;
+  return o;
+}
+
+// Workspace of the split-K partials of the two projections of BL canvas rows.
+size_t proj_part_bytes(const dg_model* m, int BL) {
+  const int Hhd = m->H * m->hd;
+  const GemmOut qkv = qkv_segments(m);
+  GemmOut yo{};
+  yo.nseg = 1;
+  yo.seg_begin[1] = m->d;
+  return std::max(plan_gemm(BL, qkv.seg_begin[3], m->d, qkv).part_bytes,
+                  plan_gemm(BL, m->d, Hhd, yo).part_bytes);
+}
 
 LoopWs loop_layout(const dg_model* m, int B, int L, int P, int window, uint8_t* base) {
   LoopWs w{};
@@ -253,6 +276,8 @@ LoopWs loop_layout(const dg_model* m, int B, int L, int P, int window, uint8_t* 
   w.y = reinterpret_cast<uint16_t*>(take(BL * m->d * 2));
   const AttnPlan ap = plan_attention(B, L, P, m->H, m->Hkv, m->hd, window);
   w.attn = take(ap.part_bytes > 0 ? ap.part_bytes : 16);
+  w.gemm_part_bytes = proj_part_bytes(m, static_cast<int>(BL));
+  w.gemm_part = take(w.gemm_part_bytes > 0 ? w.gemm_part_bytes : 16);
   const VocabPlan vp = plan_vocab(static_cast<int>(BL), m->V);
   w.parts = reinterpret_cast<VocabPart*>(take(vp.part_bytes));
   w.x0hat = reinterpret_cast<int32_t*>(take(BL * 4));
@@ -581,7 +606,8 @@ dg_status dg_sft_loss(const dg_model* m, const uint16_t* k_pre, const uint16_t* 
   qkv.ld[0] = Hhd;
   qkv.ld[1] = KVhd;
   qkv.ld[2] = KVhd;
-  e = launch_gemm(w.h, m->Wqkv, BL, Hhd + 2 * KVhd, m->d, qkv, nullptr, 0, w.status, nullptr, st);
+  e = launch_gemm(w.h, m->Wqkv, BL, Hhd + 2 * KVhd, m->d, qkv, nullptr, 0, w.status, nullptr, st,
+                  kActNone, w.gemm_part, w.gemm_part_bytes);
   if (e != cudaSuccess) return cuda_fail(e, "sft_loss: qkv gemm launch");
   e = launch_attention(w.q, k_pre, v_pre, w.k, w.v, w.o, nullptr, B, L, P, m->H, m->Hkv, m->hd,
                        window, 1.0f / std::sqrt(static_cast<float>(m->hd)), w.attn, w.status,
@@ -593,7 +619,8 @@ dg_status dg_sft_loss(const dg_model* m, const uint16_t* k_pre, const uint16_t* 
   yo.seg_begin[1] = m->d;
   yo.ptr[0] = w.y;
   yo.ld[0] = m->d;
-  e = launch_gemm(w.o, m->Wo, BL, m->d, Hhd, yo, w.h, m->d, w.status, nullptr, st);
+  e = launch_gemm(w.o, m->Wo, BL, m->d, Hhd, yo, w.h, m->d, w.status, nullptr, st, kActNone,
+                  w.gemm_part, w.gemm_part_bytes);
   if (e != cudaSuccess) return cuda_fail(e, "sft_loss: out_proj gemm launch");
   // fused LM head + cross-entropy against x_0
   e = launch_vocab_pass(w.y, m->E, BL, L, m->d, m->V, inv_tau, 0, 0, w.parts, w.status, nullptr,
@@ -781,12 +808,13 @@ dg_status run_denoise(const RunArgs& a, const dg_sampler_cfg* cfg,
                         sc && n > 0 ? w.sc_s : nullptr);
     if ((s = check_launch("loop: embed launch")) != DG_OK) return s;
     e = launch_gemm(w.h, m->Wqkv, BL, Hhd + 2 * KVhd, m->d, qkv, nullptr, 0, w.status, w.n_active,
-                    st);
+                    st, kActNone, w.gemm_part, w.gemm_part_bytes);
     if (e != cudaSuccess) return cuda_fail(e, "loop: qkv gemm launch");
     e = launch_attention(w.q, a.k_pre, a.v_pre, w.k, w.v, w.o, nullptr, B, L, a.P, m->H, m->Hkv,
                          m->hd, a.window, scale, w.attn, w.status, w.n_active, st, a.pre_stride);
     if (e != cudaSuccess) return cuda_fail(e, "loop: attention launch");
-    e = launch_gemm(w.o, m->Wo, BL, m->d, Hhd, yo, w.h, m->d, w.status, w.n_active, st);
+    e = launch_gemm(w.o, m->Wo, BL, m->d, Hhd, yo, w.h, m->d, w.status, w.n_active, st, kActNone,
+                    w.gemm_part, w.gemm_part_bytes);
     if (e != cudaSuccess) return cuda_fail(e, "loop: out_proj gemm launch");
     const bool sc_next = sc && n < cfg->T - 1;  // the last step's signal is never used
     const float inv_tau = eb ? eb_inv_tau[n] : cfg->inv_tau;

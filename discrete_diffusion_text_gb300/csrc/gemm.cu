@@ -1,10 +1,20 @@
 // Projection GEMM of the stand-in decoder on the 5th-generation tensor cores:
 //   C[M, N] = A[M, K] W[N, K]^T (+ residual), bf16 in, fp32 accumulate in tensor memory,
 //   bf16 out.
-// One 128 x BN output tile per CTA.  Warp 0 streams A/W k-blocks with TMA into a 4-stage
-// shared-memory ring (128-byte swizzle); one thread of warp 1 issues tcgen05.mma
-// (M = 128, N = BN, K = 16 per instruction) into a TMEM accumulator; warps 2..5 read the
-// accumulator back with tcgen05.ld and write bf16 rows.
+// Warp 0 streams A/W k-blocks with TMA into a shared-memory ring (128-byte swizzle); one
+// thread of warp 1 issues tcgen05.mma (M = 128, N = BN, K = 16 per instruction) into a TMEM
+// accumulator; warps 2..5 read the accumulator back with tcgen05.ld.
+//
+// Two kernels share that main loop:
+//  * gemm_bf16_kernel: one 128 x BN output tile per CTA over the whole K (many tiles: a
+//    canvas batch);
+//  * gemm_splitk_kernel: one tile per cluster of S CTAs, each CTA taking 1/S of the K range
+//    (few tiles: one canvas).  One tcgen05.mma costs about the same time for N = 64 .. 256,
+//    so with few tiles the per-CTA chain of K/16 instructions, not bandwidth, sets the time;
+//    splitting K shortens it.  CTA q of the cluster owns rows [q 128/S, (q+1) 128/S) of the
+//    tile: it keeps its own partial of those rows in shared memory, writes the other rows'
+//    partials to an fp32 workspace, and after a cluster barrier sums the S partials of its
+//    rows in rank order (deterministic), adds the residual and writes bf16.
 #include "kernels.cuh"
 #include "sm103.cuh"
 
@@ -13,6 +23,7 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
+constexpr int kThreadsG = 192;  // TMA warp, MMA warp, four epilogue warps
 
 struct GemmParams {
   int M, N, K;
@@ -30,20 +41,122 @@ __device__ __forceinline__ float gelu_tanh(float x) {
   return 0.5f * x * (1.f + tanhf(k * fmaf(0.044715f * x, x * x, x)));
 }
 
-// As many pipeline stages as fit in ~192 KiB: with one or two waves of CTAs that each run a
-// few dozen k-blocks, the copies in flight per SM (not the MMA) set the GEMM's speed.
+// As many pipeline stages as fit in ~192 KiB.
 template <int BN>
 struct GemmLayout {
   static constexpr int kABytes = kBM * kBK * 2;
   static constexpr int kBBytes = BN * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages = (192 * 1024) / kStageBytes;
-  static constexpr int kBarOff = kStages * kStageBytes;
+  static constexpr int kRingBytes = kStages * kStageBytes;
+  static constexpr int kBarOff = kRingBytes;
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers + 1 KiB alignment slack
 };
 
+// Destination of the output columns starting at col (a tile never straddles two segments).
+struct SegDst {
+  uint16_t* base;
+  int ld, beg;
+};
+__device__ __forceinline__ SegDst segment_of(const GemmOut& out, int col) {
+  // static indices only: no local-memory copy of the parameters
+  SegDst d{out.ptr[0], out.ld[0], out.seg_begin[0]};
+  if (out.nseg > 1 && col >= out.seg_begin[1]) d = SegDst{out.ptr[1], out.ld[1], out.seg_begin[1]};
+  if (out.nseg > 2 && col >= out.seg_begin[2]) d = SegDst{out.ptr[2], out.ld[2], out.seg_begin[2]};
+  return d;
+}
+
+// Producer (one thread): k-blocks kb0 .. kb0 + nk - 1 of A rows m0.. and W rows n0.. into the
+// ring.  After an abort it waits (briefly) for the copies already in flight to land.
 template <int BN>
-__global__ void __launch_bounds__(192, 1)
+__device__ __forceinline__ void gemm_produce(const CUtensorMap* tmA, const CUtensorMap* tmB,
+                                             uint8_t* smem, uint64_t* full, uint64_t* empty,
+                                             int kb0, int nk, int m0, int n0,
+                                             volatile int* abort_flag) {
+  using Lay = GemmLayout<BN>;
+  tma_prefetch_map(tmA);
+  tma_prefetch_map(tmB);
+  int issued = 0;
+  for (int i = 0; i < nk; ++i) {
+    const int s = i % Lay::kStages;
+    const uint32_t r = i / Lay::kStages;
+    if (!mbar_wait(&empty[s], (r & 1) ^ 1, abort_flag)) break;
+    uint8_t* sa = smem + s * Lay::kStageBytes;
+    mbar_arrive_expect_tx(&full[s], Lay::kStageBytes);
+    tma_load_2d(sa, tmA, &full[s], (kb0 + i) * kBK, m0);
+    tma_load_2d(sa + Lay::kABytes, tmB, &full[s], (kb0 + i) * kBK, n0);
+    ++issued;
+  }
+  if (*abort_flag) {
+    for (int i = (issued > Lay::kStages ? issued - Lay::kStages : 0); i < issued; ++i)
+      mbar_wait_drain(&full[i % Lay::kStages], (i / Lay::kStages) & 1);
+  }
+}
+
+// MMA issuer (one thread): nk k-blocks into the accumulator, then one arrival on acc_full.
+template <int BN>
+__device__ __forceinline__ void gemm_mma(uint32_t tmem, uint8_t* smem, uint64_t* full,
+                                         uint64_t* empty, uint64_t* acc_full, int nk,
+                                         volatile int* abort_flag) {
+  using Lay = GemmLayout<BN>;
+  constexpr uint32_t idesc = idesc_bf16(kBM, BN, false);
+  for (int i = 0; i < nk; ++i) {
+    const int s = i % Lay::kStages;
+    const uint32_t r = i / Lay::kStages;
+    if (!mbar_wait(&full[s], r & 1, abort_flag)) break;
+    tc_fence_after();
+    const uint32_t sa = smem_u32(smem + s * Lay::kStageBytes);
+    const uint32_t sb = sa + Lay::kABytes;
+#pragma unroll
+    for (int k = 0; k < kBK / 16; ++k)
+      mma_bf16_ss(tmem, sdesc_sw128(sa + k * 32, 16, 1024), sdesc_sw128(sb + k * 32, 16, 1024),
+                  idesc, (i | k) != 0);
+    mma_commit(&empty[s]);
+  }
+  mma_commit(acc_full);
+  if (*abort_flag) mbar_wait_drain(acc_full, 0);
+}
+
+// Barriers and flags after the data region: full[kStages], empty[kStages], acc_full, the TMEM
+// base address and the abort flag.
+struct GemmSync {
+  uint64_t *full, *empty, *acc_full;
+  uint32_t* tmem_slot;
+  volatile int* abort_flag;
+};
+template <int kStages>
+__device__ __forceinline__ GemmSync gemm_sync_at(uint8_t* p) {
+  GemmSync g;
+  g.full = reinterpret_cast<uint64_t*>(p);
+  g.empty = g.full + kStages;
+  g.acc_full = g.empty + kStages;
+  g.tmem_slot = reinterpret_cast<uint32_t*>(g.acc_full + 1);
+  g.abort_flag = reinterpret_cast<volatile int*>(g.tmem_slot + 1);
+  return g;
+}
+
+template <int kStages>
+__device__ __forceinline__ void gemm_init(const GemmSync& g, int tmem_cols) {
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&g.full[s], 1);
+      mbar_init(&g.empty[s], 1);
+    }
+    mbar_init(g.acc_full, 1);
+    *g.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if ((threadIdx.x >> 5) == 1) {
+    tmem_alloc(g.tmem_slot, tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kThreadsG, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, GemmParams p) {
   using Lay = GemmLayout<BN>;
@@ -52,80 +165,24 @@ __global__ void __launch_bounds__(192, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lay::kBarOff);
-  uint64_t* empty = full + Lay::kStages;
-  uint64_t* acc_full = empty + Lay::kStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
+  const GemmSync g = gemm_sync_at<Lay::kStages>(smem + Lay::kBarOff);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * BN;
   const int m0 = blockIdx.y * kBM;
-  const int nkb = p.K / kBK;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < Lay::kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    mbar_init(acc_full, 1);
-    *abort_flag = 0;
-    fence_barrier_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(tmem_slot, BN);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  gemm_init<Lay::kStages>(g, BN);
+  const uint32_t tmem = *g.tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0) {
-      tma_prefetch_map(&tmA);
-      tma_prefetch_map(&tmB);
-      int issued = 0;
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % Lay::kStages;
-        const uint32_t r = kb / Lay::kStages;
-        if (!mbar_wait(&empty[s], (r & 1) ^ 1, abort_flag)) break;
-        uint8_t* sa = smem + s * Lay::kStageBytes;
-        mbar_arrive_expect_tx(&full[s], Lay::kStageBytes);
-        tma_load_2d(sa, &tmA, &full[s], kb * kBK, m0);
-        tma_load_2d(sa + Lay::kABytes, &tmB, &full[s], kb * kBK, n0);
-        ++issued;
-      }
-      if (*abort_flag) {  // let copies already in flight land before the CTA exits
-        for (int kb = (issued > Lay::kStages ? issued - Lay::kStages : 0); kb < issued; ++kb)
-          mbar_wait_drain(&full[kb % Lay::kStages], (kb / Lay::kStages) & 1);
-      }
-    }
+    if (lane == 0)
+      gemm_produce<BN>(&tmA, &tmB, smem, g.full, g.empty, 0, p.K / kBK, m0, n0, g.abort_flag);
   } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(kBM, BN, false);
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % Lay::kStages;
-        const uint32_t r = kb / Lay::kStages;
-        if (!mbar_wait(&full[s], r & 1, abort_flag)) break;
-        tc_fence_after();
-        const uint32_t sa = smem_u32(smem + s * Lay::kStageBytes);
-        const uint32_t sb = sa + Lay::kABytes;
-#pragma unroll
-        for (int k = 0; k < kBK / 16; ++k) {
-          mma_bf16_ss(tmem, sdesc_sw128(sa + k * 32, 16, 1024), sdesc_sw128(sb + k * 32, 16, 1024),
-                      idesc, (kb | k) != 0);
-        }
-        mma_commit(&empty[s]);
-      }
-      mma_commit(acc_full);
-      if (*abort_flag) mbar_wait_drain(acc_full, 0);
-    }
+    if (lane == 0) gemm_mma<BN>(tmem, smem, g.full, g.empty, g.acc_full, p.K / kBK, g.abort_flag);
   } else {
-    const bool ok = warp_wait(acc_full, 0, abort_flag);
+    const bool ok = warp_wait(g.acc_full, 0, g.abort_flag);
     tc_fence_after();
     const int row = m0 + (warp & 3) * 32 + lane;
+    const SegDst dst = segment_of(p.out, n0);
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
       float v[32];
@@ -141,8 +198,7 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&ws[e]);
-            const float2 f = __bfloat1622float2(b2);
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[e]));
             v[q * 8 + 2 * e] += f.x;
             v[q * 8 + 2 * e + 1] += f.y;
           }
@@ -152,22 +208,8 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
         for (int e = 0; e < 32; ++e) v[e] = gelu_tanh(v[e]);
       }
-      // output segment of this column (static indices only: no local-memory copy of params)
-      uint16_t* base = p.out.ptr[0];
-      int ld = p.out.ld[0];
-      int beg = p.out.seg_begin[0];
-      if (p.out.nseg > 1 && col >= p.out.seg_begin[1]) {
-        base = p.out.ptr[1];
-        ld = p.out.ld[1];
-        beg = p.out.seg_begin[1];
-      }
-      if (p.out.nseg > 2 && col >= p.out.seg_begin[2]) {
-        base = p.out.ptr[2];
-        ld = p.out.ld[2];
-        beg = p.out.seg_begin[2];
-      }
-      uint16_t* dst = base + static_cast<int64_t>(row) * ld + (col - beg);
-      uint4* d4 = reinterpret_cast<uint4*>(dst);
+      uint4* d4 = reinterpret_cast<uint4*>(dst.base + static_cast<int64_t>(row) * dst.ld +
+                                           (col - dst.beg));
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         d4[q] = make_uint4(pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]),
@@ -186,52 +228,287 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     tmem_dealloc(tmem, BN);
   }
-  if (threadIdx.x == 0 && *abort_flag) atomicOr(p.status, kStatusTimeout);
+  if (threadIdx.x == 0 && *g.abort_flag) atomicOr(p.status, kStatusTimeout);
+}
+
+// Split-K layout: the ring as above; once the main loop is done the ring's memory holds this
+// CTA's own rows ([kR][BN] fp32, 16-byte chunks XOR-swizzled by row so that the row-per-thread
+// writes and the column-per-thread reads are both free of bank conflicts) and the fp32 sums of
+// those rows ([kR][BN + 4], padded for the same reason).
+template <int BN, int S>
+struct SplitLayout {
+  using Ring = GemmLayout<BN>;
+  static constexpr int kR = kBM / S;  // rows of the tile summed by one CTA
+  static constexpr int kOwnOff = 0;
+  static constexpr int kOwnBytes = kR * BN * 4;
+  static constexpr int kSumLd = BN + 4;
+  static constexpr int kSumOff = kOwnBytes;
+  static constexpr int kSumBytes = kR * kSumLd * 4;
+  static_assert(kSumOff + kSumBytes <= Ring::kRingBytes, "split-K scratch exceeds the ring");
+};
+
+// grid (S, N / BN, M tiles), cluster (S, 1, 1); part: [tiles][S][BN / 4][128] float4.
+template <int BN, int S>
+__global__ void __launch_bounds__(kThreadsG, 1)
+    gemm_splitk_kernel(const __grid_constant__ CUtensorMap tmA,
+                       const __grid_constant__ CUtensorMap tmB, GemmParams p,
+                       float4* __restrict__ part) {
+  using Lay = SplitLayout<BN, S>;
+  using Ring = GemmLayout<BN>;
+  constexpr int c4n = BN / 4;
+  pdl_wait();
+  if (p.n_active && *p.n_active == 0) return;  // the same for every CTA of the grid
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const GemmSync g = gemm_sync_at<Ring::kStages>(smem + Ring::kBarOff);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int q = static_cast<int>(cluster_ctarank());
+  const int n0 = blockIdx.y * BN;
+  const int m0 = blockIdx.z * kBM;
+  const int nkb = p.K / kBK;
+  const int kb0 = q * nkb / S;
+  const int nk = (q + 1) * nkb / S - kb0;
+  float4* tile_part =
+      part + static_cast<int64_t>(blockIdx.z * gridDim.y + blockIdx.y) * S * c4n * kBM;
+  gemm_init<Ring::kStages>(g, BN);
+  const uint32_t tmem = *g.tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0)
+      gemm_produce<BN>(&tmA, &tmB, smem, g.full, g.empty, kb0, nk, m0, n0, g.abort_flag);
+  } else if (warp == 1) {
+    if (lane == 0) gemm_mma<BN>(tmem, smem, g.full, g.empty, g.acc_full, nk, g.abort_flag);
+  } else {
+    // partial accumulator: own rows to shared memory, the others to the workspace in a
+    // [chunk][row] layout so that a warp's 32 rows of one 16-byte chunk are 512 contiguous
+    // bytes (the ring is idle: every MMA that read it has completed)
+    warp_wait(g.acc_full, 0, g.abort_flag);
+    tc_fence_after();
+    const int row = (warp & 3) * 32 + lane;
+    const bool own = row / Lay::kR == q;
+    float4* gp = tile_part + static_cast<int64_t>(q) * c4n * kBM + row;
+    uint8_t* orow = smem + Lay::kOwnOff + (row - q * Lay::kR) * (BN * 4);
+#pragma unroll 1
+    for (int c = 0; c < BN / 64; ++c) {
+      float v[64];
+      tmem_ld64(tmem + tmem_lane_base(warp) + c * 64, v);
+      if (own) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int ch = (c * 16 + j) ^ (row & 7);
+          *reinterpret_cast<float4*>(orow + ch * 16) =
+              make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          __stcg(gp + static_cast<int64_t>(c * 16 + j) * kBM,
+                 make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+      }
+    }
+  }
+  tc_fence_before();
+  __syncwarp();
+  cluster_arrive();  // this CTA's partials are written (and its TMEM reads are done)
+  cluster_wait();    // ... and so are every other CTA's of the cluster
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, BN);
+  }
+
+  // this CTA's kR rows: the S partials summed in rank order (the same order for every row,
+  // whichever CTA sums it), into fp32 sums in shared memory
+  constexpr int nitems = Lay::kR * c4n;
+  constexpr int kU = 4;  // items in flight per thread
+  float* sums = reinterpret_cast<float*>(smem + Lay::kSumOff);
+  for (int i0 = threadIdx.x; i0 < nitems; i0 += kU * kThreadsG) {
+    float4 v[kU][S];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i = i0 + u * kThreadsG < nitems ? i0 + u * kThreadsG : i0;
+      const int rr = i % Lay::kR, c4 = i / Lay::kR;
+      const int trow = q * Lay::kR + rr;
+#pragma unroll
+      for (int j = 0; j < S; ++j) {
+        if (j == q)
+          v[u][j] = *reinterpret_cast<const float4*>(smem + Lay::kOwnOff + rr * (BN * 4) +
+                                                     ((c4 ^ (trow & 7)) * 16));
+        else
+          v[u][j] = __ldcg(tile_part + (static_cast<int64_t>(j) * c4n + c4) * kBM + trow);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i = i0 + u * kThreadsG;
+      if (i < nitems) {
+        const int rr = i % Lay::kR, c4 = i / Lay::kR;
+        float4 a = v[u][0];
+#pragma unroll
+        for (int j = 1; j < S; ++j) {
+          a.x += v[u][j].x;
+          a.y += v[u][j].y;
+          a.z += v[u][j].z;
+          a.w += v[u][j].w;
+        }
+        *reinterpret_cast<float4*>(sums + rr * Lay::kSumLd + c4 * 4) = a;
+      }
+    }
+  }
+  __syncthreads();
+
+  // residual, activation, bf16: eight columns a thread, consecutive threads along a row
+  const bool good = !*g.abort_flag;
+  const SegDst dst = segment_of(p.out, n0);
+  constexpr int c8n = BN / 8;
+#pragma unroll 2
+  for (int i = threadIdx.x; i < Lay::kR * c8n; i += kThreadsG) {
+    const int rr = i / c8n, c8 = i % c8n;
+    const int row = m0 + q * Lay::kR + rr;
+    if (!good || row >= p.M) continue;
+    const float4 s0 = *reinterpret_cast<const float4*>(sums + rr * Lay::kSumLd + c8 * 8);
+    const float4 s1 = *reinterpret_cast<const float4*>(sums + rr * Lay::kSumLd + c8 * 8 + 4);
+    float o[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+    const int col = n0 + c8 * 8;
+    if (p.residual) {
+      const uint4 rv =
+          *reinterpret_cast<const uint4*>(p.residual + static_cast<int64_t>(row) * p.ld_res + col);
+      const uint32_t w[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+        o[2 * e] += f.x;
+        o[2 * e + 1] += f.y;
+      }
+    }
+    if (p.act == kActGeluTanh) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = gelu_tanh(o[e]);
+    }
+    *reinterpret_cast<uint4*>(dst.base + static_cast<int64_t>(row) * dst.ld + (col - dst.beg)) =
+        make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
+                   pack_bf16x2(o[6], o[7]));
+  }
+  pdl_trigger();
+  if (threadIdx.x == 0 && *g.abort_flag) atomicOr(p.status, kStatusTimeout);
+}
+
+template <typename Kernel>
+cudaError_t set_smem_once(Kernel kernel, int bytes, int* configured_device) {
+  const int dev = device_id();
+  if (*configured_device == dev) return cudaSuccess;
+  const cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) *configured_device = dev;
+  return e;
 }
 
 template <int BN>
 cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
                       cudaStream_t st) {
   using Lay = GemmLayout<BN>;
-  static int configured_device = -1;  // attribute is per device; set on first use of each
-  const int dev = device_id();
-  if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel<BN>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Lay::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured_device = dev;
-  }
+  static int configured_device = -1;  // the attribute is per device; set on first use of each
+  cudaError_t e = set_smem_once(gemm_bf16_kernel<BN>, Lay::kSmemBytes, &configured_device);
+  if (e != cudaSuccess) return e;
   dim3 grid(p.N / BN, (p.M + kBM - 1) / kBM);
-  return launch_dependent(gemm_bf16_kernel<BN>, grid, dim3(192), Lay::kSmemBytes, st, ta, tb, p);
+  return launch_dependent(gemm_bf16_kernel<BN>, grid, dim3(kThreadsG), Lay::kSmemBytes, st, ta,
+                          tb, p);
+}
+
+template <int BN, int S>
+cudaError_t launch_split(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
+                         float* part, cudaStream_t st) {
+  using Lay = GemmLayout<BN>;
+  static int configured_device = -1;
+  cudaError_t e =
+      set_smem_once(gemm_splitk_kernel<BN, S>, Lay::kSmemBytes, &configured_device);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(S, p.N / BN, (p.M + kBM - 1) / kBM);
+  cfg.blockDim = dim3(kThreadsG);
+  cfg.dynamicSmemBytes = Lay::kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = S;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, gemm_splitk_kernel<BN, S>, ta, tb, p,
+                            reinterpret_cast<float4*>(part));
+}
+
+bool divides_segments(const GemmOut& out, int N, int bn) {
+  if (N % bn != 0) return false;
+  for (int s = 0; s <= out.nseg; ++s)
+    if (out.seg_begin[s] % bn != 0) return false;
+  return true;
 }
 
 }  // namespace
 
+GemmPlan plan_gemm(int M, int N, int K, const GemmOut& out) {
+  GemmPlan pl{};
+  pl.S = 1;
+  const int mt = (M + kBM - 1) / kBM;
+  const int nkb = K / kBK;
+  const int64_t nsm = num_sms();
+  // single-CTA tiles: the largest N tile that divides every output-segment boundary (a tile
+  // never straddles two outputs) and still gives at least two CTAs per SM; 64 otherwise
+  pl.BN = 64;
+  if (divides_segments(out, N, 256) && static_cast<int64_t>(mt) * (N / 256) >= 2 * nsm)
+    pl.BN = 256;
+  else if (divides_segments(out, N, 128) && static_cast<int64_t>(mt) * (N / 128) >= 2 * nsm)
+    pl.BN = 128;
+  if (mt <= 0 || static_cast<int64_t>(mt) * (N / 64) > nsm) return pl;
+  // at most one wave of 64-column tiles: split K over clusters instead, with as many CTAs as
+  // fit in one wave (ties: the longer split, then the wider tile)
+  int best_ctas = 0, best_bn = 0, best_s = 0;
+  for (int bn : {256, 128}) {
+    if (!divides_segments(out, N, bn)) continue;
+    for (int s : {4, 2}) {
+      if (s > nkb) continue;
+      const int64_t ctas = static_cast<int64_t>(mt) * (N / bn) * s;
+      if (ctas > nsm) continue;
+      if (ctas > best_ctas || (ctas == best_ctas && s > best_s)) {
+        best_ctas = static_cast<int>(ctas);
+        best_bn = bn;
+        best_s = s;
+      }
+    }
+  }
+  if (best_ctas == 0) return pl;
+  pl.BN = best_bn;
+  pl.S = best_s;
+  pl.part_bytes = static_cast<size_t>(mt) * (N / best_bn) * best_s * kBM * best_bn * 4;
+  return pl;
+}
+
 cudaError_t launch_gemm(const uint16_t* A, const uint16_t* W, int M, int N, int K,
                         const GemmOut& out, const uint16_t* residual, int ld_res,
-                        uint32_t* status, const int* n_active, cudaStream_t st, int act) {
-  // Largest N tile that divides every output-segment boundary (a tile never straddles two
-  // outputs) and still gives at least two CTAs per SM; 64 otherwise.
+                        uint32_t* status, const int* n_active, cudaStream_t st, int act,
+                        void* part_ws, size_t part_ws_bytes) {
   if (N % 64 != 0 || K % kBK != 0) return cudaErrorInvalidValue;
   for (int s = 0; s <= out.nseg; ++s)
     if (out.seg_begin[s] % 64 != 0) return cudaErrorInvalidValue;
-  const int mt = (M + kBM - 1) / kBM;
-  auto fits = [&](int bn) {
-    for (int s = 0; s <= out.nseg; ++s)
-      if (out.seg_begin[s] % bn != 0) return false;
-    return static_cast<int64_t>(mt) * (N / bn) >= 2 * num_sms();
-  };
-  int BN = 64;
-  if (fits(256)) BN = 256;
-  else if (fits(128)) BN = 128;
+  GemmPlan pl = plan_gemm(M, N, K, out);
+  if (pl.S > 1 && (part_ws == nullptr || part_ws_bytes < pl.part_bytes ||
+                   (reinterpret_cast<uintptr_t>(part_ws) & 15) != 0)) {
+    // no room for the split partials: one CTA per tile over the whole K
+    pl.S = 1;
+    pl.BN = 64;
+  }
 
   CUtensorMap ta, tb;
   const uint64_t dA[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
   const uint64_t sA[1] = {static_cast<uint64_t>(K) * 2};
   const uint32_t bA[2] = {static_cast<uint32_t>(kBK), static_cast<uint32_t>(kBM)};
   const uint64_t dB[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N)};
-  const uint32_t bB[2] = {static_cast<uint32_t>(kBK), static_cast<uint32_t>(BN)};
+  const uint32_t bB[2] = {static_cast<uint32_t>(kBK), static_cast<uint32_t>(pl.BN)};
   if (!make_tmap_bf16(&ta, A, 2, dA, sA, bA)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tb, W, 2, dB, sA, bB)) return cudaErrorInvalidValue;
 
@@ -245,11 +522,16 @@ cudaError_t launch_gemm(const uint16_t* A, const uint16_t* W, int M, int N, int 
   p.status = status;
   p.n_active = n_active;
   p.act = act;
+  float* part = static_cast<float*>(part_ws);
   timer_begin(3, st);
   cudaError_t e;
-  switch (BN) {
-    case 256: e = launch_bn<256>(ta, tb, p, st); break;
-    case 128: e = launch_bn<128>(ta, tb, p, st); break;
+  switch (pl.S * 1000 + pl.BN) {
+    case 4256: e = launch_split<256, 4>(ta, tb, p, part, st); break;
+    case 2256: e = launch_split<256, 2>(ta, tb, p, part, st); break;
+    case 4128: e = launch_split<128, 4>(ta, tb, p, part, st); break;
+    case 2128: e = launch_split<128, 2>(ta, tb, p, part, st); break;
+    case 1256: e = launch_bn<256>(ta, tb, p, st); break;
+    case 1128: e = launch_bn<128>(ta, tb, p, st); break;
     default: e = launch_bn<64>(ta, tb, p, st); break;
   }
   timer_end(3, st);

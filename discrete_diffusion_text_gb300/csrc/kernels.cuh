@@ -113,10 +113,19 @@ struct GemmOut {
 
 constexpr int kActNone = 0;
 constexpr int kActGeluTanh = 1;
+// Tile width and K split chosen for a shape; part_bytes: the fp32 workspace the split needs
+// (0 without a split).
+struct GemmPlan {
+  int BN, S;
+  size_t part_bytes;
+};
+GemmPlan plan_gemm(int M, int N, int K, const GemmOut& out);
+// part_ws: workspace for the split partials (16-byte aligned); without one, or with fewer than
+// plan_gemm(...).part_bytes bytes, every tile runs on one CTA over the whole K.
 cudaError_t launch_gemm(const uint16_t* A, const uint16_t* W, int M, int N, int K,
                         const GemmOut& out, const uint16_t* residual, int ld_res,
                         uint32_t* status, const int* n_active, cudaStream_t st,
-                        int act = kActNone);
+                        int act = kActNone, void* part_ws = nullptr, size_t part_ws_bytes = 0);
 
 // ------------------------------------------------------------ self-conditioning -----
 struct ScPlan {

@@ -313,7 +313,9 @@ cudaError_t launch_self_condition(const uint16_t* p_til, const float* m_ref, con
   o1.seg_begin[1] = dsc;
   o1.ptr[0] = u;
   o1.ld[0] = dsc;
-  err = launch_gemm(e, W1, R, dsc, d, o1, nullptr, 0, status, n_active, st, kActGeluTanh);
+  // the contraction's partials are consumed: their buffer takes the GEMMs' split partials
+  err = launch_gemm(e, W1, R, dsc, d, o1, nullptr, 0, status, n_active, st, kActGeluTanh, part,
+                    pl.part_bytes);
   if (err != cudaSuccess) return err;
   GemmOut o2{};
   o2.nseg = 1;
@@ -321,7 +323,8 @@ cudaError_t launch_self_condition(const uint16_t* p_til, const float* m_ref, con
   o2.seg_begin[1] = d;
   o2.ptr[0] = s;
   o2.ld[0] = d;
-  return launch_gemm(u, W2, R, d, dsc, o2, nullptr, 0, status, n_active, st);
+  return launch_gemm(u, W2, R, d, dsc, o2, nullptr, 0, status, n_active, st, kActNone, part,
+                     pl.part_bytes);
 }
 
 }  // namespace dg

@@ -124,6 +124,26 @@ __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// ------------------------------------------------------------------ thread-block cluster -----
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Split cluster barrier: every thread of every CTA in the cluster arrives once and later waits
+// once per phase; the arrive releases and the wait acquires this thread's prior memory
+// accesses (global and shared) at cluster scope.  Both are warp-aligned: a whole warp executes
+// them together.  A hardware barrier (no polling): it completes when all threads of the
+// cluster have arrived, so every path through a kernel that uses it must reach each arrive.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // ----------------------------------------------------------------------------- TMA -----
 
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
