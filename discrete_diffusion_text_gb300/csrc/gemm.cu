@@ -9,9 +9,10 @@
 //  * gemm_bf16_kernel: one 128 x BN output tile per CTA over the whole K (many tiles: a
 //    canvas batch);
 //  * gemm_splitk_kernel: one tile per cluster of S CTAs, each CTA taking 1/S of the K range
-//    (few tiles: one canvas).  One tcgen05.mma costs about the same time for N = 64 .. 256,
-//    so with few tiles the per-CTA chain of K/16 instructions, not bandwidth, sets the time;
-//    splitting K shortens it.  CTA q of the cluster owns rows [q 128/S, (q+1) 128/S) of the
+//    (few tiles: one canvas).  The issuing thread is held about as long in one tcgen05.mma
+//    for N = 64 as for N = 256 (where a single issuer keeps the pipe busy), so with few tiles
+//    the per-CTA chain of K/16 instructions, not bandwidth, sets the time; splitting K
+//    shortens it.  CTA q of the cluster owns rows [q 128/S, (q+1) 128/S) of the
 //    tile: it keeps its own partial of those rows in shared memory, writes the other rows'
 //    partials to an fp32 workspace, and after a cluster barrier sums the S partials of its
 //    rows in rank order (deterministic), adds the residual and writes bf16.
