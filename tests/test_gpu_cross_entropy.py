@@ -97,3 +97,37 @@ def test_sft_loss_on_noised_canvases_matches_oracle(dgc):
     ref, rxt = O.sft_loss(om, f64(kp), f64(vp), w.window, x0, keep, 91)
     assert np.array_equal(xt.cpu().numpy(), rxt)
     assert np.abs(loss.cpu().numpy() - ref).max() <= LOSS_TOL
+
+
+def test_sft_loss_window1k_sampled_rows(dgc):
+    """SFT loss at the window1k dims (d_model 2,048, 16q/8kv x 128, vocabulary 262,144, prefix
+    1,024 in a 1,024 window), where one canvas's projections run as cluster split-K: noising
+    bit-exact for the whole canvas; the oracle recomputes the decoder for the whole canvas and
+    the loss at 16 sampled positions.  With the tied head a kept position's loss is
+    lse - 2 y.E[x_t] at 1/tau = 2: a projection that dropped a quarter of its K range would move
+    it by ~1e-2, while the attention's bf16 probabilities in P.V move y.E[x_t] by ~3e-4 (so
+    1/tau = 20 would put legitimate rounding at the tolerance)."""
+    w = synth.WINDOW1K
+    m = synth.make_model(w, DEV)
+    kp, vp = synth.make_prefix_kv(w, DEV)
+    x0 = synth.zipf_tokens(w.B, w.L, w.V, 1.1, 96)
+    keep = O.keep_threshold_from_t(O.SCHED_LINEAR, synth.uniform_times(w.B, 97))
+    md = dgc.make_model(m["E"], m["Wqkv"], m["Wo"], w.H, w.Hkv, w.hd)
+    ws = dgc.workspace(dgc.dg_denoise_loop_workspace(md, w.B, w.L, w.P, w.window))
+    x0d = torch.tensor(x0, dtype=torch.int32, device=DEV)
+    xt = torch.empty_like(x0d)
+    loss = torch.empty((w.B, w.L), dtype=torch.float32, device=DEV)
+    keep_d = torch.tensor(keep.astype(np.int64), device=DEV)
+    dgc.dg_sft_loss(md, kp, vp, w.window, x0d, keep_d, 98, xt, loss, 2.0, ws)
+    dgc.dg_workspace_status(ws)
+    E = f64(m["E"])
+    rxt = O.forward_noise(x0, keep, w.V, 98)
+    assert np.array_equal(xt.cpu().numpy(), rxt)
+    h, q, kc, vc = O.decoder_front(rxt, E, f64(m["Wqkv"]), w.H, w.Hkv, w.hd)
+    Oa, _ = O.canvas_attention(q, f64(kp), f64(vp), kc, vc, w.window, w.hd ** -0.5)
+    y = O.decoder_back(h, Oa, f64(m["Wo"])).reshape(w.L, w.d)
+    rows = np.sort(np.random.default_rng(99).choice(w.L, 16, replace=False))
+    ref, _ = O.cross_entropy(y[rows], E, 2.0, x0.reshape(-1)[rows])
+    got = loss.cpu().numpy().reshape(-1)[rows]
+    assert np.std(ref) > 0.05  # the loss varies from row to row
+    assert np.abs(got - ref).max() <= LOSS_TOL
