@@ -318,6 +318,11 @@ typedef struct {
   float stop_entropy;       /* adaptive-stopping threshold on the mean entropy */
 } dg_sampler_cfg;
 
+/* Bytes of device workspace dg_denoise_loop (and dg_sft_loss, dg_block_generate's loop part)
+ * needs: the status word, activations, attention and vocabulary partials, the fp32 partials of
+ * the split-K projections (present when one launch of them would not fill the GPU, as for one
+ * canvas) and, with self-conditioning, its buffers.  Depends on the device's SM count.  Host
+ * only. */
 size_t dg_denoise_loop_workspace(const dg_model* m, int B, int L, int P, int window);
 
 /* Number of kernels one dg_denoise_loop call launches for `steps` steps on this device (its
