@@ -16,6 +16,9 @@
 //    tile: it keeps its own partial of those rows in shared memory, writes the other rows'
 //    partials to an fp32 workspace, and after a cluster barrier sums the S partials of its
 //    rows in rank order (deterministic), adds the residual and writes bf16.
+#include <mutex>
+#include <vector>
+
 #include "kernels.cuh"
 #include "sm103.cuh"
 
@@ -443,6 +446,45 @@ cudaError_t launch_split(const CUtensorMap& ta, const CUtensorMap& tb, const Gem
                             reinterpret_cast<float4*>(part));
 }
 
+// Whether a cluster of S split-K CTAs (each with the whole ring of shared memory) can be
+// resident on this device at all (a partitioned GPU may not offer it); asked once per device.
+template <int BN, int S>
+bool split_cluster_fits() {
+  static std::mutex mu;
+  static std::vector<int> known;  // per device: 0 unknown, 1 fits, 2 does not
+  const int dev = device_id();
+  std::lock_guard<std::mutex> lk(mu);
+  if (static_cast<int>(known.size()) <= dev) known.resize(dev + 1, 0);
+  if (known[dev] == 0) {
+    using Lay = GemmLayout<BN>;
+    int n = 0;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(S, 1, 1);
+    cfg.blockDim = dim3(kThreadsG);
+    cfg.dynamicSmemBytes = Lay::kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const bool ok =
+        cudaFuncSetAttribute(gemm_splitk_kernel<BN, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Lay::kSmemBytes) == cudaSuccess &&
+        cudaOccupancyMaxActiveClusters(&n, gemm_splitk_kernel<BN, S>, &cfg) == cudaSuccess &&
+        n > 0;
+    if (!ok) cudaGetLastError();  // clear the query's error, if any
+    known[dev] = ok ? 1 : 2;
+  }
+  return known[dev] == 1;
+}
+
+bool split_fits(int bn, int s) {
+  if (bn == 256) return s == 4 ? split_cluster_fits<256, 4>() : split_cluster_fits<256, 2>();
+  return s == 4 ? split_cluster_fits<128, 4>() : split_cluster_fits<128, 2>();
+}
+
 bool divides_segments(const GemmOut& out, int N, int bn) {
   if (N % bn != 0) return false;
   for (int s = 0; s <= out.nseg; ++s)
@@ -474,7 +516,7 @@ GemmPlan plan_gemm(int M, int N, int K, const GemmOut& out) {
     for (int s : {4, 2}) {
       if (s > nkb) continue;
       const int64_t ctas = static_cast<int64_t>(mt) * (N / bn) * s;
-      if (ctas > nsm) continue;
+      if (ctas > nsm || !split_fits(bn, s)) continue;
       if (ctas > best_ctas || (ctas == best_ctas && s > best_s)) {
         best_ctas = static_cast<int>(ctas);
         best_bn = bn;
