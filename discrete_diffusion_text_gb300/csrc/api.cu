@@ -702,11 +702,15 @@ int dg_denoise_loop_kernel_count(const dg_model* m, int B, int L, int P, int win
     return -1;
   const AttnPlan ap = plan_attention(B, L, P, m->H, m->Hkv, m->hd, window);
   // loop init, then per step: embedding gather, QKV GEMM, attention (+ split merge),
-  // output projection, vocabulary pass, finalisation; with self-conditioning, every step but
-  // the run's last (counted here as the last of these `steps`) adds the rescale, the
-  // contraction, its reduction and the two feed-forward GEMMs
-  const int sc_steps = m->Wsc1 != nullptr && steps > 0 ? steps - 1 : 0;
-  return 1 + steps * (6 + (ap.splits > 1 ? 1 : 0)) + 5 * sc_steps;
+  // output projection, vocabulary pass, finalisation (Euler sampler).  Without
+  // self-conditioning a step's finalisation shares the next step's embedding launch, so the
+  // call's last step alone adds one.  With self-conditioning, every step but the run's last
+  // (counted here as the last of these `steps`) adds the rescale, the contraction, its
+  // reduction and the two feed-forward GEMMs.
+  const bool sc = m->Wsc1 != nullptr;
+  const int sc_steps = sc && steps > 0 ? steps - 1 : 0;
+  const int per_step = 5 + (ap.splits > 1 ? 1 : 0) + (sc ? 1 : 0);
+  return 1 + steps * per_step + (!sc && steps > 0 ? 1 : 0) + 5 * sc_steps;
 }
 
 }  // extern "C"
@@ -801,12 +805,22 @@ dg_status run_denoise(const RunArgs& a, const dg_sampler_cfg* cfg,
   const uint32_t k0 = static_cast<uint32_t>(a.seed), k1 = static_cast<uint32_t>(a.seed >> 32);
 
   const bool sc = has_sc(m);
+  // Euler without self-conditioning: each step's finalisation runs inside the next step's
+  // embedding launch (one kernel boundary fewer per step); the call's last step is finalised
+  // on its own at the end.
+  const bool fuse = !eb && !sc;
+  FinalizeParams pending{};
   for (int n = a.start; n < a.end; ++n) {
-    // the signal of the previous step (none at step 0; a resumed run reads the one its
-    // previous call left in the workspace)
-    launch_embed_gather(a.canvas, m->E, w.h, BL, m->V, m->d, w.n_active, st,
-                        sc && n > 0 ? w.sc_s : nullptr);
-    if ((s = check_launch("loop: embed launch")) != DG_OK) return s;
+    if (fuse && n > a.start) {
+      launch_embed_finalize(pending, B, m->E, w.h, m->V, m->d, st);
+      if ((s = check_launch("loop: embed + finalize launch")) != DG_OK) return s;
+    } else {
+      // the signal of the previous step (none at step 0; a resumed run reads the one its
+      // previous call left in the workspace)
+      launch_embed_gather(a.canvas, m->E, w.h, BL, m->V, m->d, w.n_active, st,
+                          sc && n > 0 ? w.sc_s : nullptr);
+      if ((s = check_launch("loop: embed launch")) != DG_OK) return s;
+    }
     e = launch_gemm(w.h, m->Wqkv, BL, Hhd + 2 * KVhd, m->d, qkv, nullptr, 0, w.status, w.n_active,
                     st, kActNone, w.gemm_part, w.gemm_part_bytes);
     if (e != cudaSuccess) return cuda_fail(e, "loop: qkv gemm launch");
@@ -872,8 +886,12 @@ dg_status run_denoise(const RunArgs& a, const dg_sampler_cfg* cfg,
       fp.stop_when_all_locked = cfg->stop_when_all_locked;
       fp.unlocked = w.counters;
       fp.cta_done = w.counters + B;
-      launch_vocab_finalize(fp, B, st);
-      if ((s = check_launch("loop: finalize launch")) != DG_OK) return s;
+      if (fuse) {
+        pending = fp;
+      } else {
+        launch_vocab_finalize(fp, B, st);
+        if ((s = check_launch("loop: finalize launch")) != DG_OK) return s;
+      }
     }
     if (sc_next) {
       e = launch_self_condition(w.sc_p, w.sc_m, w.sc_lse, m->E, m->Wsc1, m->Wsc2, BL, m->V,
@@ -881,6 +899,10 @@ dg_status run_denoise(const RunArgs& a, const dg_sampler_cfg* cfg,
                                 w.n_active, st);
       if (e != cudaSuccess) return cuda_fail(e, "loop: self-conditioning launch");
     }
+  }
+  if (fuse && a.end > a.start) {
+    launch_vocab_finalize(pending, B, st);
+    if ((s = check_launch("loop: finalize launch")) != DG_OK) return s;
   }
   return DG_OK;
 }

@@ -121,17 +121,18 @@ __device__ __forceinline__ VocabPart shfl_xor_part(const VocabPart& a, int off) 
   return o;
 }
 
-__global__ void __launch_bounds__(kFinRows * 32) vocab_finalize_kernel(FinalizeParams p) {
-  pdl_wait();
-  pdl_trigger();
-  if (p.n_active && *p.n_active == 0) return;
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int row = blockIdx.x * kFinRows + warp;  // L is a multiple of kFinRows
+// One position: the lanes of a warp merge its tuples; lane 0 writes the posterior outputs and
+// applies the Euler step.  Returns (valid in lane 0) whether the position is locked after the
+// step and its token.
+struct RowFinal {
+  bool locked_after;
+  int32_t token;
+};
+
+__device__ __forceinline__ RowFinal finalize_row(const FinalizeParams& p, int row, int lane) {
   const int b = row / p.L;
   const int i = row % p.L;
   const bool is_active = p.active == nullptr || p.active[b] != 0;
-
   const int mt = row >> 7;
   const int row_in = row & 127;
   VocabPart acc = empty_part();
@@ -150,7 +151,7 @@ __global__ void __launch_bounds__(kFinRows * 32) vocab_finalize_kernel(FinalizeP
     }
   }
 
-  bool locked_after = false;
+  RowFinal r{false, 0};
   if (lane == 0) {
     const float lse = acc.m + logf(acc.s);
     const float lp_top1 = acc.top_z - lse;
@@ -172,33 +173,80 @@ __global__ void __launch_bounds__(kFinRows * 32) vocab_finalize_kernel(FinalizeP
       p.x_out[row] = o.x;
       if (p.lock) p.lock[row] = o.lock ? 1 : 0;
       if (p.jump) p.jump[row] = o.jump ? 1 : 0;
-      locked_after = o.lock && p.lock != nullptr;
+      r.locked_after = o.lock && p.lock != nullptr;
+      r.token = o.x;
     } else if (p.x_in != nullptr) {
-      if (p.x_out != p.x_in) p.x_out[row] = p.x_in[row];
+      const int32_t x = p.x_in[row];
+      if (p.x_out != p.x_in) p.x_out[row] = x;
       if (p.jump) p.jump[row] = 0;
-      locked_after = p.lock != nullptr && p.lock[row] != 0;
+      r.locked_after = p.lock != nullptr && p.lock[row] != 0;
+      r.token = x;
     }
   }
-  const int unlocked = __syncthreads_count(lane == 0 && !locked_after ? 1 : 0);
-  if (threadIdx.x == 0) {
-    if (unlocked) atomicAdd(&p.unlocked[b], unlocked);
+  return r;
+}
+
+// One thread per CTA, after the CTA's positions of canvas b are final: adds their unlocked
+// count; the last of the canvas's ctas_per_canvas CTAs to get here (an atomic ticket, no
+// waiting) sets `done`, updates the loop bookkeeping and resets the counters.
+__device__ __forceinline__ void finalize_ticket(const FinalizeParams& p, int b, int unlocked,
+                                                int ctas_per_canvas) {
+  const bool is_active = p.active == nullptr || p.active[b] != 0;
+  if (unlocked) atomicAdd(&p.unlocked[b], unlocked);
+  __threadfence();
+  const int ticket = atomicAdd(&p.cta_done[b], 1);
+  if (ticket == ctas_per_canvas - 1) {  // the last CTA of this canvas
     __threadfence();
-    const int ticket = atomicAdd(&p.cta_done[b], 1);
-    if (ticket == p.L / kFinRows - 1) {  // the last CTA of this canvas
-      __threadfence();
-      const bool all = atomicAdd(&p.unlocked[b], 0) == 0;
-      if (p.done) p.done[b] = all ? 1 : 0;
-      if (is_active && p.x_in != nullptr) {
-        if (p.steps_taken) p.steps_taken[b] += 1;
-        if (p.active && p.stop_when_all_locked && all) {
-          p.active[b] = 0;
-          if (p.n_active) atomicSub(p.n_active, 1);
-        }
+    const bool all = atomicAdd(&p.unlocked[b], 0) == 0;
+    if (p.done) p.done[b] = all ? 1 : 0;
+    if (is_active && p.x_in != nullptr) {
+      if (p.steps_taken) p.steps_taken[b] += 1;
+      if (p.active && p.stop_when_all_locked && all) {
+        p.active[b] = 0;
+        if (p.n_active) atomicSub(p.n_active, 1);
       }
-      p.unlocked[b] = 0;
-      p.cta_done[b] = 0;
+    }
+    p.unlocked[b] = 0;
+    p.cta_done[b] = 0;
+  }
+}
+
+__global__ void __launch_bounds__(kFinRows * 32) vocab_finalize_kernel(FinalizeParams p) {
+  pdl_wait();
+  pdl_trigger();
+  if (p.n_active && *p.n_active == 0) return;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kFinRows + warp;  // L is a multiple of kFinRows
+  const RowFinal r = finalize_row(p, row, lane);
+  const int unlocked = __syncthreads_count(lane == 0 && !r.locked_after ? 1 : 0);
+  if (threadIdx.x == 0) finalize_ticket(p, row / p.L, unlocked, p.L / kFinRows);
+}
+
+// The previous step's finalisation fused with this step's embedding gather: one CTA per
+// position; warp 0 finalises the position (as above), then the CTA gathers E at its new token.
+__global__ void __launch_bounds__(256) embed_finalize_kernel(FinalizeParams p,
+                                                             const uint4* __restrict__ E,
+                                                             uint4* __restrict__ h, int V,
+                                                             int d16) {
+  pdl_wait();
+  pdl_trigger();
+  if (p.n_active && *p.n_active == 0) return;
+  const int row = blockIdx.x;
+  __shared__ int32_t s_token;
+  if (threadIdx.x < 32) {
+    const RowFinal r = finalize_row(p, row, threadIdx.x);
+    if (threadIdx.x == 0) {
+      s_token = r.token;
+      finalize_ticket(p, row / p.L, r.locked_after ? 0 : 1, p.L);
     }
   }
+  __syncthreads();
+  const int id = s_token;
+  const bool ok = id >= 0 && id < V;
+  for (int c = threadIdx.x; c < d16; c += blockDim.x)
+    h[static_cast<int64_t>(row) * d16 + c] =
+        ok ? E[static_cast<int64_t>(id) * d16 + c] : make_uint4(0, 0, 0, 0);
 }
 
 // Entropy-bounded step [TR "DiffusionGemma 샘플러"]: one CTA per canvas, one thread per
@@ -289,6 +337,16 @@ void launch_vocab_finalize(const FinalizeParams& p, int B, cudaStream_t st) {
   const int rows = B * p.L;
   timer_begin(4, st);
   launch_dependent(vocab_finalize_kernel, dim3(rows / kFinRows), dim3(kFinRows * 32), 0, st, p);
+  timer_end(4, st);
+}
+
+void launch_embed_finalize(const FinalizeParams& p, int B, const uint16_t* E, uint16_t* h, int V,
+                           int d, cudaStream_t st) {
+  const int d16 = d / 8;
+  const int threads = d16 < 256 ? ((d16 + 31) / 32) * 32 : 256;
+  timer_begin(4, st);
+  launch_dependent(embed_finalize_kernel, dim3(B * p.L), dim3(threads), 0, st, p,
+                   reinterpret_cast<const uint4*>(E), reinterpret_cast<uint4*>(h), V, d16);
   timer_end(4, st);
 }
 

@@ -76,6 +76,10 @@ void launch_euler_update(const int32_t* x_in, const int32_t* x0hat, const int32_
                          uint8_t* done, int B, int L, uint64_t seed, int step, uint64_t jump_thr,
                          float lock_logthr, cudaStream_t st);
 void launch_vocab_finalize(const FinalizeParams& p, int B, cudaStream_t st);
+// The finalisation of p (the previous step) fused with the embedding gather h = E[x_out] of
+// the next step (no self-conditioning signal); p.x_in and p.x_out must be set.
+void launch_embed_finalize(const FinalizeParams& p, int B, const uint16_t* E, uint16_t* h, int V,
+                           int d, cudaStream_t st);
 void launch_loop_init(const uint8_t* lock, uint8_t* active, int* n_active, int32_t* steps_taken,
                       int B, int L, int stop_when_all_locked, cudaStream_t st);
 // h = E[x] (+ s when s != NULL: the self-conditioning signal, bf16 [BL, d]).

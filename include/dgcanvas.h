@@ -325,8 +325,9 @@ typedef struct {
  * only. */
 size_t dg_denoise_loop_workspace(const dg_model* m, int B, int L, int P, int window);
 
-/* Number of kernels one dg_denoise_loop call launches for `steps` steps on this device (its
- * launch plan depends on the SM count); -1 on invalid arguments.  Host only. */
+/* Number of kernels one dg_denoise_loop call with the Euler sampler launches for `steps` steps
+ * on this device (its launch plan depends on the SM count); -1 on invalid arguments.  Host
+ * only. */
 int dg_denoise_loop_kernel_count(const dg_model* m, int B, int L, int P, int window, int steps);
 dg_status dg_denoise_loop(const dg_model* m, const uint16_t* k_pre, const uint16_t* v_pre, int B,
                           int L, int P, int window, int32_t* canvas, uint8_t* lock,
