@@ -354,9 +354,13 @@ def run_ours(args, w):
             "achieved_tflops": flops_per_launch / sc_avg_s / 1e12 if sc_n else None,
             "hbm_gbs_algorithmic": (2.0 * w.V * w.d + 2.0 * B * w.L * w.V) / sc_avg_s / 1e9
             if sc_n else None}
-    # the entropy-bounded sampler launches one more kernel (its update) per denoising step
+    # the count is the Euler sampler's; the entropy-bounded sampler launches one more kernel
+    # (its update) per denoising step and, without self-conditioning, keeps every step's
+    # finalisation as its own launch (the Euler loop folds all but the last into the next
+    # step's embedding launch)
+    eb_extra = (w.T + (w.T - 1 if not sc else 0)) if eb else 0
     launches = args.steps * (1 + dgc.dg_denoise_loop_kernel_count(model, B, w.L, w.P, w.window,
-                                                                  w.T) + (w.T if eb else 0))
+                                                                  w.T) + eb_extra)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -326,8 +326,10 @@ typedef struct {
 size_t dg_denoise_loop_workspace(const dg_model* m, int B, int L, int P, int window);
 
 /* Number of kernels one dg_denoise_loop call with the Euler sampler launches for `steps` steps
- * on this device (its launch plan depends on the SM count); -1 on invalid arguments.  Host
- * only. */
+ * on this device (its launch plan depends on the SM count); -1 on invalid arguments.  (The
+ * entropy-bounded sampler adds its update kernel per step and, without self-conditioning,
+ * steps - 1 finalisation launches that the Euler loop folds into its embedding launches.)
+ * Host only. */
 int dg_denoise_loop_kernel_count(const dg_model* m, int B, int L, int P, int window, int steps);
 dg_status dg_denoise_loop(const dg_model* m, const uint16_t* k_pre, const uint16_t* v_pre, int B,
                           int L, int P, int window, int32_t* canvas, uint8_t* lock,
