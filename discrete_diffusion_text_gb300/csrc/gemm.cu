@@ -495,39 +495,37 @@ bool divides_segments(const GemmOut& out, int N, int bn) {
 }  // namespace
 
 GemmPlan plan_gemm(int M, int N, int K, const GemmOut& out) {
+  // Cost in units of one k-block of one CTA (~0.3 us): the issuing thread spends about the
+  // same time on an MMA whatever N <= 256, so a CTA's time is its k-block count whatever the
+  // tile width, and the cost is waves x k-blocks per CTA (one CTA per SM: the ring fills its
+  // shared memory).  A K split adds the write-out and sum of its fp32 partials: measured
+  // ~10 k-blocks per 96 KiB a CTA writes ((S - 1)/S of its 128 x BN partial).  Ties: the
+  // wider tile, then no split.
   GemmPlan pl{};
+  pl.BN = 64;
   pl.S = 1;
   const int mt = (M + kBM - 1) / kBM;
   const int nkb = K / kBK;
   const int64_t nsm = num_sms();
-  // single-CTA tiles: the largest N tile that divides every output-segment boundary (a tile
-  // never straddles two outputs) and still gives at least two CTAs per SM; 64 otherwise
-  pl.BN = 64;
-  if (divides_segments(out, N, 256) && static_cast<int64_t>(mt) * (N / 256) >= 2 * nsm)
-    pl.BN = 256;
-  else if (divides_segments(out, N, 128) && static_cast<int64_t>(mt) * (N / 128) >= 2 * nsm)
-    pl.BN = 128;
-  if (mt <= 0 || static_cast<int64_t>(mt) * (N / 64) > nsm) return pl;
-  // at most one wave of 64-column tiles: split K over clusters instead, with as many CTAs as
-  // fit in one wave (ties: the longer split, then the wider tile)
-  int best_ctas = 0, best_bn = 0, best_s = 0;
-  for (int bn : {256, 128}) {
+  if (mt <= 0 || nkb <= 0) return pl;
+  double best = -1.0;
+  for (int bn : {256, 128, 64}) {
     if (!divides_segments(out, N, bn)) continue;
-    for (int s : {4, 2}) {
-      if (s > nkb) continue;
+    for (int s : {1, 2, 4}) {
+      if (s > 1 && (bn == 64 || s > nkb || !split_fits(bn, s))) continue;
       const int64_t ctas = static_cast<int64_t>(mt) * (N / bn) * s;
-      if (ctas > nsm || !split_fits(bn, s)) continue;
-      if (ctas > best_ctas || (ctas == best_ctas && s > best_s)) {
-        best_ctas = static_cast<int>(ctas);
-        best_bn = bn;
-        best_s = s;
+      const int64_t waves = (ctas + nsm - 1) / nsm;
+      const double written_kib = (s - 1) * (kBM / s) * bn * 4 / 1024.0;
+      const double cost = static_cast<double>(waves) * ((nkb + s - 1) / s + written_kib / 9.6);
+      if (best < 0 || cost < best - 1e-9) {
+        best = cost;
+        pl.BN = bn;
+        pl.S = s;
       }
     }
   }
-  if (best_ctas == 0) return pl;
-  pl.BN = best_bn;
-  pl.S = best_s;
-  pl.part_bytes = static_cast<size_t>(mt) * (N / best_bn) * best_s * kBM * best_bn * 4;
+  pl.part_bytes =
+      pl.S > 1 ? static_cast<size_t>(mt) * (N / pl.BN) * pl.S * kBM * pl.BN * 4 : 0;
   return pl;
 }
 
@@ -541,9 +539,10 @@ cudaError_t launch_gemm(const uint16_t* A, const uint16_t* W, int M, int N, int 
   GemmPlan pl = plan_gemm(M, N, K, out);
   if (pl.S > 1 && (part_ws == nullptr || part_ws_bytes < pl.part_bytes ||
                    (reinterpret_cast<uintptr_t>(part_ws) & 15) != 0)) {
-    // no room for the split partials: one CTA per tile over the whole K
+    // no room for the split partials: one CTA per tile over the whole K, as wide as the
+    // output segments allow (the fewest tiles)
     pl.S = 1;
-    pl.BN = 64;
+    pl.BN = divides_segments(out, N, 256) ? 256 : divides_segments(out, N, 128) ? 128 : 64;
   }
 
   CUtensorMap ta, tb;

@@ -1,6 +1,8 @@
 """GPU parity of the fused SFT cross-entropy (LM head + log-sum-exp + target logit in one pass)
 and of the SFT loss on noised canvases, against the CPU oracle, through the C ABI."""
 
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -76,8 +78,6 @@ def test_cross_entropy_full_vocabulary_sampled_rows(dgc):
 def test_sft_loss_on_noised_canvases_matches_oracle(dgc):
     """Zipf(1.1) clean canvases noised at per-canvas t (keep thresholds from t), the stand-in
     decoder over them with the prefix KV, and the cross-entropy against x_0."""
-    import dataclasses
-
     w = dataclasses.replace(synth.TINY, B=4)
     m = synth.make_model(w)
     kp, vp = synth.make_prefix_kv(w)
@@ -99,15 +99,17 @@ def test_sft_loss_on_noised_canvases_matches_oracle(dgc):
     assert np.abs(loss.cpu().numpy() - ref).max() <= LOSS_TOL
 
 
-def test_sft_loss_window1k_sampled_rows(dgc):
+@pytest.mark.parametrize("B", [1, 2])
+def test_sft_loss_window1k_sampled_rows(dgc, B):
     """SFT loss at the window1k dims (d_model 2,048, 16q/8kv x 128, vocabulary 262,144, prefix
-    1,024 in a 1,024 window), where one canvas's projections run as cluster split-K: noising
-    bit-exact for the whole canvas; the oracle recomputes the decoder for the whole canvas and
-    the loss at 16 sampled positions.  With the tied head a kept position's loss is
+    1,024 in a 1,024 window) for one and two canvases, whose projections run as cluster split-K
+    (QKV 4- or 2-way, the output projection 4-way at 128 or 256 columns): noising bit-exact for
+    every canvas; the oracle recomputes the decoder for every canvas and the loss at 16 sampled
+    positions.  With the tied head a kept position's loss is
     lse - 2 y.E[x_t] at 1/tau = 2: a projection that dropped a quarter of its K range would move
     it by ~1e-2, while the attention's bf16 probabilities in P.V move y.E[x_t] by ~3e-4 (so
     1/tau = 20 would put legitimate rounding at the tolerance)."""
-    w = synth.WINDOW1K
+    w = dataclasses.replace(synth.WINDOW1K, B=B)
     m = synth.make_model(w, DEV)
     kp, vp = synth.make_prefix_kv(w, DEV)
     x0 = synth.zipf_tokens(w.B, w.L, w.V, 1.1, 96)
@@ -125,8 +127,8 @@ def test_sft_loss_window1k_sampled_rows(dgc):
     assert np.array_equal(xt.cpu().numpy(), rxt)
     h, q, kc, vc = O.decoder_front(rxt, E, f64(m["Wqkv"]), w.H, w.Hkv, w.hd)
     Oa, _ = O.canvas_attention(q, f64(kp), f64(vp), kc, vc, w.window, w.hd ** -0.5)
-    y = O.decoder_back(h, Oa, f64(m["Wo"])).reshape(w.L, w.d)
-    rows = np.sort(np.random.default_rng(99).choice(w.L, 16, replace=False))
+    y = O.decoder_back(h, Oa, f64(m["Wo"])).reshape(w.B * w.L, w.d)
+    rows = np.sort(np.random.default_rng(99).choice(w.B * w.L, 16, replace=False))
     ref, _ = O.cross_entropy(y[rows], E, 2.0, x0.reshape(-1)[rows])
     got = loss.cpu().numpy().reshape(-1)[rows]
     assert np.std(ref) > 0.05  # the loss varies from row to row

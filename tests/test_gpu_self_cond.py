@@ -92,16 +92,18 @@ def test_self_condition_matches_oracle(dgc, B, L, V, d, dsc, ystd, inv_tau):
     _check_ffw(s_gpu, e_gpu, W1, W2)
 
 
-def test_self_condition_window1k_sampled_rows(dgc):
+@pytest.mark.parametrize("B", [1, 2])
+def test_self_condition_window1k_sampled_rows(dgc, B):
     """window1k shapes at full size (vocabulary 262,144, d 2,048, d_sc 1,920: 7.9M feed-forward
-    parameters); the oracle computes 8 sampled rows."""
+    parameters) for one and two canvases, whose feed-forward GEMMs take different K splits
+    (4-way over 30 or 32 k-blocks; 2- and 4-way); the oracle computes 8 sampled rows."""
     w = synth.WINDOW1K
     m = synth.make_model(w, DEV)
     W1 = synth.normal_bf16((1920, w.d), 0.02, 85)
     W2 = synth.normal_bf16((w.d, 1920), 0.02, 86)
-    y = synth.normal_bf16((w.L, w.d), 0.5, 87)
-    e_gpu, s_gpu = _run_sc(dgc, y, m["E"], W1, W2, 1, w.L, 1.0)
-    rows = np.sort(np.random.default_rng(3).choice(w.L, 8, replace=False))
+    y = synth.normal_bf16((B * w.L, w.d), 0.5, 87)
+    e_gpu, s_gpu = _run_sc(dgc, y, m["E"], W1, W2, B, w.L, 1.0)
+    rows = np.sort(np.random.default_rng(3).choice(B * w.L, 8, replace=False))
     _check_e(e_gpu, y, m["E"].cpu(), 1.0, rows)
     _check_ffw(s_gpu[rows], e_gpu[rows], W1, W2)
 
