@@ -494,13 +494,14 @@ bool divides_segments(const GemmOut& out, int N, int bn) {
 
 }  // namespace
 
-GemmPlan plan_gemm(int M, int N, int K, const GemmOut& out) {
+namespace {
+GemmPlan plan_gemm_impl(int M, int N, int K, const GemmOut& out, bool allow_split) {
   // Cost in units of one k-block of one CTA (~0.3 us): the issuing thread spends about the
   // same time on an MMA whatever N <= 256, so a CTA's time is its k-block count whatever the
   // tile width, and the cost is waves x k-blocks per CTA (one CTA per SM: the ring fills its
   // shared memory).  A K split adds the write-out and sum of its fp32 partials: measured
-  // ~10 k-blocks per 96 KiB a CTA writes ((S - 1)/S of its 128 x BN partial).  Ties: the
-  // wider tile, then no split.
+  // ~10 k-blocks per 96 KiB a CTA writes ((S - 1)/S of its 128 x BN partial).  Ties: more
+  // CTAs (the narrower tiles' smaller epilogues and spread loads measured slightly faster).
   GemmPlan pl{};
   pl.BN = 64;
   pl.S = 1;
@@ -509,16 +510,18 @@ GemmPlan plan_gemm(int M, int N, int K, const GemmOut& out) {
   const int64_t nsm = num_sms();
   if (mt <= 0 || nkb <= 0) return pl;
   double best = -1.0;
+  int64_t best_ctas = 0;
   for (int bn : {256, 128, 64}) {
     if (!divides_segments(out, N, bn)) continue;
     for (int s : {1, 2, 4}) {
-      if (s > 1 && (bn == 64 || s > nkb || !split_fits(bn, s))) continue;
+      if (s > 1 && (!allow_split || bn == 64 || s > nkb || !split_fits(bn, s))) continue;
       const int64_t ctas = static_cast<int64_t>(mt) * (N / bn) * s;
       const int64_t waves = (ctas + nsm - 1) / nsm;
       const double written_kib = (s - 1) * (kBM / s) * bn * 4 / 1024.0;
       const double cost = static_cast<double>(waves) * ((nkb + s - 1) / s + written_kib / 9.6);
-      if (best < 0 || cost < best - 1e-9) {
+      if (best < 0 || cost < best - 1e-9 || (cost < best + 1e-9 && ctas > best_ctas)) {
         best = cost;
+        best_ctas = ctas;
         pl.BN = bn;
         pl.S = s;
       }
@@ -527,6 +530,11 @@ GemmPlan plan_gemm(int M, int N, int K, const GemmOut& out) {
   pl.part_bytes =
       pl.S > 1 ? static_cast<size_t>(mt) * (N / pl.BN) * pl.S * kBM * pl.BN * 4 : 0;
   return pl;
+}
+}  // namespace
+
+GemmPlan plan_gemm(int M, int N, int K, const GemmOut& out) {
+  return plan_gemm_impl(M, N, K, out, true);
 }
 
 cudaError_t launch_gemm(const uint16_t* A, const uint16_t* W, int M, int N, int K,
@@ -539,10 +547,8 @@ cudaError_t launch_gemm(const uint16_t* A, const uint16_t* W, int M, int N, int 
   GemmPlan pl = plan_gemm(M, N, K, out);
   if (pl.S > 1 && (part_ws == nullptr || part_ws_bytes < pl.part_bytes ||
                    (reinterpret_cast<uintptr_t>(part_ws) & 15) != 0)) {
-    // no room for the split partials: one CTA per tile over the whole K, as wide as the
-    // output segments allow (the fewest tiles)
-    pl.S = 1;
-    pl.BN = divides_segments(out, N, 256) ? 256 : divides_segments(out, N, 128) ? 128 : 64;
+    // no room for the split partials: one CTA per tile over the whole K
+    pl = plan_gemm_impl(M, N, K, out, false);
   }
 
   CUtensorMap ta, tb;
