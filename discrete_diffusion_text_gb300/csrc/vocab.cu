@@ -13,6 +13,8 @@
 //                by their log-sum-exps, then an inverse-CDF pick inside the winning chunk.
 // Only rows' partial tuples are written; a finalisation kernel merges them in a fixed order and
 // applies the Euler step (the chunk scores merge like any Gumbel-max scores).
+#include <type_traits>
+
 #include "kernels.cuh"
 #include "sm103.cuh"
 
@@ -43,14 +45,26 @@ struct VocabParams {
   const int* n_active;
 };
 
+// Shared memory.  Unified ring: kStages stages of (y k-block, W k-block).  Split rings (one
+// wave of CTAs, i.e. one canvas): kWStages W k-blocks from the TMA warp and kYStages y
+// k-blocks from a second TMA warp, so more of the memory holds the weight stream from DRAM
+// (the y tiles come from L2).
+template <bool kSplit>
 struct VocabLayout {
-  static constexpr int kABytes = kBM * kBK * 2;   // 16 KiB
-  static constexpr int kBBytes = kBN * kBK * 2;   // 32 KiB
+  static constexpr int kABytes = kBM * kBK * 2;   // 16 KiB: a y k-block
+  static constexpr int kBBytes = kBN * kBK * 2;   // 32 KiB: a W k-block
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kScratchOff = kStages * kStageBytes;
+  static constexpr int kWStages = kSplit ? 5 : kStages;
+  static constexpr int kYStages = kSplit ? 3 : 0;
+  static constexpr int kYOff = kWStages * kBBytes;  // split rings only
+  static constexpr int kRingBytes =
+      kSplit ? kWStages * kBBytes + kYStages * kABytes : kStages * kStageBytes;
+  static constexpr int kScratchOff = kRingBytes;
   static constexpr int kScratchBytes = (kGroups - 1) * kBM * sizeof(VocabPart);
   static constexpr int kBarOff = kScratchOff + kScratchBytes;
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;
+  static constexpr int kThreadsT = kThreads + (kSplit ? 32 : 0);  // + the y TMA warp
+  static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -174,21 +188,27 @@ __device__ __forceinline__ void process_chunk(RowState& st, const float (&z)[32]
   }
 }
 
-template <bool kCE, bool kEnt, bool kSC>
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool kCE, bool kEnt, bool kSC, bool kSplit>
+__global__ void __launch_bounds__(VocabLayout<kSplit>::kThreadsT, 1)
     vocab_posterior_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB, VocabParams p) {
-  using Lay = VocabLayout;
+  using Lay = VocabLayout<kSplit>;
+  constexpr int kWS = Lay::kWStages;
+  constexpr int kYS = Lay::kYStages;
   pdl_wait();
   if (p.n_active && *p.n_active == 0) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   VocabPart* scratch = reinterpret_cast<VocabPart*>(smem + Lay::kScratchOff);
+  // full/empty: the unified stages, or the W stages of the split rings; yfull/yempty: the y
+  // stages of the split rings (none otherwise)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lay::kBarOff);
-  uint64_t* empty = full + kStages;
-  uint64_t* tfull = empty + kStages;  // [2]
-  uint64_t* tempty = tfull + 2;       // [2]
+  uint64_t* empty = full + kWS;
+  uint64_t* yfull = empty + kWS;
+  uint64_t* yempty = yfull + kYS;
+  uint64_t* tfull = yempty + kYS;  // [2]
+  uint64_t* tempty = tfull + 2;    // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -197,9 +217,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nkb = p.d / kBK;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kWS; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < kYS; ++s) {
+      mbar_init(&yfull[s], 1);
+      mbar_init(&yempty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -231,18 +255,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int vt1 = min(vt0 + p.per, p.nvt);
         for (int vt = vt0; ok && vt < vt1; ++vt) {
           for (int kb = 0; kb < nkb; ++kb, ++g) {
-            const int s = g % kStages;
-            if (!mbar_wait(&empty[s], ((g / kStages) & 1) ^ 1, abort_flag)) { ok = false; break; }
-            uint8_t* sa = smem + s * Lay::kStageBytes;
-            mbar_arrive_expect_tx(&full[s], Lay::kStageBytes);
-            tma_load_2d(sa, &tmA, &full[s], kb * kBK, mt * kBM);
-            tma_load_2d_hint(sa + Lay::kABytes, &tmB, &full[s], kb * kBK, vt * kBN, stream_once);
+            const int s = g % kWS;
+            if (!mbar_wait(&empty[s], ((g / kWS) & 1) ^ 1, abort_flag)) { ok = false; break; }
+            if constexpr (kSplit) {  // the W k-block alone (warp 18 loads y)
+              uint8_t* sb = smem + s * Lay::kBBytes;
+              mbar_arrive_expect_tx(&full[s], Lay::kBBytes);
+              tma_load_2d_hint(sb, &tmB, &full[s], kb * kBK, vt * kBN, stream_once);
+            } else {
+              uint8_t* sa = smem + s * Lay::kStageBytes;
+              mbar_arrive_expect_tx(&full[s], Lay::kStageBytes);
+              tma_load_2d(sa, &tmA, &full[s], kb * kBK, mt * kBM);
+              tma_load_2d_hint(sa + Lay::kABytes, &tmB, &full[s], kb * kBK, vt * kBN,
+                               stream_once);
+            }
           }
         }
       }
       if (!ok) {
-        for (uint32_t q = (g > kStages ? g - kStages : 0); q < g; ++q)
-          mbar_wait_drain(&full[q % kStages], (q / kStages) & 1);
+        for (uint32_t q = (g > kWS ? g - kWS : 0); q < g; ++q)
+          mbar_wait_drain(&full[q % kWS], (q / kWS) & 1);
+      }
+    }
+  } else if (kSplit && warp == kThreads / 32) {
+    // ------------------------------------------- y producer (split rings only) -----
+    if (lane == 0) {
+      uint32_t g = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+        const int mt = u % p.num_mt;
+        const int chunk = u / p.num_mt;
+        const int vt0 = chunk * p.per;
+        const int vt1 = min(vt0 + p.per, p.nvt);
+        for (int vt = vt0; ok && vt < vt1; ++vt) {
+          for (int kb = 0; kb < nkb; ++kb, ++g) {
+            const int s = g % kYS;
+            if (!mbar_wait(&yempty[s], ((g / kYS) & 1) ^ 1, abort_flag)) { ok = false; break; }
+            uint8_t* sa = smem + Lay::kYOff + s * Lay::kABytes;
+            mbar_arrive_expect_tx(&yfull[s], Lay::kABytes);
+            tma_load_2d(sa, &tmA, &yfull[s], kb * kBK, mt * kBM);
+          }
+        }
+      }
+      if (!ok) {
+        for (uint32_t q = (g > kYS ? g - kYS : 0); q < g; ++q)
+          mbar_wait_drain(&yfull[q % kYS], (q / kYS) & 1);
       }
     }
   } else if (warp == 1) {
@@ -260,16 +316,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t d_tmem = tmem + buf * kBN;
           for (int kb = 0; kb < nkb; ++kb, ++g) {
-            const int s = g % kStages;
-            if (!mbar_wait(&full[s], (g / kStages) & 1, abort_flag)) { ok = false; break; }
+            const int s = g % kWS;
+            if (!mbar_wait(&full[s], (g / kWS) & 1, abort_flag)) { ok = false; break; }
+            uint32_t sa, sb;
+            int ys = 0;
+            if constexpr (kSplit) {
+              ys = g % kYS;
+              if (!mbar_wait(&yfull[ys], (g / kYS) & 1, abort_flag)) { ok = false; break; }
+              sa = smem_u32(smem + Lay::kYOff + ys * Lay::kABytes);
+              sb = smem_u32(smem + s * Lay::kBBytes);
+            } else {
+              sa = smem_u32(smem + s * Lay::kStageBytes);
+              sb = sa + Lay::kABytes;
+            }
             tc_fence_after();
-            const uint32_t sa = smem_u32(smem + s * Lay::kStageBytes);
-            const uint32_t sb = sa + Lay::kABytes;
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k)
               mma_bf16_ss(d_tmem, sdesc_sw128(sa + k * 32, 16, 1024),
                           sdesc_sw128(sb + k * 32, 16, 1024), idesc, (kb | k) != 0);
             mma_commit(&empty[s]);
+            if constexpr (kSplit) mma_commit(&yempty[ys]);
           }
           if (ok) mma_commit(&tfull[buf]);
         }
@@ -444,32 +510,53 @@ cudaError_t launch_vocab_pass(const uint16_t* y, const uint16_t* W, int R, int L
   const int dev = device_id();
   if (configured_device != dev) {
     cudaError_t e = cudaSuccess;
-    for (auto fn : {vocab_posterior_kernel<false, false, false>,
-                    vocab_posterior_kernel<false, true, false>,
-                    vocab_posterior_kernel<true, false, false>,
-                    vocab_posterior_kernel<false, false, true>,
-                    vocab_posterior_kernel<false, true, true>,
-                    vocab_posterior_kernel<true, false, true>})
+    for (auto fn : {vocab_posterior_kernel<false, false, false, false>,
+                    vocab_posterior_kernel<false, true, false, false>,
+                    vocab_posterior_kernel<true, false, false, false>,
+                    vocab_posterior_kernel<false, false, true, false>,
+                    vocab_posterior_kernel<false, true, true, false>,
+                    vocab_posterior_kernel<true, false, true, false>})
       if (e == cudaSuccess)
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 VocabLayout::kSmemBytes);
+                                 VocabLayout<false>::kSmemBytes);
+    for (auto fn : {vocab_posterior_kernel<false, false, false, true>,
+                    vocab_posterior_kernel<false, true, false, true>,
+                    vocab_posterior_kernel<true, false, false, true>,
+                    vocab_posterior_kernel<false, false, true, true>,
+                    vocab_posterior_kernel<false, true, true, true>,
+                    vocab_posterior_kernel<true, false, true, true>})
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 VocabLayout<true>::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
   timer_begin(0, st);
   // cross-entropy mode (targets, or the self-conditioning pass alone: no sampling), or
   // sampling with or without the entropy accumulator; each with or without the
-  // self-conditioning store
+  // self-conditioning store.  Split rings when the pass is a single wave (one unit per CTA:
+  // one canvas) and its epilogue is light: measured at one canvas, cross-entropy 0.1998 ->
+  // 0.1922 ms and the self-conditioning store 0.269 -> 0.256 ms, but sampling unchanged and
+  // the entropy accumulator slower (the extra TMA warp takes issue slots from the heavier
+  // epilogues); with several waves the unified ring is faster (-7 % at 16 canvases).
   const bool sc = sc_p != nullptr;
   const bool ce = targets != nullptr || ce_only;
-  auto fn = ce ? (sc ? vocab_posterior_kernel<true, false, true>
-                     : vocab_posterior_kernel<true, false, false>)
-               : entropy ? (sc ? vocab_posterior_kernel<false, true, true>
-                               : vocab_posterior_kernel<false, true, false>)
-                         : (sc ? vocab_posterior_kernel<false, false, true>
-                               : vocab_posterior_kernel<false, false, false>);
-  cudaError_t e = launch_dependent(fn, dim3(pl.grid), dim3(kThreads), VocabLayout::kSmemBytes, st,
-                                   ta, tb, p);
+  cudaError_t e;
+  auto launch = [&](auto split_tag) {
+    constexpr bool kS = decltype(split_tag)::value;
+    auto fn = ce ? (sc ? vocab_posterior_kernel<true, false, true, kS>
+                       : vocab_posterior_kernel<true, false, false, kS>)
+                 : entropy ? (sc ? vocab_posterior_kernel<false, true, true, kS>
+                                 : vocab_posterior_kernel<false, true, false, kS>)
+                           : (sc ? vocab_posterior_kernel<false, false, true, kS>
+                                 : vocab_posterior_kernel<false, false, false, kS>);
+    return launch_dependent(fn, dim3(pl.grid), dim3(VocabLayout<kS>::kThreadsT),
+                            VocabLayout<kS>::kSmemBytes, st, ta, tb, p);
+  };
+  if (pl.units <= pl.grid && (ce || sc))
+    e = launch(std::true_type{});
+  else
+    e = launch(std::false_type{});
   timer_end(0, st);
   return e;
 }
