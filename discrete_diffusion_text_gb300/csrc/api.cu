@@ -594,12 +594,7 @@ dg_status dg_sft_loss(const dg_model* m, const uint16_t* k_pre, const uint16_t* 
   if ((s = check_launch("sft_loss: noise launch")) != DG_OK) return s;
   launch_embed_gather(xt, m->E, w.h, BL, m->V, m->d, nullptr, st);
   if ((s = check_launch("sft_loss: embed launch")) != DG_OK) return s;
-  GemmOut qkv{};
-  qkv.nseg = 3;
-  qkv.seg_begin[0] = 0;
-  qkv.seg_begin[1] = Hhd;
-  qkv.seg_begin[2] = Hhd + KVhd;
-  qkv.seg_begin[3] = Hhd + 2 * KVhd;
+  GemmOut qkv = qkv_segments(m);  // the segments the workspace's split-K plan was sized for
   qkv.ptr[0] = w.q;
   qkv.ptr[1] = w.k;
   qkv.ptr[2] = w.v;
@@ -783,12 +778,7 @@ dg_status run_denoise(const RunArgs& a, const dg_sampler_cfg* cfg,
                           eb ? 0 : cfg->stop_when_all_locked, st);
   if ((s = check_launch("loop init launch")) != DG_OK) return s;
 
-  GemmOut qkv{};
-  qkv.nseg = 3;
-  qkv.seg_begin[0] = 0;
-  qkv.seg_begin[1] = Hhd;
-  qkv.seg_begin[2] = Hhd + KVhd;
-  qkv.seg_begin[3] = Hhd + 2 * KVhd;
+  GemmOut qkv = qkv_segments(m);  // the segments the workspace's split-K plan was sized for
   qkv.ptr[0] = w.q;
   qkv.ptr[1] = w.k;
   qkv.ptr[2] = w.v;
