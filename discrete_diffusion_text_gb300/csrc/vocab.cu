@@ -65,6 +65,7 @@ struct VocabLayout {
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;
   static constexpr int kThreadsT = kThreads + (kSplit ? 32 : 0);  // + the y TMA warp
   static_assert(kSmemBytes <= 232448, "shared memory");
+  static_assert(!kSplit || kYOff + kYStages * kABytes == kRingBytes, "y ring after the W ring");
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -104,10 +105,12 @@ __device__ __forceinline__ float open_unit(uint32_t u) {
 // reference m it was taken against (at *sc_mdst); NULL pointers for rows past the end.  The
 // normalised posterior of the self-conditioning contraction is that value times
 // exp(m - lse), applied once lse is known.
+// u_gumbel: the chunk's Gumbel draw, word c & 3 of Philox(c >> 2, pos, canvas, c3) for chunk
+// c = vbase / 32 (computed by the caller, once for the chunks that share a counter).
 template <bool kCE, bool kEnt, bool kSC>
 __device__ __forceinline__ void process_chunk(RowState& st, const float (&z)[32], int vbase,
                                               float inv_tau, uint32_t pos, uint32_t canvas,
-                                              const PhiloxKeys& keys, uint32_t c3,
+                                              const PhiloxKeys& keys, uint32_t u_gumbel,
                                               uint32_t c3_pick, int target, uint16_t* sc_dst,
                                               float* sc_mdst) {
   float mx[4] = {z[0], z[1], z[2], z[3]};  // four partial maxima: short dependency chains
@@ -166,10 +169,7 @@ __device__ __forceinline__ void process_chunk(RowState& st, const float (&z)[32]
     return;
   }
   const uint32_t c = static_cast<uint32_t>(vbase) >> 5;
-  const Words4 w = philox4x32_10(c >> 2, pos, canvas, c3, keys);
-  const uint32_t q = c & 3;
-  const uint32_t u = q == 0 ? w.x : (q == 1 ? w.y : (q == 2 ? w.z : w.w));
-  const float score = st.m + logf(sc) - logf(-log1pf(-open_unit(u)));
+  const float score = st.m + logf(sc) - logf(-log1pf(-open_unit(u_gumbel)));
   if (score > st.best) {
     const float target_mass = open_unit(philox4x32_10(c, pos, canvas, c3_pick, keys).x) * sc;
     float cum = 0.f;
@@ -278,6 +278,7 @@ __global__ void __launch_bounds__(VocabLayout<kSplit>::kThreadsT, 1)
     }
   } else if (kSplit && warp == kThreads / 32) {
     // ------------------------------------------- y producer (split rings only) -----
+    if constexpr (kSplit) {
     if (lane == 0) {
       uint32_t g = 0;
       bool ok = true;
@@ -300,6 +301,7 @@ __global__ void __launch_bounds__(VocabLayout<kSplit>::kThreadsT, 1)
         for (uint32_t q = (g > kYS ? g - kYS : 0); q < g; ++q)
           mbar_wait_drain(&yfull[q % kYS], (q / kYS) & 1);
       }
+    }
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -387,6 +389,16 @@ __global__ void __launch_bounds__(VocabLayout<kSplit>::kThreadsT, 1)
         // buffer goes back to the MMA warp after the second read, which leaves it a whole tile
         // of slack (the MMA needs this buffer again only after the other one)
         const int col = grp * kGroupCols;
+        // this thread's two chunks, 8 vt + 2 grp and the next, share the Gumbel counter
+        // (chunk >> 2): one Philox call gives both draws
+        static_assert(kGroupCols == 64, "two 32-column chunks per thread and tile");
+        uint32_t ug[2] = {0u, 0u};
+        if (!kCE) {
+          const uint32_t c0 = static_cast<uint32_t>(vt * kBN + col) >> 5;  // even
+          const Words4 w = philox4x32_10(c0 >> 2, pos, canvas, p.c3, keys);
+          ug[0] = (c0 & 2) ? w.z : w.x;
+          ug[1] = (c0 & 2) ? w.w : w.y;
+        }
 #pragma unroll 1
         for (int c = 0; c < kGroupCols / 32; ++c) {
           float z[32];
@@ -396,8 +408,9 @@ __global__ void __launch_bounds__(VocabLayout<kSplit>::kThreadsT, 1)
             mbar_arrive(&tempty[buf]);
           }
           const int vb = vt * kBN + col + c * 32;
-          process_chunk<kCE, kEnt, kSC>(st, z, vb, p.inv_tau, pos, canvas, keys, p.c3,
-                                        p.c3_pick, target, sc_row ? sc_row + vb : nullptr,
+          process_chunk<kCE, kEnt, kSC>(st, z, vb, p.inv_tau, pos, canvas, keys,
+                                        c == 0 ? ug[0] : ug[1], p.c3_pick, target,
+                                        sc_row ? sc_row + vb : nullptr,
                                         scm_row ? scm_row + (vb >> 5) : nullptr);
         }
       }
