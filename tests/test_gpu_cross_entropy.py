@@ -99,17 +99,17 @@ def test_sft_loss_on_noised_canvases_matches_oracle(dgc):
     assert np.abs(loss.cpu().numpy() - ref).max() <= LOSS_TOL
 
 
-@pytest.mark.parametrize("B", [1, 2])
-def test_sft_loss_window1k_sampled_rows(dgc, B):
+@pytest.mark.parametrize("B,L", [(1, 256), (2, 256), (1, 192)])
+def test_sft_loss_window1k_sampled_rows(dgc, B, L):
     """SFT loss at the window1k dims (d_model 2,048, 16q/8kv x 128, vocabulary 262,144, prefix
-    1,024 in a 1,024 window) for one and two canvases, whose projections run as cluster split-K
-    (QKV 4- or 2-way, the output projection 4-way at 128 or 256 columns): noising bit-exact for
-    every canvas; the oracle recomputes the decoder for every canvas and the loss at 16 sampled
-    positions.  With the tied head a kept position's loss is
+    1,024 in a 1,024 window) for one and two canvases and a 192-position canvas (a ragged last
+    row tile), whose projections run as cluster split-K (QKV 4- or 2-way, the output projection
+    4-way at 128 or 256 columns): noising bit-exact for every canvas; the oracle recomputes the
+    decoder for every canvas and the loss at 16 sampled positions.  With the tied head a kept position's loss is
     lse - 2 y.E[x_t] at 1/tau = 2: a projection that dropped a quarter of its K range would move
     it by ~1e-2, while the attention's bf16 probabilities in P.V move y.E[x_t] by ~3e-4 (so
     1/tau = 20 would put legitimate rounding at the tolerance)."""
-    w = dataclasses.replace(synth.WINDOW1K, B=B)
+    w = dataclasses.replace(synth.WINDOW1K, B=B, L=L)
     m = synth.make_model(w, DEV)
     kp, vp = synth.make_prefix_kv(w, DEV)
     x0 = synth.zipf_tokens(w.B, w.L, w.V, 1.1, 96)
