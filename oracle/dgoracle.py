@@ -46,12 +46,13 @@ draw the method makes, so that both implementations see identical random bits:
   chunk Gumbel noise    : counter (c>>2, pos, canvas, (2<<24)|step); chunk c uses word c&3
   Euler jump            : counter (0, pos, canvas, (3<<24)|step); word 0
   re-noising (entropy-bounded sampler) : counter (pos, canvas, 0, (4<<24)|step); word 0
-  within-chunk pick     : counter (c, pos, canvas, (5<<24)|step); word 0
+  within-chunk Gumbel   : counter (v>>2, pos, canvas, (5<<24)|step); entry v uses word v&3
 
-Posterior sample x_hat_0 ~ p_hat_0 (exact, two levels): the vocabulary is cut into aligned
-chunks of 32 entries; a chunk is chosen by Gumbel-max over the chunks' log-sum-exps (so chunk
-c is chosen with probability sum_{v in c} p_v), then an entry of that chunk by inverse CDF in
-vocabulary order (probability p_v / sum_{v' in c} p_v').  The product is p_v.
+Posterior sample x_hat_0 ~ p_hat_0 (exact, Gumbel-max at two levels): the vocabulary is cut
+into aligned chunks of 32 entries; a chunk is chosen by Gumbel-max over the chunks'
+log-sum-exps (so chunk c is chosen with probability sum_{v in c} p_v), then an entry of that
+chunk by Gumbel-max over its tempered logits with an independent family of Gumbels
+(probability p_v / sum_{v' in c} p_v').  The product is p_v.
 
 Entropy-bounded sampler [TR "DiffusionGemma 샘플러"], readings taken where the section is silent:
   * the entropy of a position is that of the tempered posterior used for sampling at the step,
@@ -330,18 +331,21 @@ def decoder_back(h, O, Wo):
 # ----------------------------------------------------------------------------------------
 
 def two_level_sample(z, pos, canvas, step: int, seed: int):
-    """One exact draw from Softmax(z) per row of tempered logits z [c, V] (float64):
+    """One exact draw from Softmax(z) per row of tempered logits z [c, V] (float64), by
+    Gumbel-max at two levels over the aligned 32-entry chunks c of the vocabulary:
 
-      lse_c  = log sum_{v in c} exp(z_v)          for the aligned 32-entry chunks c
-      c*     = argmax_c (lse_c + g_c)             (Gumbel-max over chunks, lowest c on ties)
-      x0hat  = the first v of c* with sum_{v' <= v, v' in c*} exp(z_v' - lse_c*) > U
+      lse_c  = log sum_{v in c} exp(z_v)
+      c*     = argmax_c (lse_c + g_c)             (chunk c is chosen with probability
+                                                   sum_{v in c} p_v; lowest c on ties)
+      x0hat  = argmax_{v in c*} (z_v + g'_v)      (entry v of c* with probability
+                                                   p_v / sum_{v' in c*} p_v'; lowest v on ties)
 
-    g_c comes from the chunk Gumbel stream (word c&3 of counter (c>>2, pos, canvas, 2<<24 |
-    step)), U from the pick stream (word 0 of (c*, pos, canvas, 5<<24 | step)).  Returns x0hat
-    and, for the parity bars, the decision's margin in logit units: the smaller of the gap
-    between the two largest chunk scores and, for the cumulative boundaries C next to U, the
-    logit change that would move C onto U, |U - C| / (2 C (1 - C)) (a shift of every logit by at
-    most delta moves a boundary by at most 2 delta C (1 - C))."""
+    The two Gumbel families are independent, so x0hat = v with probability p_v exactly.  g_c
+    comes from the chunk Gumbel stream (word c&3 of counter (c>>2, pos, canvas, 2<<24 | step)),
+    g'_v from the pick stream (word v&3 of counter (v>>2, pos, canvas, 5<<24 | step)); only the
+    winning chunk's g'_v are ever needed.  Returns x0hat and, for the parity bars, the
+    decision's margin: the smaller of the gaps between the two largest perturbed scores at
+    either level (chunk scores; perturbed logits inside c*)."""
     n, V = z.shape
     nc = (V + SAMPLE_CHUNK - 1) // SAMPLE_CHUNK
     pad = np.full((n, nc * SAMPLE_CHUNK), -np.inf)
@@ -350,36 +354,30 @@ def two_level_sample(z, pos, canvas, step: int, seed: int):
     mc = zc.max(axis=2, keepdims=True)
     lse_c = (mc + np.log(np.exp(zc - mc).sum(axis=2, keepdims=True)))[:, :, 0]
     k0, k1 = seed_key(seed)
-    c = np.arange(nc, dtype=np.uint64)
-    words = philox4x32_10(c[None, :] >> np.uint64(2), pos, canvas,
-                          (STREAM_GUMBEL << 24) | int(step), k0, k1)
-    sel = (c & np.uint64(3)).astype(np.int64)[None, :]
-    u = np.choose(np.broadcast_to(sel, (n, nc)), words)
-    score = lse_c + gumbel_from_u32(u)
-    cstar = np.argmax(score, axis=1)
-    if nc > 1:
-        two = -np.partition(-score, 1, axis=1)[:, :2]
-        gap = two[:, 0] - two[:, 1]
-    else:
-        gap = np.full(n, np.inf)
-    w = philox4x32_10(cstar.astype(np.uint64)[:, None], pos, canvas,
-                      (STREAM_PICK << 24) | int(step), k0, k1)[0][:, 0]
-    U = u32_to_open_unit(w)
-    idx = np.arange(n)
-    p = np.exp(zc[idx, cstar] - lse_c[idx, cstar][:, None])   # [n, 32], sums to 1
-    cum = np.cumsum(p, axis=1)
-    # (rounding can leave the last cumulative value a hair below U: the last real entry then)
-    j = np.minimum((cum <= U[:, None]).sum(axis=1),
-                   np.minimum(SAMPLE_CHUNK - 1, V - 1 - cstar * SAMPLE_CHUNK))
-    def logit_margin(C, present):
-        m = np.abs(U - C) / np.maximum(2.0 * C * (1.0 - C), 1e-300)
-        return np.where(present, m, np.inf)
 
-    lo = cum[idx, np.maximum(j - 1, 0)]
-    hi = cum[idx, j]
-    last = np.minimum(SAMPLE_CHUNK - 1, V - 1 - cstar * SAMPLE_CHUNK)
-    margin = np.minimum(logit_margin(lo, j > 0), logit_margin(hi, j < last))
-    return cstar * SAMPLE_CHUNK + j, np.minimum(gap, margin)
+    def word_of(counter0, sel, tag):
+        words = philox4x32_10(counter0, pos, canvas, (tag << 24) | int(step), k0, k1)
+        return np.choose(np.broadcast_to(sel, counter0.shape), words)
+
+    def top2_gap(score):
+        if score.shape[1] < 2:
+            return np.full(score.shape[0], np.inf)
+        two = -np.partition(-score, 1, axis=1)[:, :2]
+        return two[:, 0] - two[:, 1]
+
+    c = np.arange(nc, dtype=np.uint64)[None, :]
+    chunk_score = lse_c + gumbel_from_u32(
+        word_of(np.broadcast_to(c >> np.uint64(2), (n, nc)), (c & np.uint64(3)).astype(np.int64),
+                STREAM_GUMBEL))
+    cstar = np.argmax(chunk_score, axis=1)
+    v = cstar.astype(np.uint64)[:, None] * np.uint64(SAMPLE_CHUNK) + \
+        np.arange(SAMPLE_CHUNK, dtype=np.uint64)[None, :]            # [n, 32] entries of c*
+    g_pick = gumbel_from_u32(word_of(v >> np.uint64(2), (v & np.uint64(3)).astype(np.int64),
+                                     STREAM_PICK))
+    entry_score = zc[np.arange(n), cstar] + g_pick                    # -inf past the end
+    j = np.argmax(entry_score, axis=1)
+    margin = np.minimum(top2_gap(chunk_score), top2_gap(entry_score))
+    return cstar * SAMPLE_CHUNK + j, margin
 
 
 def posterior(y, E, inv_tau: float, seed: int, step: int, L: int, rows=None, chunk=None):

@@ -313,9 +313,9 @@ def test_posterior_normalisation_and_temperature():
 
 
 def test_posterior_sample_is_the_softmax():
-    """The posterior sample over 10^6 rows with distinct counters (one chunk: the inverse-CDF
-    pick alone) is a categorical draw from Softmax(z / tau): chi-square against the exact
-    probabilities."""
+    """The posterior sample over 10^6 rows with distinct counters (one chunk: the within-chunk
+    Gumbel-max alone) is a categorical draw from Softmax(z / tau): chi-square against the
+    exact probabilities."""
     V, d = 16, 16
     z_target = np.linspace(-1.5, 1.0, V)
     E = np.eye(V, d)
@@ -351,7 +351,11 @@ def test_two_level_sample_over_many_chunks_is_the_softmax():
 def test_two_level_sample_hand_cases():
     """(a) All mass on one entry: always that entry.
     (b) Two equal entries in different chunks: the chunk whose Gumbel is larger wins (the
-    lower chunk on an exact tie); the pick inside a one-entry chunk is that entry."""
+    lower chunk on an exact tie); inside a chunk with one live entry that entry is taken.
+    (c) Two equal entries in one chunk: the entry whose own Gumbel (word v&3 of the pick
+    stream's counter v>>2) is larger wins.
+    (d) The reported margin is the smaller of the two levels' top-2 gaps, counted by brute
+    force over the perturbed scores."""
     V, L = 64, 16
     z = np.full((6, V), -1e4)
     z[:, 21] = 3.0
@@ -369,6 +373,35 @@ def test_two_level_sample_hand_cases():
     g0, g1 = O.gumbel_from_u32(w[0]), O.gumbel_from_u32(w[1])   # chunks 0 and 1: words 0, 1
     assert np.array_equal(x, np.where(g0 >= g1, 5, 40))
     assert 5 < (x == 5).sum() < 35
+    # (c) entries 5 and 10 of chunk 0: counters 1 and 2, words 1 and 2 of the pick stream
+    z = np.full((40, V), -1e4)
+    z[:, 5] = 0.0
+    z[:, 10] = 0.0
+    x, _ = O.two_level_sample(z, pos, can, 6, 17)
+    k0, k1 = O.seed_key(17)
+    tag = (O.STREAM_PICK << 24) | 6
+    g5 = O.gumbel_from_u32(O.philox4x32_10(1, pos[:, 0], can[:, 0], tag, k0, k1)[1])
+    g10 = O.gumbel_from_u32(O.philox4x32_10(2, pos[:, 0], can[:, 0], tag, k0, k1)[2])
+    assert np.array_equal(x, np.where(g5 >= g10, 5, 10))
+    assert 5 < (x == 5).sum() < 35
+    # (d) margins by brute force over every chunk score and the winning chunk's entries
+    rng = np.random.default_rng(5)
+    z = rng.standard_normal((40, V)) * 0.3
+    x, margin = O.two_level_sample(z, pos, can, 3, 11)
+    k0, k1 = O.seed_key(11)
+    for r in range(40):
+        cs = []
+        for c in range(V // 32):
+            u = O.philox4x32_10(c // 4, pos[r, 0], can[r, 0], (O.STREAM_GUMBEL << 24) | 3, k0, k1)
+            cs.append(logsumexp(z[r, 32 * c:32 * c + 32]) + O.gumbel_from_u32(u[c % 4]))
+        cstar = int(np.argmax(cs))
+        es = []
+        for v in range(32 * cstar, 32 * cstar + 32):
+            u = O.philox4x32_10(v // 4, pos[r, 0], can[r, 0], (O.STREAM_PICK << 24) | 3, k0, k1)
+            es.append(z[r, v] + O.gumbel_from_u32(u[v % 4]))
+        assert x[r] == 32 * cstar + int(np.argmax(es))
+        gaps = [np.diff(np.sort(a)[-2:])[0] for a in (np.array(cs), np.array(es))]
+        assert math.isclose(margin[r], min(gaps), rel_tol=1e-12)
 
 
 def test_posterior_rows_subset_equals_full():
