@@ -771,8 +771,12 @@ dg_status run_denoise(const RunArgs& a, const dg_sampler_cfg* cfg,
   const VocabPlan vp = plan_vocab(BL, m->V);
   dg_status s;
 
+  // the vocabulary pass's sampling bars are cleared once here; each step's finalisation clears
+  // them again for the next step
+  uint32_t* bars = vocab_bars(w.parts, BL, m->V);
   cudaError_t e = cudaMemsetAsync(w.n_active, 0, sizeof(int), st);
   if (e == cudaSuccess) e = cudaMemsetAsync(w.counters, 0, 2 * sizeof(int) * B, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(bars, 0, static_cast<size_t>(BL) * 4, st);
   if (e != cudaSuccess) return cuda_fail(e, "loop: memset");
   launch_loop_init_masked(a.lock, a.gen_active, w.active, w.n_active, a.steps_taken, B, L,
                           eb ? 0 : cfg->stop_when_all_locked, st);
@@ -824,10 +828,11 @@ dg_status run_denoise(const RunArgs& a, const dg_sampler_cfg* cfg,
     const float inv_tau = eb ? eb_inv_tau[n] : cfg->inv_tau;
     e = launch_vocab_pass(w.y, m->E, BL, L, m->d, m->V, inv_tau, a.seed, n, w.parts, w.status,
                           w.n_active, st, nullptr, eb, sc_next ? w.sc_p : nullptr,
-                          sc_next ? w.sc_m : nullptr);
+                          sc_next ? w.sc_m : nullptr, false, /*bars_clear=*/true);
     if (e != cudaSuccess) return cuda_fail(e, "loop: vocab pass launch");
     FinalizeParams fp{};
     fp.parts = w.parts;
+    fp.bar = bars;
     fp.num_mt = vp.num_mt;
     fp.S = vp.S;
     fp.L = L;

@@ -153,6 +153,7 @@ __device__ __forceinline__ RowFinal finalize_row(const FinalizeParams& p, int ro
 
   RowFinal r{false, 0};
   if (lane == 0) {
+    if (p.bar) p.bar[row] = 0u;  // the row's tuples are merged: clear its bar for the next pass
     const float lse = acc.m + logf(acc.s);
     const float lp_top1 = acc.top_z - lse;
     if (p.out_x0hat) p.out_x0hat[row] = acc.best_idx;

@@ -31,6 +31,7 @@ struct FinalizeParams {
   int stop_when_all_locked;
   int* unlocked;  // [B] per-canvas counters, zero before the first call; reset by the kernel
   int* cta_done;  // [B]
+  uint32_t* bar;  // the vocabulary pass's sampling bars: zeroed per row once merged (or NULL)
 };
 
 // One step of the entropy-bounded sampler for every canvas (one CTA per canvas).
@@ -163,19 +164,24 @@ cudaError_t launch_attention(const uint16_t* q, const uint16_t* k_pre, const uin
 // -------------------------------------------------------------- vocabulary pass -----
 struct VocabPlan {
   int num_mt, nvt, per, S, units, grid;
-  size_t part_bytes;
+  size_t part_bytes;  // the partial tuples, then one 32-bit sampling bar per row
 };
 VocabPlan plan_vocab(int R, int V);
+// The per-row sampling bars inside a partials area of plan_vocab(R, V).part_bytes bytes: the
+// best chunk score published so far in a sampling launch; zero before each sampling launch.
+uint32_t* vocab_bars(VocabPart* parts, int R, int V);
 // targets != NULL: cross-entropy mode (no Gumbel draws; the tuples carry the target's logit).
 // entropy: the tuples also carry the entropy accumulator (otherwise it stays 0).
 // sc_p, sc_m != NULL: also store bf16 exp(z~ - m_ref) [R, V] and m_ref [R, V / 32] for the
 // self-conditioning contraction.  ce_only: no sampling even without targets (lse only).
+// bars_clear: the caller guarantees the sampling bars are zero (a finalisation since the last
+// sampling launch reset them, or the caller cleared them); otherwise the launch clears them.
 cudaError_t launch_vocab_pass(const uint16_t* y, const uint16_t* W, int R, int L, int d, int V,
                               float inv_tau, uint64_t seed, int step, VocabPart* parts,
                               uint32_t* status, const int* n_active, cudaStream_t st,
                               const int32_t* targets = nullptr, bool entropy = false,
                               uint16_t* sc_p = nullptr, float* sc_m = nullptr,
-                              bool ce_only = false);
+                              bool ce_only = false, bool bars_clear = false);
 
 // Optional CUDA-event timing around kernels (kind 0: vocabulary pass, 1: attention with its
 // merge, 2: self-conditioning contraction, 3: projection GEMM, 4: finalisation).

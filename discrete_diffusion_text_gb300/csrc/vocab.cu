@@ -10,7 +10,7 @@
 //                tile, one thread per row: tempered logits z~ = z / tau, online (max, sum exp)
 //                for the log-sum-exp, the top-1 (lowest index on ties), and the exact
 //                two-level posterior sample: Gumbel-max over aligned 32-entry chunks scored
-//                by their log-sum-exps, then an inverse-CDF pick inside the winning chunk.
+//                by their log-sum-exps, then Gumbel-max over the winning chunk's entries.
 // Only rows' partial tuples are written; a finalisation kernel merges them in a fixed order and
 // applies the Euler step (the chunk scores merge like any Gumbel-max scores).
 #include <type_traits>
@@ -41,6 +41,8 @@ struct VocabParams {
   uint16_t* sc_p;          // self-conditioning: bf16 exp(z~ - m_ref) [R, V]
   float* sc_m;             // and m_ref per row and 32-column chunk [R, V / 32]
   VocabPart* parts;
+  uint32_t* bar;           // sampling: per row, the best chunk score published so far in this
+                           // launch (order-preserving key; 0 = none), zeroed before the launch
   uint32_t* status;
   const int* n_active;
 };
@@ -87,6 +89,22 @@ __device__ __forceinline__ float open_unit(uint32_t u) {
   return fmaf(__uint2float_rn(u), 2.3283064365386963e-10f, 1.1641532182693481e-10f);
 }
 
+// Order-preserving 32-bit key of a float (a < b iff key(a) < key(b)); key 0 is below every
+// float, so a zeroed word means "no score published".
+__device__ __forceinline__ uint32_t score_key(float x) {
+  const uint32_t b = __float_as_uint(x);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float score_from_key(uint32_t k) {
+  if (k == 0u) return -INFINITY;
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // One 32-column chunk of raw logits z (tempered here: z~ = z * inv_tau, inv_tau > 0); the
 // chunk is one of the aligned 32-entry chunks of the two-level posterior sample.
 //  - The chunk max is taken on raw z: rounding is monotone, so max(fl(z * c)) = fl(max(z) * c).
@@ -94,10 +112,9 @@ __device__ __forceinline__ float open_unit(uint32_t u) {
 //    values, sc, is also the chunk's mass relative to the running max.
 //  - Sampling (not kCE): the chunk's score is lse_c + g_c = m + log(sc) + g_c with g_c the chunk
 //    Gumbel (word c&3 of counter (c>>2, pos, canvas, c3)); a chunk that beats the row's best so
-//    far (strictly: an earlier chunk keeps ties) picks its entry at once by inverse CDF in
-//    vocabulary order with one uniform U from the pick stream: the first j whose running sum
-//    of exp(z~ - m) exceeds U sc (the last entry if rounding leaves the sum short).  The draws
-//    cost one Philox call and three logarithms per 32 logits, plus a rare pick.
+//    far (strictly: an earlier chunk keeps ties) picks its entry at once by Gumbel-max over its
+//    32 tempered logits with Gumbels from the pick stream.  The draws cost one Philox call
+//    and three logarithms per 32 logits, plus the pick of each chunk that takes the lead.
 // kCE (cross-entropy mode): no draws; instead the tempered logit of the row's target token is
 // captured (in the best-sample fields, which that mode does not otherwise use).
 // kEnt: also accumulate t = sum exp(z~ - m)(z~ - m) for the entropy (one FMA per logit).
@@ -107,12 +124,19 @@ __device__ __forceinline__ float open_unit(uint32_t u) {
 // exp(m - lse), applied once lse is known.
 // u_gumbel: the chunk's Gumbel draw, word c & 3 of Philox(c >> 2, pos, canvas, c3) for chunk
 // c = vbase / 32 (computed by the caller, once for the chunks that share a counter).
+// bar / bar_ptr: the row's best chunk score published by any thread of the launch so far (as
+// read at the start of this tile) and the row's word to publish to.  A chunk that leads this
+// thread's sequence but scores below the bar cannot be the row's sample (some chunk of the row
+// scores strictly higher), so its entry is not picked; the leading state records the score
+// with no entry, which loses every merge against the published chunk.  Only chunks at or above
+// the bar pick (and publish), which keeps the costly pick to about one per warp and unit
+// instead of one per lane that leads (the 32 lanes of a warp hold 32 different rows).
 template <bool kCE, bool kEnt, bool kSC>
 __device__ __forceinline__ void process_chunk(RowState& st, const float (&z)[32], int vbase,
                                               float inv_tau, uint32_t pos, uint32_t canvas,
                                               const PhiloxKeys& keys, uint32_t u_gumbel,
                                               uint32_t c3_pick, int target, uint16_t* sc_dst,
-                                              float* sc_mdst) {
+                                              float* sc_mdst, float bar, uint32_t* bar_ptr) {
   float mx[4] = {z[0], z[1], z[2], z[3]};  // four partial maxima: short dependency chains
 #pragma unroll
   for (int e = 4; e < 32; ++e) mx[e & 3] = fmaxf(mx[e & 3], z[e]);
@@ -171,20 +195,37 @@ __device__ __forceinline__ void process_chunk(RowState& st, const float (&z)[32]
   const uint32_t c = static_cast<uint32_t>(vbase) >> 5;
   const float score = st.m + logf(sc) - logf(-log1pf(-open_unit(u_gumbel)));
   if (score > st.best) {
-    const float target_mass = open_unit(philox4x32_10(c, pos, canvas, c3_pick, keys).x) * sc;
-    float cum = 0.f;
-    int j = 31;
-#pragma unroll
-    for (int e = 0; e < 31; ++e) {
-      cum += ex2_approx(fmaf(z[e], scale, -mlog2));
-      if (j == 31 && cum > target_mass) j = e;
-    }
-    float zj = z[0];
-#pragma unroll
-    for (int k = 1; k < 32; ++k) zj = j == k ? z[k] : zj;  // static indices only
     st.best = score;
+    if (score < bar) {  // another chunk of the row scores higher: no entry needed
+      st.best_idx = 0x7FFFFFFF;
+      st.best_z = -INFINITY;
+      return;
+    }
+    // The chunk leads the row so far: pick its entry by Gumbel-max over z~_v + g'_v with the
+    // pick stream's Gumbels (entry v: word v & 3 of Philox(v >> 2, pos, canvas, c3_pick)),
+    // lowest entry on ties.  The draws depend only on v, so the entry is the same whichever
+    // thread, and whenever, the chunk is picked.
+    float bs = -INFINITY, zj = 0.f;
+    int j = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const Words4 w = philox4x32_10((static_cast<uint32_t>(vbase) >> 2) + q, pos, canvas,
+                                     c3_pick, keys);
+      const uint32_t wq[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float zt = z[4 * q + r] * inv_tau;
+        const float se = zt - logf(-log1pf(-open_unit(wq[r])));
+        if (se > bs) {
+          bs = se;
+          j = 4 * q + r;
+          zj = zt;
+        }
+      }
+    }
     st.best_idx = vbase + j;
-    st.best_z = zj * inv_tau;
+    st.best_z = zj;
+    if (bar_ptr) atomicMax(bar_ptr, score_key(score));
   }
 }
 
@@ -371,6 +412,7 @@ __global__ void __launch_bounds__(VocabLayout<kSplit>::kThreadsT, 1)
       uint16_t* sc_row = kSC && row < p.R ? p.sc_p + static_cast<int64_t>(row) * p.V : nullptr;
       float* scm_row = kSC && row < p.R ? p.sc_m + static_cast<int64_t>(row) * (p.V / 32)
                                         : nullptr;
+      uint32_t* bar_row = !kCE && p.bar && row < p.R ? p.bar + row : nullptr;
       RowState st;
       st.m = -INFINITY;
       st.s = 0.f;
@@ -382,6 +424,8 @@ __global__ void __launch_bounds__(VocabLayout<kSplit>::kThreadsT, 1)
       st.best_z = -INFINITY;
       for (int vt = vt0; vt < vt1; ++vt, ++j) {
         const int buf = j & 1;
+        // the row's published best, read before the wait so the load's latency is hidden
+        const float bar = bar_row ? score_from_key(ld_relaxed(bar_row)) : -INFINITY;
         if (ok) ok = warp_wait(&tfull[buf], (j >> 1) & 1, abort_flag);
         if (!ok) continue;
         tc_fence_after();
@@ -411,7 +455,7 @@ __global__ void __launch_bounds__(VocabLayout<kSplit>::kThreadsT, 1)
           process_chunk<kCE, kEnt, kSC>(st, z, vb, p.inv_tau, pos, canvas, keys,
                                         c == 0 ? ug[0] : ug[1], p.c3_pick, target,
                                         sc_row ? sc_row + vb : nullptr,
-                                        scm_row ? scm_row + (vb >> 5) : nullptr);
+                                        scm_row ? scm_row + (vb >> 5) : nullptr, bar, bar_row);
         }
       }
       // Merge the column groups of each row through shared memory, in group order.
@@ -478,15 +522,21 @@ VocabPlan plan_vocab(int R, int V) {
   pl.per = best_per;
   pl.units = pl.num_mt * pl.S;
   pl.grid = pl.units < sms ? pl.units : sms;
-  pl.part_bytes = static_cast<size_t>(pl.units) * kBM * sizeof(VocabPart);
+  // the partial tuples, then one 32-bit bar word per row (16-byte aligned)
+  pl.part_bytes = static_cast<size_t>(pl.units) * kBM * sizeof(VocabPart) +
+                  ((static_cast<size_t>(R) * 4 + 15) & ~static_cast<size_t>(15));
   return pl;
+}
+
+uint32_t* vocab_bars(VocabPart* parts, int R, int V) {
+  return reinterpret_cast<uint32_t*>(parts + static_cast<size_t>(plan_vocab(R, V).units) * kBM);
 }
 
 cudaError_t launch_vocab_pass(const uint16_t* y, const uint16_t* W, int R, int L, int d, int V,
                               float inv_tau, uint64_t seed, int step, VocabPart* parts,
                               uint32_t* status, const int* n_active, cudaStream_t st,
                               const int32_t* targets, bool entropy, uint16_t* sc_p,
-                              float* sc_m, bool ce_only) {
+                              float* sc_m, bool ce_only, bool bars_clear) {
   const VocabPlan pl = plan_vocab(R, V);
   CUtensorMap ta, tb;
   const uint64_t dA[2] = {static_cast<uint64_t>(d), static_cast<uint64_t>(R)};
@@ -516,6 +566,7 @@ cudaError_t launch_vocab_pass(const uint16_t* y, const uint16_t* W, int R, int L
   p.sc_p = sc_p;
   p.sc_m = sc_m;
   p.parts = parts;
+  p.bar = nullptr;
   p.status = status;
   p.n_active = n_active;
 
@@ -544,7 +595,6 @@ cudaError_t launch_vocab_pass(const uint16_t* y, const uint16_t* W, int R, int L
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  timer_begin(0, st);
   // cross-entropy mode (targets, or the self-conditioning pass alone: no sampling), or
   // sampling with or without the entropy accumulator; each with or without the
   // self-conditioning store.  Split rings when the pass is a single wave (one unit per CTA:
@@ -554,6 +604,14 @@ cudaError_t launch_vocab_pass(const uint16_t* y, const uint16_t* W, int R, int L
   // epilogues); with several waves the unified ring is faster (-7 % at 16 canvases).
   const bool sc = sc_p != nullptr;
   const bool ce = targets != nullptr || ce_only;
+  if (!ce) {  // every sampling launch starts with no bar published
+    p.bar = vocab_bars(parts, R, V);
+    if (!bars_clear) {
+      const cudaError_t em = cudaMemsetAsync(p.bar, 0, static_cast<size_t>(R) * 4, st);
+      if (em != cudaSuccess) return em;
+    }
+  }
+  timer_begin(0, st);
   cudaError_t e;
   auto launch = [&](auto split_tag) {
     constexpr bool kS = decltype(split_tag)::value;

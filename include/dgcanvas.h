@@ -24,8 +24,11 @@
  *   - Random draws are Philox4x32-10 [P11] keyed by the 64-bit seed (low word = key 0) with
  *     counters that depend only on (stream, step, canvas, position, vocab index):
  *       noising / canvas init: (position, canvas, 0, 1<<24); word 0 = keep draw, word 1 = token
- *       Gumbel noise:          (v >> 2, position, canvas, (2<<24) | step); vocab v uses word v & 3
+ *       chunk Gumbel:          (c >> 2, position, canvas, (2<<24) | step); the 32-entry
+ *                              vocabulary chunk c = v / 32 uses word c & 3
  *       Euler jump:            (0, position, canvas, (3<<24) | step); word 0
+ *       re-noising:            (position, canvas, 0, (4<<24) | step); word 0
+ *       within-chunk Gumbel:   (v >> 2, position, canvas, (5<<24) | step); vocab v uses word v & 3
  *     so results do not depend on launch shape, and a run can be resumed at any step.
  *   - A probability p is passed as the integer threshold floor(p * 2^32) (p = 1 -> 2^32); a
  *     32-bit draw u "passes" iff u < threshold.  Decisions are therefore exact integer tests.
@@ -147,8 +150,12 @@ dg_status dg_out_proj(const uint16_t* h, const uint16_t* O, const uint16_t* Wo, 
  * position r % L), with z~ = z * inv_tau:
  *     lse        = log sum_v exp(z~_v)
  *     top1       = argmax_v z~_v (lowest index on ties);   logp_top1 = z~_top1 - lse
- *     x0hat      = argmax_v (z~_v + g_v)  (Gumbel-max sample; g from the Gumbel stream at `step`;
- *                  lowest index on ties);                  logp_x0hat = z~_x0hat - lse
+ *     x0hat      = an exact sample of Softmax(z~), by Gumbel-max at two levels over the aligned
+ *                  32-entry chunks c of the vocabulary: c* = argmax_c (lse_c + g_c) with
+ *                  lse_c = log sum_{v in c} exp(z~_v) and g_c from the chunk Gumbel stream,
+ *                  then x0hat = argmax_{v in c*} (z~_v + g'_v) with g'_v from the within-chunk
+ *                  Gumbel stream (lowest index on ties at both levels); P(x0hat = v) = p_v.
+ *                                                          logp_x0hat = z~_x0hat - lse
  *     entropy    = -sum_v p_v log p_v of p = Softmax(z~) [TR "DiffusionGemma 샘플러"], accumulated
  *                  online in the same pass (log s - t / s with s = sum exp(z~ - m),
  *                  t = sum exp(z~ - m) (z~ - m)), clamped at 0
