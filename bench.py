@@ -33,6 +33,7 @@ sys.path.insert(0, ROOT)
 METRIC = "canvas tokens/sec·step (256×batch×steps/s) at 1 GB300; % of tensor/HBM roofline"
 UNIT = "canvas_token_steps/s"
 PROFILE_DIR = os.path.join(ROOT, "profiles")
+DEFAULT_WORKLOAD = "sweep4k"
 
 
 def parse():
@@ -40,8 +41,13 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default="window1k")
-    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch (default: 64 for sweep4k, the largest "
+                         "batch of its sweep; the workload's own otherwise)")
+    ap.add_argument("--no-sub", action="store_true",
+                    help="skip the other configurations (window1k, batch16, long128k) that the "
+                         "default run times under 'workloads'")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--mode", default="denoise", choices=["denoise", "sft", "blockar"],
@@ -118,16 +124,17 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def traffic_from_profile(kernel_file: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current
-    source of the kernel (the summary records the kernel source's sha256); else None."""
+def traffic_from_profile(kernel_file: str, workload: str):
+    """DRAM bytes per launch of the kernel at the workload, from the committed ncu summary,
+    if it was taken on the current source of the kernel (the summary records the kernel
+    source's sha256); else None."""
     p = os.path.join(PROFILE_DIR, "traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
     src = os.path.join(ROOT, "discrete_diffusion_text_gb300", "csrc", kernel_file)
     h = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    e = d.get(kernel_file)
+    e = d.get(kernel_file, {}).get(workload)
     if not e or e.get("source_sha256") != h:
         return None
     return e.get("dram_bytes_per_launch")
@@ -136,20 +143,23 @@ def traffic_from_profile(kernel_file: str):
 # ------------------------------------------------------------------------ oracle arm -----
 
 class OracleSample:
-    """One denoising step of the workload by the CPU oracle: the decoder over the whole canvas
-    of one batch element, then the posterior and Euler step for `rows` positions.  The seeded
-    inputs are made once; each call returns the seconds of one step."""
+    """One denoising step of one canvas of the workload by the CPU oracle: the decoder over
+    the whole 256-token canvas, then the posterior over the whole vocabulary and the Euler
+    step for every position.  The seeded inputs (one canvas: model and prefix drawn on the
+    host) are made once; each call returns the seconds of one canvas-step, the posterior and
+    the canvas it started from."""
 
     def __init__(self, w):
         from discrete_diffusion_text_gb300 import synth
 
         self.w = w
-        m = synth.make_model(w)
-        kp, vp = synth.make_prefix_kv(w, B=1)
-        self.om = {k: (v.double().numpy() if hasattr(v, "double") else v) for k, v in m.items()}
-        self.kp, self.vp = kp.double().numpy(), vp.double().numpy()
+        self.m = synth.make_model(w)
+        self.kp, self.vp = synth.make_prefix_kv(w, B=1)
+        self.om = {k: (v.double().numpy() if hasattr(v, "double") else v)
+                   for k, v in self.m.items()}
+        self.okp, self.ovp = self.kp.double().numpy(), self.vp.double().numpy()
 
-    def __call__(self, rows: int, seed_shift: int = 0) -> float:
+    def __call__(self, seed_shift: int = 0):
         import numpy as np
 
         from oracle import dgoracle as O
@@ -160,13 +170,13 @@ class OracleSample:
         n = w.T - 1
         t0 = time.perf_counter()
         h, q, k, v = O.decoder_front(x, om["E"], om["Wqkv"], w.H, w.Hkv, w.hd)
-        Oa, _ = O.canvas_attention(q, self.kp, self.vp, k, v, w.window, w.hd ** -0.5)
+        Oa, _ = O.canvas_attention(q, self.okp, self.ovp, k, v, w.window, w.hd ** -0.5)
         y = O.decoder_back(h, Oa, om["Wo"]).reshape(w.L, w.d)
-        post = O.posterior(y, om["E"], w.inv_tau, w.seed, n, w.L, rows=np.arange(rows))
-        O.euler_update(x[:, :rows], post["x0hat"][None], post["top1"][None],
-                       post["logp_top1"][None].astype(np.float32), np.zeros((1, rows), np.uint8),
-                       w.seed, n, int(jump[n]), math.inf)
-        return time.perf_counter() - t0
+        post = O.posterior(y, om["E"], w.inv_tau, w.seed + seed_shift, n, w.L)
+        O.euler_update(x, post["x0hat"][None], post["top1"][None],
+                       post["logp_top1"][None].astype(np.float32), np.zeros((1, w.L), np.uint8),
+                       w.seed + seed_shift, n, int(jump[n]), math.inf)
+        return time.perf_counter() - t0, post, x
 
 
 def cpu_cores() -> int:
@@ -176,20 +186,23 @@ def cpu_cores() -> int:
         return os.cpu_count() or 1
 
 
+def oracle_sample_text(w) -> str:
+    return (f"one canvas-step of the {w.name} workload per benchmark step (decoder over the "
+            f"{w.L}-token canvas, posterior over all {w.V:,} tokens and Euler step for all "
+            f"{w.L} positions), numpy float64 with threaded BLAS; the metric is per canvas-step "
+            f"and extrapolates linearly to the workload's {w.B} canvases x {w.T} steps")
+
+
 def run_reference(args, w):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    rows = 32
     sample_step = OracleSample(w)
     for i in range(args.warmup):
-        sample_step(rows, i)
-    ts = [sample_step(rows, 100 + i) for i in range(args.steps)]
+        sample_step(i)
+    ts = [sample_step(100 + i)[0] for i in range(args.steps)]
     sec = sum(ts) / len(ts)
-    value = rows / sec
-    sample = (f"one denoising step of the {w.name} workload per benchmark step: decoder over the "
-              f"256-token canvas, posterior + Euler step for {rows} of the 256 positions "
-              f"(numpy float64; BLAS threaded, elementwise work on one thread)")
+    value = w.L / sec
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": sec * 1000, "higher_is_better": True, "scaling": "weak",
@@ -197,7 +210,7 @@ def run_reference(args, w):
             "config": {"workload": w.describe(), "global_batch": w.B, "seq_len": w.L,
                        "prefix": w.P, "parallelism": "cpu"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-                             "sample": sample},
+                             "sample": oracle_sample_text(w)},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -205,30 +218,34 @@ def run_reference(args, w):
 
 # -------------------------------------------------------------------------- GPU arm -----
 
-def run_ours(args, w):
+def attention_work(w):
+    """Algorithmic FLOPs and prefix K/V bytes of one canvas attention launch: every canvas
+    query of every head against its visible prefix keys and the whole canvas."""
+    if w.window:
+        vis = sum(min(w.P, max(0, w.window - 1 - i)) for i in range(w.L))  # keys k > P + i - W
+        rows = min(w.P, w.window - 1)
+    else:
+        vis = w.P * w.L
+        rows = w.P
+    flops = 4.0 * w.B * w.H * w.hd * (vis + w.L * w.L)
+    kv_bytes = 4.0 * w.B * rows * w.Hkv * w.hd
+    return flops, kv_bytes
+
+
+def measure_denoise(w, dev, steps, warmup, *, rank=0, world=1, dist=None, sc=0, eb=False,
+                    e2e=True, timer_steps=None, noising=0):
+    """Times `steps` benchmark steps of workload w.  One step: (with `noising` = n canvases)
+    forward noising of n Zipf(1.1) clean canvases at t ~ U(0, 1), then the uniform-prior
+    canvases and dg_denoise_loop over all of the sampler's steps.  Returns a dict of results."""
     import numpy as np
     import torch
 
     from discrete_diffusion_text_gb300 import dgcanvas as dgc
     from discrete_diffusion_text_gb300 import replicas, synth
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    dgc.load()
-
     B = w.B
     m = synth.make_model(w, dev)
     kp, vp = synth.make_prefix_kv(w, dev)
-    sc = args.selfcond
     if sc:
         m["Wsc1"] = synth.normal_bf16((sc, w.d), 0.02, 1000 * w.seed + 6, dev)
         m["Wsc2"] = synth.normal_bf16((w.d, sc), 0.02, 1000 * w.seed + 7, dev)
@@ -242,7 +259,12 @@ def run_ours(args, w):
     steps_taken = torch.zeros(B, dtype=torch.int32, device=dev)
     keep0 = torch.zeros(B, dtype=torch.int64, device=dev)
     stream = torch.cuda.current_stream(dev)
-    eb = args.sampler == "eb"
+    if noising:  # training-style noising of clean canvases (the workload's Zipf(1.1) tokens)
+        x0_h = torch.tensor(synth.zipf_tokens(noising, w.L, w.V, 1.1, w.seed), dtype=torch.int32)
+        t = synth.uniform_times(noising, w.seed)
+        keep_h = torch.tensor(dgc.dg_keep_thresholds(synth.SCHED_LINEAR, t).astype(np.int64))
+        x0_d, keep_d = x0_h.to(dev), keep_h.to(dev)
+        xt_d = torch.empty_like(x0_d)
 
     def make_cfg(seed):
         if eb:
@@ -251,42 +273,48 @@ def run_ours(args, w):
         return dgc.make_cfg(w.T, w.schedule, w.inv_tau, lock_thr, seed,
                             stop_when_all_locked=w.stop_when_all_locked)
 
-    def step(i):
+    def step(i, kpd=kp, vpd=vp, x0=None, keep=None):
         seed = replicas.replica_seed(w.seed, rank, i)
+        if noising:
+            dgc.dg_forward_noise(x0_d if x0 is None else x0, xt_d,
+                                 keep_d if keep is None else keep, w.V, seed)
         dgc.dg_forward_noise(canvas, canvas, keep0, w.V, seed)        # x_1: uniform prior
         lock.zero_()
-        dgc.dg_denoise_loop(model, kp, vp, w.window, canvas, lock, steps_taken, make_cfg(seed), ws)
+        dgc.dg_denoise_loop(model, kpd, vpd, w.window, canvas, lock, steps_taken, make_cfg(seed),
+                            ws)
 
-    for i in range(args.warmup):
+    for i in range(warmup):
         step(i)
     dgc.dg_workspace_status(ws)
     torch.cuda.synchronize()
 
     # ---- device-timed region (the library's kernel timer off: its events between kernels
     # would stop each kernel from being scheduled while its predecessor finishes)
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(int(str(dev).split(":")[-1]) if ":" in str(dev) else 0)
     clocks.start()
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
-    steps_done = 0
-    for i in range(args.steps):
-        step(args.warmup + i)
+    for i in range(steps):
+        step(warmup + i)
     ev1.record(stream)
     torch.cuda.synchronize()
-    steps_done = int(steps_taken.sum().item())  # last step's canvases (all run T steps here)
     if dist:
         dist.barrier()
     clk = clocks.stop()
     ms = ev0.elapsed_time(ev1)
     dgc.dg_workspace_status(ws)
-    # ---- the same K steps again with the kernel timer on: per-launch durations of the LM-head,
+    # state of the last benchmark step's canvases
+    st_last = steps_taken.cpu().numpy().astype(np.float64)
+    lock_frac = float(lock.float().mean().item())
+    # ---- the same steps again with the kernel timer on: per-launch durations of the LM-head,
     # attention and self-conditioning kernels (CUDA events on the launching stream)
+    tsteps = steps if timer_steps is None else timer_steps
     dgc.dg_kernel_timer_enable(True)
-    for i in range(args.steps):
-        step(args.warmup + args.steps + i)
+    for i in range(tsteps):
+        step(warmup + steps + i)
     torch.cuda.synchronize()
     vocab_ms, vocab_n = dgc.dg_kernel_timer_read(0)
     attn_ms, attn_n = dgc.dg_kernel_timer_read(1)
@@ -294,62 +322,88 @@ def run_ours(args, w):
     dgc.dg_kernel_timer_enable(False)
     dgc.dg_workspace_status(ws)
     ms = replicas.max_over_ranks(ms)
-    ms_per_step = ms / args.steps
-    # denoising steps per canvas in the last benchmark step (all steps alike unless the
-    # workload stops canvases early)
-    denoise_steps = steps_done / B if steps_done else w.T
+    ms_per_step = ms / steps
+    denoise_steps = float(st_last.mean()) if st_last.sum() else float(w.T)
     value = replicas.job_throughput(world, w.L, B, denoise_steps, ms_per_step / 1000.0)
 
+    res = {"value": value, "ms_per_step": ms_per_step, "clocks": clk,
+           "steps_per_canvas": denoise_steps,
+           "steps_per_canvas_max": float(st_last.max()) if B else 0.0,
+           # tokens per forward of one canvas (no canvas is appended to a cache here, so the
+           # pages' K - 1 encode term is 0) and effective denoising steps
+           "tpf": w.L / denoise_steps, "eds": denoise_steps, "lock_fraction": lock_frac}
+
     # ---- end to end through the public API with host buffers: the prefix KV of the step's
-    # requests goes host -> device, the final canvas and step counts come back.
-    kp_h = kp.cpu().pin_memory()
-    vp_h = vp.cpu().pin_memory()
-    out_h = torch.empty((B, w.L), dtype=torch.int32).pin_memory()
-    st_h = torch.empty(B, dtype=torch.int32).pin_memory()
-    kp_d, vp_d = torch.empty_like(kp), torch.empty_like(vp)
+    # requests (and the clean canvases and keep thresholds of the noising leg) go host ->
+    # device; the final canvases, their step counts (and the noised canvases) come back.
+    if e2e:
+        kp_h = kp.cpu().pin_memory()
+        vp_h = vp.cpu().pin_memory()
+        out_h = torch.empty((B, w.L), dtype=torch.int32).pin_memory()
+        st_h = torch.empty(B, dtype=torch.int32).pin_memory()
+        kp_d, vp_d = torch.empty_like(kp), torch.empty_like(vp)
+        if noising:
+            x0_hp, keep_hp = x0_h.pin_memory(), keep_h.pin_memory()
+            x0_dd, keep_dd = torch.empty_like(x0_d), torch.empty_like(keep_d)
+            xt_h = torch.empty_like(x0_h).pin_memory()
 
-    def e2e_step(i):
-        kp_d.copy_(kp_h, non_blocking=True)
-        vp_d.copy_(vp_h, non_blocking=True)
-        seed = replicas.replica_seed(w.seed, rank, 7777 + i)
-        dgc.dg_forward_noise(canvas, canvas, keep0, w.V, seed)
-        lock.zero_()
-        dgc.dg_denoise_loop(model, kp_d, vp_d, w.window, canvas, lock, steps_taken, make_cfg(seed),
-                            ws)
-        out_h.copy_(canvas, non_blocking=True)
-        st_h.copy_(steps_taken, non_blocking=True)
+        def e2e_step(i):
+            kp_d.copy_(kp_h, non_blocking=True)
+            vp_d.copy_(vp_h, non_blocking=True)
+            if noising:
+                x0_dd.copy_(x0_hp, non_blocking=True)
+                keep_dd.copy_(keep_hp, non_blocking=True)
+            step(7777 + i, kp_d, vp_d, x0_dd if noising else None, keep_dd if noising else None)
+            out_h.copy_(canvas, non_blocking=True)
+            st_h.copy_(steps_taken, non_blocking=True)
+            if noising:
+                xt_h.copy_(xt_d, non_blocking=True)
 
-    for i in range(args.warmup):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(args.steps):
-        e2e_step(i)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = replicas.max_over_ranks(e0.elapsed_time(e1))
-    e2e_steps = float(st_h.sum().item()) / B if int(st_h.sum().item()) else w.T
-    e2e_value = replicas.job_throughput(world, w.L, B, e2e_steps, e2e_ms / args.steps / 1000.0)
-    h2d = kp.numel() * 2 * 2
-    d2h = out_h.numel() * 4 + st_h.numel() * 4
+        for i in range(min(warmup, 3)):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            e2e_step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = replicas.max_over_ranks(e0.elapsed_time(e1))
+        e2e_steps = float(st_h.sum().item()) / B if int(st_h.sum().item()) else w.T
+        h2d = kp.numel() * 2 * 2 + (x0_h.numel() * 4 + keep_h.numel() * 8 if noising else 0)
+        d2h = out_h.numel() * 4 + st_h.numel() * 4 + (x0_h.numel() * 4 if noising else 0)
+        res["e2e"] = {"value": replicas.job_throughput(world, w.L, B, e2e_steps,
+                                                       e2e_ms / steps / 1000.0),
+                      "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     hbm, tf_burst, tf_sust, peak_kind = peaks()
     flops_per_launch = 2.0 * B * w.L * w.d * w.V
     vocab_avg_s = vocab_ms / max(vocab_n, 1) / 1000.0
     achieved = flops_per_launch / vocab_avg_s / 1e12
-    roofline = {"kernel": "vocab_posterior_kernel (fused LM head + posterior + exact two-level sample)",
-                "bound": "tensor", "achieved": achieved, "peak": tf_sust, "unit": "TFLOP/s",
-                "frac": achieved / tf_sust, "traffic": traffic_from_profile("vocab.cu"),
-                "peak_kind": f"{peak_kind} sustained bf16",
-                "launches": vocab_n, "avg_ms": vocab_avg_s * 1000.0,
-                "hbm_frac": (2.0 * w.V * w.d + 2.0 * B * w.L * w.d) / vocab_avg_s / 1e9 / hbm,
-                "attention_avg_ms": attn_ms / max(attn_n, 1)}
+    res["lm_head"] = {
+        "kernel": "vocab_posterior_kernel (fused LM head + posterior + two-level Gumbel-max "
+                  "sample)",
+        "bound": "tensor", "achieved": achieved, "peak": tf_burst, "unit": "TFLOP/s",
+        "frac": achieved / tf_burst, "peak_sustained": tf_sust,
+        "frac_sustained": achieved / tf_sust, "peak_kind": f"{peak_kind} bf16 (burst; sustained "
+                                                          f"beside)",
+        "traffic": traffic_from_profile("vocab.cu", w.name),
+        "launches": vocab_n, "avg_ms": vocab_avg_s * 1000.0,
+        "hbm_frac": (2.0 * w.V * w.d + 2.0 * B * w.L * w.d) / vocab_avg_s / 1e9 / hbm}
+    a_flops, a_bytes = attention_work(w)
+    attn_avg_s = attn_ms / max(attn_n, 1) / 1000.0
+    res["attention"] = {
+        "kernel": "canvas_attn_kernel + attn_merge_kernel", "avg_ms": attn_avg_s * 1000.0,
+        "launches": attn_n, "achieved_tflops": a_flops / attn_avg_s / 1e12 if attn_n else None,
+        "frac_burst": a_flops / attn_avg_s / 1e12 / tf_burst if attn_n else None,
+        "frac_sustained": a_flops / attn_avg_s / 1e12 / tf_sust if attn_n else None,
+        "kv_gbs": a_bytes / attn_avg_s / 1e9 if attn_n else None,
+        "hbm_frac": a_bytes / attn_avg_s / 1e9 / hbm if attn_n else None}
     if sc:  # the self-conditioning contraction p_hat E: the same FLOPs as the LM head
         sc_avg_s = sc_ms / max(sc_n, 1) / 1000.0
-        roofline["selfcond_contraction"] = {
+        res["selfcond_contraction"] = {
             "kernel": "sc_gemm_kernel", "avg_ms": sc_avg_s * 1000.0, "launches": sc_n,
             "achieved_tflops": flops_per_launch / sc_avg_s / 1e12 if sc_n else None,
             "hbm_gbs_algorithmic": (2.0 * w.V * w.d + 2.0 * B * w.L * w.V) / sc_avg_s / 1e9
@@ -359,36 +413,125 @@ def run_ours(args, w):
     # finalisation as its own launch (the Euler loop folds all but the last into the next
     # step's embedding launch)
     eb_extra = (w.T + (w.T - 1 if not sc else 0)) if eb else 0
-    launches = args.steps * (1 + dgc.dg_denoise_loop_kernel_count(model, B, w.L, w.P, w.window,
-                                                                  w.T) + eb_extra)
+    per_step = (1 + (1 if noising else 0) + dgc.dg_denoise_loop_kernel_count(
+        model, B, w.L, w.P, w.window, int(round(denoise_steps))) + eb_extra)
+    res["gpu_launches"] = steps * per_step
+    del model, ws, m, kp, vp
+    torch.cuda.empty_cache()
+    return res
 
-    cpu = None
+
+def parity_probe(w, dev, oracle: "OracleSample", seed_shift: int, result):
+    """The oracle sample's canvas-step on the GPU: the same canvas, model and prefix (one
+    canvas), the loop's last step (lambda = 1, so every position takes its posterior sample);
+    counts positions whose sampled token differs from the oracle's and the oracle's near-ties
+    (two best perturbed scores within 1e-3 at either level of the sample)."""
+    import torch
+
+    from discrete_diffusion_text_gb300 import dgcanvas as dgc
+
+    _, post, x = result
+    md = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in oracle.m.items()}
+    model = dgc.make_model(md["E"], md["Wqkv"], md["Wo"], w.H, w.Hkv, w.hd)
+    ws = dgc.workspace(dgc.dg_denoise_loop_workspace(model, 1, w.L, w.P, w.window), dev)
+    c = torch.tensor(x, dtype=torch.int32, device=dev)
+    lk = torch.zeros((1, w.L), dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    n = w.T - 1
+    cfg = dgc.make_cfg(w.T, w.schedule, w.inv_tau, math.inf, w.seed + seed_shift,
+                       start_step=n, end_step=n + 1)
+    dgc.dg_denoise_loop(model, oracle.kp.to(dev), oracle.vp.to(dev), w.window, c, lk, st, cfg,
+                        ws)
+    dgc.dg_workspace_status(ws)
+    got = c.cpu().numpy().reshape(-1)
+    diff = got != post["x0hat"]
+    near = post["gap_perturbed"] < 1e-3
+    del model, ws, md
+    torch.cuda.empty_cache()
+    return {"positions": int(w.L), "sampled_token_mismatches": int(diff.sum()),
+            "mismatches_off_near_tie": int((diff & ~near).sum()),
+            "oracle_near_ties": int(near.sum()),
+            "near_tie_rule": "two best perturbed scores within 1e-3 at either level of the "
+                             "sample (chunk scores, or perturbed logits in the chosen chunk)"}
+
+
+def run_ours(args, w):
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from discrete_diffusion_text_gb300 import dgcanvas as dgc
+    from discrete_diffusion_text_gb300 import synth
+
+    dgc.load()
+    sc = args.selfcond
+    eb = args.sampler == "eb"
+    noising = w.B if w.name.startswith("sweep4k") else 0   # the sweep's noising leg
+    main = measure_denoise(w, dev, args.steps, args.warmup, rank=rank, world=world, dist=dist,
+                           sc=sc, eb=eb, noising=noising)
+
+    # the other full-size configurations, same contract, fewer steps (rank 0 alone at N = 1)
+    subs = {}
+    if world == 1 and not args.no_sub and args.workload == DEFAULT_WORKLOAD and not sc and not eb:
+        for name, k in (("window1k", args.steps), ("batch16", max(3, args.steps // 4)),
+                        ("long128k", args.steps)):
+            sw = synth.WORKLOADS[name]
+            r = measure_denoise(sw, dev, k, 3, e2e=False, timer_steps=min(k, 3))
+            subs[name] = {"workload": sw.describe(), "value": r["value"], "unit": UNIT,
+                          "steps": k, "warmup": 3, "ms_per_step": r["ms_per_step"],
+                          "steps_per_canvas": r["steps_per_canvas"],
+                          "lock_fraction": r["lock_fraction"], "clocks": r["clocks"],
+                          "lm_head": r["lm_head"], "attention": r["attention"],
+                          "gpu_launches": r["gpu_launches"]}
+
+    cpu = parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rows = 256
-        sec = OracleSample(w)(rows)
-        cpu = {"value": rows / sec, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-               "sample": f"one denoising step of the {w.name} workload (decoder over the canvas, "
-                         f"posterior over all 262,144 tokens and Euler step for all {rows} "
-                         f"positions), numpy float64; BLAS threaded, elementwise on one thread"}
+        oracle = OracleSample(w)
+        res = oracle(0)
+        cpu = {"value": w.L / res[0], "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+               "sample": oracle_sample_text(w)}
+        parity = parity_probe(w, dev, oracle, 0, res)
 
     if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        roofline = dict(main["lm_head"])
+        roofline["attention"] = main["attention"]
+        if sc:
+            roofline["selfcond_contraction"] = main["selfcond_contraction"]
+        line = {"metric": METRIC, "value": main["value"], "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": main["ms_per_step"],
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16", "data": "synthetic (seeded N(0,0.02) weights, N(0,1) prefix KV, "
-                                         "uniform-prior canvases)",
+                                         "uniform-prior canvases"
+                                         + ("; Zipf(1.1) clean canvases noised at t ~ U(0,1)"
+                                            if noising else "") + ")",
                 "config": {"workload": w.describe() + (
                                "; entropy-bounded sampler (tau 0.8->0.4, gamma 0.1, stop at mean "
                                "entropy 0.005, cap T)" if eb else "") + (
-                               f"; self-conditioning FFW d_sc {sc}" if sc else ""),
-                           "global_batch": B * world, "seq_len": w.L,
-                           "prefix": w.P, "denoise_steps": w.T,
+                               f"; self-conditioning FFW d_sc {sc}" if sc else "") + (
+                               f"; each step also noises {noising} x {w.L} Zipf(1.1) clean "
+                               f"tokens at t ~ U(0,1)" if noising else ""),
+                           "global_batch": w.B * world, "seq_len": w.L,
+                           "prefix": w.P, "denoise_steps_cap": w.T,
                            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                            "l2": "inputs larger than L2: the 1 GiB LM-head weight and the prefix "
                                  "KV are streamed every denoising step; no flush"},
-                "clocks": clk, "e2e": {"value": e2e_value, "unit": UNIT,
-                                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-                "gpu_launches": launches, "roofline": roofline, "cpu_baseline": cpu}
+                "clocks": main["clocks"], "e2e": main["e2e"],
+                "gpu_launches": main["gpu_launches"], "roofline": roofline,
+                "steps_per_canvas": main["steps_per_canvas"],
+                "steps_per_canvas_max": main["steps_per_canvas_max"],
+                "tpf": main["tpf"], "eds": main["eds"], "lock_fraction": main["lock_fraction"],
+                "parity_probe": parity, "cpu_baseline": cpu}
+        if subs:
+            line["workloads"] = subs
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
@@ -546,8 +689,9 @@ def main():
     from discrete_diffusion_text_gb300 import synth
 
     w = synth.WORKLOADS[args.workload]
-    if args.batch:
-        w = w.with_batch(args.batch)
+    batch = args.batch or (max(synth.SWEEP_BATCHES) if args.workload == "sweep4k" else 0)
+    if batch:
+        w = w.with_batch(batch)
     if args.impl == "reference":
         run_reference(args, w)
     elif args.mode == "sft":
