@@ -52,6 +52,16 @@ int num_sms() {
   return cache[d];
 }
 
+// ----------------------------------------------------------------- bounded waits -----
+
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s
+constexpr uint64_t kMaxWaitNs = 60000000000ull;     // 60 s
+static thread_local uint64_t g_wait_limit_ns = kDefaultWaitNs;
+static thread_local bool g_wait_skip_loads = false;
+
+uint64_t wait_limit_ns() { return g_wait_limit_ns; }
+bool wait_test_skip_loads() { return g_wait_skip_loads; }
+
 // Library-owned status word for calls that take no workspace.
 __device__ uint32_t g_fallback_status_word;
 
@@ -389,7 +399,7 @@ dg_status dg_embed_qkv(const int32_t* x, const uint16_t* E, const uint16_t* Wqkv
   if (bad_ptr(x) || bad_ptr(E) || bad_ptr(Wqkv) || bad_ptr(h) || bad_ptr(q) || bad_ptr(k) || bad_ptr(v))
     return fail(DG_EINVAL, "embed_qkv: NULL or misaligned pointer");
   cudaStream_t st = as_stream(stream);
-  launch_embed_gather(x, E, h, BL, V, d, nullptr, st);
+  launch_embed_gather(x, E, h, BL, V, d, nullptr, st, nullptr);
   dg_status s = check_launch("embed gather launch");
   if (s != DG_OK) return s;
   GemmOut out{};
@@ -592,7 +602,7 @@ dg_status dg_sft_loss(const dg_model* m, const uint16_t* k_pre, const uint16_t* 
   // x_t = forward noising of x_0 at each canvas's keep threshold
   launch_forward_noise(x0, xt, keep_thr, B, L, m->V, seed, st);
   if ((s = check_launch("sft_loss: noise launch")) != DG_OK) return s;
-  launch_embed_gather(xt, m->E, w.h, BL, m->V, m->d, nullptr, st);
+  launch_embed_gather(xt, m->E, w.h, BL, m->V, m->d, nullptr, st, w.status);
   if ((s = check_launch("sft_loss: embed launch")) != DG_OK) return s;
   GemmOut qkv = qkv_segments(m);  // the segments the workspace's split-K plan was sized for
   qkv.ptr[0] = w.q;
@@ -811,7 +821,7 @@ dg_status run_denoise(const RunArgs& a, const dg_sampler_cfg* cfg,
     } else {
       // the signal of the previous step (none at step 0; a resumed run reads the one its
       // previous call left in the workspace)
-      launch_embed_gather(a.canvas, m->E, w.h, BL, m->V, m->d, w.n_active, st,
+      launch_embed_gather(a.canvas, m->E, w.h, BL, m->V, m->d, w.n_active, st, w.status,
                           sc && n > 0 ? w.sc_s : nullptr);
       if ((s = check_launch("loop: embed launch")) != DG_OK) return s;
     }
@@ -833,6 +843,7 @@ dg_status run_denoise(const RunArgs& a, const dg_sampler_cfg* cfg,
     FinalizeParams fp{};
     fp.parts = w.parts;
     fp.bar = bars;
+    fp.status = w.status;
     fp.num_mt = vp.num_mt;
     fp.S = vp.S;
     fp.L = L;
@@ -937,7 +948,7 @@ dg_status run_encode_append(const dg_model* m, const int32_t* canvas, uint16_t* 
   const int Hhd = m->H * m->hd;
   const int KVhd = m->Hkv * m->hd;
   dg_status s;
-  launch_embed_gather(canvas, m->E, h, BL, m->V, m->d, n_run, st);
+  launch_embed_gather(canvas, m->E, h, BL, m->V, m->d, n_run, st, status);
   if ((s = check_launch("encode-append: embed launch")) != DG_OK) return s;
   GemmOut kv{};
   kv.nseg = 2;
@@ -1227,6 +1238,13 @@ dg_status dg_block_generate(const dg_model* m, uint16_t* k_cache, uint16_t* v_ca
                         n_tokens, steps, B, L, NB, j, eos, st);
     if ((s = check_launch("block generate: record launch")) != DG_OK) return s;
   }
+  return DG_OK;
+}
+
+dg_status dg_set_wait_control(uint64_t limit_ns, int skip_loads) {
+  if (limit_ns > kMaxWaitNs) return fail(DG_EINVAL, "wait control: limit above 60 s");
+  g_wait_limit_ns = limit_ns ? limit_ns : kDefaultWaitNs;
+  g_wait_skip_loads = skip_loads != 0;
   return DG_OK;
 }
 

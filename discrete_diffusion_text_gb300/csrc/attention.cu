@@ -52,6 +52,7 @@ struct AttnParams {
   float* part_ml;  // [splits][B*H*L][2]
   uint32_t* status;
   const int* n_active;
+  uint64_t wait_ns;  // limit of every on-chip wait
 };
 
 template <int HD>
@@ -219,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued = 0;
       for (int i = 0; i < 2 * nt; ++i) {
         const int rs = i % kRing;
-        if (!mbar_wait(&kv_empty[rs], ((i / kRing) & 1) ^ 1, abort_flag)) break;
+        if (!mbar_wait(&kv_empty[rs], ((i / kRing) & 1) ^ 1, abort_flag, p.wait_ns)) break;
         const int t = t_begin + (i >> 1);
         const bool pre = t < n_pre;
         const int kb = pre ? (t_lo + t) * kKTile : (t - n_pre) * kKTile;
@@ -240,9 +241,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // warp 1 + s (s < 2): the score MMAs of slot s; warp 3: the P.V MMAs of both slots
       constexpr uint32_t idesc_s = idesc_bf16(128, kKTile, false);
       constexpr uint32_t idesc_o = idesc_bf16(128, HD, true);
-      bool ok = mbar_wait(q_full, 0, abort_flag);
+      bool ok = mbar_wait(q_full, 0, abort_flag, p.wait_ns);
       auto wait_kv = [&](int i) {
-        return mbar_wait(&kv_full[i % kRing], (i / kRing) & 1, abort_flag);
+        return mbar_wait(&kv_full[i % kRing], (i / kRing) & 1, abort_flag, p.wait_ns);
       };
       if (warp < 3) {
         const int s = warp - 1;
@@ -250,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; ok && j < nt; ++j) {
           if (!(ok = wait_kv(2 * j))) break;
           // S_s(j) overwrites the buffer whose first columns hold P_s(j-2)
-          if (j >= 2 && !(ok = mbar_wait(&pv_done[2 * s + (j & 1)], ((j - 2) >> 1) & 1, abort_flag)))
+          if (j >= 2 && !(ok = mbar_wait(&pv_done[2 * s + (j & 1)], ((j - 2) >> 1) & 1, abort_flag, p.wait_ns)))
             break;
           tc_fence_after();
           const uint32_t ka = smem_u32(kv_buf(2 * j));
@@ -269,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = wait_kv(2 * j + 1))) break;
           const uint32_t va = smem_u32(kv_buf(2 * j + 1));
           for (int s = 0; ok && s < nslots; ++s) {
-            if (!(ok = mbar_wait(&p_full[2 * s + (j & 1)], (j >> 1) & 1, abort_flag))) break;
+            if (!(ok = mbar_wait(&p_full[2 * s + (j & 1)], (j >> 1) & 1, abort_flag, p.wait_ns))) break;
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < kKTile / 16; ++kk) {
@@ -300,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float c = p.scale_log2;
       for (int j = 0; j < nt; ++j) {
         const int b = j & 1;
-        if (!warp_wait(&s_full[2 * slot + b], (j >> 1) & 1, abort_flag)) { ok = false; break; }
+        if (!warp_wait(&s_full[2 * slot + b], (j >> 1) & 1, abort_flag, p.wait_ns)) { ok = false; break; }
         tc_fence_after();
         const int t = t_begin + j;
         const bool pre = t < n_pre;
@@ -351,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
         l = l * f + rs;
         if (__any_sync(0xFFFFFFFFu, need)) {  // O *= f once PV of tile j - 1 has completed
-          if (!warp_wait(&pv_done[2 * slot + ((j - 1) & 1)], ((j - 1) >> 1) & 1, abort_flag)) {
+          if (!warp_wait(&pv_done[2 * slot + ((j - 1) & 1)], ((j - 1) >> 1) & 1, abort_flag, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -370,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&p_full[2 * slot + b]);
       }
       if (ok)
-        ok = warp_wait(&pv_done[2 * slot + ((nt - 1) & 1)], ((nt - 1) >> 1) & 1, abort_flag);
+        ok = warp_wait(&pv_done[2 * slot + ((nt - 1) & 1)], ((nt - 1) >> 1) & 1, abort_flag, p.wait_ns);
       tc_fence_after();
       const bool write = ok && qi < p.L;
       if (p.splits == 1) {
@@ -594,6 +595,7 @@ cudaError_t launch_attention(const uint16_t* q, const uint16_t* k_pre, const uin
   p.part_ml = pl.splits > 1 ? p.part_o + static_cast<size_t>(pl.splits) * B * H * L * hd : nullptr;
   p.status = status;
   p.n_active = n_active;
+  p.wait_ns = wait_limit_ns();
   return hd == 64 ? launch_hd<64>(maps, p, st) : launch_hd<128>(maps, p, st);
 }
 

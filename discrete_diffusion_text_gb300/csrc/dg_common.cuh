@@ -183,6 +183,12 @@ uint32_t* status_or_fallback(uint32_t* status);
 
 // ------------------------------------------------------------------- host helpers -----
 
+// The limit of every on-chip wait of kernels the calling thread enqueues (set with
+// dg_set_wait_control; 2 s by default), and the LM-head kernel's test switch that makes its
+// load warps issue nothing (so its waits run out with no copy or tensor-core work in flight).
+uint64_t wait_limit_ns();
+bool wait_test_skip_loads();
+
 void set_error(const std::string& msg);
 dg_status fail(dg_status code, const std::string& msg);
 dg_status cuda_fail(cudaError_t e, const char* what);

@@ -245,6 +245,7 @@ __global__ void __launch_bounds__(256) embed_finalize_kernel(FinalizeParams p,
   __syncthreads();
   const int id = s_token;
   const bool ok = id >= 0 && id < V;
+  if (!ok && threadIdx.x == 0) atomicOr(p.status, kStatusBadIndex);
   for (int c = threadIdx.x; c < d16; c += blockDim.x)
     h[static_cast<int64_t>(row) * d16 + c] =
         ok ? E[static_cast<int64_t>(id) * d16 + c] : make_uint4(0, 0, 0, 0);
@@ -341,8 +342,10 @@ void launch_vocab_finalize(const FinalizeParams& p, int B, cudaStream_t st) {
   timer_end(4, st);
 }
 
-void launch_embed_finalize(const FinalizeParams& p, int B, const uint16_t* E, uint16_t* h, int V,
-                           int d, cudaStream_t st) {
+void launch_embed_finalize(const FinalizeParams& p0, int B, const uint16_t* E, uint16_t* h,
+                           int V, int d, cudaStream_t st) {
+  FinalizeParams p = p0;
+  p.status = status_or_fallback(p.status);
   const int d16 = d / 8;
   const int threads = d16 < 256 ? ((d16 + 31) / 32) * 32 : 256;
   timer_begin(4, st);
@@ -469,13 +472,14 @@ void launch_block_record(const int32_t* canvas, const int32_t* steps_taken, int3
 // h = E[x] (+ s, the self-conditioning signal, summed in fp32 and rounded to bf16).
 __global__ void embed_gather_kernel(const int32_t* __restrict__ x, const uint4* __restrict__ E,
                                     const uint4* __restrict__ s, uint4* __restrict__ h, int V,
-                                    int d16, const int* n_active) {
+                                    int d16, const int* n_active, uint32_t* status) {
   pdl_wait();
   pdl_trigger();
   if (n_active && *n_active == 0) return;
   const int r = blockIdx.x;
   const int id = x[r];
   const bool ok = id >= 0 && id < V;
+  if (!ok && threadIdx.x == 0) atomicOr(status, kStatusBadIndex);
   for (int c = threadIdx.x; c < d16; c += blockDim.x) {
     uint4 w = ok ? E[static_cast<int64_t>(id) * d16 + c] : make_uint4(0, 0, 0, 0);
     if (s) {
@@ -495,12 +499,13 @@ __global__ void embed_gather_kernel(const int32_t* __restrict__ x, const uint4* 
 }
 
 void launch_embed_gather(const int32_t* x, const uint16_t* E, uint16_t* h, int BL, int V, int d,
-                         const int* n_active, cudaStream_t st, const uint16_t* s) {
+                         const int* n_active, cudaStream_t st, uint32_t* status,
+                         const uint16_t* s) {
   const int d16 = d / 8;
   const int threads = d16 < 256 ? ((d16 + 31) / 32) * 32 : 256;
   launch_dependent(embed_gather_kernel, dim3(BL), dim3(threads), 0, st, x,
                    reinterpret_cast<const uint4*>(E), reinterpret_cast<const uint4*>(s),
-                   reinterpret_cast<uint4*>(h), V, d16, n_active);
+                   reinterpret_cast<uint4*>(h), V, d16, n_active, status_or_fallback(status));
 }
 
 }  // namespace dg

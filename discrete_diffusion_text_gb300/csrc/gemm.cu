@@ -37,6 +37,7 @@ struct GemmParams {
   uint32_t* status;
   const int* n_active;
   int act;  // kActNone or kActGeluTanh, applied after the residual
+  uint64_t wait_ns;  // limit of every on-chip wait
 };
 
 // GELU, tanh form: x/2 (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
@@ -76,7 +77,7 @@ template <int BN>
 __device__ __forceinline__ void gemm_produce(const CUtensorMap* tmA, const CUtensorMap* tmB,
                                              uint8_t* smem, uint64_t* full, uint64_t* empty,
                                              int kb0, int nk, int m0, int n0,
-                                             volatile int* abort_flag) {
+                                             volatile int* abort_flag, uint64_t wait_ns) {
   using Lay = GemmLayout<BN>;
   tma_prefetch_map(tmA);
   tma_prefetch_map(tmB);
@@ -84,7 +85,7 @@ __device__ __forceinline__ void gemm_produce(const CUtensorMap* tmA, const CUten
   for (int i = 0; i < nk; ++i) {
     const int s = i % Lay::kStages;
     const uint32_t r = i / Lay::kStages;
-    if (!mbar_wait(&empty[s], (r & 1) ^ 1, abort_flag)) break;
+    if (!mbar_wait(&empty[s], (r & 1) ^ 1, abort_flag, wait_ns)) break;
     uint8_t* sa = smem + s * Lay::kStageBytes;
     mbar_arrive_expect_tx(&full[s], Lay::kStageBytes);
     tma_load_2d(sa, tmA, &full[s], (kb0 + i) * kBK, m0);
@@ -101,13 +102,13 @@ __device__ __forceinline__ void gemm_produce(const CUtensorMap* tmA, const CUten
 template <int BN>
 __device__ __forceinline__ void gemm_mma(uint32_t tmem, uint8_t* smem, uint64_t* full,
                                          uint64_t* empty, uint64_t* acc_full, int nk,
-                                         volatile int* abort_flag) {
+                                         volatile int* abort_flag, uint64_t wait_ns) {
   using Lay = GemmLayout<BN>;
   constexpr uint32_t idesc = idesc_bf16(kBM, BN, false);
   for (int i = 0; i < nk; ++i) {
     const int s = i % Lay::kStages;
     const uint32_t r = i / Lay::kStages;
-    if (!mbar_wait(&full[s], r & 1, abort_flag)) break;
+    if (!mbar_wait(&full[s], r & 1, abort_flag, wait_ns)) break;
     tc_fence_after();
     const uint32_t sa = smem_u32(smem + s * Lay::kStageBytes);
     const uint32_t sb = sa + Lay::kABytes;
@@ -179,11 +180,13 @@ __global__ void __launch_bounds__(kThreadsG, 1)
 
   if (warp == 0) {
     if (lane == 0)
-      gemm_produce<BN>(&tmA, &tmB, smem, g.full, g.empty, 0, p.K / kBK, m0, n0, g.abort_flag);
+      gemm_produce<BN>(&tmA, &tmB, smem, g.full, g.empty, 0, p.K / kBK, m0, n0, g.abort_flag,
+                       p.wait_ns);
   } else if (warp == 1) {
-    if (lane == 0) gemm_mma<BN>(tmem, smem, g.full, g.empty, g.acc_full, p.K / kBK, g.abort_flag);
+    if (lane == 0) gemm_mma<BN>(tmem, smem, g.full, g.empty, g.acc_full, p.K / kBK, g.abort_flag,
+                                    p.wait_ns);
   } else {
-    const bool ok = warp_wait(g.acc_full, 0, g.abort_flag);
+    const bool ok = warp_wait(g.acc_full, 0, g.abort_flag, p.wait_ns);
     tc_fence_after();
     const int row = m0 + (warp & 3) * 32 + lane;
     const SegDst dst = segment_of(p.out, n0);
@@ -281,14 +284,15 @@ __global__ void __launch_bounds__(kThreadsG, 1)
 
   if (warp == 0) {
     if (lane == 0)
-      gemm_produce<BN>(&tmA, &tmB, smem, g.full, g.empty, kb0, nk, m0, n0, g.abort_flag);
+      gemm_produce<BN>(&tmA, &tmB, smem, g.full, g.empty, kb0, nk, m0, n0, g.abort_flag,
+                       p.wait_ns);
   } else if (warp == 1) {
-    if (lane == 0) gemm_mma<BN>(tmem, smem, g.full, g.empty, g.acc_full, nk, g.abort_flag);
+    if (lane == 0) gemm_mma<BN>(tmem, smem, g.full, g.empty, g.acc_full, nk, g.abort_flag, p.wait_ns);
   } else {
     // partial accumulator: own rows to shared memory, the others to the workspace in a
     // [chunk][row] layout so that a warp's 32 rows of one 16-byte chunk are 512 contiguous
     // bytes (the ring is idle: every MMA that read it has completed)
-    warp_wait(g.acc_full, 0, g.abort_flag);
+    warp_wait(g.acc_full, 0, g.abort_flag, p.wait_ns);
     tc_fence_after();
     const int row = (warp & 3) * 32 + lane;
     const bool own = row / Lay::kR == q;
@@ -569,6 +573,7 @@ cudaError_t launch_gemm(const uint16_t* A, const uint16_t* W, int M, int N, int 
   p.ld_res = ld_res;
   p.status = status;
   p.n_active = n_active;
+  p.wait_ns = wait_limit_ns();
   p.act = act;
   float* part = static_cast<float*>(part_ws);
   timer_begin(3, st);

@@ -32,6 +32,7 @@ struct FinalizeParams {
   int* unlocked;  // [B] per-canvas counters, zero before the first call; reset by the kernel
   int* cta_done;  // [B]
   uint32_t* bar;  // the vocabulary pass's sampling bars: zeroed per row once merged (or NULL)
+  uint32_t* status;  // embed_finalize_kernel: kStatusBadIndex for a token outside [0, V)
 };
 
 // One step of the entropy-bounded sampler for every canvas (one CTA per canvas).
@@ -83,9 +84,11 @@ void launch_embed_finalize(const FinalizeParams& p, int B, const uint16_t* E, ui
                            int d, cudaStream_t st);
 void launch_loop_init(const uint8_t* lock, uint8_t* active, int* n_active, int32_t* steps_taken,
                       int B, int L, int stop_when_all_locked, cudaStream_t st);
-// h = E[x] (+ s when s != NULL: the self-conditioning signal, bf16 [BL, d]).
+// h = E[x] (+ s when s != NULL: the self-conditioning signal, bf16 [BL, d]).  An id outside
+// [0, V) gives a zero row and sets kStatusBadIndex in *status (NULL: the library's word).
 void launch_embed_gather(const int32_t* x, const uint16_t* E, uint16_t* h, int BL, int V, int d,
-                         const int* n_active, cudaStream_t st, const uint16_t* s = nullptr);
+                         const int* n_active, cudaStream_t st, uint32_t* status,
+                         const uint16_t* s = nullptr);
 
 // Launch with programmatic stream serialisation: the kernel may be scheduled while the
 // previous kernel in the stream finishes (its launch latency hidden behind that kernel); it

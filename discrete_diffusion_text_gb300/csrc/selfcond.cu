@@ -46,6 +46,7 @@ struct ScGemmParams {
   float* part;         // [S, R, d]
   uint32_t* status;
   const int* n_active;
+  uint64_t wait_ns;  // limit of every on-chip wait
 };
 
 __global__ void __launch_bounds__(192, 1)
@@ -100,7 +101,7 @@ __global__ void __launch_bounds__(192, 1)
       for (int kb = kb0; kb < kb1; ++kb, ++issued) {
         const int s = issued % kScStages;
         const uint32_t r = issued / kScStages;
-        if (!mbar_wait(&empty[s], (r & 1) ^ 1, abort_flag)) break;
+        if (!mbar_wait(&empty[s], (r & 1) ^ 1, abort_flag, p.wait_ns)) break;
         uint8_t* sa = smem + s * kScStageBytes;
         mbar_arrive_expect_tx(&full[s], kScStageBytes);
         tma_load_2d(sa, &tmA, &full[s], kb * kScBK, m0);
@@ -120,7 +121,7 @@ __global__ void __launch_bounds__(192, 1)
       int q = 0;
       for (int kb = kb0; kb < kb1; ++kb, ++q) {
         const int s = q % kScStages;
-        if (!mbar_wait(&scaled[s], (q / kScStages) & 1, abort_flag)) break;
+        if (!mbar_wait(&scaled[s], (q / kScStages) & 1, abort_flag, p.wait_ns)) break;
         tc_fence_after();
         const uint32_t sb = smem_u32(smem + s * kScStageBytes) + kScABytes;
         const uint32_t ta = tmem + kScBN + s * 32;
@@ -152,7 +153,7 @@ __global__ void __launch_bounds__(192, 1)
       const int s = q % kScStages;
       const float2 mr = mr_next;
       if (live && kb + 1 < kb1) mr_next = *reinterpret_cast<const float2*>(mrow + kb * 2 + 2);
-      if (ok) ok = warp_wait(&full[s], (q / kScStages) & 1, abort_flag);
+      if (ok) ok = warp_wait(&full[s], (q / kScStages) & 1, abort_flag, p.wait_ns);
       if (ok) {
         const float c0 = live ? ex2_approx((mr.x - lse) * kScLog2e) : 0.f;
         const float c1 = live ? ex2_approx((mr.y - lse) * kScLog2e) : 0.f;
@@ -176,7 +177,7 @@ __global__ void __launch_bounds__(192, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&scaled[s]);
     }
-    ok = ok && warp_wait(acc_full, 0, abort_flag);
+    ok = ok && warp_wait(acc_full, 0, abort_flag, p.wait_ns);
     tc_fence_after();
     float* dst = p.part + (static_cast<int64_t>(blockIdx.z) * p.R + row) * p.d + n0;
 #pragma unroll 1
@@ -295,6 +296,7 @@ cudaError_t launch_self_condition(const uint16_t* p_til, const float* m_ref, con
   gp.part = part;
   gp.status = status;
   gp.n_active = n_active;
+  gp.wait_ns = wait_limit_ns();
   timer_begin(2, st);
   cudaError_t err = launch_dependent(sc_gemm_kernel, dim3(pl.nt, pl.mt, pl.S), dim3(192),
                                      kScSmemBytes, st, ta, tb, gp);

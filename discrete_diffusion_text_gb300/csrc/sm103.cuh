@@ -1,9 +1,10 @@
 // Blackwell (sm_103a) building blocks written as inline PTX: mbarriers with bounded waits,
 // TMA tile loads, and the tcgen05 tensor-core / tensor-memory instructions.
 //
-// Every wait in this library is bounded: after kWaitLimitNs of polling, the waiter raises a
-// per-CTA abort flag in shared memory (and the kernel then reports DG_ETIMEOUT through its
-// device status word) instead of spinning forever.
+// Every wait in this library is bounded: after the call's wait limit (kernel parameter; 2 s
+// unless the caller set another) the waiter raises a per-CTA abort flag in shared memory (and
+// the kernel then reports DG_ETIMEOUT through its device status word) instead of spinning
+// forever.
 #pragma once
 
 #include <cuda.h>
@@ -13,7 +14,7 @@
 
 namespace dg {
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -68,14 +69,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits until the phase with the given parity has completed.  Returns false (and raises
-// *abort) when the wait exceeds the limit, or at once when another thread has raised *abort.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+// *abort) when the wait exceeds limit_ns, or at once when another thread has raised *abort.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       *abort = 1;
       return false;
     }
@@ -93,8 +95,9 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) 
 
 // Every lane waits; the outcome is made warp-uniform so that a following warp-collective
 // instruction (tcgen05.ld / st) is never reached by only part of the warp.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  const bool r = mbar_wait(bar, parity, abort);
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns) {
+  const bool r = mbar_wait(bar, parity, abort, limit_ns);
   return __all_sync(0xFFFFFFFFu, r ? 1 : 0) != 0;
 }
 

@@ -45,6 +45,8 @@ struct VocabParams {
                            // launch (order-preserving key; 0 = none), zeroed before the launch
   uint32_t* status;
   const int* n_active;
+  uint64_t wait_ns;  // limit of every on-chip wait
+  int skip_loads;    // nonzero: the load warps issue nothing (tests of the timeout path)
 };
 
 // Shared memory.  Unified ring: kStages stages of (y k-block, W k-block).  Split rings (one
@@ -289,7 +291,7 @@ __global__ void __launch_bounds__(VocabLayout<kSplit>::kThreadsT, 1)
       const uint64_t stream_once = l2_policy_evict_first();
       uint32_t g = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+      for (int u = blockIdx.x; ok && !p.skip_loads && u < p.units; u += gridDim.x) {
         const int mt = u % p.num_mt;
         const int chunk = u / p.num_mt;
         const int vt0 = chunk * p.per;
@@ -297,7 +299,7 @@ __global__ void __launch_bounds__(VocabLayout<kSplit>::kThreadsT, 1)
         for (int vt = vt0; ok && vt < vt1; ++vt) {
           for (int kb = 0; kb < nkb; ++kb, ++g) {
             const int s = g % kWS;
-            if (!mbar_wait(&empty[s], ((g / kWS) & 1) ^ 1, abort_flag)) { ok = false; break; }
+            if (!mbar_wait(&empty[s], ((g / kWS) & 1) ^ 1, abort_flag, p.wait_ns)) { ok = false; break; }
             if constexpr (kSplit) {  // the W k-block alone (warp 18 loads y)
               uint8_t* sb = smem + s * Lay::kBBytes;
               mbar_arrive_expect_tx(&full[s], Lay::kBBytes);
@@ -323,7 +325,7 @@ __global__ void __launch_bounds__(VocabLayout<kSplit>::kThreadsT, 1)
     if (lane == 0) {
       uint32_t g = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+      for (int u = blockIdx.x; ok && !p.skip_loads && u < p.units; u += gridDim.x) {
         const int mt = u % p.num_mt;
         const int chunk = u / p.num_mt;
         const int vt0 = chunk * p.per;
@@ -331,7 +333,7 @@ __global__ void __launch_bounds__(VocabLayout<kSplit>::kThreadsT, 1)
         for (int vt = vt0; ok && vt < vt1; ++vt) {
           for (int kb = 0; kb < nkb; ++kb, ++g) {
             const int s = g % kYS;
-            if (!mbar_wait(&yempty[s], ((g / kYS) & 1) ^ 1, abort_flag)) { ok = false; break; }
+            if (!mbar_wait(&yempty[s], ((g / kYS) & 1) ^ 1, abort_flag, p.wait_ns)) { ok = false; break; }
             uint8_t* sa = smem + Lay::kYOff + s * Lay::kABytes;
             mbar_arrive_expect_tx(&yfull[s], Lay::kABytes);
             tma_load_2d(sa, &tmA, &yfull[s], kb * kBK, mt * kBM);
@@ -355,17 +357,17 @@ __global__ void __launch_bounds__(VocabLayout<kSplit>::kThreadsT, 1)
         const int vt1 = min(vt0 + p.per, p.nvt);
         for (int vt = vt0; ok && vt < vt1; ++vt, ++j) {
           const int buf = j & 1;
-          if (!mbar_wait(&tempty[buf], ((j >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&tempty[buf], ((j >> 1) & 1) ^ 1, abort_flag, p.wait_ns)) { ok = false; break; }
           tc_fence_after();
           const uint32_t d_tmem = tmem + buf * kBN;
           for (int kb = 0; kb < nkb; ++kb, ++g) {
             const int s = g % kWS;
-            if (!mbar_wait(&full[s], (g / kWS) & 1, abort_flag)) { ok = false; break; }
+            if (!mbar_wait(&full[s], (g / kWS) & 1, abort_flag, p.wait_ns)) { ok = false; break; }
             uint32_t sa, sb;
             int ys = 0;
             if constexpr (kSplit) {
               ys = g % kYS;
-              if (!mbar_wait(&yfull[ys], (g / kYS) & 1, abort_flag)) { ok = false; break; }
+              if (!mbar_wait(&yfull[ys], (g / kYS) & 1, abort_flag, p.wait_ns)) { ok = false; break; }
               sa = smem_u32(smem + Lay::kYOff + ys * Lay::kABytes);
               sb = smem_u32(smem + s * Lay::kBBytes);
             } else {
@@ -426,7 +428,7 @@ __global__ void __launch_bounds__(VocabLayout<kSplit>::kThreadsT, 1)
         const int buf = j & 1;
         // the row's published best, read before the wait so the load's latency is hidden
         const float bar = bar_row ? score_from_key(ld_relaxed(bar_row)) : -INFINITY;
-        if (ok) ok = warp_wait(&tfull[buf], (j >> 1) & 1, abort_flag);
+        if (ok) ok = warp_wait(&tfull[buf], (j >> 1) & 1, abort_flag, p.wait_ns);
         if (!ok) continue;
         tc_fence_after();
         // this thread's 64 columns, 32 at a time (fewer live registers); the accumulator
@@ -569,6 +571,8 @@ cudaError_t launch_vocab_pass(const uint16_t* y, const uint16_t* W, int R, int L
   p.bar = nullptr;
   p.status = status;
   p.n_active = n_active;
+  p.wait_ns = wait_limit_ns();
+  p.skip_loads = wait_test_skip_loads() ? 1 : 0;
 
   static int configured_device = -1;
   const int dev = device_id();

@@ -91,6 +91,7 @@ SIGNATURES = {
     "dg_block_generate": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P,
                                _SZ, _P]),
     "dg_workspace_status": (_I, [_P, _P]),
+    "dg_set_wait_control": (_I, [_U64, _I]),
     "dg_kernel_timer_enable": (_I, [_I]),
     "dg_kernel_timer_read": (_I, [_I, _P, _P]),
 }
@@ -421,6 +422,13 @@ def dg_block_generate(m: dg_model, k_cache, v_cache, P0: int, L: int, window: in
 
 def dg_workspace_status(ws=None, stream=None):
     _check(load().dg_workspace_status(_ptr(ws), _stream(stream)), "dg_workspace_status")
+
+
+def dg_set_wait_control(limit_ns: int = 0, skip_loads: bool = False):
+    """Limit (ns) of every on-chip wait of the calls this thread enqueues next (0 = 2 s);
+    skip_loads makes the LM-head kernel's load warps issue nothing (timeout-path tests)."""
+    _check(load().dg_set_wait_control(int(limit_ns), 1 if skip_loads else 0),
+           "dg_set_wait_control")
 
 
 def dg_kernel_timer_enable(on: bool):

@@ -35,8 +35,11 @@
  *   - Errors: every call validates its arguments on the host and returns DG_EINVAL /
  *     DG_ENOTSUP before launching anything; a CUDA launch or API failure returns DG_ECUDA.
  *     dg_last_error() returns a thread-local message for the last non-OK status.  Kernels
- *     that wait on on-chip barriers never spin without limit: a wait that exceeds 2 s sets
- *     a flag in the call's workspace, read by dg_workspace_status().
+ *     that wait on on-chip barriers never spin without limit: a wait that exceeds the call's
+ *     limit (2 s unless dg_set_wait_control set another) sets a flag in the call's
+ *     workspace, read by dg_workspace_status().  A kernel that meets a token id outside
+ *     [0, V) where it gathers an embedding row uses a zero row instead of reading out of
+ *     bounds and sets another flag, reported as DG_EKERNEL.
  *   - Threading: calls are thread-compatible; the only global state is the thread-local error
  *     text, a per-device cache of device properties and the optional kernel timer.
  */
@@ -423,8 +426,19 @@ dg_status dg_block_generate(const dg_model* m, uint16_t* k_cache, uint16_t* v_ca
 /* ----------------------------------------------------------------- status and timing ----
  * dg_workspace_status: synchronises `stream`, reads and clears the status word at the start
  * of a workspace used by dg_canvas_attn, dg_vocab_posterior_step, dg_denoise_loop,
- * dg_encode_append, dg_block_generate or dg_self_condition, and
- * returns DG_OK, DG_ETIMEOUT or DG_EKERNEL accordingly (DG_ECUDA if the stream failed).
+ * dg_encode_append, dg_block_generate or dg_self_condition (ws = NULL: the library's word
+ * shared by every call made without a workspace), and returns DG_OK, DG_ETIMEOUT (a kernel
+ * gave up waiting on an on-chip barrier) or DG_EKERNEL (a kernel met an out-of-range token
+ * id) accordingly, DG_ECUDA if the stream failed.
+ *
+ * dg_set_wait_control: the limit, in nanoseconds, of every on-chip barrier wait in the
+ * kernels the calling thread enqueues from now on (0 = the default 2 s; at most 60 s, else
+ * DG_EINVAL).  A wait that runs out raises the CTA's abort flag; the CTA's other waits then
+ * give up at once, the kernel drains what it has in flight (bounded), frees its tensor memory
+ * and returns, and the status word reports DG_ETIMEOUT.  skip_loads != 0 (for tests of that
+ * path) makes the LM-head kernel's load warps issue nothing, so its consumers' waits run out
+ * with no copy or tensor-core operation in flight; its results are then meaningless.  The
+ * setting is thread-local and stays until changed.
  *
  * dg_kernel_timer_enable(1) makes the library record CUDA events on the launching stream
  * around every launch of its LM-head/posterior kernel (kind 0), attention kernels (kind 1),
@@ -434,6 +448,7 @@ dg_status dg_block_generate(const dg_model* m, uint16_t* k_cache, uint16_t* v_ca
  * number of launches since the last reset; dg_kernel_timer_enable(0) stops and resets.
  */
 dg_status dg_workspace_status(const void* ws, void* stream);
+dg_status dg_set_wait_control(uint64_t limit_ns, int skip_loads);
 dg_status dg_kernel_timer_enable(int enable);
 dg_status dg_kernel_timer_read(int kind, double* total_ms, int* launches);
 
