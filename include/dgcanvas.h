@@ -196,18 +196,25 @@ dg_status dg_vocab_posterior_step(const uint16_t* y, const uint16_t* W, int B, i
  * no handle to its memory pool, processes whose device memory is reserved up front, and
  * loops that must not risk the device synchronisation of cudaMalloc / cudaFree.
  *   - Same arguments, layouts, results and errors as dg_vocab_posterior_step, without ws.
- *   - Scratch lives in one file-scope device array of 16 MiB, held by every GPU that loads the
- *     library until the process exits.  The call allocates nothing (no cudaMalloc, cudaFree or
- *     allocating library routine); it clears the part of the array that must start at zero.
- *   - Sizes whose scratch exceeds 16 MiB (about 2,000 canvases of 256 positions or more at a
+ *   - Scratch lives in one file-scope device array of 16 MiB.  The call allocates nothing (no
+ *     cudaMalloc, cudaFree or allocating library routine); it clears the part of the array
+ *     that must start at zero.
+ *   - The array belongs to a module that CUDA loads lazily (the default module loading): the
+ *     first call on each device loads it, which is when the driver reserves the 16 MiB on that
+ *     device (held until the process exits), and looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current.  So that first call can still fail for
+ *     lack of memory, or synchronise the device: make it at start-up, before the process
+ *     reserves the rest of its device memory and before any stream capture.
+ *   - Sizes whose scratch exceeds 16 MiB (about 1,800 canvases of 256 positions or more at a
  *     262,144-token vocabulary on a 152-SM GPU; the need is the dg_vocab_posterior_workspace
  *     size less 256 bytes) return DG_ENOTSUP with a message; use dg_vocab_posterior_step with
  *     a workspace for those.
- *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress)
- *     with that device current; make that first call before any stream capture.
  *   - Every call shares the one array: calls that may overlap on the GPU (different streams
  *     without ordering between them) race on it.  Order them on one stream.
- *   - Kernel timeouts are reported by dg_workspace_status(NULL, stream).
+ *   - Kernel timeouts and out-of-range indices are reported through the library's status word
+ *     that every call made without a workspace shares; dg_workspace_status(NULL, stream) reads
+ *     and clears it, so read it on the same stream right after the call (another caller's read
+ *     would otherwise consume the report, or this call's read could see another call's).
  */
 dg_status dg_vocab_posterior_step_noalloc(const uint16_t* y, const uint16_t* W, int B, int L,
                                           int d, int V, float inv_tau, uint64_t seed, int step,

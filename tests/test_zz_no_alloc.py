@@ -5,7 +5,8 @@ a host framework that only receives its input and output buffers, a process whos
 memory is reserved up front, a loop that must not risk cudaMalloc's device synchronisation).
 dg_vocab_posterior_step_noalloc serves them from a fixed device array inside the library.
 This file checks, through the C ABI, that two calls in a row give the same results as the
-workspace entry point, and that a size beyond the array is refused.  It is collected last and
+workspace entry point, that the second call leaves the device's free memory and torch's
+allocations unchanged, and that a size beyond the array is refused.  It is collected last and
 also runs on its own in a fresh process.
 """
 
@@ -62,6 +63,32 @@ def _run(dgc, fn, y, E, B, L, inv_tau, seed, step, x_in, lock_in, jump_thr, thr,
     return res
 
 
+def _run_bare(dgc, y, E, B, L, inv_tau, seed, step, x_in, lock_in, jump_thr, thr):
+    """The allocation-free call alone, with every buffer made beforehand (the caller's)."""
+    R = B * L
+    bufs = dict(out=_outputs(R), x=x_in.clone(), lock=lock_in.clone(),
+                jump=torch.zeros(R, dtype=torch.uint8, device=DEV),
+                done=torch.zeros(B, dtype=torch.uint8, device=DEV))
+    torch.cuda.synchronize()
+    free0, alloc0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
+    dgc.dg_vocab_posterior_step_noalloc(y, E, B, L, inv_tau, seed, step, x_in=bufs["x"],
+                                        x_out=bufs["x"], lock=bufs["lock"], jump=bufs["jump"],
+                                        done=bufs["done"], jump_thr=jump_thr, lock_logthr=thr,
+                                        out=bufs["out"])
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0  # the device's free memory (driver view)
+    assert torch.cuda.memory_allocated() == alloc0
+    return bufs
+
+
+def _collect(dgc, bufs):
+    dgc.dg_workspace_status(None)
+    res = {k: v.cpu().numpy() for k, v in bufs["out"].items()}
+    res.update(x=bufs["x"].cpu().numpy(), lock=bufs["lock"].cpu().numpy(),
+               jump=bufs["jump"].cpu().numpy(), done=bufs["done"].cpu().numpy())
+    return res
+
+
 def _same(a, b):
     for k in ("lse", "logp_top1", "logp_x0hat"):
         assert np.abs(a[k] - b[k]).max() <= LOGP_TOL, k
@@ -81,8 +108,12 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(dgc):
     # two calls in a row with different inputs, each checked against the workspace call
     for call, (ystd, inv_tau, step) in enumerate(((1.0, 20.0, 4), (0.05, 1.0, 9))):
         y = synth.normal_bf16((B * L, d), ystd, 72 + call).to(DEV)
-        a = _run(dgc, dgc.dg_vocab_posterior_step_noalloc, y, E, B, L, inv_tau, 99, step, x0,
-                 lock0, int(jumps[step]), thr)
+        if call == 1:  # the first call loaded the array's module; from now on nothing is taken
+            a = _collect(dgc, _run_bare(dgc, y, E, B, L, inv_tau, 99, step, x0, lock0,
+                                        int(jumps[step]), thr))
+        else:
+            a = _run(dgc, dgc.dg_vocab_posterior_step_noalloc, y, E, B, L, inv_tau, 99, step, x0,
+                     lock0, int(jumps[step]), thr)
         b = _run(dgc, dgc.dg_vocab_posterior_step, y, E, B, L, inv_tau, 99, step, x0, lock0,
                  int(jumps[step]), thr, ws=ws)
         _same(a, b)
