@@ -12,7 +12,9 @@
 //                two-level posterior sample: Gumbel-max over aligned 32-entry chunks scored
 //                by their log-sum-exps, then Gumbel-max over the winning chunk's entries.
 // Only rows' partial tuples are written; a finalisation kernel merges them in a fixed order and
-// applies the Euler step (the chunk scores merge like any Gumbel-max scores).
+// applies the Euler step (the chunk scores merge like any Gumbel-max scores).  With many row
+// tiles the CTAs run as clusters of two that share each weight k-block by TMA multicast.
+#include <algorithm>
 #include <type_traits>
 
 #include "kernels.cuh"
@@ -30,6 +32,7 @@ constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kThreads = 64 + kEpiThreads;      // TMA warp + MMA warp + epilogue
 constexpr int kGroups = kEpiWarps / 4;          // column groups of the tile
 constexpr int kGroupCols = kBN / kGroups;       // 64 columns per group
+constexpr int kManyRowTiles = 16;  // from this many row tiles: multicast clusters, W kept in L2
 
 struct VocabParams {
   int R, L, d, V;
@@ -47,6 +50,8 @@ struct VocabParams {
   const int* n_active;
   uint64_t wait_ns;  // limit of every on-chip wait
   int skip_loads;    // nonzero: the load warps issue nothing (tests of the timeout path)
+  int w_keep;        // nonzero: W tiles use the normal L2 policy (many row tiles share them);
+                     // zero: evict-first (each W tile is read once, by a few CTAs at a time)
 };
 
 // Shared memory.  Unified ring: kStages stages of (y k-block, W k-block).  Split rings (one
@@ -194,7 +199,6 @@ __device__ __forceinline__ void process_chunk(RowState& st, const float (&z)[32]
     }
     return;
   }
-  const uint32_t c = static_cast<uint32_t>(vbase) >> 5;
   const float score = st.m + logf(sc) - logf(-log1pf(-open_unit(u_gumbel)));
   if (score > st.best) {
     st.best = score;
@@ -231,10 +235,16 @@ __device__ __forceinline__ void process_chunk(RowState& st, const float (&z)[32]
   }
 }
 
-template <bool kCE, bool kEnt, bool kSC, bool kSplit>
+// kMc (unified ring only): the kernel runs as clusters of two CTAs that take row tiles 2k and
+// 2k + 1 of the same vocabulary chunk in lockstep.  Each CTA loads its own y k-block and one
+// 128-row half of the W k-block, multicast into both CTAs' stage (tmB then addresses 128-row
+// boxes), so the W tile is read from L2 once per two row tiles; a stage is refilled only after
+// both CTAs' MMAs have read it (each MMA commit arrives on both CTAs' empty barrier).
+template <bool kCE, bool kEnt, bool kSC, bool kSplit, bool kMc>
 __global__ void __launch_bounds__(VocabLayout<kSplit>::kThreadsT, 1)
     vocab_posterior_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB, VocabParams p) {
+  static_assert(!(kMc && kSplit), "multicast with the unified ring only");
   using Lay = VocabLayout<kSplit>;
   constexpr int kWS = Lay::kWStages;
   constexpr int kYS = Lay::kYStages;
@@ -258,11 +268,12 @@ __global__ void __launch_bounds__(VocabLayout<kSplit>::kThreadsT, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int nkb = p.d / kBK;
+  const uint32_t rank = kMc ? cluster_ctarank() : 0u;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kWS; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], kMc ? 2 : 1);
     }
     for (int s = 0; s < kYS; ++s) {
       mbar_init(&yfull[s], 1);
@@ -281,6 +292,10 @@ __global__ void __launch_bounds__(VocabLayout<kSplit>::kThreadsT, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (kMc) {  // the peer's barriers are initialised before any multicast data or commit arrives
+    cluster_arrive();
+    cluster_wait();
+  }
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -288,7 +303,9 @@ __global__ void __launch_bounds__(VocabLayout<kSplit>::kThreadsT, 1)
     if (lane == 0) {
       tma_prefetch_map(&tmA);
       tma_prefetch_map(&tmB);
-      const uint64_t stream_once = l2_policy_evict_first();
+      // y is read by every vocabulary tile: it stays in L2 (evict-last).  W: see w_keep.
+      const uint64_t stream_once = p.w_keep ? l2_policy_evict_normal() : l2_policy_evict_first();
+      const uint64_t y_pol = l2_policy_evict_last();
       uint32_t g = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && !p.skip_loads && u < p.units; u += gridDim.x) {
@@ -306,10 +323,15 @@ __global__ void __launch_bounds__(VocabLayout<kSplit>::kThreadsT, 1)
               tma_load_2d_hint(sb, &tmB, &full[s], kb * kBK, vt * kBN, stream_once);
             } else {
               uint8_t* sa = smem + s * Lay::kStageBytes;
-              mbar_arrive_expect_tx(&full[s], Lay::kStageBytes);
-              tma_load_2d(sa, &tmA, &full[s], kb * kBK, mt * kBM);
-              tma_load_2d_hint(sa + Lay::kABytes, &tmB, &full[s], kb * kBK, vt * kBN,
-                               stream_once);
+              mbar_arrive_expect_tx(&full[s], Lay::kStageBytes);  // y + both W halves
+              tma_load_2d_hint(sa, &tmA, &full[s], kb * kBK, mt * kBM, y_pol);
+              if constexpr (kMc)
+                tma_load_2d_multicast(sa + Lay::kABytes + rank * (Lay::kBBytes / 2), &tmB,
+                                      &full[s], kb * kBK, vt * kBN + rank * (kBN / 2), 0x3,
+                                      stream_once);
+              else
+                tma_load_2d_hint(sa + Lay::kABytes, &tmB, &full[s], kb * kBK, vt * kBN,
+                                 stream_once);
             }
           }
         }
@@ -317,12 +339,18 @@ __global__ void __launch_bounds__(VocabLayout<kSplit>::kThreadsT, 1)
       if (!ok) {
         for (uint32_t q = (g > kWS ? g - kWS : 0); q < g; ++q)
           mbar_wait_drain(&full[q % kWS], (q / kWS) & 1);
+      } else if (kMc) {
+        // every stage this CTA filled has been released by both MMAs, so no commit of the
+        // peer is still on its way to this CTA's barriers when it leaves
+        for (uint32_t q = (g > kWS ? g - kWS : 0); ok && q < g; ++q)
+          ok = mbar_wait(&empty[q % kWS], (q / kWS) & 1, abort_flag, p.wait_ns);
       }
     }
   } else if (kSplit && warp == kThreads / 32) {
     // ------------------------------------------- y producer (split rings only) -----
     if constexpr (kSplit) {
     if (lane == 0) {
+      const uint64_t y_pol = l2_policy_evict_last();  // y is read by every vocabulary tile
       uint32_t g = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && !p.skip_loads && u < p.units; u += gridDim.x) {
@@ -336,7 +364,7 @@ __global__ void __launch_bounds__(VocabLayout<kSplit>::kThreadsT, 1)
             if (!mbar_wait(&yempty[s], ((g / kYS) & 1) ^ 1, abort_flag, p.wait_ns)) { ok = false; break; }
             uint8_t* sa = smem + Lay::kYOff + s * Lay::kABytes;
             mbar_arrive_expect_tx(&yfull[s], Lay::kABytes);
-            tma_load_2d(sa, &tmA, &yfull[s], kb * kBK, mt * kBM);
+            tma_load_2d_hint(sa, &tmA, &yfull[s], kb * kBK, mt * kBM, y_pol);
           }
         }
       }
@@ -379,7 +407,10 @@ __global__ void __launch_bounds__(VocabLayout<kSplit>::kThreadsT, 1)
             for (int k = 0; k < kBK / 16; ++k)
               mma_bf16_ss(d_tmem, sdesc_sw128(sa + k * 32, 16, 1024),
                           sdesc_sw128(sb + k * 32, 16, 1024), idesc, (kb | k) != 0);
-            mma_commit(&empty[s]);
+            if constexpr (kMc)
+              mma_commit_multicast(&empty[s], 0x3);  // both CTAs' copy of this stage
+            else
+              mma_commit(&empty[s]);
             if constexpr (kSplit) mma_commit(&yempty[ys]);
           }
           if (ok) mma_commit(&tfull[buf]);
@@ -483,6 +514,10 @@ __global__ void __launch_bounds__(VocabLayout<kSplit>::kThreadsT, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (kMc) {  // neither CTA leaves while the other may still write to it
+    cluster_arrive();
+    cluster_wait();
+  }
   // every warp of this CTA is done: the next kernel in the stream may be scheduled (not
   // earlier: its waiting CTAs would share the SM with this kernel's epilogue)
   pdl_trigger();
@@ -573,30 +608,63 @@ cudaError_t launch_vocab_pass(const uint16_t* y, const uint16_t* W, int R, int L
   p.n_active = n_active;
   p.wait_ns = wait_limit_ns();
   p.skip_loads = wait_test_skip_loads() ? 1 : 0;
+  // With many row tiles each W tile is read by every row tile's CTA over a window in which
+  // the L2 also holds y: evict-first W lines left the L2 before most readers came (64
+  // canvases: 12.4 GB of DRAM reads per launch for 1.14 GB of data); the normal policy with y
+  // kept (evict-last) reads 2.7 GB and runs 9.5 % faster (5.2 % at 16 canvases, 7.0 % at 32).
+  // With few row tiles a W tile is read once, by a few CTAs together: evict-first keeps the
+  // stream from displacing the other kernels' weights and caches.
+  p.w_keep = pl.num_mt >= kManyRowTiles ? 1 : 0;
 
   static int configured_device = -1;
+  static int max_pairs = 0;  // clusters of two multicast CTAs that can be resident at once
   const int dev = device_id();
   if (configured_device != dev) {
     cudaError_t e = cudaSuccess;
-    for (auto fn : {vocab_posterior_kernel<false, false, false, false>,
-                    vocab_posterior_kernel<false, true, false, false>,
-                    vocab_posterior_kernel<true, false, false, false>,
-                    vocab_posterior_kernel<false, false, true, false>,
-                    vocab_posterior_kernel<false, true, true, false>,
-                    vocab_posterior_kernel<true, false, true, false>})
+    for (auto fn : {vocab_posterior_kernel<false, false, false, false, false>,
+                    vocab_posterior_kernel<false, true, false, false, false>,
+                    vocab_posterior_kernel<true, false, false, false, false>,
+                    vocab_posterior_kernel<false, false, true, false, false>,
+                    vocab_posterior_kernel<false, true, true, false, false>,
+                    vocab_posterior_kernel<true, false, true, false, false>,
+                    vocab_posterior_kernel<false, false, false, false, true>,
+                    vocab_posterior_kernel<false, true, false, false, true>,
+                    vocab_posterior_kernel<true, false, false, false, true>,
+                    vocab_posterior_kernel<false, false, true, false, true>,
+                    vocab_posterior_kernel<false, true, true, false, true>,
+                    vocab_posterior_kernel<true, false, true, false, true>})
       if (e == cudaSuccess)
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  VocabLayout<false>::kSmemBytes);
-    for (auto fn : {vocab_posterior_kernel<false, false, false, true>,
-                    vocab_posterior_kernel<false, true, false, true>,
-                    vocab_posterior_kernel<true, false, false, true>,
-                    vocab_posterior_kernel<false, false, true, true>,
-                    vocab_posterior_kernel<false, true, true, true>,
-                    vocab_posterior_kernel<true, false, true, true>})
+    for (auto fn : {vocab_posterior_kernel<false, false, false, true, false>,
+                    vocab_posterior_kernel<false, true, false, true, false>,
+                    vocab_posterior_kernel<true, false, false, true, false>,
+                    vocab_posterior_kernel<false, false, true, true, false>,
+                    vocab_posterior_kernel<false, true, true, true, false>,
+                    vocab_posterior_kernel<true, false, true, true, false>})
       if (e == cudaSuccess)
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  VocabLayout<true>::kSmemBytes);
     if (e != cudaSuccess) return e;
+    {
+      cudaLaunchConfig_t cfg{};
+      cfg.gridDim = dim3(2 * (num_sms() / 2));
+      cfg.blockDim = dim3(VocabLayout<false>::kThreadsT);
+      cfg.dynamicSmemBytes = VocabLayout<false>::kSmemBytes;
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = 2;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, vocab_posterior_kernel<false, false, false, false, true>,
+                                         &cfg) != cudaSuccess)
+        n = 0;
+      cudaGetLastError();  // an unsupported query leaves no sticky error; the pass runs unpaired
+      max_pairs = n;
+    }
     configured_device = dev;
   }
   // cross-entropy mode (targets, or the self-conditioning pass alone: no sampling), or
@@ -615,23 +683,53 @@ cudaError_t launch_vocab_pass(const uint16_t* y, const uint16_t* W, int R, int L
       if (em != cudaSuccess) return em;
     }
   }
+  // Multicast clusters from 16 row tiles (eight canvases) up, where the pass runs under the
+  // power cap: halving the W reads from L2 lowers its power, and the clock rises more than the
+  // clusters' lockstep costs (measured: 64 canvases +3.7 % throughput at 1,725 against 1,627 MHz,
+  // 16 canvases +3.0 %); at one canvas (not power-bound) it was 0.7 % slower.
+  const bool split = pl.units <= pl.grid && (ce || sc);
+  const bool mc = !split && max_pairs > 0 && pl.num_mt % 2 == 0 && pl.num_mt >= kManyRowTiles;
   timer_begin(0, st);
   cudaError_t e;
-  auto launch = [&](auto split_tag) {
+  auto pick = [&](auto split_tag, auto mc_tag) {
     constexpr bool kS = decltype(split_tag)::value;
-    auto fn = ce ? (sc ? vocab_posterior_kernel<true, false, true, kS>
-                       : vocab_posterior_kernel<true, false, false, kS>)
-                 : entropy ? (sc ? vocab_posterior_kernel<false, true, true, kS>
-                                 : vocab_posterior_kernel<false, true, false, kS>)
-                           : (sc ? vocab_posterior_kernel<false, false, true, kS>
-                                 : vocab_posterior_kernel<false, false, false, kS>);
-    return launch_dependent(fn, dim3(pl.grid), dim3(VocabLayout<kS>::kThreadsT),
-                            VocabLayout<kS>::kSmemBytes, st, ta, tb, p);
+    constexpr bool kM = decltype(mc_tag)::value;
+    return ce ? (sc ? vocab_posterior_kernel<true, false, true, kS, kM>
+                    : vocab_posterior_kernel<true, false, false, kS, kM>)
+              : entropy ? (sc ? vocab_posterior_kernel<false, true, true, kS, kM>
+                              : vocab_posterior_kernel<false, true, false, kS, kM>)
+                        : (sc ? vocab_posterior_kernel<false, false, true, kS, kM>
+                              : vocab_posterior_kernel<false, false, false, kS, kM>);
   };
-  if (pl.units <= pl.grid && (ce || sc))
-    e = launch(std::true_type{});
-  else
-    e = launch(std::false_type{});
+  if (mc) {
+    // W in 128-row boxes (each CTA of a cluster loads one half of a 256-row k-block)
+    const uint32_t bH[2] = {static_cast<uint32_t>(kBK), static_cast<uint32_t>(kBN / 2)};
+    CUtensorMap th;
+    if (!make_tmap_bf16(&th, W, 2, dB, sA, bH)) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(std::min(pl.units, 2 * max_pairs));
+    cfg.blockDim = dim3(VocabLayout<false>::kThreadsT);
+    cfg.dynamicSmemBytes = VocabLayout<false>::kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    at[1].id = cudaLaunchAttributeClusterDimension;
+    at[1].val.clusterDim.x = 2;
+    at[1].val.clusterDim.y = 1;
+    at[1].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 2;
+    e = cudaLaunchKernelEx(&cfg, pick(std::false_type{}, std::true_type{}), ta, th, p);
+  } else if (split) {
+    e = launch_dependent(pick(std::true_type{}, std::false_type{}), dim3(pl.grid),
+                         dim3(VocabLayout<true>::kThreadsT), VocabLayout<true>::kSmemBytes, st,
+                         ta, tb, p);
+  } else {
+    e = launch_dependent(pick(std::false_type{}, std::false_type{}), dim3(pl.grid),
+                         dim3(VocabLayout<false>::kThreadsT), VocabLayout<false>::kSmemBytes, st,
+                         ta, tb, p);
+  }
   timer_end(0, st);
   return e;
 }

@@ -178,3 +178,29 @@ def test_loop_step_prefix_8192_two_canvases(dgc):
     post = O.posterior(y, om["E"], 1.0, w.seed, n, w.L, rows=rows)
     diff = gx.reshape(-1)[rows] != post["x0hat"]
     assert not np.any(diff & (post["gap_perturbed"] >= 1e-3)), int(diff.sum())
+
+
+def test_loop_step_eight_canvases_multicast_lm_head(dgc):
+    """The window1k dimensions with eight canvases (16 row tiles: the LM head runs as two-CTA
+    clusters sharing each weight k-block by multicast): the loop's last step from the uniform
+    prior; the oracle recomputes the decoder and the posterior of 4 positions per canvas."""
+    import dataclasses
+
+    w = dataclasses.replace(synth.WINDOW1K, B=8)
+    side = Side(dgc, w, 8)
+    x0 = O.initial_canvas(8, w.L, w.V, 21)
+    lock0 = np.zeros((8, w.L), np.uint8)
+    n = w.T - 1
+    gx, gl, st = side.run(x0, lock0, dgc.make_cfg(w.T, w.schedule, 1.0, math.inf, 21,
+                                                  start_step=n, end_step=n + 1))
+    assert np.all(st == 1)
+    om = side.om
+    h, q, k, v = O.decoder_front(x0, om["E"], om["Wqkv"], w.H, w.Hkv, w.hd)
+    Oa, _ = O.canvas_attention(q, side.okp, side.ovp, k, v, w.window, w.hd ** -0.5)
+    y = O.decoder_back(h, Oa, om["Wo"]).reshape(8 * w.L, w.d)
+    rng = np.random.default_rng(9)
+    rows = np.sort(np.concatenate([b * w.L + rng.choice(w.L, 4, replace=False)
+                                   for b in range(8)]))
+    post = O.posterior(y, om["E"], 1.0, 21, n, w.L, rows=rows)
+    diff = gx.reshape(-1)[rows] != post["x0hat"]
+    assert not np.any(diff & (post["gap_perturbed"] >= 1e-3)), int(diff.sum())

@@ -235,6 +235,7 @@ def _vocab_run(dgc, y, E, B, L, inv_tau, seed, step):
     (1, 256, 4096, 256, 0.05, 1.0),     # tiny workload: near-uniform posterior
     (16, 256, 4096, 256, 0.05, 1.0),    # many canvases: counters of canvas and position
     (3, 192, 4096, 256, 1.0, 50.0),     # ragged row tile; sharp, peaked posteriors
+    (13, 192, 4096, 256, 1.0, 50.0),    # 20 row tiles: two-CTA multicast clusters, ragged tail
     (1, 64, 8192, 512, 0.5, 5.0),
 ])
 def test_vocab_posterior_matches_oracle(dgc, B, L, V, d, ystd, inv_tau):
