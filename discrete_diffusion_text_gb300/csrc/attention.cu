@@ -26,6 +26,8 @@
 // so the result is unchanged while O (in TMEM) is rescaled rarely.
 // With several key splits, each writes unnormalised fp32 partials (O, m, l) and a merge kernel
 // combines them with the log-sum-exp rule.
+// A second kernel (canvas_attn1_kernel, below) takes one query head per CTA with 128-key
+// tiles; plan_attention picks it where the K/V work is short (see there).
 #include "kernels.cuh"
 #include "sm103.cuh"
 
@@ -425,6 +427,359 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0 && *abort_flag) atomicOr(p.status, kStatusTimeout);
 }
 
+// ------------------------------------------------------------ one query head per CTA -----
+// For long prefixes: one CTA serves one (canvas, query head, 128-query tile) over one key
+// split, in key tiles of 128.  Every MMA is 128 wide (S = Q K^T: M128 N128; O += P V: M128,
+// N = hd, K = 128 keys), where the two-slot kernel's 64-key score MMAs run at three quarters
+// of the pipe's rate.  TMEM: two 128-column score buffers and O (hd columns), so S(j+1) is
+// computed while the softmax of tile j runs and S(j+2) waits only for P(j).V.
+//   warp 0       TMA: Q once, then K_0, V_0, K_1, ... (128-key tiles, 32 KiB at hd = 128)
+//   warp 1       one thread issues the score MMAs, warp 2 one thread the P.V MMAs
+//   warps 4..7   softmax of keys 0..63 of each tile, warps 8..11 of keys 64..127: a thread
+//                owns one query row's half tile; the two halves exchange their row maxima
+//                through shared memory, so both apply the same reference max, and each writes
+//                its P half as bf16 pairs into the buffer's first 64 columns (keys 0..63 in
+//                columns 0..31, keys 64..127 in 32..63: the A operand of P.V); each half keeps
+//                its own running sum l and rescales its half of O.
+constexpr int kKT1 = 128;  // keys per tile
+
+template <int HD>
+struct Attn1Layout {
+  static constexpr int kRing = 5;                    // K/V tiles (K_j and V_j alternate)
+  static constexpr int kQChunk = kQTile * 128;       // [128 rows][64 bf16]
+  static constexpr int kKVChunk = kKT1 * 128;        // [128 keys][64 bf16]
+  static constexpr int kQBytes = (HD / 64) * kQChunk;
+  static constexpr int kKVBytes = (HD / 64) * kKVChunk;
+  static constexpr int kQOff = 0;
+  static constexpr int kKVOff = kQOff + kQBytes;
+  static constexpr int kXOff = kKVOff + kRing * kKVBytes;  // row-max exchange [2][2][128] f32
+  static constexpr int kLOff = kXOff + 2 * 2 * kQTile * 4;  // l exchange [128] f32
+  static constexpr int kBarOff = kLOff + kQTile * 4;
+  static constexpr int kSmemBytes = kBarOff + 256 + 1024;
+  static_assert(kSmemBytes <= 232448, "shared memory");
+};
+
+__device__ __forceinline__ void attn1_unit(int u, const AttnParams& p, int& b, int& h, int& qt) {
+  qt = u % p.n_qtiles;
+  h = (u / p.n_qtiles) % p.H;
+  b = u / (p.n_qtiles * p.H);
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+    canvas_attn1_kernel(const __grid_constant__ CUtensorMap tmQ,
+                        const __grid_constant__ CUtensorMap tmKp,
+                        const __grid_constant__ CUtensorMap tmVp,
+                        const __grid_constant__ CUtensorMap tmKc,
+                        const __grid_constant__ CUtensorMap tmVc, AttnParams p) {
+  using Lay = Attn1Layout<HD>;
+  constexpr int kRing = Lay::kRing;
+  pdl_wait();
+  if (p.n_active && *p.n_active == 0) return;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  float* xmax = reinterpret_cast<float*>(smem + Lay::kXOff);  // [tile parity][half][row]
+  float* xl = reinterpret_cast<float*>(smem + Lay::kLOff);    // [row]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBarOff);
+  uint64_t* q_full = bars + 0;
+  uint64_t* kv_full = bars + 1;             // [kRing]
+  uint64_t* kv_empty = bars + 1 + kRing;    // [kRing]
+  uint64_t* s_full = bars + 1 + 2 * kRing;  // [buffer]
+  uint64_t* p_full = s_full + 2;            // [buffer]
+  uint64_t* pv_done = s_full + 4;           // [buffer]
+  uint64_t* drain = s_full + 6;             // [issuer]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  int b, hq, qt;
+  attn1_unit(blockIdx.x, p, b, hq, qt);
+  const int g = (hq * p.Hkv) / p.H;
+  const int split = blockIdx.y;
+
+  int t_lo = 0;  // first 128-key prefix tile a query of this tile can see
+  if (p.window > 0) {
+    const int kmin = p.P + qt * kQTile - p.window + 1;
+    t_lo = kmin > 0 ? kmin / kKT1 : 0;
+    if (t_lo > p.n_pre_tiles) t_lo = p.n_pre_tiles;
+  }
+  const int n_pre = p.n_pre_tiles - t_lo;
+  const int nt_all = n_pre + p.n_can_tiles;
+  const int t_begin = static_cast<int>(static_cast<int64_t>(split) * nt_all / p.splits);
+  const int t_end = static_cast<int>(static_cast<int64_t>(split + 1) * nt_all / p.splits);
+  const int nt = t_end > t_begin ? t_end - t_begin : 0;
+
+  const int half = warp >= 8 ? 1 : 0;         // softmax warps: which 64 keys of a tile
+  const int row_in = (warp & 3) * 32 + lane;  // TMEM lane quarter of this warp
+  const int qi = qt * kQTile + row_in;
+  const int64_t out_row = (static_cast<int64_t>(b) * p.H + hq) * p.L + qi;  // (b, h, i)
+  const int64_t part_rows = static_cast<int64_t>(p.B) * p.H * p.L;
+
+  if (nt == 0) {  // nothing to do: empty partials (only when splits > 1)
+    if (warp >= 4 && qi < p.L) {
+      if (half == 0) {
+        float* ml = p.part_ml + (split * part_rows + out_row) * 2;
+        ml[0] = -INFINITY;
+        ml[1] = 0.f;
+      }
+      float* po = p.part_o + (split * part_rows + out_row) * HD + half * (HD / 2);
+      for (int c = 0; c < HD / 2; ++c) po[c] = 0.f;
+    }
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);  // K slots: the score thread; V slots: the P.V thread
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&p_full[s], 8);  // one arrival per softmax warp
+      mbar_init(&pv_done[s], 1);
+      mbar_init(&drain[s], 1);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  auto tm_s = [&](int bf) { return tmem + bf * kKT1; };
+  const uint32_t tm_o = tmem + 2 * kKT1;
+  uint8_t* q_buf = smem + Lay::kQOff;
+  auto kv_buf = [&](int i) { return smem + Lay::kKVOff + (i % kRing) * Lay::kKVBytes; };
+
+  if (warp < 4) {
+    regs_decrease<kRegsControl>();
+    if (warp == 0 && lane == 0) {
+      // ------------------------------------------------------------------ producer -----
+      tma_prefetch_map(&tmQ);
+      mbar_arrive_expect_tx(q_full, Lay::kQBytes);
+      for (int c = 0; c < HD / 64; ++c)
+        tma_load_4d(q_buf + c * Lay::kQChunk, &tmQ, q_full, c * 64, hq, qt * kQTile, b);
+      int issued = 0;
+      for (int i = 0; i < 2 * nt; ++i) {
+        const int rs = i % kRing;
+        if (!mbar_wait(&kv_empty[rs], ((i / kRing) & 1) ^ 1, abort_flag, p.wait_ns)) break;
+        const int t = t_begin + (i >> 1);
+        const bool pre = t < n_pre;
+        const int kb = pre ? (t_lo + t) * kKT1 : (t - n_pre) * kKT1;
+        const CUtensorMap* m = (i & 1) ? (pre ? &tmVp : &tmVc) : (pre ? &tmKp : &tmKc);
+        uint8_t* dst = kv_buf(i);
+        mbar_arrive_expect_tx(&kv_full[rs], Lay::kKVBytes);
+        for (int c = 0; c < HD / 64; ++c)
+          tma_load_4d(dst + c * Lay::kKVChunk, m, &kv_full[rs], c * 64, g, kb, b);
+        ++issued;
+      }
+      if (*abort_flag) {
+        mbar_wait_drain(q_full, 0);
+        for (int i = (issued > kRing ? issued - kRing : 0); i < issued; ++i)
+          mbar_wait_drain(&kv_full[i % kRing], (i / kRing) & 1);
+      }
+    } else if ((warp == 1 || warp == 2) && lane == 0) {
+      // ------------------------------------------------------------------ MMA issuers -----
+      constexpr uint32_t idesc_s = idesc_bf16(128, kKT1, false);
+      constexpr uint32_t idesc_o = idesc_bf16(128, HD, true);
+      bool ok = mbar_wait(q_full, 0, abort_flag, p.wait_ns);
+      auto wait_kv = [&](int i) {
+        return mbar_wait(&kv_full[i % kRing], (i / kRing) & 1, abort_flag, p.wait_ns);
+      };
+      if (warp == 1) {
+        const uint32_t qa = smem_u32(q_buf);
+        for (int j = 0; ok && j < nt; ++j) {
+          if (!(ok = wait_kv(2 * j))) break;
+          // S(j) overwrites the buffer whose first columns hold P(j-2)
+          if (j >= 2 && !(ok = mbar_wait(&pv_done[j & 1], ((j - 2) >> 1) & 1, abort_flag,
+                                         p.wait_ns)))
+            break;
+          tc_fence_after();
+          const uint32_t ka = smem_u32(kv_buf(2 * j));
+#pragma unroll
+          for (int kk = 0; kk < HD / 16; ++kk)
+            mma_bf16_ss(tm_s(j & 1),
+                        sdesc_sw128(qa + (kk >> 2) * Lay::kQChunk + (kk & 3) * 32, 16, 1024),
+                        sdesc_sw128(ka + (kk >> 2) * Lay::kKVChunk + (kk & 3) * 32, 16, 1024),
+                        idesc_s, kk > 0 ? 1u : 0u);
+          mma_commit(&s_full[j & 1]);
+          mma_commit(&kv_empty[(2 * j) % kRing]);
+        }
+      } else {
+        for (int j = 0; ok && j < nt; ++j) {
+          if (!(ok = wait_kv(2 * j + 1))) break;
+          if (!(ok = mbar_wait(&p_full[j & 1], (j >> 1) & 1, abort_flag, p.wait_ns))) break;
+          tc_fence_after();
+          const uint32_t va = smem_u32(kv_buf(2 * j + 1));
+#pragma unroll
+          for (int kk = 0; kk < kKT1 / 16; ++kk)
+            mma_bf16_ts(tm_o, tm_s(j & 1) + kk * 8,
+                        sdesc_sw128(va + kk * 2048, Lay::kKVChunk, 1024), idesc_o,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&pv_done[j & 1]);
+          mma_commit(&kv_empty[(2 * j + 1) % kRing]);
+        }
+      }
+      if (*abort_flag) {  // make sure no MMA is still writing TMEM before it is released
+        mma_commit(&drain[warp - 1]);
+        mbar_wait_drain(&drain[warp - 1], 0);
+      }
+    }
+  } else {
+    regs_increase<kRegsSoftmax>();
+    // --------------------------------------------------------------- softmax warps -----
+    const uint32_t lane_base = tmem_lane_base(warp);
+    float m_ref = -INFINITY;
+    float l = 0.f;  // this half's running sum
+    bool ok = true;
+    const int kmin = p.window > 0 ? p.P + qi - p.window + 1 : 0;
+    const float c = p.scale_log2;
+    for (int j = 0; j < nt; ++j) {
+      const int bf = j & 1;
+      // both halves take every step of the loop (the exchange barrier below), even after an
+      // abort; only the waits, loads and stores are skipped
+      if (ok) ok = warp_wait(&s_full[bf], (j >> 1) & 1, abort_flag, p.wait_ns);
+      tc_fence_after();
+      const int t = t_begin + j;
+      const bool pre = t < n_pre;
+      const int kb = (pre ? (t_lo + t) * kKT1 : (t - n_pre) * kKT1) + half * 64;
+      const int klim = pre ? p.P : p.L;
+      const int klo = pre ? kmin : 0;
+      float sv[64];
+      if (ok) {
+        tmem_ld64(tm_s(bf) + lane_base + half * 64, sv);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 64; ++e) sv[e] = -INFINITY;
+      }
+      if (!(kb >= klo && kb + 64 <= klim)) {
+#pragma unroll
+        for (int e = 0; e < 64; ++e) {
+          const int key = kb + e;
+          if (!(key < klim && key >= klo)) sv[e] = -INFINITY;
+        }
+      }
+      float mx[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) mx[q] = sv[q];
+#pragma unroll
+      for (int e = 8; e < 64; e += 2) mx[(e >> 1) & 7] = fmax3(mx[(e >> 1) & 7], sv[e], sv[e + 1]);
+      float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      // the row's max over both halves (the exchange slot of this tile's parity is free: the
+      // other half passed the previous tile's barrier only after reading it)
+      xmax[(bf * 2 + half) * kQTile + row_in] = mt;
+      named_bar_sync(1, 256);
+      mt = fmaxf(mt, xmax[(bf * 2 + (half ^ 1)) * kQTile + row_in]);
+      const float m_new = fmaxf(m_ref, mt * c);
+      const bool need = j > 0 && m_new > m_ref + kRescaleLog2;
+      const float f = need ? ex2_approx(m_ref - m_new) : 1.f;
+      if (j == 0 || need) m_ref = m_new;
+      const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+      float ps[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) ps[q] = 0.f;
+      uint32_t pk[32];
+#pragma unroll
+      for (int e = 0; e < 64; e += 2) {
+        const float a = ex2_approx(fmaf(sv[e], c, -m_use));
+        const float bb = ex2_approx(fmaf(sv[e + 1], c, -m_use));
+        ps[e & 7] += a;
+        ps[(e + 1) & 7] += bb;
+        pk[e >> 1] = pack_bf16x2(a, bb);
+      }
+      // P of this half: columns half * 32 .. + 32 (the other half's raw scores there were
+      // read before the exchange barrier)
+      if (ok) tmem_st32(tm_s(bf) + lane_base + half * 32, pk);
+      const float rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      l = l * f + rs;
+      if (ok && __any_sync(0xFFFFFFFFu, need)) {  // O *= f (this half's columns) after P(j-1).V
+        if (!warp_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.wait_ns)) {
+          ok = false;
+        } else {
+          tc_fence_after();
+#pragma unroll 1
+          for (int cc = 0; cc < HD / 64; ++cc) {
+            float o[32];
+            tmem_ld32(tm_o + lane_base + half * (HD / 2) + cc * 32, o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] *= f;
+            tmem_st32(tm_o + lane_base + half * (HD / 2) + cc * 32, o);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[bf]);
+    }
+    if (ok) ok = warp_wait(&pv_done[(nt - 1) & 1], ((nt - 1) >> 1) & 1, abort_flag, p.wait_ns);
+    tc_fence_after();
+    // the row's sum over both halves
+    if (half == 1) xl[row_in] = l;
+    named_bar_sync(1, 256);
+    const float lt = half == 0 ? l + xl[row_in] : 0.f;
+    if (half == 0) xl[row_in] = lt;
+    named_bar_sync(1, 256);
+    const float l_row = xl[row_in];
+    const bool write = ok && qi < p.L;
+    if (p.splits == 1) {
+      const float inv_l = 1.f / l_row;
+      uint16_t* dst = p.out + ((static_cast<int64_t>(b) * p.L + qi) * p.H + hq) * HD +
+                      half * (HD / 2);
+#pragma unroll 1
+      for (int cc = 0; cc < HD / 64; ++cc) {
+        float o[32];
+        tmem_ld32(tm_o + lane_base + half * (HD / 2) + cc * 32, o);
+        if (write) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            d4[q] = make_uint4(pack_bf16x2(o[q * 8 + 0] * inv_l, o[q * 8 + 1] * inv_l),
+                               pack_bf16x2(o[q * 8 + 2] * inv_l, o[q * 8 + 3] * inv_l),
+                               pack_bf16x2(o[q * 8 + 4] * inv_l, o[q * 8 + 5] * inv_l),
+                               pack_bf16x2(o[q * 8 + 6] * inv_l, o[q * 8 + 7] * inv_l));
+        }
+      }
+      if (write && half == 0 && p.lse)
+        p.lse[out_row] = (m_ref + __log2f(l_row)) * 0.6931471805599453f;
+    } else {
+      const int64_t prow = split * part_rows + out_row;
+      float* po = p.part_o + prow * HD + half * (HD / 2);
+#pragma unroll 1
+      for (int cc = 0; cc < HD / 64; ++cc) {
+        float o[32];
+        tmem_ld32(tm_o + lane_base + half * (HD / 2) + cc * 32, o);
+        if (write) {
+          float4* d4 = reinterpret_cast<float4*>(po + cc * 32);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            d4[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+        }
+      }
+      if (write && half == 0) {
+        p.part_ml[prow * 2] = m_ref;
+        p.part_ml[prow * 2 + 1] = l_row;
+      }
+    }
+  }
+
+  pdl_trigger();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+  if (threadIdx.x == 0 && *abort_flag) atomicOr(p.status, kStatusTimeout);
+}
+
 // Combines split partials: O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.  One warp per
 // (b, h, i) row; lane s holds the (m, l) of splits s and s + 32, so the weights need one load
 // round trip, and the O loads of consecutive splits are independent.
@@ -476,29 +831,37 @@ __global__ void attn_merge_kernel(AttnParams p) {
 }
 
 template <int HD>
-cudaError_t launch_hd(const CUtensorMap* maps, const AttnParams& p, cudaStream_t st) {
+cudaError_t launch_hd(const CUtensorMap* maps, const AttnParams& p, bool one, cudaStream_t st) {
   using Lay = AttnLayout<HD>;
+  using Lay1 = Attn1Layout<HD>;
   static int configured_device = -1;
   const int dev = device_id();
   if (configured_device != dev) {
     cudaError_t e = cudaFuncSetAttribute(canvas_attn_kernel<HD>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Lay::kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(canvas_attn1_kernel<HD>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, Lay1::kSmemBytes);
     if (e != cudaSuccess) return e;
     // The register split must fit the block's launch allocation, or an increase would never
     // be granted: refuse to launch a build where it does not.
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, canvas_attn_kernel<HD>);
-    if (e != cudaSuccess) return e;
-    if (static_cast<long>(fa.numRegs) * kThreads < 128L * kRegsControl + 256L * kRegsSoftmax)
-      return cudaErrorInvalidConfiguration;
+    for (auto fn : {canvas_attn_kernel<HD>, canvas_attn1_kernel<HD>}) {
+      cudaFuncAttributes fa;
+      e = cudaFuncGetAttributes(&fa, fn);
+      if (e != cudaSuccess) return e;
+      if (static_cast<long>(fa.numRegs) * kThreads < 128L * kRegsControl + 256L * kRegsSoftmax)
+        return cudaErrorInvalidConfiguration;
+    }
     configured_device = dev;
   }
   dim3 grid(p.units, p.splits);
   timer_begin(1, st);
-  cudaError_t e = launch_dependent(canvas_attn_kernel<HD>, grid, dim3(kThreads),
-                                   Lay::kSmemBytes, st, maps[0], maps[1], maps[2], maps[3],
-                                   maps[4], p);
+  cudaError_t e =
+      one ? launch_dependent(canvas_attn1_kernel<HD>, grid, dim3(kThreads), Lay1::kSmemBytes, st,
+                             maps[0], maps[1], maps[2], maps[3], maps[4], p)
+          : launch_dependent(canvas_attn_kernel<HD>, grid, dim3(kThreads), Lay::kSmemBytes, st,
+                             maps[0], maps[1], maps[2], maps[3], maps[4], p);
   if (e != cudaSuccess) return e;
   if (p.splits > 1) {
     const int64_t rows = static_cast<int64_t>(p.B) * p.H * p.L;
@@ -520,21 +883,33 @@ int attn_units(int B, int L, int H, int Hkv) {
 }  // namespace
 
 AttnPlan plan_attention(int B, int L, int P, int H, int Hkv, int hd, int window) {
-  const int units = attn_units(B, L, H, Hkv);
+  // Kernel: the two-slot kernel (two query heads of a GQA group share each 64-key K/V tile,
+  // half the K/V bytes per FLOP) keeps long K/V streams fed; where the work is short (at most
+  // ~32 of its key tiles per SM) fixed per-CTA costs and latency dominate, and the one-slot
+  // kernel (128-key tiles, full-rate MMAs, twice the CTAs) is faster.  Measured: window1k
+  // 0.0234 -> 0.0193 ms, one canvas with a 4,096-key prefix 0.029 -> 0.025 ms; but long128k
+  // 0.234 -> 0.260 ms, 16 canvases at 8,192 keys 0.277 -> 0.308 ms, 64 canvases at 4,096 keys
+  // 0.537 -> 0.607 ms (there the one-slot kernel waits on its K/V stream).
   const int eff_p = (window > 0 && window < P) ? window + L : P;  // keys a query tile may see
-  const int nt_all = (eff_p + kKTile - 1) / kKTile + (L + kKTile - 1) / kKTile;
   const int sms = num_sms();
-  // Cost in units of one 64-key tile of a CTA (~0.9 us): waves x (tiles per split + a fixed
-  // ~6 per CTA for start-up, pipeline fill and the partial write), plus ~6 for the merge
-  // kernel when keys are split; ties go to fewer splits.  With at least one CTA per SM
-  // already, keys are not split.
+  const int64_t two_slot_tiles = static_cast<int64_t>(attn_units(B, L, H, Hkv)) *
+                                 ((eff_p + kKTile - 1) / kKTile + (L + kKTile - 1) / kKTile);
+  const bool one = hd == 128 && two_slot_tiles <= 32ll * sms;
+  const int kt = one ? kKT1 : kKTile;
+  const int units = one ? B * H * ((L + kQTile - 1) / kQTile) : attn_units(B, L, H, Hkv);
+  const int nt_all = (eff_p + kt - 1) / kt + (L + kt - 1) / kt;
+  // Cost in units of one key tile of a CTA: waves x (tiles per split + a fixed cost per CTA
+  // for start-up, pipeline fill and the partial write: ~6 64-key tiles, ~3 128-key tiles),
+  // plus the same for the merge kernel when keys are split; ties go to fewer splits.  With at
+  // least one CTA per SM already, keys are not split.
+  const int fixed = one ? 3 : 6;
   int best = 1;
   int64_t best_cost = -1;
   for (int s = 1; s <= nt_all && s <= 64 && (s == 1 || units < sms); ++s) {
     const int per = (nt_all + s - 1) / s;
     const int64_t ctas = static_cast<int64_t>(units) * s;
     const int64_t waves = (ctas + sms - 1) / sms;
-    const int64_t cost = waves * (per + 6) + (s > 1 ? 6 : 0);
+    const int64_t cost = waves * (per + fixed) + (s > 1 ? fixed : 0);
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best = s;
@@ -542,6 +917,8 @@ AttnPlan plan_attention(int B, int L, int P, int H, int Hkv, int hd, int window)
   }
   AttnPlan pl;
   pl.splits = best;
+  pl.one = one ? 1 : 0;
+  pl.units = units;
   pl.part_bytes = best > 1 ? static_cast<size_t>(best) * B * H * L * (hd + 2) * sizeof(float) : 0;
   return pl;
 }
@@ -562,7 +939,8 @@ cudaError_t launch_attention(const uint16_t* q, const uint16_t* k_pre, const uin
                              static_cast<uint64_t>(L) * H * hd * 2};
     if (!make_tmap_bf16(&maps[0], q, 4, dims, str, box)) return cudaErrorInvalidValue;
   }
-  const uint32_t kvbox[4] = {64u, 1u, static_cast<uint32_t>(kKTile), 1u};
+  const int kt = pl.one ? kKT1 : kKTile;
+  const uint32_t kvbox[4] = {64u, 1u, static_cast<uint32_t>(kt), 1u};
   const uint16_t* kv_src[4] = {k_pre, v_pre, k_can, v_can};
   for (int m = 0; m < 4; ++m) {
     const int rows = m < 2 ? (P > 0 ? P : 1) : L;
@@ -584,11 +962,11 @@ cudaError_t launch_attention(const uint16_t* q, const uint16_t* k_pre, const uin
   p.hd = hd;
   p.window = window;
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.n_pre_tiles = (P + kKTile - 1) / kKTile;
-  p.n_can_tiles = (L + kKTile - 1) / kKTile;
+  p.n_pre_tiles = (P + kt - 1) / kt;
+  p.n_can_tiles = (L + kt - 1) / kt;
   p.n_qtiles = (L + kQTile - 1) / kQTile;
   p.splits = pl.splits;
-  p.units = attn_units(B, L, H, Hkv);
+  p.units = pl.units;
   p.out = out;
   p.lse = lse;
   p.part_o = reinterpret_cast<float*>(part_ws);
@@ -596,7 +974,8 @@ cudaError_t launch_attention(const uint16_t* q, const uint16_t* k_pre, const uin
   p.status = status;
   p.n_active = n_active;
   p.wait_ns = wait_limit_ns();
-  return hd == 64 ? launch_hd<64>(maps, p, st) : launch_hd<128>(maps, p, st);
+  return hd == 64 ? launch_hd<64>(maps, p, pl.one != 0, st)
+                  : launch_hd<128>(maps, p, pl.one != 0, st);
 }
 
 }  // namespace dg

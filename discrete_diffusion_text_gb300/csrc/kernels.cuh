@@ -154,6 +154,8 @@ cudaError_t launch_self_condition(const uint16_t* p_til, const float* m_ref, con
 // ------------------------------------------------------------------- attention -----
 struct AttnPlan {
   int splits;
+  int one;    // 1: one query head per CTA with 128-key tiles; 0: two heads per CTA, 64-key tiles
+  int units;  // CTAs per split
   size_t part_bytes;  // fp32 partials for split > 1
 };
 AttnPlan plan_attention(int B, int L, int P, int H, int Hkv, int hd, int window);
