@@ -37,6 +37,7 @@ namespace {
 constexpr int kQTile = 128;  // queries per slot
 constexpr int kKTile = 64;   // keys per tile
 constexpr float kRescaleLog2 = 8.f;
+constexpr float kRaiseSum = 256.f;  // 2^kRescaleLog2: a row sum above it may hide a p above it
 constexpr int kRingMax = 16;
 constexpr int kThreads = 384;      // warpgroup 0: TMA + MMA warps; warpgroups 1, 2: softmax
 constexpr int kRegsControl = 104;  // registers per thread of warpgroup 0 after the split
@@ -321,37 +322,55 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(key < klim && key >= klo)) sv[e] = -INFINITY;
           }
         }
-        float mx[8];  // eight partial maxima: short dependency chains
-#pragma unroll
-        for (int q = 0; q < 8; ++q) mx[q] = sv[q];
-#pragma unroll
-        for (int e = 8; e < kKTile; e += 2) mx[(e >> 1) & 7] = fmax3(mx[(e >> 1) & 7], sv[e], sv[e + 1]);
-        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-        const float m_new = fmaxf(m_ref, mt * c);
-        // raise the reference max only when the row max grew by more than 2^8; f rescales the
-        // accumulated O and l (applied below, once this tile's P is written)
-        const bool need = j > 0 && m_new > m_ref + kRescaleLog2;
-        const float f = need ? ex2_approx(m_ref - m_new) : 1.f;
-        if (j == 0 || need) m_ref = m_new;
-        const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-        // P = exp2(s * c - m), summed with eight partial sums, packed to bf16 pairs and written
-        // over the first 32 columns of this score buffer
+        // P = exp2(s * c - m_ref).  With a reference already set the tile is exponentiated
+        // against it at once (no row-max reduction on the common path): the reference is raised
+        // only when some p would exceed 2^8, which the row sum of p then also exceeds; such a
+        // rare tile is redone against its own max.  The first tile of a row (no reference yet)
+        // takes the max first.
         float ps[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) ps[q] = 0.f;
         uint32_t pk[kKTile / 2];
+        float f = 1.f;
+        bool need = false;
+        auto exp_tile = [&](float m_use) {
 #pragma unroll
-        for (int e = 0; e < kKTile; e += 2) {
-          const float a = ex2_approx(fmaf(sv[e], c, -m_use));
-          const float bb = ex2_approx(fmaf(sv[e + 1], c, -m_use));
-          ps[e & 7] += a;
-          ps[(e + 1) & 7] += bb;
-          pk[e >> 1] = pack_bf16x2(a, bb);
+          for (int q = 0; q < 8; ++q) ps[q] = 0.f;
+#pragma unroll
+          for (int e = 0; e < kKTile; e += 2) {
+            const float a = ex2_approx(fmaf(sv[e], c, -m_use));
+            const float bb = ex2_approx(fmaf(sv[e + 1], c, -m_use));
+            ps[e & 7] += a;
+            ps[(e + 1) & 7] += bb;
+            pk[e >> 1] = pack_bf16x2(a, bb);
+          }
+          return ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+        };
+        auto tile_max = [&]() {
+          float mx[8];  // eight partial maxima: short dependency chains
+#pragma unroll
+          for (int q = 0; q < 8; ++q) mx[q] = sv[q];
+#pragma unroll
+          for (int e = 8; e < kKTile; e += 2)
+            mx[(e >> 1) & 7] = fmax3(mx[(e >> 1) & 7], sv[e], sv[e + 1]);
+          return fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        };
+        float rs;
+        if (m_ref == -INFINITY) {
+          m_ref = tile_max() * c;  // stays -inf for a fully masked tile
+          rs = exp_tile(m_ref == -INFINITY ? 0.f : m_ref);
+        } else {
+          rs = exp_tile(m_ref);
+          if (rs > kRaiseSum) {  // some p may exceed 2^8: raise the reference to this tile's max
+            const float m_new = fmaxf(m_ref, tile_max() * c);
+            if (m_new > m_ref) {
+              need = true;
+              f = ex2_approx(m_ref - m_new);
+              m_ref = m_new;
+              rs = exp_tile(m_ref);
+            }
+          }
         }
         tmem_st32(tm_s(slot, b) + lane_base, pk);
-        const float rs =
-            ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
         l = l * f + rs;
         if (__any_sync(0xFFFFFFFFu, need)) {  // O *= f once PV of tile j - 1 has completed
           if (!warp_wait(&pv_done[2 * slot + ((j - 1) & 1)], ((j - 1) >> 1) & 1, abort_flag, p.wait_ns)) {
