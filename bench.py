@@ -309,18 +309,6 @@ def measure_denoise(w, dev, steps, warmup, *, rank=0, world=1, dist=None, sc=0, 
     # state of the last benchmark step's canvases
     st_last = steps_taken.cpu().numpy().astype(np.float64)
     lock_frac = float(lock.float().mean().item())
-    # ---- the same steps again with the kernel timer on: per-launch durations of the LM-head,
-    # attention and self-conditioning kernels (CUDA events on the launching stream)
-    tsteps = steps if timer_steps is None else timer_steps
-    dgc.dg_kernel_timer_enable(True)
-    for i in range(tsteps):
-        step(warmup + steps + i)
-    torch.cuda.synchronize()
-    vocab_ms, vocab_n = dgc.dg_kernel_timer_read(0)
-    attn_ms, attn_n = dgc.dg_kernel_timer_read(1)
-    sc_ms, sc_n = dgc.dg_kernel_timer_read(2)
-    dgc.dg_kernel_timer_enable(False)
-    dgc.dg_workspace_status(ws)
     ms = replicas.max_over_ranks(ms)
     ms_per_step = ms / steps
     denoise_steps = float(st_last.mean()) if st_last.sum() else float(w.T)
@@ -362,6 +350,8 @@ def measure_denoise(w, dev, steps, warmup, *, rank=0, world=1, dist=None, sc=0, 
         for i in range(min(warmup, 3)):
             e2e_step(i)
         torch.cuda.synchronize()
+        e2e_clocks = ClockSampler(int(str(dev).split(":")[-1]) if ":" in str(dev) else 0)
+        e2e_clocks.start()
         if dist:
             dist.barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -370,14 +360,28 @@ def measure_denoise(w, dev, steps, warmup, *, rank=0, world=1, dist=None, sc=0, 
             e2e_step(i)
         e1.record(stream)
         torch.cuda.synchronize()
+        e2e_clk = e2e_clocks.stop()
         e2e_ms = replicas.max_over_ranks(e0.elapsed_time(e1))
         e2e_steps = float(st_h.sum().item()) / B if int(st_h.sum().item()) else w.T
         h2d = kp.numel() * 2 * 2 + (x0_h.numel() * 4 + keep_h.numel() * 8 if noising else 0)
         d2h = out_h.numel() * 4 + st_h.numel() * 4 + (x0_h.numel() * 4 if noising else 0)
         res["e2e"] = {"value": replicas.job_throughput(world, w.L, B, e2e_steps,
                                                        e2e_ms / steps / 1000.0),
-                      "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+                      "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                      "clocks": e2e_clk}
 
+    # ---- the same steps again with the kernel timer on: per-launch durations of the LM-head,
+    # attention and self-conditioning kernels (CUDA events on the launching stream)
+    tsteps = steps if timer_steps is None else timer_steps
+    dgc.dg_kernel_timer_enable(True)
+    for i in range(tsteps):
+        step(warmup + steps + i)
+    torch.cuda.synchronize()
+    vocab_ms, vocab_n = dgc.dg_kernel_timer_read(0)
+    attn_ms, attn_n = dgc.dg_kernel_timer_read(1)
+    sc_ms, sc_n = dgc.dg_kernel_timer_read(2)
+    dgc.dg_kernel_timer_enable(False)
+    dgc.dg_workspace_status(ws)
     hbm, tf_burst, tf_sust, peak_kind = peaks()
     flops_per_launch = 2.0 * B * w.L * w.d * w.V
     vocab_avg_s = vocab_ms / max(vocab_n, 1) / 1000.0
