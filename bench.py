@@ -323,32 +323,55 @@ def measure_denoise(w, dev, steps, warmup, *, rank=0, world=1, dist=None, sc=0, 
 
     # ---- end to end through the public API with host buffers: the prefix KV of the step's
     # requests (and the clean canvases and keep thresholds of the noising leg) go host ->
-    # device; the final canvases, their step counts (and the noised canvases) come back.
+    # device; the final canvases, their step counts (and the noised canvases) come back.  The
+    # inputs are double-buffered on the device: a copy stream brings step i + 1's inputs while
+    # step i computes (every copy is inside the timed region; a step starts only once its own
+    # inputs have landed, and a buffer is refilled only after the step that read it is done).
     if e2e:
         kp_h = kp.cpu().pin_memory()
         vp_h = vp.cpu().pin_memory()
         out_h = torch.empty((B, w.L), dtype=torch.int32).pin_memory()
         st_h = torch.empty(B, dtype=torch.int32).pin_memory()
-        kp_d, vp_d = torch.empty_like(kp), torch.empty_like(vp)
+        bufs = [(torch.empty_like(kp), torch.empty_like(vp)) for _ in range(2)]
         if noising:
             x0_hp, keep_hp = x0_h.pin_memory(), keep_h.pin_memory()
-            x0_dd, keep_dd = torch.empty_like(x0_d), torch.empty_like(keep_d)
+            nbufs = [(torch.empty_like(x0_d), torch.empty_like(keep_d)) for _ in range(2)]
             xt_h = torch.empty_like(x0_h).pin_memory()
+        copy_stream = torch.cuda.Stream(dev)
+        landed = [torch.cuda.Event() for _ in range(2)]
+        consumed = [torch.cuda.Event() for _ in range(2)]
 
-        def e2e_step(i):
-            kp_d.copy_(kp_h, non_blocking=True)
-            vp_d.copy_(vp_h, non_blocking=True)
-            if noising:
-                x0_dd.copy_(x0_hp, non_blocking=True)
-                keep_dd.copy_(keep_hp, non_blocking=True)
-            step(7777 + i, kp_d, vp_d, x0_dd if noising else None, keep_dd if noising else None)
-            out_h.copy_(canvas, non_blocking=True)
-            st_h.copy_(steps_taken, non_blocking=True)
-            if noising:
-                xt_h.copy_(xt_d, non_blocking=True)
+        def issue_copy(i):  # step i's inputs into buffer i % 2, on the copy stream
+            k = i % 2
+            with torch.cuda.stream(copy_stream):
+                if i >= 2:
+                    copy_stream.wait_event(consumed[k])
+                bufs[k][0].copy_(kp_h, non_blocking=True)
+                bufs[k][1].copy_(vp_h, non_blocking=True)
+                if noising:
+                    nbufs[k][0].copy_(x0_hp, non_blocking=True)
+                    nbufs[k][1].copy_(keep_hp, non_blocking=True)
+                landed[k].record(copy_stream)
 
-        for i in range(min(warmup, 3)):
-            e2e_step(i)
+        def e2e_run(n, first):
+            copy_stream.wait_event(first)  # no copy before the region starts
+            issue_copy(0)
+            for i in range(n):
+                if i + 1 < n:
+                    issue_copy(i + 1)
+                k = i % 2
+                stream.wait_event(landed[k])
+                step(7777 + i, bufs[k][0], bufs[k][1], nbufs[k][0] if noising else None,
+                     nbufs[k][1] if noising else None)
+                consumed[k].record(stream)
+                out_h.copy_(canvas, non_blocking=True)
+                st_h.copy_(steps_taken, non_blocking=True)
+                if noising:
+                    xt_h.copy_(xt_d, non_blocking=True)
+
+        w0 = torch.cuda.Event()
+        w0.record(stream)
+        e2e_run(min(warmup, 3), w0)
         torch.cuda.synchronize()
         e2e_clocks = ClockSampler(int(str(dev).split(":")[-1]) if ":" in str(dev) else 0)
         e2e_clocks.start()
@@ -356,8 +379,7 @@ def measure_denoise(w, dev, steps, warmup, *, rank=0, world=1, dist=None, sc=0, 
             dist.barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for i in range(steps):
-            e2e_step(i)
+        e2e_run(steps, e0)
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_clk = e2e_clocks.stop()

@@ -331,15 +331,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pk[kKTile / 2];
         float f = 1.f;
         bool need = false;
-        auto exp_tile = [&](float m_use) {
+        auto exp_tile = [&](float m_use) {  // two scores per packed fp32 instruction
 #pragma unroll
           for (int q = 0; q < 8; ++q) ps[q] = 0.f;
 #pragma unroll
           for (int e = 0; e < kKTile; e += 2) {
-            const float a = ex2_approx(fmaf(sv[e], c, -m_use));
-            const float bb = ex2_approx(fmaf(sv[e + 1], c, -m_use));
-            ps[e & 7] += a;
-            ps[(e + 1) & 7] += bb;
+            float xa, xb;
+            ffma2(xa, xb, sv[e], sv[e + 1], c, c, -m_use, -m_use);
+            const float a = ex2_approx(xa);
+            const float bb = ex2_approx(xb);
+            const int q = (e >> 1) & 3;
+            fadd2(ps[2 * q], ps[2 * q + 1], ps[2 * q], ps[2 * q + 1], a, bb);
             pk[e >> 1] = pack_bf16x2(a, bb);
           }
           return ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
@@ -707,11 +709,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int q = 0; q < 8; ++q) ps[q] = 0.f;
       uint32_t pk[32];
 #pragma unroll
-      for (int e = 0; e < 64; e += 2) {
-        const float a = ex2_approx(fmaf(sv[e], c, -m_use));
-        const float bb = ex2_approx(fmaf(sv[e + 1], c, -m_use));
-        ps[e & 7] += a;
-        ps[(e + 1) & 7] += bb;
+      for (int e = 0; e < 64; e += 2) {  // two scores per packed fp32 instruction
+        float xa, xb;
+        ffma2(xa, xb, sv[e], sv[e + 1], c, c, -m_use, -m_use);
+        const float a = ex2_approx(xa);
+        const float bb = ex2_approx(xb);
+        const int q = (e >> 1) & 3;
+        fadd2(ps[2 * q], ps[2 * q + 1], ps[2 * q], ps[2 * q + 1], a, bb);
         pk[e >> 1] = pack_bf16x2(a, bb);
       }
       // P of this half: columns half * 32 .. + 32 (the other half's raw scores there were

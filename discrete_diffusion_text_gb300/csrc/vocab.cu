@@ -91,6 +91,13 @@ struct RowState {
   float best_z;  // and its tempered logit
 };
 
+// Three-operand maximum (one instruction for two new elements of a running max).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ float open_unit(uint32_t u) {
   // W = (u + 1/2) / 2^32, rounded to fp32 (full relative precision near 0)
   return fmaf(__uint2float_rn(u), 2.3283064365386963e-10f, 1.1641532182693481e-10f);
@@ -146,7 +153,7 @@ __device__ __forceinline__ void process_chunk(RowState& st, const float (&z)[32]
                                               float* sc_mdst, float bar, uint32_t* bar_ptr) {
   float mx[4] = {z[0], z[1], z[2], z[3]};  // four partial maxima: short dependency chains
 #pragma unroll
-  for (int e = 4; e < 32; ++e) mx[e & 3] = fmaxf(mx[e & 3], z[e]);
+  for (int e = 4; e < 32; e += 2) mx[(e >> 1) & 3] = fmax3(mx[(e >> 1) & 3], z[e], z[e + 1]);
   const float cmr = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
   const float cm = cmr * inv_tau;
   // strictly greater: an equal value seen earlier (a lower index) keeps the top-1; within the
@@ -170,18 +177,19 @@ __device__ __forceinline__ void process_chunk(RowState& st, const float (&z)[32]
   float pt[4] = {0.f, 0.f, 0.f, 0.f};  // and of exp(z~ - m) (z~ - m) log2(e)
   if (kSC && sc_mdst) *sc_mdst = st.m;
   uint32_t pk[4];
-  float prev = 0.f;
 #pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    const float a = fmaf(z[e], scale, -mlog2);
-    const float pe = ex2_approx(a);
-    ps[e & 3] += pe;
-    if (kEnt) pt[e & 3] = fmaf(pe, a, pt[e & 3]);
+  for (int e = 0; e < 32; e += 2) {  // two logits per packed fp32 instruction
+    float a0, a1;
+    ffma2(a0, a1, z[e], z[e + 1], scale, scale, -mlog2, -mlog2);
+    const float p0 = ex2_approx(a0);
+    const float p1 = ex2_approx(a1);
+    const int q = (e >> 1) & 1;
+    fadd2(ps[2 * q], ps[2 * q + 1], ps[2 * q], ps[2 * q + 1], p0, p1);
+    if (kEnt) ffma2(pt[2 * q], pt[2 * q + 1], p0, p1, a0, a1, pt[2 * q], pt[2 * q + 1]);
     if (kSC) {  // eight values (16 bytes) per store
-      if (e & 1) pk[(e >> 1) & 3] = pack_bf16x2(prev, pe);
-      prev = pe;
-      if ((e & 7) == 7 && sc_dst)
-        *reinterpret_cast<uint4*>(sc_dst + (e - 7)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      pk[(e >> 1) & 3] = pack_bf16x2(p0, p1);
+      if ((e & 7) == 6 && sc_dst)
+        *reinterpret_cast<uint4*>(sc_dst + (e - 6)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
     }
   }
   const float sc = (ps[0] + ps[1]) + (ps[2] + ps[3]);
