@@ -100,6 +100,7 @@ def _posterior_with_entropy(dgc, y, E, B, L, inv_tau, seed, step):
     (1, 256, 4096, 256, 0.05, 1.25),    # near-uniform: entropy ~ log V
     (3, 192, 4096, 256, 1.0, 50.0),     # sharp posteriors: entropy ~ 0
     (2, 128, 8192, 512, 0.5, 2.5),      # in between
+    (16, 256, 4096, 256, 0.5, 2.5),     # 32 row tiles: the multicast LM-head pass
 ])
 def test_posterior_entropy_matches_oracle(dgc, B, L, V, d, ystd, inv_tau):
     E = synth.normal_bf16((V, d), 0.02 if ystd < 0.5 else 0.1, 51).to(DEV)

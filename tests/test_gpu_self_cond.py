@@ -77,10 +77,28 @@ def _check_ffw(s_gpu, e_gpu, W1, W2):
     assert (s_gpu == s).mean() > 0.9
 
 
+def _check_s_end_to_end(s_gpu, y, E, W1, W2, inv_tau):
+    """s against the oracle's own s = bf16(bf16(gelu(bf16(e) W1^T)) W2^T): the GPU's e is
+    within the _check_e bound of the exact e and the oracle rounds e once more (u |e|); that
+    difference passes through |W1|, the GELU's slope (at most 1.13 for the tanh form; 1.15
+    used), a bf16 rounding of u on each side (2u |u|), |W2| and a rounding of s (2u |s|)."""
+    y64, E64, W1_64, W2_64 = f64(y), f64(E), f64(W1), f64(W2)
+    ref = O.self_condition(y64, E64, inv_tau, W1_64, W2_64)
+    z = y64 @ E64.T * inv_tau
+    p = np.exp(z - z.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    de = 2 * U * (p @ np.abs(E64)) + 2 * U * np.abs(ref["e_exact"]) + 1e-7
+    du = 1.15 * (de @ np.abs(W1_64).T) + 2 * U * np.abs(ref["u"]) + 1e-7
+    bound = du @ np.abs(W2_64).T + 2 * U * np.abs(ref["s"]) + 1e-7
+    err = np.abs(s_gpu - ref["s"])
+    assert np.all(err <= bound), float((err / bound).max())
+
+
 @pytest.mark.parametrize("B,L,V,d,dsc,ystd,inv_tau", [
     (2, 128, 4096, 256, 128, 0.05, 1.0),    # near-uniform posterior
     (1, 256, 8192, 512, 192, 1.0, 2.0),     # sharp posterior
     (3, 64, 4096, 256, 64, 0.5, 1.25),      # in between, three canvases
+    (8, 256, 4096, 256, 128, 0.5, 1.25),    # 16 row tiles: the multicast LM-head pass
 ])
 def test_self_condition_matches_oracle(dgc, B, L, V, d, dsc, ystd, inv_tau):
     E = synth.normal_bf16((V, d), 0.1, 81)
@@ -90,6 +108,7 @@ def test_self_condition_matches_oracle(dgc, B, L, V, d, dsc, ystd, inv_tau):
     e_gpu, s_gpu = _run_sc(dgc, y, E, W1, W2, B, L, inv_tau)
     _check_e(e_gpu, y, E, inv_tau)
     _check_ffw(s_gpu, e_gpu, W1, W2)
+    _check_s_end_to_end(s_gpu, y, E, W1, W2, inv_tau)
 
 
 @pytest.mark.parametrize("B", [1, 2])
