@@ -678,10 +678,11 @@ cudaError_t launch_vocab_pass(const uint16_t* y, const uint16_t* W, int R, int L
   // cross-entropy mode (targets, or the self-conditioning pass alone: no sampling), or
   // sampling with or without the entropy accumulator; each with or without the
   // self-conditioning store.  Split rings when the pass is a single wave (one unit per CTA:
-  // one canvas) and its epilogue is light: measured at one canvas, cross-entropy 0.1998 ->
-  // 0.1922 ms and the self-conditioning store 0.269 -> 0.256 ms, but sampling unchanged and
-  // the entropy accumulator slower (the extra TMA warp takes issue slots from the heavier
-  // epilogues); with several waves the unified ring is faster (-7 % at 16 canvases).
+  // one canvas), except with the entropy accumulator: measured at one canvas, cross-entropy
+  // 0.1998 -> 0.1922 ms, the self-conditioning store 0.269 -> 0.256 ms, sampling 0.2112 ->
+  // 0.2098 ms (once its epilogue became light), but the entropy accumulator's loop 0.7 %
+  // slower (the extra TMA warp takes issue slots from the heavier epilogue); with several
+  // waves the unified ring is faster (-7 % at 16 canvases).
   const bool sc = sc_p != nullptr;
   const bool ce = targets != nullptr || ce_only;
   if (!ce) {  // every sampling launch starts with no bar published
@@ -695,7 +696,7 @@ cudaError_t launch_vocab_pass(const uint16_t* y, const uint16_t* W, int R, int L
   // power cap: halving the W reads from L2 lowers its power, and the clock rises more than the
   // clusters' lockstep costs (measured: 64 canvases +3.7 % throughput at 1,725 against 1,627 MHz,
   // 16 canvases +3.0 %); at one canvas (not power-bound) it was 0.7 % slower.
-  const bool split = pl.units <= pl.grid && (ce || sc);
+  const bool split = pl.units <= pl.grid && (ce || sc || !entropy);
   const bool mc = !split && max_pairs > 0 && pl.num_mt % 2 == 0 && pl.num_mt >= kManyRowTiles;
   timer_begin(0, st);
   cudaError_t e;
