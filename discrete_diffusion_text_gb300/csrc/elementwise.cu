@@ -224,31 +224,33 @@ __global__ void __launch_bounds__(kFinRows * 32) vocab_finalize_kernel(FinalizeP
   if (threadIdx.x == 0) finalize_ticket(p, row / p.L, unlocked, p.L / kFinRows);
 }
 
-// The previous step's finalisation fused with this step's embedding gather: one CTA per
-// position; warp 0 finalises the position (as above), then the CTA gathers E at its new token.
-__global__ void __launch_bounds__(256) embed_finalize_kernel(FinalizeParams p,
-                                                             const uint4* __restrict__ E,
-                                                             uint4* __restrict__ h, int V,
-                                                             int d16) {
+// The previous step's finalisation fused with this step's embedding gather: eight positions
+// per CTA (one warp each finalises its position, as above), then the CTA gathers E at the eight
+// new tokens, 16 bytes per thread.
+__global__ void __launch_bounds__(kFinRows * 32) embed_finalize_kernel(FinalizeParams p,
+                                                                       const uint4* __restrict__ E,
+                                                                       uint4* __restrict__ h, int V,
+                                                                       int d16) {
   pdl_wait();
   pdl_trigger();
   if (p.n_active && *p.n_active == 0) return;
-  const int row = blockIdx.x;
-  __shared__ int32_t s_token;
-  if (threadIdx.x < 32) {
-    const RowFinal r = finalize_row(p, row, threadIdx.x);
-    if (threadIdx.x == 0) {
-      s_token = r.token;
-      finalize_ticket(p, row / p.L, r.locked_after ? 0 : 1, p.L);
-    }
-  }
-  __syncthreads();
-  const int id = s_token;
-  const bool ok = id >= 0 && id < V;
-  if (!ok && threadIdx.x == 0) atomicOr(p.status, kStatusBadIndex);
-  for (int c = threadIdx.x; c < d16; c += blockDim.x)
-    h[static_cast<int64_t>(row) * d16 + c] =
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int row0 = blockIdx.x * kFinRows;  // L is a multiple of kFinRows
+  __shared__ int32_t s_token[kFinRows];
+  const RowFinal r = finalize_row(p, row0 + warp, lane);
+  if (lane == 0) s_token[warp] = r.token;
+  const int unlocked = __syncthreads_count(lane == 0 && !r.locked_after ? 1 : 0);
+  if (threadIdx.x == 0) finalize_ticket(p, row0 / p.L, unlocked, p.L / kFinRows);
+  for (int q = threadIdx.x; q < kFinRows * d16; q += blockDim.x) {
+    const int rr = q / d16;
+    const int c = q - rr * d16;
+    const int id = s_token[rr];
+    const bool ok = id >= 0 && id < V;
+    if (!ok && c == 0) atomicOr(p.status, kStatusBadIndex);
+    h[static_cast<int64_t>(row0 + rr) * d16 + c] =
         ok ? E[static_cast<int64_t>(id) * d16 + c] : make_uint4(0, 0, 0, 0);
+  }
 }
 
 // Entropy-bounded step [TR "DiffusionGemma 샘플러"]: one CTA per canvas, one thread per
@@ -347,9 +349,8 @@ void launch_embed_finalize(const FinalizeParams& p0, int B, const uint16_t* E, u
   FinalizeParams p = p0;
   p.status = status_or_fallback(p.status);
   const int d16 = d / 8;
-  const int threads = d16 < 256 ? ((d16 + 31) / 32) * 32 : 256;
   timer_begin(4, st);
-  launch_dependent(embed_finalize_kernel, dim3(B * p.L), dim3(threads), 0, st, p,
+  launch_dependent(embed_finalize_kernel, dim3(B * p.L / kFinRows), dim3(kFinRows * 32), 0, st, p,
                    reinterpret_cast<const uint4*>(E), reinterpret_cast<uint4*>(h), V, d16);
   timer_end(4, st);
 }
