@@ -28,6 +28,10 @@
 // combines them with the log-sum-exp rule.
 // A second kernel (canvas_attn1_kernel, below) takes one query head per CTA with 128-key
 // tiles; plan_attention picks it where the K/V work is short (see there).
+#include <array>
+#include <mutex>
+#include <vector>
+
 #include "kernels.cuh"
 #include "sm103.cuh"
 
@@ -56,6 +60,7 @@ struct AttnParams {
   uint32_t* status;
   const int* n_active;
   uint64_t wait_ns;  // limit of every on-chip wait
+  int cluster_merge;  // one-slot kernel: the key splits of a unit form a cluster and merge there
 };
 
 template <int HD>
@@ -478,7 +483,108 @@ struct Attn1Layout {
   static constexpr int kBarOff = kLOff + kQTile * 4;
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory");
+  // Cluster merge, in the idle K/V ring: the rows this CTA merges, as received from every
+  // split, [split][row][kPitch] fp32 (O unnormalised; the padded pitch puts a warp's 32 rows
+  // on distinct banks), and each received row's (reference max, sum) [split][row].  A CTA
+  // merges at most ceil(128 / S) rows, so S splits need at most 128 + S row slots.
+  static constexpr int kPitch = HD + 4;  // floats
+  static constexpr int kStageOff = kKVOff;
+  static constexpr int kMLOff = kStageOff + (kQTile + 8) * kPitch * 4;
+  static_assert(kMLOff + (kQTile + 8) * 8 <= kKVOff + kRing * kKVBytes, "merge staging");
 };
+
+// The split-KV merge inside a cluster (the splits of one unit, cluster rank = split).  CTA q
+// merges rows [q 128 / S, (q + 1) 128 / S) of the query tile.  Three steps, every thread of
+// every CTA taking part in the two cluster barriers:
+//   1. barrier: every CTA of the cluster is past its main loop, so every K/V ring is idle;
+//   2. each CTA stores every row of its partial (O unnormalised; the row's reference max m and
+//      sum l, base 2) into the ring of the CTA that merges the row (remote stores, no round
+//      trip); barrier: all rows have arrived;
+//   3. each CTA combines its rows from its own shared memory in rank order (the same order for
+//      every row): O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s, M = max_s m_s.  No CTA
+//      touches another's shared memory after the second barrier.
+__device__ __forceinline__ int merge_owner(int row, int S) { return ((row + 1) * S - 1) / kQTile; }
+
+// One softmax thread's half row (HD / 2 columns at column half * HD / 2) of its partial into
+// the merging CTA's receive slot; the half-0 thread also sends (m, l).
+template <int HD>
+__device__ __forceinline__ void attn1_push(uint8_t* smem, int S, int split, int row, int half,
+                                           const float* o, float m, float l) {
+  using Lay = Attn1Layout<HD>;
+  const int q = merge_owner(row, S);
+  const int rpo = (kQTile + S - 1) / S;  // row slots per split
+  const int slot = split * rpo + (row - q * kQTile / S);
+  const uint32_t dst = dsmem_addr(
+      smem_u32(smem + Lay::kStageOff) + (slot * Lay::kPitch + half * (HD / 2)) * 4, q);
+#pragma unroll
+  for (int c = 0; c < HD / 2; c += 4)
+    st_dsmem_f4(dst + c * 4, make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]));
+  if (half == 0) st_dsmem_f2(dsmem_addr(smem_u32(smem + Lay::kMLOff) + slot * 8, q),
+                             make_float2(m, l));
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  __syncwarp();  // the cluster barrier is warp-aligned
+  cluster_arrive();
+  cluster_wait();
+}
+
+// Step 3 (with the second barrier); called by every thread of the CTA once its softmax
+// threads have pushed their rows.
+template <int HD>
+__device__ __forceinline__ void attn1_cluster_merge(const AttnParams& p, uint8_t* smem, int b,
+                                                    int hq, int qt) {
+  using Lay = Attn1Layout<HD>;
+  constexpr int kCG = HD / 16;  // 16-column groups of a row
+  cluster_sync_all();  // every CTA's rows are in their merging CTAs
+  const int S = p.splits;
+  const int q = static_cast<int>(cluster_ctarank());
+  const int r0 = q * kQTile / S, r1 = (q + 1) * kQTile / S;
+  const int rpo = (kQTile + S - 1) / S;
+  const float* stage = reinterpret_cast<const float*>(smem + Lay::kStageOff);
+  const float2* mls = reinterpret_cast<const float2*>(smem + Lay::kMLOff);
+  for (int i = static_cast<int>(threadIdx.x) - 128; i >= 0 && i < (r1 - r0) * kCG; i += 256) {
+    const int lr = i / kCG;
+    const int cg = i % kCG;
+    float M = -INFINITY;
+    for (int s = 0; s < S; ++s) M = fmaxf(M, mls[s * rpo + lr].x);
+    float L = 0.f;
+    float acc[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+    for (int s = 0; s < S; ++s) {
+      const float2 ml = mls[s * rpo + lr];
+      if (ml.x == -INFINITY) continue;  // an empty partial (or one given up) adds nothing
+      const float w = ex2_approx(ml.x - M);
+      L += w * ml.y;
+      const float4* src =
+          reinterpret_cast<const float4*>(stage + (s * rpo + lr) * Lay::kPitch + cg * 16);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float4 v = src[k];
+        acc[4 * k] += w * v.x;
+        acc[4 * k + 1] += w * v.y;
+        acc[4 * k + 2] += w * v.z;
+        acc[4 * k + 3] += w * v.w;
+      }
+    }
+    const int qi = qt * kQTile + r0 + lr;
+    if (qi < p.L) {
+      const float inv_l = 1.f / L;
+      uint4* dst = reinterpret_cast<uint4*>(
+          p.out + ((static_cast<int64_t>(b) * p.L + qi) * p.H + hq) * HD + cg * 16);
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+        dst[k] = make_uint4(pack_bf16x2(acc[8 * k + 0] * inv_l, acc[8 * k + 1] * inv_l),
+                            pack_bf16x2(acc[8 * k + 2] * inv_l, acc[8 * k + 3] * inv_l),
+                            pack_bf16x2(acc[8 * k + 4] * inv_l, acc[8 * k + 5] * inv_l),
+                            pack_bf16x2(acc[8 * k + 6] * inv_l, acc[8 * k + 7] * inv_l));
+      if (cg == 0 && p.lse)
+        p.lse[(static_cast<int64_t>(b) * p.H + hq) * p.L + qi] =
+            (M + __log2f(L)) * 0.6931471805599453f;
+    }
+  }
+}
 
 __device__ __forceinline__ void attn1_unit(int u, const AttnParams& p, int& b, int& h, int& qt) {
   qt = u % p.n_qtiles;
@@ -539,6 +645,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t part_rows = static_cast<int64_t>(p.B) * p.H * p.L;
 
   if (nt == 0) {  // nothing to do: empty partials (only when splits > 1)
+    if (p.cluster_merge) {  // an empty partial for the cluster's merge, which every CTA joins
+      cluster_sync_all();  // every ring of the cluster is idle
+      if (warp >= 4) {
+        float o[HD / 2];
+        for (int c = 0; c < HD / 2; ++c) o[c] = 0.f;
+        attn1_push<HD>(smem, p.splits, split, row_in, half, o, -INFINITY, 0.f);
+      }
+      attn1_cluster_merge<HD>(p, smem, b, hq, qt);
+      return;
+    }
     if (warp >= 4 && qi < p.L) {
       if (half == 0) {
         float* ml = p.part_ml + (split * part_rows + out_row) * 2;
@@ -772,6 +888,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (write && half == 0 && p.lse)
         p.lse[out_row] = (m_ref + __log2f(l_row)) * 0.6931471805599453f;
+    } else if (p.cluster_merge) {
+      // this row's partial into the CTA that merges it, once every CTA of the cluster is past
+      // its main loop (the control warps take the same barrier in the common tail); a CTA
+      // that gave up waiting contributes nothing
+      float o[HD / 2];
+#pragma unroll
+      for (int cc = 0; cc < HD / 64; ++cc) {
+        float t[32];
+        tmem_ld32(tm_o + lane_base + half * (HD / 2) + cc * 32, t);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[cc * 32 + e] = ok ? t[e] : 0.f;
+      }
+      cluster_sync_all();  // every ring of the cluster is idle
+      attn1_push<HD>(smem, p.splits, split, row_in, half, o, ok ? m_ref : -INFINITY,
+                     ok ? l_row : 0.f);
     } else {
       const int64_t prow = split * part_rows + out_row;
       float* po = p.part_o + prow * HD + half * (HD / 2);
@@ -793,6 +924,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  if (p.cluster_merge) {
+    if (warp < 4) cluster_sync_all();  // the softmax warps took this barrier before their pushes
+    attn1_cluster_merge<HD>(p, smem, b, hq, qt);
+  }
   pdl_trigger();
   tc_fence_before();
   __syncthreads();
@@ -853,8 +988,47 @@ __global__ void attn_merge_kernel(AttnParams p) {
   if (p.lse && lane == 0) p.lse[row] = (M + __log2f(l)) * 0.6931471805599453f;
 }
 
+// How many clusters of S one-slot CTAs (cluster along the key splits) can be resident at once
+// on this device (0: none); asked once per device and S.
 template <int HD>
-cudaError_t launch_hd(const CUtensorMap* maps, const AttnParams& p, bool one, cudaStream_t st) {
+int attn1_max_clusters(int S) {
+  static std::mutex mu;
+  static std::vector<std::array<int, 9>> known;  // per device and S: -1 unknown
+  const int dev = device_id();
+  std::lock_guard<std::mutex> lk(mu);
+  while (static_cast<int>(known.size()) <= dev) {
+    std::array<int, 9> a;
+    a.fill(-1);
+    known.push_back(a);
+  }
+  int& n = known[dev][S];
+  if (n < 0) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(1, S, 1);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Attn1Layout<HD>::kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = S;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int c = 0;
+    if (cudaFuncSetAttribute(canvas_attn1_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Attn1Layout<HD>::kSmemBytes) != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&c, canvas_attn1_kernel<HD>, &cfg) != cudaSuccess) {
+      cudaGetLastError();  // clear the query's error: the launch then uses the merge kernel
+      c = 0;
+    }
+    n = c;
+  }
+  return n;
+}
+
+template <int HD>
+cudaError_t launch_hd(const CUtensorMap* maps, const AttnParams& p_in, bool one,
+                      cudaStream_t st) {
   using Lay = AttnLayout<HD>;
   using Lay1 = Attn1Layout<HD>;
   static int configured_device = -1;
@@ -878,15 +1052,40 @@ cudaError_t launch_hd(const CUtensorMap* maps, const AttnParams& p, bool one, cu
     }
     configured_device = dev;
   }
+  // One-slot kernel with 2..8 key splits: the splits of a unit run as one cluster and merge
+  // in it, when every cluster of the launch can be resident at once; otherwise the split
+  // partials go through the workspace to attn_merge_kernel.
+  AttnParams p = p_in;
+  p.cluster_merge = one && p.splits >= 2 && p.splits <= 8 &&
+                    attn1_max_clusters<HD>(p.splits) >= p.units;
   dim3 grid(p.units, p.splits);
   timer_begin(1, st);
-  cudaError_t e =
-      one ? launch_dependent(canvas_attn1_kernel<HD>, grid, dim3(kThreads), Lay1::kSmemBytes, st,
-                             maps[0], maps[1], maps[2], maps[3], maps[4], p)
-          : launch_dependent(canvas_attn_kernel<HD>, grid, dim3(kThreads), Lay::kSmemBytes, st,
-                             maps[0], maps[1], maps[2], maps[3], maps[4], p);
+  cudaError_t e;
+  if (p.cluster_merge) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Lay1::kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = p.splits;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    e = cudaLaunchKernelEx(&cfg, canvas_attn1_kernel<HD>, maps[0], maps[1], maps[2], maps[3],
+                           maps[4], p);
+  } else {
+    e = one ? launch_dependent(canvas_attn1_kernel<HD>, grid, dim3(kThreads), Lay1::kSmemBytes,
+                               st, maps[0], maps[1], maps[2], maps[3], maps[4], p)
+            : launch_dependent(canvas_attn_kernel<HD>, grid, dim3(kThreads), Lay::kSmemBytes, st,
+                               maps[0], maps[1], maps[2], maps[3], maps[4], p);
+  }
   if (e != cudaSuccess) return e;
-  if (p.splits > 1) {
+  if (p.splits > 1 && !p.cluster_merge) {
     const int64_t rows = static_cast<int64_t>(p.B) * p.H * p.L;
     const int warps_per_block = 8;
     e = launch_dependent(attn_merge_kernel<HD>,
@@ -997,6 +1196,7 @@ cudaError_t launch_attention(const uint16_t* q, const uint16_t* k_pre, const uin
   p.status = status;
   p.n_active = n_active;
   p.wait_ns = wait_limit_ns();
+  p.cluster_merge = 0;
   return hd == 64 ? launch_hd<64>(maps, p, pl.one != 0, st)
                   : launch_hd<128>(maps, p, pl.one != 0, st);
 }

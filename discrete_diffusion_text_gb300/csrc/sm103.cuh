@@ -147,6 +147,25 @@ __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Distributed shared memory: the address, in the shared memory of CTA `rank` of this cluster,
+// of this CTA's shared-memory address `addr` (every CTA of the kernel has the same layout).
+__device__ __forceinline__ uint32_t dsmem_addr(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// Stores into another CTA's shared memory (no round trip: ordered for the reader by the next
+// cluster barrier's release / acquire).
+__device__ __forceinline__ void st_dsmem_f2(uint32_t addr, float2 v) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y)
+               : "memory");
+}
+__device__ __forceinline__ void st_dsmem_f4(uint32_t addr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x),
+               "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
+}
+
 // ----------------------------------------------------------------------------- TMA -----
 
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
