@@ -127,6 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kRing = Lay::kRing;
   pdl_wait();
   if (p.n_active && *p.n_active == 0) return;
+  pdl_trigger();  // the next kernel's CTAs may start their own prologue on idle SMs
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -442,8 +443,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  // this CTA's work is done: the next kernel in the stream may be scheduled
-  pdl_trigger();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -601,8 +600,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap tmVc, AttnParams p) {
   using Lay = Attn1Layout<HD>;
   constexpr int kRing = Lay::kRing;
-  pdl_wait();
-  if (p.n_active && *p.n_active == 0) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -643,6 +640,47 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int qi = qt * kQTile + row_in;
   const int64_t out_row = (static_cast<int64_t>(b) * p.H + hq) * p.L + qi;  // (b, h, i)
   const int64_t part_rows = static_cast<int64_t>(p.B) * p.H * p.L;
+  uint8_t* q_buf = smem + Lay::kQOff;
+  auto kv_buf = [&](int i) { return smem + Lay::kKVOff + (i % kRing) * Lay::kKVBytes; };
+
+  // Before the wait for the previous kernel: the barriers, and the prefix K/V tiles of the
+  // first ring slots (the cache, which the kernels of a denoising step do not write); thread
+  // 0 is the producer.
+  int n_early = 0;
+  if (threadIdx.x == 0 && nt > 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);  // K slots: the score thread; V slots: the P.V thread
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&p_full[s], 8);  // one arrival per softmax warp
+      mbar_init(&pv_done[s], 1);
+      mbar_init(&drain[s], 1);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_map(&tmKp);
+    tma_prefetch_map(&tmVp);
+    for (int i = 0; i < 2 * nt && i < kRing; ++i) {
+      const int t = t_begin + (i >> 1);
+      if (t >= n_pre) break;
+      const CUtensorMap* m = (i & 1) ? &tmVp : &tmKp;
+      mbar_arrive_expect_tx(&kv_full[i], Lay::kKVBytes);
+      for (int c = 0; c < HD / 64; ++c)
+        tma_load_4d(kv_buf(i) + c * Lay::kKVChunk, m, &kv_full[i], c * 64, g, (t_lo + t) * kKT1,
+                    b);
+      ++n_early;
+    }
+  }
+  pdl_wait();
+  if (p.n_active && *p.n_active == 0) {  // the same for every CTA of the grid
+    if (threadIdx.x == 0)  // let the started copies land before the CTA leaves
+      for (int i = 0; i < n_early; ++i) mbar_wait_drain(&kv_full[i], 0);
+    return;
+  }
+  pdl_trigger();  // the next kernel's CTAs may start their own prologue on idle SMs
 
   if (nt == 0) {  // nothing to do: empty partials (only when splits > 1)
     if (p.cluster_merge) {  // an empty partial for the cluster's merge, which every CTA joins
@@ -667,21 +705,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
 
-  if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    for (int s = 0; s < kRing; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);  // K slots: the score thread; V slots: the P.V thread
-    }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&s_full[s], 1);
-      mbar_init(&p_full[s], 8);  // one arrival per softmax warp
-      mbar_init(&pv_done[s], 1);
-      mbar_init(&drain[s], 1);
-    }
-    *abort_flag = 0;
-    fence_barrier_init();
-  }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
@@ -692,8 +715,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   auto tm_s = [&](int bf) { return tmem + bf * kKT1; };
   const uint32_t tm_o = tmem + 2 * kKT1;
-  uint8_t* q_buf = smem + Lay::kQOff;
-  auto kv_buf = [&](int i) { return smem + Lay::kKVOff + (i % kRing) * Lay::kKVBytes; };
 
   if (warp < 4) {
     regs_decrease<kRegsControl>();
@@ -705,6 +726,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_4d(q_buf + c * Lay::kQChunk, &tmQ, q_full, c * 64, hq, qt * kQTile, b);
       int issued = 0;
       for (int i = 0; i < 2 * nt; ++i) {
+        if (i < n_early) {  // requested before the wait
+          ++issued;
+          continue;
+        }
         const int rs = i % kRing;
         if (!mbar_wait(&kv_empty[rs], ((i / kRing) & 1) ^ 1, abort_flag, p.wait_ns)) break;
         const int t = t_begin + (i >> 1);
@@ -928,7 +953,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp < 4) cluster_sync_all();  // the softmax warps took this barrier before their pushes
     attn1_cluster_merge<HD>(p, smem, b, hq, qt);
   }
-  pdl_trigger();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

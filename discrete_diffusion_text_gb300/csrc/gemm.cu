@@ -71,22 +71,44 @@ __device__ __forceinline__ SegDst segment_of(const GemmOut& out, int col) {
   return d;
 }
 
-// Producer (one thread): k-blocks kb0 .. kb0 + nk - 1 of A rows m0.. and W rows n0.. into the
-// ring.  After an abort it waits (briefly) for the copies already in flight to land.
+// Producer (one thread), before the previous kernel's writes are visible: the W halves (the
+// weights, which no kernel of the stream writes) of the first stages, each stage's barrier
+// armed for the whole stage.  Returns the number of stages started.
 template <int BN>
-__device__ __forceinline__ void gemm_produce(const CUtensorMap* tmA, const CUtensorMap* tmB,
-                                             uint8_t* smem, uint64_t* full, uint64_t* empty,
-                                             int kb0, int nk, int m0, int n0,
-                                             volatile int* abort_flag, uint64_t wait_ns) {
+__device__ __forceinline__ int gemm_prefetch_w(const CUtensorMap* tmA, const CUtensorMap* tmB,
+                                               uint8_t* smem, uint64_t* full, int kb0, int nk,
+                                               int n0) {
   using Lay = GemmLayout<BN>;
   tma_prefetch_map(tmA);
   tma_prefetch_map(tmB);
+  const int n = nk < Lay::kStages ? nk : Lay::kStages;
+  for (int i = 0; i < n; ++i) {
+    mbar_arrive_expect_tx(&full[i], Lay::kStageBytes);
+    tma_load_2d(smem + i * Lay::kStageBytes + Lay::kABytes, tmB, &full[i], (kb0 + i) * kBK, n0);
+  }
+  return n;
+}
+
+// Producer (one thread): k-blocks kb0 .. kb0 + nk - 1 of A rows m0.. and W rows n0.. into the
+// ring; the first `pre` stages already hold their W copies (gemm_prefetch_w) and get A only.
+// After an abort it waits (briefly) for the copies already in flight to land.
+template <int BN>
+__device__ __forceinline__ void gemm_produce(const CUtensorMap* tmA, const CUtensorMap* tmB,
+                                             uint8_t* smem, uint64_t* full, uint64_t* empty,
+                                             int kb0, int nk, int m0, int n0, int pre,
+                                             volatile int* abort_flag, uint64_t wait_ns) {
+  using Lay = GemmLayout<BN>;
   int issued = 0;
   for (int i = 0; i < nk; ++i) {
     const int s = i % Lay::kStages;
     const uint32_t r = i / Lay::kStages;
-    if (!mbar_wait(&empty[s], (r & 1) ^ 1, abort_flag, wait_ns)) break;
     uint8_t* sa = smem + s * Lay::kStageBytes;
+    if (i < pre) {
+      tma_load_2d(sa, tmA, &full[s], (kb0 + i) * kBK, m0);
+      ++issued;
+      continue;
+    }
+    if (!mbar_wait(&empty[s], (r & 1) ^ 1, abort_flag, wait_ns)) break;
     mbar_arrive_expect_tx(&full[s], Lay::kStageBytes);
     tma_load_2d(sa, tmA, &full[s], (kb0 + i) * kBK, m0);
     tma_load_2d(sa + Lay::kABytes, tmB, &full[s], (kb0 + i) * kBK, n0);
@@ -140,10 +162,18 @@ __device__ __forceinline__ GemmSync gemm_sync_at(uint8_t* p) {
   return g;
 }
 
-template <int kStages>
-__device__ __forceinline__ void gemm_init(const GemmSync& g, int tmem_cols) {
+// The start of both GEMM kernels, up to the tensor-memory allocation: barriers initialised,
+// the weight copies of the first stages started, then the wait for the previous kernel in the
+// stream (everything before it touches no memory that kernel writes).  Returns false when the
+// denoising loop has no active canvas left: the CTA then only lets its weight copies land and
+// leaves (every thread returns).
+template <int BN>
+__device__ __forceinline__ bool gemm_start(const GemmSync& g, const CUtensorMap* tmA,
+                                           const CUtensorMap* tmB, uint8_t* smem, int kb0, int nk,
+                                           int m0, int n0, const int* n_active, int& pre) {
+  using Lay = GemmLayout<BN>;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < Lay::kStages; ++s) {
       mbar_init(&g.full[s], 1);
       mbar_init(&g.empty[s], 1);
     }
@@ -151,13 +181,27 @@ __device__ __forceinline__ void gemm_init(const GemmSync& g, int tmem_cols) {
     *g.abort_flag = 0;
     fence_barrier_init();
   }
+  __syncthreads();
+  pre = 0;
+  if (threadIdx.x == 0) pre = gemm_prefetch_w<BN>(tmA, tmB, smem, g.full, kb0, nk, n0);
+  pdl_wait();
+  if (n_active && *n_active == 0) {  // the same for every CTA of the grid
+    if (threadIdx.x == 0) {  // complete the started stages (A is readable), let them land
+      for (int i = 0; i < pre; ++i) {
+        tma_load_2d(smem + i * Lay::kStageBytes, tmA, &g.full[i], (kb0 + i) * kBK, m0);
+        mbar_wait_drain(&g.full[i], 0);
+      }
+    }
+    return false;
+  }
   if ((threadIdx.x >> 5) == 1) {
-    tmem_alloc(g.tmem_slot, tmem_cols);
+    tmem_alloc(g.tmem_slot, BN);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  return true;
 }
 
 template <int BN>
@@ -165,8 +209,6 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, GemmParams p) {
   using Lay = GemmLayout<BN>;
-  pdl_wait();
-  if (p.n_active && *p.n_active == 0) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -175,13 +217,15 @@ __global__ void __launch_bounds__(kThreadsG, 1)
   const int lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * BN;
   const int m0 = blockIdx.y * kBM;
-  gemm_init<Lay::kStages>(g, BN);
+  int pre;
+  if (!gemm_start<BN>(g, &tmA, &tmB, smem, 0, p.K / kBK, m0, n0, p.n_active, pre)) return;
+  pdl_trigger();  // the next kernel's CTAs may start their own prologue on idle SMs
   const uint32_t tmem = *g.tmem_slot;
 
   if (warp == 0) {
     if (lane == 0)
-      gemm_produce<BN>(&tmA, &tmB, smem, g.full, g.empty, 0, p.K / kBK, m0, n0, g.abort_flag,
-                       p.wait_ns);
+      gemm_produce<BN>(&tmA, &tmB, smem, g.full, g.empty, 0, p.K / kBK, m0, n0, pre,
+                       g.abort_flag, p.wait_ns);
   } else if (warp == 1) {
     if (lane == 0) gemm_mma<BN>(tmem, smem, g.full, g.empty, g.acc_full, p.K / kBK, g.abort_flag,
                                     p.wait_ns);
@@ -227,8 +271,6 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     }
   }
 
-  // this CTA's work is done: the next kernel in the stream may be scheduled
-  pdl_trigger();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -263,8 +305,6 @@ __global__ void __launch_bounds__(kThreadsG, 1)
   using Lay = SplitLayout<BN, S>;
   using Ring = GemmLayout<BN>;
   constexpr int c4n = BN / 4;
-  pdl_wait();
-  if (p.n_active && *p.n_active == 0) return;  // the same for every CTA of the grid
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -279,12 +319,15 @@ __global__ void __launch_bounds__(kThreadsG, 1)
   const int nk = (q + 1) * nkb / S - kb0;
   float4* tile_part =
       part + static_cast<int64_t>(blockIdx.z * gridDim.y + blockIdx.y) * S * c4n * kBM;
-  gemm_init<Ring::kStages>(g, BN);
+  int pre;
+  // n_active is the same for every CTA of the grid, so a cluster leaves (or stays) whole
+  if (!gemm_start<BN>(g, &tmA, &tmB, smem, kb0, nk, m0, n0, p.n_active, pre)) return;
+  pdl_trigger();  // the next kernel's CTAs may start their own prologue on idle SMs
   const uint32_t tmem = *g.tmem_slot;
 
   if (warp == 0) {
     if (lane == 0)
-      gemm_produce<BN>(&tmA, &tmB, smem, g.full, g.empty, kb0, nk, m0, n0, g.abort_flag,
+      gemm_produce<BN>(&tmA, &tmB, smem, g.full, g.empty, kb0, nk, m0, n0, pre, g.abort_flag,
                        p.wait_ns);
   } else if (warp == 1) {
     if (lane == 0) gemm_mma<BN>(tmem, smem, g.full, g.empty, g.acc_full, nk, g.abort_flag, p.wait_ns);
@@ -398,7 +441,6 @@ __global__ void __launch_bounds__(kThreadsG, 1)
         make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
                    pack_bf16x2(o[6], o[7]));
   }
-  pdl_trigger();
   if (threadIdx.x == 0 && *g.abort_flag) atomicOr(p.status, kStatusTimeout);
 }
 

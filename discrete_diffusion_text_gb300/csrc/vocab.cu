@@ -256,8 +256,6 @@ __global__ void __launch_bounds__(VocabLayout<kSplit>::kThreadsT, 1)
   using Lay = VocabLayout<kSplit>;
   constexpr int kWS = Lay::kWStages;
   constexpr int kYS = Lay::kYStages;
-  pdl_wait();
-  if (p.n_active && *p.n_active == 0) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -278,6 +276,9 @@ __global__ void __launch_bounds__(VocabLayout<kSplit>::kThreadsT, 1)
   const int nkb = p.d / kBK;
   const uint32_t rank = kMc ? cluster_ctarank() : 0u;
 
+  // W stages started before the wait for the previous kernel (split rings: the W ring holds
+  // the weight alone, which no kernel of the stream writes); thread 0 is the W producer
+  int pre = 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kWS; ++s) {
       mbar_init(&full[s], 1);
@@ -293,6 +294,22 @@ __global__ void __launch_bounds__(VocabLayout<kSplit>::kThreadsT, 1)
     }
     *abort_flag = 0;
     fence_barrier_init();
+    if (kSplit && blockIdx.x < p.units && !p.skip_loads) {
+      tma_prefetch_map(&tmB);
+      const uint64_t pol = p.w_keep ? l2_policy_evict_normal() : l2_policy_evict_first();
+      const int vt = (static_cast<int>(blockIdx.x) / p.num_mt) * p.per;  // the first unit's
+      pre = nkb < kWS ? nkb : kWS;
+      for (int kb = 0; kb < pre; ++kb) {
+        mbar_arrive_expect_tx(&full[kb], Lay::kBBytes);
+        tma_load_2d_hint(smem + kb * Lay::kBBytes, &tmB, &full[kb], kb * kBK, vt * kBN, pol);
+      }
+    }
+  }
+  pdl_wait();
+  if (p.n_active && *p.n_active == 0) {  // the same for every CTA of the grid
+    if (threadIdx.x == 0)  // let the started copies land before the CTA leaves
+      for (int s = 0; s < pre; ++s) mbar_wait_drain(&full[s], 0);
+    return;
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
@@ -323,6 +340,7 @@ __global__ void __launch_bounds__(VocabLayout<kSplit>::kThreadsT, 1)
         const int vt1 = min(vt0 + p.per, p.nvt);
         for (int vt = vt0; ok && vt < vt1; ++vt) {
           for (int kb = 0; kb < nkb; ++kb, ++g) {
+            if (g < static_cast<uint32_t>(pre)) continue;  // started before the wait
             const int s = g % kWS;
             if (!mbar_wait(&empty[s], ((g / kWS) & 1) ^ 1, abort_flag, p.wait_ns)) { ok = false; break; }
             if constexpr (kSplit) {  // the W k-block alone (warp 18 loads y)
