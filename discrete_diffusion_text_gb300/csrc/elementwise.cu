@@ -126,6 +126,7 @@ __device__ __forceinline__ VocabPart shfl_xor_part(const VocabPart& a, int off) 
 // step and its token.
 struct RowFinal {
   bool locked_after;
+  bool changed;  // the position's token differs from the one it had before the step
   int32_t token;
 };
 
@@ -151,7 +152,7 @@ __device__ __forceinline__ RowFinal finalize_row(const FinalizeParams& p, int ro
     }
   }
 
-  RowFinal r{false, 0};
+  RowFinal r{false, false, 0};
   if (lane == 0) {
     if (p.bar) p.bar[row] = 0u;  // the row's tuples are merged: clear its bar for the next pass
     const float lse = acc.m + logf(acc.s);
@@ -169,12 +170,14 @@ __device__ __forceinline__ RowFinal finalize_row(const FinalizeParams& p, int ro
       const bool was_locked = p.lock != nullptr && p.lock[row] != 0;
       const uint32_t u = jump_draw(static_cast<uint32_t>(i), static_cast<uint32_t>(b), p.step,
                                    p.k0, p.k1);
-      const EulerOut o = euler_decide(p.x_in[row], acc.best_idx, acc.top_idx, lp_top1,
-                                      was_locked, u, p.jump_thr, p.lock_logthr);
+      const int32_t x_old = p.x_in[row];  // x_out may be x_in
+      const EulerOut o = euler_decide(x_old, acc.best_idx, acc.top_idx, lp_top1, was_locked, u,
+                                      p.jump_thr, p.lock_logthr);
       p.x_out[row] = o.x;
       if (p.lock) p.lock[row] = o.lock ? 1 : 0;
       if (p.jump) p.jump[row] = o.jump ? 1 : 0;
       r.locked_after = o.lock && p.lock != nullptr;
+      r.changed = o.x != x_old;
       r.token = o.x;
     } else if (p.x_in != nullptr) {
       const int32_t x = p.x_in[row];
@@ -225,12 +228,17 @@ __global__ void __launch_bounds__(kFinRows * 32) vocab_finalize_kernel(FinalizeP
 }
 
 // The previous step's finalisation fused with this step's embedding gather: eight positions
-// per CTA (one warp each finalises its position, as above), then the CTA gathers E at the eight
-// new tokens, 16 bytes per thread.
+// per CTA (one warp each finalises its position, as above), then the CTA gathers E at those of
+// the eight new tokens that changed, 16 bytes per thread: h already holds E[x] of every
+// position whose token the step kept (the loop's first step gathers all of them, and only
+// this kernel writes h in between).  Each thread issues its loads before any store, and the
+// per-canvas ticket's atomics run while those loads are in flight.
 __global__ void __launch_bounds__(kFinRows * 32) embed_finalize_kernel(FinalizeParams p,
                                                                        const uint4* __restrict__ E,
                                                                        uint4* __restrict__ h, int V,
                                                                        int d16) {
+  constexpr int32_t kKept = -2;  // s_token of a position whose token the step kept
+  constexpr int kU = 8;          // 16-byte loads in flight per thread
   pdl_wait();
   pdl_trigger();
   if (p.n_active && *p.n_active == 0) return;
@@ -239,17 +247,31 @@ __global__ void __launch_bounds__(kFinRows * 32) embed_finalize_kernel(FinalizeP
   const int row0 = blockIdx.x * kFinRows;  // L is a multiple of kFinRows
   __shared__ int32_t s_token[kFinRows];
   const RowFinal r = finalize_row(p, row0 + warp, lane);
-  if (lane == 0) s_token[warp] = r.token;
+  if (lane == 0) s_token[warp] = r.changed ? r.token : kKept;
   const int unlocked = __syncthreads_count(lane == 0 && !r.locked_after ? 1 : 0);
-  if (threadIdx.x == 0) finalize_ticket(p, row0 / p.L, unlocked, p.L / kFinRows);
-  for (int q = threadIdx.x; q < kFinRows * d16; q += blockDim.x) {
-    const int rr = q / d16;
-    const int c = q - rr * d16;
-    const int id = s_token[rr];
-    const bool ok = id >= 0 && id < V;
-    if (!ok && c == 0) atomicOr(p.status, kStatusBadIndex);
-    h[static_cast<int64_t>(row0 + rr) * d16 + c] =
-        ok ? E[static_cast<int64_t>(id) * d16 + c] : make_uint4(0, 0, 0, 0);
+  const int n16 = kFinRows * d16;
+  for (int q0 = threadIdx.x; q0 < n16; q0 += kU * blockDim.x) {
+    uint4 v[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int q = q0 + u * blockDim.x;
+      const int rr = q / d16;
+      const int id = q < n16 ? s_token[rr] : kKept;
+      v[u] = id >= 0 && id < V ? E[static_cast<int64_t>(id) * d16 + (q - rr * d16)]
+                               : make_uint4(0, 0, 0, 0);
+    }
+    if (q0 == threadIdx.x && threadIdx.x == 0)
+      finalize_ticket(p, row0 / p.L, unlocked, p.L / kFinRows);
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int q = q0 + u * blockDim.x;
+      const int rr = q / d16;
+      const int id = q < n16 ? s_token[rr] : kKept;
+      if (id == kKept) continue;
+      const int c = q - rr * d16;
+      if (!(id >= 0 && id < V) && c == 0) atomicOr(p.status, kStatusBadIndex);
+      h[static_cast<int64_t>(row0 + rr) * d16 + c] = v[u];
+    }
   }
 }
 
