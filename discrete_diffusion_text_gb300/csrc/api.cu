@@ -225,7 +225,7 @@ struct LoopWs {
   uint32_t* status;
   uint8_t* active;
   int* n_active;
-  int* counters;  // [2B]: per-canvas unlocked count and CTA tickets of the finalisation
+  int* counters;  // [2B]: the finalisation's per-canvas tickets (B 64-bit words)
   uint16_t *h, *q, *k, *v, *o, *y;
   void* attn;
   void* gemm_part;  // fp32 split-K partials of the projections
@@ -530,8 +530,7 @@ dg_status dg_vocab_posterior_step(const uint16_t* y, const uint16_t* W, int B, i
   fp.k0 = static_cast<uint32_t>(seed);
   fp.k1 = static_cast<uint32_t>(seed >> 32);
   fp.step = static_cast<uint32_t>(step);
-  fp.unlocked = counters;
-  fp.cta_done = counters + B;
+  fp.ticket = reinterpret_cast<unsigned long long*>(counters);
   launch_vocab_finalize(fp, B, st);
   return check_launch("vocab finalize launch");
 }
@@ -569,8 +568,7 @@ dg_status dg_cross_entropy_step(const uint16_t* y, const uint16_t* W, int B, int
   fp.L = L;
   fp.out_lse = lse;
   fp.out_loss = loss;
-  fp.unlocked = counters;
-  fp.cta_done = counters + B;
+  fp.ticket = reinterpret_cast<unsigned long long*>(counters);
   launch_vocab_finalize(fp, B, st);
   return check_launch("cross_entropy: finalize launch");
 }
@@ -638,8 +636,7 @@ dg_status dg_sft_loss(const dg_model* m, const uint16_t* k_pre, const uint16_t* 
   fp.S = vp.S;
   fp.L = L;
   fp.out_loss = loss;
-  fp.unlocked = w.counters;
-  fp.cta_done = w.counters + B;
+  fp.ticket = reinterpret_cast<unsigned long long*>(w.counters);
   launch_vocab_finalize(fp, B, st);
   return check_launch("sft_loss: finalize launch");
 }
@@ -853,8 +850,7 @@ dg_status run_denoise(const RunArgs& a, const dg_sampler_cfg* cfg,
       fp.out_top1 = w.top1;
       fp.out_entropy = w.entropy;
       fp.n_active = w.n_active;
-      fp.unlocked = w.counters;
-      fp.cta_done = w.counters + B;
+      fp.ticket = reinterpret_cast<unsigned long long*>(w.counters);
       launch_vocab_finalize(fp, B, st);
       if ((s = check_launch("loop: finalize launch")) != DG_OK) return s;
       EBParams ep{};
@@ -890,8 +886,7 @@ dg_status run_denoise(const RunArgs& a, const dg_sampler_cfg* cfg,
       fp.steps_taken = a.steps_taken;
       fp.n_active = w.n_active;
       fp.stop_when_all_locked = cfg->stop_when_all_locked;
-      fp.unlocked = w.counters;
-      fp.cta_done = w.counters + B;
+      fp.ticket = reinterpret_cast<unsigned long long*>(w.counters);
       if (fuse) {
         pending = fp;
       } else {
@@ -1120,8 +1115,7 @@ dg_status dg_self_condition(const uint16_t* y, const uint16_t* E, const uint16_t
   dg_status s;
   e = cudaMemsetAsync(counters, 0, 2 * sizeof(int) * B, st);  // finalisation counters
   if (e != cudaSuccess) return cuda_fail(e, "self-condition: memset");
-  fp.unlocked = counters;
-  fp.cta_done = counters + B;
+  fp.ticket = reinterpret_cast<unsigned long long*>(counters);
   launch_vocab_finalize(fp, B, st);
   if ((s = check_launch("self-condition: finalize launch")) != DG_OK) return s;
   e = launch_self_condition(sc_p, sc_m, lse, E, Wsc1, Wsc2, BL, V, d, d_sc, part,

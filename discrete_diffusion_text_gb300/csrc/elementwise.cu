@@ -121,24 +121,54 @@ __device__ __forceinline__ VocabPart shfl_xor_part(const VocabPart& a, int off) 
   return o;
 }
 
-// One position: the lanes of a warp merge its tuples; lane 0 writes the posterior outputs and
-// applies the Euler step.  Returns (valid in lane 0) whether the position is locked after the
-// step and its token.
+// What the Euler step of one position reads besides the posterior: the token and the lock it
+// had, whether its canvas is active, and the position's jump uniform (Philox).  None of it is
+// written by the vocabulary pass, so the fused kernel reads it before waiting for that pass.
+struct RowIn {
+  int32_t x_old;
+  bool was_locked, is_active;
+  uint32_t u;
+};
+__device__ __forceinline__ RowIn row_inputs(const FinalizeParams& p, int row) {
+  const int b = row / p.L;
+  const int i = row % p.L;
+  RowIn in;
+  in.is_active = p.active == nullptr || p.active[b] != 0;
+  in.x_old = p.x_in != nullptr ? p.x_in[row] : 0;
+  in.was_locked = p.lock != nullptr && p.lock[row] != 0;
+  in.u = jump_draw(static_cast<uint32_t>(i), static_cast<uint32_t>(b), p.step, p.k0, p.k1);
+  return in;
+}
+
+// One position: the lanes of a warp merge its tuples (each lane its own in order c = lane,
+// lane + 32, ..., four loads in flight, then a butterfly); lane 0 writes the posterior outputs
+// and applies the Euler step.  Returns (valid in lane 0) whether the position is locked after
+// the step and its token.
 struct RowFinal {
   bool locked_after;
   bool changed;  // the position's token differs from the one it had before the step
   int32_t token;
 };
 
-__device__ __forceinline__ RowFinal finalize_row(const FinalizeParams& p, int row, int lane) {
-  const int b = row / p.L;
-  const int i = row % p.L;
-  const bool is_active = p.active == nullptr || p.active[b] != 0;
+__device__ __forceinline__ RowFinal finalize_row(const FinalizeParams& p, int row, int lane,
+                                                const RowIn& in) {
+  constexpr int kB = 4;  // tuple loads in flight per lane
+  const bool is_active = in.is_active;
   const int mt = row >> 7;
   const int row_in = row & 127;
   VocabPart acc = empty_part();
-  for (int c = lane; c < p.S; c += 32)
-    merge_part(acc, p.parts[(static_cast<int64_t>(c) * p.num_mt + mt) * 128 + row_in]);
+  for (int c0 = lane; c0 < p.S; c0 += 32 * kB) {
+    VocabPart t[kB];
+#pragma unroll
+    for (int k = 0; k < kB; ++k) {
+      const int c = c0 + 32 * k;
+      t[k] = c < p.S ? p.parts[(static_cast<int64_t>(c) * p.num_mt + mt) * 128 + row_in]
+                     : empty_part();
+    }
+#pragma unroll
+    for (int k = 0; k < kB; ++k)
+      if (c0 + 32 * k < p.S) merge_part(acc, t[k]);
+  }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
     const VocabPart o = shfl_xor_part(acc, off);
@@ -167,12 +197,9 @@ __device__ __forceinline__ RowFinal finalize_row(const FinalizeParams& p, int ro
     // cross-entropy mode: the best-sample fields carry the target's tempered logit
     if (p.out_loss) p.out_loss[row] = acc.best_idx != 0x7FFFFFFF ? lse - acc.best_z : NAN;
     if (p.x_in != nullptr && is_active) {
-      const bool was_locked = p.lock != nullptr && p.lock[row] != 0;
-      const uint32_t u = jump_draw(static_cast<uint32_t>(i), static_cast<uint32_t>(b), p.step,
-                                   p.k0, p.k1);
-      const int32_t x_old = p.x_in[row];  // x_out may be x_in
-      const EulerOut o = euler_decide(x_old, acc.best_idx, acc.top_idx, lp_top1, was_locked, u,
-                                      p.jump_thr, p.lock_logthr);
+      const int32_t x_old = in.x_old;  // read before the step (x_out may be x_in)
+      const EulerOut o = euler_decide(x_old, acc.best_idx, acc.top_idx, lp_top1, in.was_locked,
+                                      in.u, p.jump_thr, p.lock_logthr);
       p.x_out[row] = o.x;
       if (p.lock) p.lock[row] = o.lock ? 1 : 0;
       if (p.jump) p.jump[row] = o.jump ? 1 : 0;
@@ -180,28 +207,28 @@ __device__ __forceinline__ RowFinal finalize_row(const FinalizeParams& p, int ro
       r.changed = o.x != x_old;
       r.token = o.x;
     } else if (p.x_in != nullptr) {
-      const int32_t x = p.x_in[row];
+      const int32_t x = in.x_old;
       if (p.x_out != p.x_in) p.x_out[row] = x;
       if (p.jump) p.jump[row] = 0;
-      r.locked_after = p.lock != nullptr && p.lock[row] != 0;
+      r.locked_after = in.was_locked;
       r.token = x;
     }
   }
   return r;
 }
 
-// One thread per CTA, after the CTA's positions of canvas b are final: adds their unlocked
-// count; the last of the canvas's ctas_per_canvas CTAs to get here (an atomic ticket, no
-// waiting) sets `done`, updates the loop bookkeeping and resets the counters.
+// One thread per CTA, after the CTA's positions of canvas b are final: one 64-bit atomic adds
+// their unlocked count (high word) and takes a ticket (low word); the CTA that draws the
+// canvas's last ticket (no waiting) sees the canvas's whole unlocked count in the value it got
+// back, sets `done`, updates the loop bookkeeping and resets the word.  (Nothing the other
+// CTAs wrote is read here, so no fence is needed; the next kernel sees all of it.)
 __device__ __forceinline__ void finalize_ticket(const FinalizeParams& p, int b, int unlocked,
                                                 int ctas_per_canvas) {
   const bool is_active = p.active == nullptr || p.active[b] != 0;
-  if (unlocked) atomicAdd(&p.unlocked[b], unlocked);
-  __threadfence();
-  const int ticket = atomicAdd(&p.cta_done[b], 1);
-  if (ticket == ctas_per_canvas - 1) {  // the last CTA of this canvas
-    __threadfence();
-    const bool all = atomicAdd(&p.unlocked[b], 0) == 0;
+  const unsigned long long old =
+      atomicAdd(&p.ticket[b], (static_cast<unsigned long long>(unlocked) << 32) | 1ull);
+  if (static_cast<int>(old & 0xFFFFFFFFull) == ctas_per_canvas - 1) {  // the last CTA
+    const bool all = static_cast<int>(old >> 32) + unlocked == 0;
     if (p.done) p.done[b] = all ? 1 : 0;
     if (is_active && p.x_in != nullptr) {
       if (p.steps_taken) p.steps_taken[b] += 1;
@@ -210,8 +237,7 @@ __device__ __forceinline__ void finalize_ticket(const FinalizeParams& p, int b, 
         if (p.n_active) atomicSub(p.n_active, 1);
       }
     }
-    p.unlocked[b] = 0;
-    p.cta_done[b] = 0;
+    p.ticket[b] = 0ull;
   }
 }
 
@@ -222,7 +248,7 @@ __global__ void __launch_bounds__(kFinRows * 32) vocab_finalize_kernel(FinalizeP
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * kFinRows + warp;  // L is a multiple of kFinRows
-  const RowFinal r = finalize_row(p, row, lane);
+  const RowFinal r = finalize_row(p, row, lane, row_inputs(p, row));
   const int unlocked = __syncthreads_count(lane == 0 && !r.locked_after ? 1 : 0);
   if (threadIdx.x == 0) finalize_ticket(p, row / p.L, unlocked, p.L / kFinRows);
 }
@@ -239,14 +265,17 @@ __global__ void __launch_bounds__(kFinRows * 32) embed_finalize_kernel(FinalizeP
                                                                        int d16) {
   constexpr int32_t kKept = -2;  // s_token of a position whose token the step kept
   constexpr int kU = 8;          // 16-byte loads in flight per thread
-  pdl_wait();
-  pdl_trigger();
-  if (p.n_active && *p.n_active == 0) return;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int row0 = blockIdx.x * kFinRows;  // L is a multiple of kFinRows
+  // the canvas, the locks and the active flags were last written by the previous step's
+  // launch of this kernel, long complete: read them before waiting for the vocabulary pass
+  const RowIn in = row_inputs(p, row0 + warp);
+  pdl_wait();
+  pdl_trigger();
+  if (p.n_active && *p.n_active == 0) return;
   __shared__ int32_t s_token[kFinRows];
-  const RowFinal r = finalize_row(p, row0 + warp, lane);
+  const RowFinal r = finalize_row(p, row0 + warp, lane, in);
   if (lane == 0) s_token[warp] = r.changed ? r.token : kKept;
   const int unlocked = __syncthreads_count(lane == 0 && !r.locked_after ? 1 : 0);
   const int n16 = kFinRows * d16;

@@ -29,8 +29,9 @@ struct FinalizeParams {
   int32_t* steps_taken;  // loop only
   int* n_active;         // loop only
   int stop_when_all_locked;
-  int* unlocked;  // [B] per-canvas counters, zero before the first call; reset by the kernel
-  int* cta_done;  // [B]
+  // [B] per canvas: (positions left unlocked << 32) + CTAs done, zero before the first call;
+  // reset by the kernel (8-byte aligned)
+  unsigned long long* ticket;
   uint32_t* bar;  // the vocabulary pass's sampling bars: zeroed per row once merged (or NULL)
   uint32_t* status;  // embed_finalize_kernel: kStatusBadIndex for a token outside [0, V)
 };

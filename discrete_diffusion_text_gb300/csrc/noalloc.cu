@@ -114,8 +114,7 @@ extern "C" dg_status dg_vocab_posterior_step_noalloc(
   fp.k0 = static_cast<uint32_t>(seed);
   fp.k1 = static_cast<uint32_t>(seed >> 32);
   fp.step = static_cast<uint32_t>(step);
-  fp.unlocked = counters;
-  fp.cta_done = counters + B;
+  fp.ticket = reinterpret_cast<unsigned long long*>(counters);
   launch_vocab_finalize(fp, B, st);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "vocab_posterior_noalloc: finalize launch");
