@@ -52,8 +52,6 @@ struct ScGemmParams {
 __global__ void __launch_bounds__(192, 1)
     sc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    ScGemmParams p) {
-  pdl_wait();
-  if (p.n_active && *p.n_active == 0) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -71,6 +69,20 @@ __global__ void __launch_bounds__(192, 1)
   const int kb0 = blockIdx.z * p.per;
   const int kb1 = min(kb0 + p.per, p.nkb);  // the plan leaves no split empty
 
+  // Before the wait for the previous kernel (the finalisation, which writes lse): the barriers
+  // and the first stages' copies.  P~ and m_ref come from the vocabulary pass before it, which
+  // has completed once this kernel can start; E is the model's.  Thread 0 is the producer.
+  const uint64_t stream_once = l2_policy_evict_first();
+  auto load_stage = [&](int s, int kb) {
+    uint8_t* sa = smem + s * kScStageBytes;
+    mbar_arrive_expect_tx(&full[s], kScStageBytes);
+    tma_load_2d(sa, &tmA, &full[s], kb * kScBK, m0);
+#pragma unroll
+    for (int c = 0; c < kScBN / 64; ++c)
+      tma_load_2d_hint(sa + kScABytes + c * kScBChunk, &tmB, &full[s], n0 + c * 64, kb * kScBK,
+                       stream_once);
+  };
+  int pre = 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kScStages; ++s) {
       mbar_init(&full[s], 1);
@@ -80,7 +92,17 @@ __global__ void __launch_bounds__(192, 1)
     mbar_init(acc_full, 1);
     *abort_flag = 0;
     fence_barrier_init();
+    tma_prefetch_map(&tmA);
+    tma_prefetch_map(&tmB);
+    for (; pre < kScStages && kb0 + pre < kb1; ++pre) load_stage(pre, kb0 + pre);
   }
+  pdl_wait();
+  if (p.n_active && *p.n_active == 0) {  // the same for every CTA of the grid
+    if (threadIdx.x == 0)  // let the started copies land before the CTA leaves
+      for (int s = 0; s < pre; ++s) mbar_wait_drain(&full[s], 0);
+    return;
+  }
+  pdl_trigger();  // the next kernel's CTAs may start their own prologue on idle SMs
   // TMEM: the fp32 accumulator in columns [0, 256); the normalised A operand in a ring of
   // kScStages slots of 32 columns (64 bf16 per lane) from column 256.
   if (warp == 1) {
@@ -94,21 +116,12 @@ __global__ void __launch_bounds__(192, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      tma_prefetch_map(&tmA);
-      tma_prefetch_map(&tmB);
-      const uint64_t stream_once = l2_policy_evict_first();
-      int issued = 0;
-      for (int kb = kb0; kb < kb1; ++kb, ++issued) {
+      int issued = pre;  // the first stages were started before the wait
+      for (int kb = kb0 + pre; kb < kb1; ++kb, ++issued) {
         const int s = issued % kScStages;
         const uint32_t r = issued / kScStages;
         if (!mbar_wait(&empty[s], (r & 1) ^ 1, abort_flag, p.wait_ns)) break;
-        uint8_t* sa = smem + s * kScStageBytes;
-        mbar_arrive_expect_tx(&full[s], kScStageBytes);
-        tma_load_2d(sa, &tmA, &full[s], kb * kScBK, m0);
-#pragma unroll
-        for (int c = 0; c < kScBN / 64; ++c)
-          tma_load_2d_hint(sa + kScABytes + c * kScBChunk, &tmB, &full[s], n0 + c * 64,
-                           kb * kScBK, stream_once);
+        load_stage(s, kb);
       }
       if (*abort_flag) {  // let copies already in flight land before the CTA exits
         for (int q = (issued > kScStages ? issued - kScStages : 0); q < issued; ++q)
@@ -192,8 +205,6 @@ __global__ void __launch_bounds__(192, 1)
     }
   }
 
-  // this CTA's work is done: the next kernel in the stream may be scheduled
-  pdl_trigger();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
