@@ -148,6 +148,7 @@ ATTN_CASES = [
     (1, 256, 2048, 4, 2, 128, 0, 4.0),      # sharp scores: exercises the max rescaling
     (1, 256, 512, 8, 4, 128, 0, 1.0),       # six key splits merged inside a cluster (ragged rows)
     (1, 128, 2048, 16, 8, 128, 0, 1.0),     # nine key splits: more than a cluster, merge kernel
+    (1, 256, 2048, 16, 8, 128, 128, 1.0),   # narrow window: cluster splits with no key tile
 ]
 
 
