@@ -125,9 +125,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tmVc, AttnParams p) {
   using Lay = AttnLayout<HD>;
   constexpr int kRing = Lay::kRing;
-  pdl_wait();
-  if (p.n_active && *p.n_active == 0) return;
-  pdl_trigger();  // the next kernel's CTAs may start their own prologue on idle SMs
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -171,19 +168,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int hq = slot ? sl.h1 : sl.h0;
   const int64_t out_row = (static_cast<int64_t>(sl.b) * p.H + hq) * p.L + qi;  // (b, h, i)
   const int64_t part_rows = static_cast<int64_t>(p.B) * p.H * p.L;
+  auto q_buf = [&](int s) { return smem + Lay::kQOff + s * Lay::kQBytes; };
+  auto kv_buf = [&](int i) { return smem + Lay::kKVOff + (i % kRing) * Lay::kKVBytes; };
 
-  if (nt == 0) {  // nothing to do: empty partials (only when splits > 1)
-    if (warp >= 4 && (slot == 0 || sl.valid1) && qi < p.L) {
-      float* ml = p.part_ml + (split * part_rows + out_row) * 2;
-      ml[0] = -INFINITY;
-      ml[1] = 0.f;
-      float* po = p.part_o + (split * part_rows + out_row) * HD;
-      for (int c = 0; c < HD; ++c) po[c] = 0.f;
-    }
-    return;
-  }
-
-  if (threadIdx.x == 0) {
+  // Before the wait for the previous kernel: the barriers, and the prefix K/V tiles of the
+  // first ring slots (the cache, which the kernels of a denoising step do not write); thread
+  // 0 is the producer.
+  int n_early = 0;
+  if (threadIdx.x == 0 && nt > 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < kRing; ++s) {
       mbar_init(&kv_full[s], 1);
@@ -197,7 +189,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < 3; ++s) mbar_init(&drain[s], 1);
     *abort_flag = 0;
     fence_barrier_init();
+    tma_prefetch_map(&tmKp);
+    tma_prefetch_map(&tmVp);
+    for (int i = 0; i < 2 * nt && i < kRing; ++i) {
+      const int t = t_begin + (i >> 1);
+      if (t >= n_pre) break;
+      const CUtensorMap* m = (i & 1) ? &tmVp : &tmKp;
+      mbar_arrive_expect_tx(&kv_full[i], Lay::kKVBytes);
+      for (int c = 0; c < HD / 64; ++c)
+        tma_load_4d(kv_buf(i) + c * Lay::kKVChunk, m, &kv_full[i], c * 64, sl.g,
+                    (t_lo + t) * kKTile, sl.b);
+      ++n_early;
+    }
   }
+  pdl_wait();
+  if (p.n_active && *p.n_active == 0) {  // the same for every CTA of the grid
+    if (threadIdx.x == 0)  // let the started copies land before the CTA leaves
+      for (int i = 0; i < n_early; ++i) mbar_wait_drain(&kv_full[i], 0);
+    return;
+  }
+  pdl_trigger();  // the next kernel's CTAs may start their own prologue on idle SMs
+
+  if (nt == 0) {  // nothing to do: empty partials (only when splits > 1)
+    if (warp >= 4 && (slot == 0 || sl.valid1) && qi < p.L) {
+      float* ml = p.part_ml + (split * part_rows + out_row) * 2;
+      ml[0] = -INFINITY;
+      ml[1] = 0.f;
+      float* po = p.part_o + (split * part_rows + out_row) * HD;
+      for (int c = 0; c < HD; ++c) po[c] = 0.f;
+    }
+    return;
+  }
+
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
@@ -208,8 +231,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   auto tm_s = [&](int s, int b) { return tmem + (2 * s + b) * kKTile; };
   auto tm_o = [&](int s) { return tmem + 256 + s * 128; };
-  auto q_buf = [&](int s) { return smem + Lay::kQOff + s * Lay::kQBytes; };
-  auto kv_buf = [&](int i) { return smem + Lay::kKVOff + (i % kRing) * Lay::kKVBytes; };
 
   // Register split (each warpgroup changes its budget in its own branch): the control
   // warpgroup (TMA and MMA warps) needs few registers, each softmax thread holds a score row.
@@ -228,6 +249,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // load index i: K_j for i = 2j, V_j for i = 2j + 1, into ring slot i % kRing
       int issued = 0;
       for (int i = 0; i < 2 * nt; ++i) {
+        if (i < n_early) {  // requested before the wait
+          ++issued;
+          continue;
+        }
         const int rs = i % kRing;
         if (!mbar_wait(&kv_empty[rs], ((i / kRing) & 1) ^ 1, abort_flag, p.wait_ns)) break;
         const int t = t_begin + (i >> 1);
