@@ -27,7 +27,9 @@
 // With several key splits, each writes unnormalised fp32 partials (O, m, l) and a merge kernel
 // combines them with the log-sum-exp rule.
 // A second kernel (canvas_attn1_kernel, below) takes one query head per CTA with 128-key
-// tiles; plan_attention picks it where the K/V work is short (see there).
+// tiles; plan_attention picks it where the K/V work is short (see there).  Its 2..8 key
+// splits of a unit run as one thread-block cluster and merge there (attn1_cluster_merge).
+// Both kernels request their first prefix K/V tiles before waiting for the previous kernel.
 #include <array>
 #include <mutex>
 #include <vector>

@@ -3,7 +3,9 @@
 //   bf16 out.
 // Warp 0 streams A/W k-blocks with TMA into a shared-memory ring (128-byte swizzle); one
 // thread of warp 1 issues tcgen05.mma (M = 128, N = BN, K = 16 per instruction) into a TMEM
-// accumulator; warps 2..5 read the accumulator back with tcgen05.ld.
+// accumulator; warps 2..5 read the accumulator back with tcgen05.ld.  The W halves of the
+// first stages are requested before the wait for the previous kernel (gemm_start): the weights
+// are never written by the stream's kernels, only A (the activations) has to wait.
 //
 // Two kernels share that main loop:
 //  * gemm_bf16_kernel: one 128 x BN output tile per CTA over the whole K (many tiles: a

@@ -13,7 +13,9 @@
 //                by their log-sum-exps, then Gumbel-max over the winning chunk's entries.
 // Only rows' partial tuples are written; a finalisation kernel merges them in a fixed order and
 // applies the Euler step (the chunk scores merge like any Gumbel-max scores).  With many row
-// tiles the CTAs run as clusters of two that share each weight k-block by TMA multicast.
+// tiles the CTAs run as clusters of two that share each weight k-block by TMA multicast.  With
+// separate weight and y rings (single-wave passes) the first weight stages are requested
+// before the wait for the previous kernel, which only y depends on.
 #include <algorithm>
 #include <type_traits>
 
