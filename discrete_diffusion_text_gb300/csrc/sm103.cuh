@@ -166,6 +166,13 @@ __device__ __forceinline__ void st_dsmem_f4(uint32_t addr, float4 v) {
                : "memory");
 }
 
+// 32 bytes (a whole L2 sector) in one store; the address must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&v)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
 // ----------------------------------------------------------------------------- TMA -----
 
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {

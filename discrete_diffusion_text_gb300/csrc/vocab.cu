@@ -137,7 +137,9 @@ __device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
 // kSC: also store the chunk's exp(z~ - m) as bf16 (32 values, 64 bytes at sc_dst) with the
 // reference m it was taken against (at *sc_mdst); NULL pointers for rows past the end.  The
 // normalised posterior of the self-conditioning contraction is that value times
-// exp(m - lse), applied once lse is known.
+// exp(m - lse), applied once lse is known.  Sixteen values go out per store: one 32-byte
+// store (a whole sector: the 32 lanes of a warp write 32 different rows) when sc_v8 (the
+// buffer is 32-byte aligned), else two 16-byte stores.
 // u_gumbel: the chunk's Gumbel draw, word c & 3 of Philox(c >> 2, pos, canvas, c3) for chunk
 // c = vbase / 32 (computed by the caller, once for the chunks that share a counter).
 // bar / bar_ptr: the row's best chunk score published by any thread of the launch so far (as
@@ -152,7 +154,8 @@ __device__ __forceinline__ void process_chunk(RowState& st, const float (&z)[32]
                                               float inv_tau, uint32_t pos, uint32_t canvas,
                                               const PhiloxKeys& keys, uint32_t u_gumbel,
                                               uint32_t c3_pick, int target, uint16_t* sc_dst,
-                                              float* sc_mdst, float bar, uint32_t* bar_ptr) {
+                                              float* sc_mdst, bool sc_v8, float bar,
+                                              uint32_t* bar_ptr) {
   float mx[4] = {z[0], z[1], z[2], z[3]};  // four partial maxima: short dependency chains
 #pragma unroll
   for (int e = 4; e < 32; e += 2) mx[(e >> 1) & 3] = fmax3(mx[(e >> 1) & 3], z[e], z[e + 1]);
@@ -178,7 +181,7 @@ __device__ __forceinline__ void process_chunk(RowState& st, const float (&z)[32]
   float ps[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums of exp(z~ - m)
   float pt[4] = {0.f, 0.f, 0.f, 0.f};  // and of exp(z~ - m) (z~ - m) log2(e)
   if (kSC && sc_mdst) *sc_mdst = st.m;
-  uint32_t pk[4];
+  uint32_t pk[8];
 #pragma unroll
   for (int e = 0; e < 32; e += 2) {  // two logits per packed fp32 instruction
     float a0, a1;
@@ -188,10 +191,17 @@ __device__ __forceinline__ void process_chunk(RowState& st, const float (&z)[32]
     const int q = (e >> 1) & 1;
     fadd2(ps[2 * q], ps[2 * q + 1], ps[2 * q], ps[2 * q + 1], p0, p1);
     if (kEnt) ffma2(pt[2 * q], pt[2 * q + 1], p0, p1, a0, a1, pt[2 * q], pt[2 * q + 1]);
-    if (kSC) {  // eight values (16 bytes) per store
-      pk[(e >> 1) & 3] = pack_bf16x2(p0, p1);
-      if ((e & 7) == 6 && sc_dst)
-        *reinterpret_cast<uint4*>(sc_dst + (e - 6)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    if (kSC) {  // sixteen values (32 bytes) per store
+      pk[(e >> 1) & 7] = pack_bf16x2(p0, p1);
+      if ((e & 15) == 14 && sc_dst) {
+        uint16_t* d = sc_dst + (e - 14);
+        if (sc_v8) {
+          st_global_v8(d, pk);
+        } else {
+          reinterpret_cast<uint4*>(d)[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          reinterpret_cast<uint4*>(d)[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+      }
     }
   }
   const float sc = (ps[0] + ps[1]) + (ps[2] + ps[3]);
@@ -461,6 +471,8 @@ __global__ void __launch_bounds__(VocabLayout<kSplit>::kThreadsT, 1)
     // unit's named barriers); only the waits, loads and stores are skipped.
     uint32_t j = 0;
     bool ok = true;
+    // rows start 2V bytes apart and chunks 64 bytes apart: the base's alignment decides
+    const bool sc_v8 = kSC && (reinterpret_cast<uintptr_t>(p.sc_p) & 31) == 0 && (p.V & 15) == 0;
     for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
       const int mt = u % p.num_mt;
       const int chunk = u / p.num_mt;
@@ -516,7 +528,8 @@ __global__ void __launch_bounds__(VocabLayout<kSplit>::kThreadsT, 1)
           process_chunk<kCE, kEnt, kSC>(st, z, vb, p.inv_tau, pos, canvas, keys,
                                         c == 0 ? ug[0] : ug[1], p.c3_pick, target,
                                         sc_row ? sc_row + vb : nullptr,
-                                        scm_row ? scm_row + (vb >> 5) : nullptr, bar, bar_row);
+                                        scm_row ? scm_row + (vb >> 5) : nullptr, sc_v8, bar,
+                                        bar_row);
         }
       }
       // Merge the column groups of each row through shared memory, in group order.
