@@ -236,6 +236,9 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     tc_fence_after();
     const int row = m0 + (warp & 3) * 32 + lane;
     const SegDst dst = segment_of(p.out, n0);
+    // one thread per row: 32-byte stores write whole L2 sectors (rows lie ld apart) when the
+    // segment's base and row pitch allow them
+    const bool v8 = (reinterpret_cast<uintptr_t>(dst.base) & 31) == 0 && (dst.ld & 15) == 0;
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
       float v[32];
@@ -261,14 +264,19 @@ __global__ void __launch_bounds__(kThreadsG, 1)
 #pragma unroll
         for (int e = 0; e < 32; ++e) v[e] = gelu_tanh(v[e]);
       }
-      uint4* d4 = reinterpret_cast<uint4*>(dst.base + static_cast<int64_t>(row) * dst.ld +
-                                           (col - dst.beg));
+      uint16_t* d = dst.base + static_cast<int64_t>(row) * dst.ld + (col - dst.beg);
+      uint32_t pk[2][8];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        d4[q] = make_uint4(pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]),
-                           pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]),
-                           pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]),
-                           pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]));
+      for (int e = 0; e < 16; ++e) pk[e >> 3][e & 7] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
+      if (v8) {
+        st_global_v8(d, pk[0]);
+        st_global_v8(d + 16, pk[1]);
+      } else {
+        uint4* d4 = reinterpret_cast<uint4*>(d);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          d4[q] = make_uint4(pk[q >> 1][4 * (q & 1)], pk[q >> 1][4 * (q & 1) + 1],
+                             pk[q >> 1][4 * (q & 1) + 2], pk[q >> 1][4 * (q & 1) + 3]);
       }
     }
   }

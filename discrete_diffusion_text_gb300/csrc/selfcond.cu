@@ -193,15 +193,27 @@ __global__ void __launch_bounds__(192, 1)
     ok = ok && warp_wait(acc_full, 0, abort_flag, p.wait_ns);
     tc_fence_after();
     float* dst = p.part + (static_cast<int64_t>(blockIdx.z) * p.R + row) * p.d + n0;
+    // one thread per row: 32-byte stores write whole L2 sectors when the base allows them
+    const bool v8 = (reinterpret_cast<uintptr_t>(p.part) & 31) == 0;
 #pragma unroll 1
     for (int c = 0; c < kScBN / 32; ++c) {
       float v[32];
       tmem_ld32(tmem + tmem_lane_base(warp) + c * 32, v);
       if (!ok || row >= p.R) continue;
-      float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+      if (v8) {
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        d4[q] = make_float4(v[q * 4], v[q * 4 + 1], v[q * 4 + 2], v[q * 4 + 3]);
+        for (int q = 0; q < 4; ++q) {
+          uint32_t w[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) w[e] = __float_as_uint(v[q * 8 + e]);
+          st_global_v8(dst + c * 32 + q * 8, w);
+        }
+      } else {
+        float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          d4[q] = make_float4(v[q * 4], v[q * 4 + 1], v[q * 4 + 2], v[q * 4 + 3]);
+      }
     }
   }
 
