@@ -111,8 +111,10 @@ def test_euler_update_bit_exact(dgc, B, L, lock_on):
 
 # --------------------------------------------------------- embedding + projections -----
 
-@pytest.mark.parametrize("wname", ["tiny", "window1k"])
+@pytest.mark.parametrize("wname", ["tiny", "window1k", "batch16"])
 def test_embed_qkv_and_out_proj(dgc, wname):
+    """batch16 (4,096 rows): more output tiles than SMs (several waves of the one-tile-per-CTA
+    kernel, the output projection with its residual)."""
     w = synth.WORKLOADS[wname]
     m = synth.make_model(w)
     BL = w.B * w.L
