@@ -104,9 +104,15 @@ class ClockSampler:
         self.proc.terminate()
         self.proc.wait(timeout=10)
         self.fh.close()
-        sm, smax, reasons = [], [], set()
+        return self.parse(self.path)
+
+    @staticmethod
+    def parse(path):
+        """Median SM clock, the maximum clock, the throttle reasons seen and the median board
+        power (W) of the samples in the csv file."""
+        sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
+        for line in open(path):
             f = [x.strip() for x in line.split(",")]
             if len(f) < 9:
                 continue
@@ -115,13 +121,20 @@ class ClockSampler:
                 smax.append(float(f[2]))
             except ValueError:
                 continue
+            try:
+                power.append(float(f[3]))
+            except ValueError:
+                pass
             for n, v in zip(names, f[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+               "reasons": sorted(reasons), "samples": len(sm)}
+        if power:
+            out["power_w"] = statistics.median(power)
+        return out
 
 
 def traffic_from_profile(kernel_file: str, workload: str):

@@ -1,6 +1,7 @@
-"""The benchmark's reference arm (the CPU oracle timed on the host cores), run as the driver
-runs it: one JSON line with the base contract's keys, on the same metric, unit and workload as
-the GPU arm; ranks other than 0 exit without work."""
+"""The benchmark's host-side parts, without a GPU: the reference arm (the CPU oracle timed on
+the host cores), run as the driver runs it (one JSON line with the base contract's keys, on the
+same metric, unit and workload as the GPU arm; ranks other than 0 exit without work), and the
+parsing of the clock samples taken during the timed region."""
 
 import json
 import os
@@ -44,3 +45,20 @@ def test_reference_arm_line():
 
 def test_reference_arm_other_ranks_do_nothing():
     assert _run({"RANK": "1"}) == []
+
+
+def test_clock_samples_parse(tmp_path):
+    """The timed region's nvidia-smi samples: median SM clock, maximum clock, the throttle
+    reasons seen at least once, and the median board power."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    f = tmp_path / "clocks.csv"
+    f.write_text("0, 1650, 2070, 1380.5, 0x4, Not Active, Not Active, Not Active, Active\n"
+                 "0, 1700, 2070, 1395.0, 0x0, Not Active, Not Active, Not Active, Not Active\n"
+                 "0, 1600, 2070, [N/A], 0x4, Not Active, Not Active, Not Active, Active\n"
+                 "garbage line\n")
+    c = bench.ClockSampler.parse(str(f))
+    assert c["sm_mhz"] == 1650 and c["sm_max_mhz"] == 2070 and c["samples"] == 3
+    assert c["reasons"] == ["sw_power_cap"]
+    assert c["power_w"] == (1380.5 + 1395.0) / 2
