@@ -93,7 +93,7 @@ void launch_embed_gather(const int32_t* x, const uint16_t* E, uint16_t* h, int B
 
 // Launch with programmatic stream serialisation: the kernel may be scheduled while the
 // previous kernel in the stream finishes (its launch latency hidden behind that kernel); it
-// must call pdl_wait() before touching global memory.
+// must call pdl_wait() before touching memory that kernel writes (see pdl_wait).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                              cudaStream_t st, Args&&... args) {

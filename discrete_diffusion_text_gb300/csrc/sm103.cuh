@@ -119,8 +119,11 @@ __device__ __forceinline__ void regs_increase() {
 // ------------------------------------------------------- programmatic dependent launch ----
 // A kernel launched as a programmatic dependent (launch_dependent below) may start while the
 // previous kernel in the stream is still running; pdl_wait blocks until that kernel has
-// completed and its writes are visible (a no-op for an ordinary launch), and must precede
-// every global-memory access.  pdl_trigger lets the next dependent kernel be scheduled once
+// completed and its writes are visible (a no-op for an ordinary launch).  It must precede every
+// access to memory that the previous kernel writes (and every write the previous kernel may
+// still read).  Data written two or more kernels back may be read before it: every kernel here
+// calls pdl_trigger only after its own pdl_wait, so when a kernel starts, all kernels before
+// its predecessor have completed.  pdl_trigger lets the next dependent kernel be scheduled once
 // every CTA of this grid has issued it (or exited); it carries no memory ordering.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
